@@ -1,0 +1,391 @@
+"""fp64 CPU oracle for the DSA attention step (index-K store -> lightning
+indexer -> top-2048 -> sparse MLA).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this module; only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` do.  It shares no code, constant or helper with the
+CUDA library: every constant below is restated from the pages on its own.
+
+Sources (the four web pages collected for dsa_sparse_attention_indexer):
+
+* "vLLM 推理链路概览：以 GLM-5.2 为例", section "DSA Indexer": the indexer score
+  s_ij = sum_m w_im ReLU(<q_im, k_j>) and I_i = TopK_{j,2048}(s_ij); section
+  "Sparse MLA Attention": alpha = softmax_{j in I, j <= i}(q k^T / sqrt(256)),
+  o = sum alpha v.
+* "GLM-5.3 推理全链路(十一)", section "索引器缓存里存的是什么": index key = k_norm
+  (LayerNorm) -> RoPE on the first 64 dims -> FP8 with one 4-byte ue8m0 scale
+  per 128 dims, 132 B/token, 64-token pages of 8448 B; section "主 KV 缓存里存的
+  是什么": latent row = 512 FP8 + four 4-byte scales (+ 64 RoPE dims), 656 B.
+  Section "优化二: 短上下文直接跳过打分": context <= 2048 selects [0..L-1, -1...].
+  Section "配置里的 78 个字符": the indexer_types list and the freq/offset rule.
+* "GLM-5.3 推理全链路(一)", section 4.5: indexer_rope_interleave=True, and the
+  full layers 0, 1, 2, 6, 10, ..., 74 (21 full, 57 shared).
+
+Readings where the pages are silent (each also listed in the design notes):
+LayerNorm eps 1e-6 with optional affine; interleaved RoPE pairs (2i, 2i+1),
+angle = pos * base^(-2i/64), base 10000; the ue8m0 scale rounds UP (smallest
+power of two with amax <= 448 * scale, amax == 0 -> scale 1) and is stored as an
+fp32 power of two; an index-K page stores the 64 payload rows first and then the
+64 fp32 scales; a latent row is [512 FP8 | 4 x fp32 scale | 64 bf16 RoPE];
+ties in the top-k go to the lower position, -0.0 equals +0.0, and the selected
+positions are listed in ascending order followed by -1 padding.
+
+Parity pins: every function here is pinned by tests under ``-m "not gpu"``
+(codec vs the format definition and torch's float8 casts, layout constants the
+pages print, the 21/57 schedule, brute-force top-k, sparse == dense attention
+when the context fits in the top-k, closed forms).  The LayerNorm eps, RoPE base
+and RoPE pairing are NOT fixed by the pages: "parity unpinned" for those three
+parameters - the tests check only self-consistency (moments, pair norms, the
+rotation group law) for them.
+"""
+
+from __future__ import annotations
+
+import math
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# Constants restated from the pages ("GLM-5.3 推理全链路(十一)", index cache and
+# main KV cache sections; "vLLM 推理链路概览", DSA Indexer / Sparse MLA).
+# ----------------------------------------------------------------------------
+PAGE_TOKENS = 64                   # page_size == 64 (asserted on the CUDA path)
+INDEX_HEAD_DIM = 128               # index_head_dim == 128
+INDEX_HEADS = 32                   # 32 indexer query heads
+INDEX_TOKEN_BYTES = 128 + 4        # FP8 key + one 4-byte scale per 128 dims
+INDEX_PAGE_BYTES = PAGE_TOKENS * INDEX_TOKEN_BYTES   # 8448
+LATENT_DIM = 512                   # kv_lora_rank
+ROPE_DIM = 64                      # qk_rope_head_dim
+LATENT_TOKEN_BYTES = 512 + 4 * 4 + 64 * 2            # 656
+LATENT_PAGE_BYTES = PAGE_TOKENS * LATENT_TOKEN_BYTES  # 41984
+MLA_HEADS = 64
+TOPK = 2048                        # index_topk
+SOFTMAX_SCALE = 1.0 / math.sqrt(256.0)
+E4M3_MAX = 448.0
+
+
+# ----------------------------------------------------------------------------
+# FP8 E4M3 codec written from the OCP FP8 format definition: 1 sign bit, 4
+# exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is NaN.
+# ----------------------------------------------------------------------------
+def e4m3_decode_table() -> np.ndarray:
+    """Value of each of the 256 codes, in fp64 (NaN for the two NaN codes)."""
+    out = np.empty(256, dtype=np.float64)
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        exp = (code >> 3) & 0xF
+        man = code & 0x7
+        if exp == 0xF and man == 0x7:
+            out[code] = np.nan
+        elif exp == 0:
+            out[code] = sign * (man / 8.0) * 2.0 ** (1 - 7)      # subnormal
+        else:
+            out[code] = sign * (1.0 + man / 8.0) * 2.0 ** (exp - 7)
+    return out
+
+
+_E4M3_TABLE = e4m3_decode_table()
+# Non-negative finite codes 0x00..0x7E in increasing value order.
+_E4M3_POS_CODES = np.arange(0x7F, dtype=np.int64)
+_E4M3_POS_VALS = _E4M3_TABLE[:0x7F]
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8).astype(np.int64)]
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Round each |x| <= 448 to the nearest E4M3 value, ties to the even code.
+
+    The caller guarantees |x| <= 448 (the scale rule below ensures it), so no
+    saturation rule is needed.  A value that rounds to zero keeps its sign.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    if np.any(ax > E4M3_MAX) or np.any(~np.isfinite(ax)):
+        raise ValueError("e4m3_encode: input outside [-448, 448]")
+    hi = np.searchsorted(_E4M3_POS_VALS, ax, side="left")       # first value >= ax
+    hi = np.minimum(hi, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E4M3_POS_VALS[hi] - ax
+    d_lo = ax - _E4M3_POS_VALS[lo]
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & ((lo & 1) == 0))
+    code = np.where(pick_lo, lo, hi)
+    code = np.where(ax == _E4M3_POS_VALS[hi], hi, code)          # exact hits
+    sign = np.signbit(x).astype(np.int64) << 7
+    return (code | sign).astype(np.uint8)
+
+
+def e4m3_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of E4M3 values around |v| (the step used for the 1-ulp bar)."""
+    av = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(av, 2.0 ** -6)))
+    return 2.0 ** (e - 3)
+
+
+# ----------------------------------------------------------------------------
+# ue8m0 block scale: a pure power of two, one per 128 values.
+# ----------------------------------------------------------------------------
+def ue8m0_exponent(amax):
+    """Smallest integer e with amax <= 448 * 2**e; amax == 0 gives e = 0.
+
+    Works elementwise.  The logarithm only gives a starting guess; the result
+    is settled by exact comparisons against powers of two (ldexp is exact in
+    fp64).
+    """
+    a = np.asarray(amax, dtype=np.float64)
+    e = np.zeros(a.shape, dtype=np.int64)
+    nz = a > 0
+    e[nz] = np.floor(np.log2(a[nz] / E4M3_MAX)).astype(np.int64)
+    for _ in range(4):
+        up = nz & (a > np.ldexp(E4M3_MAX, e))
+        e[up] += 1
+        down = nz & (a <= np.ldexp(E4M3_MAX, e - 1))
+        e[down] -= 1
+    assert np.all(a[nz] <= np.ldexp(E4M3_MAX, e[nz]))
+    assert np.all(a[nz] > np.ldexp(E4M3_MAX, e[nz] - 1))
+    return e if e.ndim else int(e)
+
+
+def quantize_blocks_128(x: np.ndarray):
+    """Quantise each run of 128 values: returns (E4M3 codes, fp64 scales 2**e)."""
+    x = np.asarray(x, dtype=np.float64)
+    assert x.shape[-1] == 128
+    e = np.asarray(ue8m0_exponent(np.max(np.abs(x), axis=-1)))
+    scales = np.ldexp(1.0, e)
+    codes = e4m3_encode(x / scales[..., None])
+    return codes, scales
+
+
+# ----------------------------------------------------------------------------
+# Index-key preparation: k_norm (LayerNorm) -> RoPE on dims 0..63 -> FP8.
+# ----------------------------------------------------------------------------
+def layer_norm(x: np.ndarray, gamma=None, beta=None, eps: float = 1e-6) -> np.ndarray:
+    """LayerNorm over the last axis with biased variance."""
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    y = (x - mu) / np.sqrt(var + eps)
+    if gamma is not None:
+        y = y * np.asarray(gamma, dtype=np.float64)
+    if beta is not None:
+        y = y + np.asarray(beta, dtype=np.float64)
+    return y
+
+
+def rope_interleaved(x: np.ndarray, pos: np.ndarray, base: float = 10000.0,
+                     rope_dims: int = 64) -> np.ndarray:
+    """Rotate the pairs (x[2i], x[2i+1]), i < rope_dims/2, by pos * base**(-2i/rope_dims).
+
+    Dims >= rope_dims pass through unchanged.
+    """
+    x = np.array(x, dtype=np.float64, copy=True)
+    pos = np.asarray(pos, dtype=np.float64).reshape(-1, 1)
+    i = np.arange(rope_dims // 2, dtype=np.float64)
+    theta = base ** (-2.0 * i / rope_dims)
+    ang = pos * theta[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    x0 = x[..., 0:rope_dims:2].copy()
+    x1 = x[..., 1:rope_dims:2].copy()
+    x[..., 0:rope_dims:2] = x0 * c - x1 * s
+    x[..., 1:rope_dims:2] = x0 * s + x1 * c
+    return x
+
+
+def index_k_prepare(k: np.ndarray, pos: np.ndarray, gamma=None, beta=None,
+                    eps: float = 1e-6, rope_base: float = 10000.0):
+    """The index key of each token before caching: (E4M3 codes [n,128], scale [n])."""
+    y = layer_norm(k, gamma, beta, eps)
+    y = rope_interleaved(y, pos, rope_base, 64)
+    return quantize_blocks_128(y)
+
+
+# ----------------------------------------------------------------------------
+# Paged cache byte layouts.
+# ----------------------------------------------------------------------------
+def index_cache_write(cache: np.ndarray, slot: np.ndarray, codes: np.ndarray,
+                      scales: np.ndarray) -> None:
+    """Write tokens into an index-K cache [num_pages, 8448] (uint8).
+
+    Within a page: bytes [0, 8192) hold the 64 FP8 rows of 128 B, bytes
+    [8192, 8448) hold the 64 scales as little-endian fp32.  slot < 0 is skipped.
+    """
+    assert cache.dtype == np.uint8 and cache.shape[1] == INDEX_PAGE_BYTES
+    slot = np.asarray(slot, dtype=np.int64)
+    keep = slot >= 0
+    page, row = np.divmod(slot[keep], PAGE_TOKENS)
+    cache[page[:, None], row[:, None] * 128 + np.arange(128)] = np.asarray(codes)[keep]
+    sbytes = np.asarray(scales, dtype="<f4")[keep].view(np.uint8).reshape(-1, 4)
+    cache[page[:, None], PAGE_TOKENS * 128 + 4 * row[:, None] + np.arange(4)] = sbytes
+
+
+def index_cache_read(cache: np.ndarray, page_table_row: np.ndarray, n_tokens: int):
+    """Read logical tokens 0..n-1 of one request: (codes [n,128], scales fp64 [n])."""
+    j = np.arange(n_tokens, dtype=np.int64)
+    page = np.asarray(page_table_row, dtype=np.int64)[j // PAGE_TOKENS]
+    row = j % PAGE_TOKENS
+    codes = cache[page[:, None], row[:, None] * 128 + np.arange(128)]
+    sb = cache[page[:, None], PAGE_TOKENS * 128 + 4 * row[:, None] + np.arange(4)]
+    scales = np.ascontiguousarray(sb).view("<f4").reshape(-1).astype(np.float64)
+    return codes, scales
+
+
+def latent_quantize(c: np.ndarray):
+    """Latent c [n,512] -> (codes [n,512], scales [n,4]) with one scale per 128 dims."""
+    c = np.asarray(c, dtype=np.float64)
+    codes, scales = quantize_blocks_128(c.reshape(c.shape[0], 4, 128))
+    return codes.reshape(c.shape[0], 512), scales
+
+
+def latent_cache_write(cache: np.ndarray, slot: np.ndarray, codes: np.ndarray,
+                       scales: np.ndarray, rope_bf16_bits: np.ndarray) -> None:
+    """Write tokens into a latent cache [num_pages, 41984] (uint8).
+
+    Token row of 656 B at 656 * (slot % 64): [0,512) FP8 latent, [512,528) four
+    little-endian fp32 scales, [528,656) 64 RoPE values as raw bf16 bits.
+    """
+    assert cache.dtype == np.uint8 and cache.shape[1] == LATENT_PAGE_BYTES
+    slot = np.asarray(slot, dtype=np.int64)
+    keep = slot >= 0
+    page, row = np.divmod(slot[keep], PAGE_TOKENS)
+    base = row[:, None] * LATENT_TOKEN_BYTES
+    cache[page[:, None], base + np.arange(512)] = np.asarray(codes)[keep]
+    sb = np.asarray(scales, dtype="<f4")[keep].view(np.uint8).reshape(-1, 16)
+    cache[page[:, None], base + 512 + np.arange(16)] = sb
+    rb = np.ascontiguousarray(np.asarray(rope_bf16_bits, dtype="<u2")[keep]).view(np.uint8)
+    cache[page[:, None], base + 528 + np.arange(128)] = rb.reshape(-1, 128)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def latent_cache_read_rows(cache: np.ndarray, page_table_row: np.ndarray,
+                           positions: np.ndarray) -> np.ndarray:
+    """Dequantised 576-d rows [len(positions), 576]: (c * scale | rope)."""
+    j = np.asarray(positions, dtype=np.int64)
+    page = np.asarray(page_table_row, dtype=np.int64)[j // PAGE_TOKENS]
+    base = (j % PAGE_TOKENS)[:, None] * LATENT_TOKEN_BYTES
+    rows = cache[page[:, None], base + np.arange(LATENT_TOKEN_BYTES)]
+    out = np.empty((len(j), LATENT_DIM + ROPE_DIM), dtype=np.float64)
+    sc = np.ascontiguousarray(rows[:, 512:528]).view("<f4").astype(np.float64)   # [n,4]
+    out[:, :512] = e4m3_decode(rows[:, :512]) * np.repeat(sc, 128, axis=1)
+    out[:, 512:] = bf16_bits_to_f64(np.ascontiguousarray(rows[:, 528:656]).view("<u2"))
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Lightning indexer ("vLLM 推理链路概览", DSA Indexer).
+# ----------------------------------------------------------------------------
+def index_q_quantize(q: np.ndarray):
+    """Indexer query [T,32,128] -> (E4M3 codes, per-head scales [T,32])."""
+    return quantize_blocks_128(q)
+
+
+def indexer_scores(q_codes, q_scales, w, k_codes, k_scales) -> np.ndarray:
+    """s_j = sum_m w_m * ReLU(<q_m, k_j>) on the dequantised FP8 values.
+
+    q_codes [32,128], q_scales [32], w [32], k_codes [L,128], k_scales [L];
+    returns fp64 [L].
+    """
+    q = e4m3_decode(q_codes) * np.asarray(q_scales, np.float64)[:, None]
+    k = e4m3_decode(k_codes) * np.asarray(k_scales, np.float64)[:, None]
+    dots = k @ q.T                                   # [L, 32]
+    return np.maximum(dots, 0.0) @ np.asarray(w, dtype=np.float64)
+
+
+def score_magnitude(q_codes, q_scales, w, k_codes, k_scales) -> np.ndarray:
+    """D_j = sum_m |w_m| * |<q_m, k_j>|: the scale against which a score's
+    relative error is measured (>= |s_j|, equal to it without cancellation)."""
+    q = e4m3_decode(q_codes) * np.asarray(q_scales, np.float64)[:, None]
+    k = e4m3_decode(k_codes) * np.asarray(k_scales, np.float64)[:, None]
+    dots = k @ q.T
+    return np.abs(dots) @ np.abs(np.asarray(w, dtype=np.float64))
+
+
+def topk_positions(scores: np.ndarray, n_valid: int, k: int = TOPK) -> np.ndarray:
+    """Top-k positions among scores[0:n_valid] as int32 [k], ascending, -1 padded.
+
+    n_valid <= k selects every valid position ("优化二").  Otherwise the order is
+    descending score, ties to the lower position; -0.0 and +0.0 are equal.
+    """
+    out = np.full(k, -1, dtype=np.int32)
+    if n_valid <= k:
+        out[:n_valid] = np.arange(n_valid, dtype=np.int32)
+        return out
+    s = np.asarray(scores[:n_valid], dtype=np.float64) + 0.0    # -0.0 -> +0.0
+    order = np.lexsort((np.arange(n_valid), -s))
+    out[:] = np.sort(order[:k]).astype(np.int32)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Sparse MLA in absorbed (MQA) form ("vLLM 推理链路概览", Sparse MLA Attention).
+# ----------------------------------------------------------------------------
+def sparse_mla(q: np.ndarray, positions: np.ndarray, kv_rows: np.ndarray,
+               query_pos: int, scale: float = SOFTMAX_SCALE):
+    """One query token: q [64,576], positions [k] (-1 = empty), kv_rows [k,576]
+    dequantised rows for those positions.  Returns (out [64,512], lse [64]).
+
+    Only positions j with 0 <= j <= query_pos take part (the causal mask).
+    """
+    positions = np.asarray(positions)
+    keep = (positions >= 0) & (positions <= query_pos)
+    kv = np.asarray(kv_rows, dtype=np.float64)[keep]
+    q = np.asarray(q, dtype=np.float64)
+    if kv.shape[0] == 0:
+        return np.zeros((q.shape[0], LATENT_DIM)), np.full(q.shape[0], -np.inf)
+    s = (q @ kv.T) * scale                           # [64, n]
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m)
+    l = p.sum(axis=1, keepdims=True)
+    out = (p @ kv[:, :LATENT_DIM]) / l
+    lse = (m + np.log(l))[:, 0]
+    return out, lse
+
+
+# ----------------------------------------------------------------------------
+# Full / shared layer schedule ("配置里的 78 个字符").
+# ----------------------------------------------------------------------------
+def parse_indexer_types(types) -> list:
+    """True for a full layer (runs the indexer), False for a shared layer."""
+    out = []
+    for t in types:
+        if t == "full":
+            out.append(True)
+        elif t == "shared":
+            out.append(False)
+        else:
+            raise ValueError(f"unknown indexer type {t!r}")
+    return out
+
+
+def layer_skips_topk(layer_id: int, freq: int, offset: int) -> bool:
+    """The parameterised form: skip (shared) iff max(l - offset + 1, 0) % freq != 0."""
+    return max(layer_id - offset + 1, 0) % freq != 0
+
+
+# ----------------------------------------------------------------------------
+# One request through the whole step, for the tests and the CPU baseline.
+# ----------------------------------------------------------------------------
+def request_topk(q_idx, w, idx_cache, page_table_row, seq_len, q_len):
+    """Indexer + top-k for one request's query tokens.
+
+    q_idx [q_len,32,128] fp64, w [q_len,32].  Query token t sits at position
+    p = seq_len - q_len + t and sees the L_t = p + 1 positions 0..p.  Returns
+    (topk int32 [q_len, 2048], scores list of fp64 [L_t] or None when L_t <= 2048).
+    """
+    k_codes, k_scales = index_cache_read(idx_cache, page_table_row, seq_len)
+    out = np.empty((q_len, TOPK), dtype=np.int32)
+    all_scores = []
+    for t in range(q_len):
+        n_valid = seq_len - q_len + t + 1
+        if n_valid <= TOPK:
+            out[t] = topk_positions(None, n_valid)
+            all_scores.append(None)
+            continue
+        qc, qs = index_q_quantize(q_idx[t])
+        s = indexer_scores(qc, qs, w[t], k_codes[:n_valid], k_scales[:n_valid])
+        out[t] = topk_positions(s, n_valid)
+        all_scores.append(s)
+    return out, all_scores

@@ -1,0 +1,308 @@
+"""Pins for the fp64 oracle, independent of the oracle's own formulas.
+
+Each test checks the oracle against something other than itself: the format
+definition through torch's float8 casts (a library routine), numbers the pages
+print (tests/golden/pages_constants.json), closed forms, invariants, brute force
+on tiny inputs, and textbook special cases (sparse attention over the whole
+context equals dense attention computed by torch's SDPA).
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dsa_oracle as O
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_constants.json")))
+
+
+def g(name):
+    return GOLDEN[name]["value"]
+
+
+# ------------------------------------------------------------------ FP8 codec
+def test_e4m3_decode_matches_torch_for_all_256_codes():
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = O.e4m3_decode_table()
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(mine))
+    assert np.array_equal(ref[~nan], mine[~nan])
+    assert mine[0x7E] == 448.0 and mine[0x01] == 2.0 ** -9      # max normal, min subnormal
+
+
+def test_e4m3_encode_matches_torch_cast_on_random_values():
+    rng = np.random.default_rng(1)
+    mags = np.exp2(rng.uniform(-12, np.log2(448.0), 200000))
+    x = (mags * rng.choice([-1.0, 1.0], mags.size)).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(x.astype(np.float64)), ref)
+
+
+def test_e4m3_encode_ties_to_even_at_every_midpoint():
+    vals = O.e4m3_decode_table()[:0x7F]
+    mids = (vals[:-1] + vals[1:]) / 2.0                   # exactly representable in fp32
+    ref = torch.from_numpy(mids.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    mine = O.e4m3_encode(mids)
+    assert np.array_equal(mine, ref)
+    assert np.all(mine % 2 == 0)                          # the even neighbour wins
+
+
+def test_e4m3_roundtrip_every_finite_code():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    assert np.array_equal(O.e4m3_encode(O.e4m3_decode(codes)), codes)
+
+
+# ------------------------------------------------------------------ ue8m0 scale
+@pytest.mark.parametrize("amax,e", [(448.0, 0), (448.0001, 1), (1.0, -8), (0.875, -9),
+                                    (0.0, 0), (3.5, -7), (3.5000001, -6), (896.0, 1)])
+def test_ue8m0_hand_values(amax, e):
+    assert O.ue8m0_exponent(amax) == e
+
+
+def test_ue8m0_defining_property_and_e8m0_representable():
+    rng = np.random.default_rng(2)
+    a = np.exp2(rng.uniform(-60, 60, 10000))
+    e = O.ue8m0_exponent(a)
+    assert np.all(a <= 448.0 * np.exp2(e)) and np.all(a > 448.0 * np.exp2(e - 1))
+    s = torch.from_numpy(np.exp2(e).astype(np.float32))
+    back = s.to(torch.float8_e8m0fnu).to(torch.float32)       # a power of two survives e8m0
+    assert torch.equal(back, s)
+
+
+def test_quantised_block_within_half_ulp_and_no_saturation():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((500, 128)) * np.exp2(rng.uniform(-20, 20, (500, 1)))
+    codes, scales = O.quantize_blocks_128(x)
+    deq = O.e4m3_decode(codes) * scales[:, None]
+    assert np.all(np.abs(deq / scales[:, None]) <= 448.0)
+    err = np.abs(deq - x) / scales[:, None]
+    assert np.all(err <= O.e4m3_ulp(x / scales[:, None]) / 2 + 1e-300)
+
+
+# ------------------------------------------------------------------ LayerNorm / RoPE
+def test_layer_norm_matches_torch_and_moments():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((64, 128)) * 3 + 1
+    gm, bt = rng.standard_normal(128), rng.standard_normal(128)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (128,), torch.from_numpy(gm),
+                                         torch.from_numpy(bt), eps=1e-6).numpy()
+    assert np.allclose(O.layer_norm(x, gm, bt, 1e-6), ref, rtol=1e-12, atol=1e-12)
+    y = O.layer_norm(x)
+    assert np.allclose(y.mean(-1), 0, atol=1e-12) and np.allclose(y.var(-1), 1, atol=1e-5)
+
+
+def test_rope_equals_complex_rotation_and_keeps_pair_norms():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((10, 128))
+    pos = rng.integers(0, 2 ** 20, 10)
+    y = O.rope_interleaved(x, pos, 10000.0, 64)
+    z = x[:, 0:64:2] + 1j * x[:, 1:64:2]
+    theta = 10000.0 ** (-np.arange(32) * 2 / 64)
+    zr = z * np.exp(1j * pos[:, None] * theta[None, :])
+    assert np.allclose(y[:, 0:64:2], zr.real, atol=1e-9) and np.allclose(y[:, 1:64:2], zr.imag, atol=1e-9)
+    assert np.array_equal(y[:, 64:], x[:, 64:])                     # dims 64..127 untouched
+    assert np.allclose(np.abs(z), np.hypot(y[:, 0:64:2], y[:, 1:64:2]))
+    assert np.allclose(O.rope_interleaved(x, np.zeros(10), 10000.0), x)   # position 0 = identity
+    a, b = 1234, 98765                                              # R(a) R(b) = R(a + b)
+    ab = O.rope_interleaved(O.rope_interleaved(x, np.full(10, a)), np.full(10, b))
+    assert np.allclose(ab, O.rope_interleaved(x, np.full(10, a + b)), atol=1e-9)
+
+
+# ------------------------------------------------------------------ layouts
+def test_layout_constants_match_the_pages():
+    assert O.INDEX_TOKEN_BYTES == g("index_k_token_bytes")
+    assert O.INDEX_PAGE_BYTES == g("index_k_page_bytes")
+    assert O.PAGE_TOKENS == g("page_size")
+    assert O.INDEX_HEAD_DIM == g("index_head_dim")
+    assert O.LATENT_TOKEN_BYTES == g("latent_token_bytes")
+    assert O.LATENT_DIM + O.ROPE_DIM == g("latent_dims")
+    assert O.LATENT_PAGE_BYTES == 64 * 656 == 41984
+    assert O.TOPK == g("index_topk") and O.INDEX_HEADS == g("indexer_heads")
+    assert O.MLA_HEADS == g("mla_heads")
+    assert O.SOFTMAX_SCALE == 1.0 / math.sqrt(g("softmax_denominator_sqrt")) == 1.0 / 16
+    assert O.TOPK * 4 == g("topk_row_bytes")
+
+
+def test_byte_accounting_printed_on_the_pages():
+    assert O.INDEX_TOKEN_BYTES * 10 ** 5 == g("read_bytes_per_layer_L1e5")
+    assert abs(21 * O.INDEX_TOKEN_BYTES * 10 ** 5 - g("read_bytes_21_layers_L1e5")) < 0.01 * 277e6
+    assert O.INDEX_TOKEN_BYTES * 10 ** 6 == g("read_bytes_per_layer_L1e6")
+    flops = 2 * O.MLA_HEADS * O.LATENT_DIM * O.TOPK
+    assert abs(flops - g("sparse_mla_flops_per_layer")) < 0.01 * flops
+
+
+def test_index_cache_roundtrip_and_page_layout():
+    rng = np.random.default_rng(6)
+    cache = np.zeros((5, O.INDEX_PAGE_BYTES), dtype=np.uint8)
+    pt = np.array([3, 0, 4], dtype=np.int32)
+    n = 150
+    codes = rng.integers(0, 256, (n, 128)).astype(np.uint8)
+    scales = np.exp2(rng.integers(-10, 3, n)).astype(np.float64)
+    slots = pt[np.arange(n) // 64] * 64 + np.arange(n) % 64
+    slots[7] = -1                                                 # skipped
+    O.index_cache_write(cache, slots, codes, scales)
+    c2, s2 = O.index_cache_read(cache, pt, n)
+    keep = np.arange(n) != 7
+    assert np.array_equal(c2[keep], codes[keep]) and np.array_equal(s2[keep], scales[keep])
+    # token 65 is logical page 1 -> physical page 0, row 1
+    assert np.array_equal(cache[0, 128:256], codes[65])
+    assert np.frombuffer(cache[0, 8192 + 4:8192 + 8].tobytes(), "<f4")[0] == scales[65]
+    assert not cache[3, 7 * 128:8 * 128].any()                    # the skipped slot
+
+
+def test_latent_cache_roundtrip_dequantises_exactly():
+    rng = np.random.default_rng(7)
+    n = 70
+    c = rng.standard_normal((n, 512))
+    rope = torch.randn(n, 64, dtype=torch.float32).to(torch.bfloat16)
+    codes, scales = O.latent_quantize(c)
+    cache = np.zeros((2, O.LATENT_PAGE_BYTES), dtype=np.uint8)
+    pt = np.array([1, 0], dtype=np.int32)
+    slots = pt[np.arange(n) // 64] * 64 + np.arange(n) % 64
+    O.latent_cache_write(cache, slots, codes, scales, rope.view(torch.int16).numpy().view(np.uint16))
+    rows = O.latent_cache_read_rows(cache, pt, np.arange(n))
+    assert np.array_equal(rows[:, :512], O.e4m3_decode(codes) * np.repeat(scales, 128, axis=1))
+    assert np.array_equal(rows[:, 512:], rope.to(torch.float64).numpy())
+    assert np.max(np.abs(rows[:, :512] - c) / np.repeat(scales, 128, axis=1)) <= 16.0  # half an ulp at 448
+
+
+# ------------------------------------------------------------------ schedule
+def test_schedule_matches_the_printed_full_layers():
+    full = g("full_layers")
+    types = ["full" if l in full else "shared" for l in range(g("num_layers"))]
+    is_full = O.parse_indexer_types(types)
+    assert sum(is_full) == g("n_full") and len(is_full) - sum(is_full) == g("n_shared")
+    assert types[:7] == g("indexer_types_prefix")
+    freq, off = g("index_topk_freq"), g("index_skip_topk_offset")
+    assert [not O.layer_skips_topk(l, freq, off) for l in range(78)] == is_full
+    with pytest.raises(ValueError):
+        O.parse_indexer_types(["full", "dense"])
+
+
+# ------------------------------------------------------------------ indexer scores
+def _brute_scores(qd, w, kd):
+    L = kd.shape[0]
+    out = np.zeros(L)
+    for j in range(L):
+        tot = 0.0
+        for m in range(qd.shape[0]):
+            dot = 0.0
+            for d in range(qd.shape[1]):
+                dot += qd[m, d] * kd[j, d]
+            tot += w[m] * (dot if dot > 0 else 0.0)
+        out[j] = tot
+    return out
+
+
+def test_indexer_scores_brute_force():
+    rng = np.random.default_rng(8)
+    L = 9
+    q = rng.standard_normal((32, 128))
+    k = rng.standard_normal((L, 128))
+    w = rng.standard_normal(32) / math.sqrt(32)
+    qc, qs = O.index_q_quantize(q)
+    kc, ks = O.quantize_blocks_128(k)
+    s = O.indexer_scores(qc, qs, w, kc, ks)
+    ref = _brute_scores(O.e4m3_decode(qc) * qs[:, None], w, O.e4m3_decode(kc) * ks[:, None])
+    assert np.allclose(s, ref, rtol=1e-12, atol=1e-12)
+    # a positive rescale of the head weights rescales every score exactly
+    assert np.array_equal(O.indexer_scores(qc, qs, 4.0 * w, kc, ks), 4.0 * s)
+    D = O.score_magnitude(qc, qs, w, kc, ks)
+    assert np.all(D >= np.abs(s) - 1e-12)
+
+
+# ------------------------------------------------------------------ top-k
+def _brute_topk(s, k):
+    """Repeated extraction of the best remaining (score desc, position asc)."""
+    s = list(s)
+    taken = set()
+    for _ in range(k):
+        best = None
+        for j, v in enumerate(s):
+            if j in taken:
+                continue
+            if best is None or v > s[best]:
+                best = j
+        taken.add(best)
+    return sorted(taken)
+
+
+@pytest.mark.parametrize("L", [2049, 2100, 2600])
+def test_topk_brute_force_with_heavy_ties(L):
+    rng = np.random.default_rng(L)
+    s = rng.integers(-3, 4, L).astype(np.float64)         # only 7 distinct values
+    s[rng.integers(0, L, 50)] = -0.0
+    got = O.topk_positions(s, L)
+    assert got.dtype == np.int32 and np.all(got >= 0)
+    assert got.tolist() == _brute_topk([v + 0.0 for v in s], 2048)
+
+
+def test_topk_brute_force_small_k_distinct_and_signed_zero():
+    s = np.array([0.0, -0.0, 1.0, -0.0, 0.0, 2.0, -1.0])
+    assert O.topk_positions(s, 7, k=4).tolist() == [0, 1, 2, 5]      # -0 ties +0: lower positions win
+    assert O.topk_positions(s, 7, k=3).tolist() == [0, 2, 5]
+
+
+@pytest.mark.parametrize("L", [0, 1, 63, 64, 2047, 2048])
+def test_short_context_selects_everything(L):
+    out = O.topk_positions(None, L)
+    assert out.tolist() == list(range(L)) + [-1] * (2048 - L)
+
+
+def test_request_topk_short_context_rule_and_causality():
+    rng = np.random.default_rng(9)
+    L, q_len = 2051, 6                      # query tokens at positions 2045..2050
+    cache = np.zeros((33, O.INDEX_PAGE_BYTES), np.uint8)
+    pt = rng.permutation(33).astype(np.int32)
+    kc, ks = O.index_k_prepare(rng.standard_normal((L, 128)), np.arange(L))
+    O.index_cache_write(cache, pt[np.arange(L) // 64] * 64 + np.arange(L) % 64, kc, ks)
+    qi = rng.standard_normal((q_len, 32, 128))
+    w = rng.standard_normal((q_len, 32))
+    topk, scores = O.request_topk(qi, w, cache, pt, L, q_len)
+    for t in range(q_len):
+        n = L - q_len + t + 1
+        if n <= 2048:
+            assert topk[t].tolist() == list(range(n)) + [-1] * (2048 - n)
+            assert scores[t] is None
+        else:
+            assert topk[t].max() <= n - 1 and len(set(topk[t].tolist())) == 2048
+            assert len(scores[t]) == n
+
+
+# ------------------------------------------------------------------ sparse MLA
+def test_sparse_mla_equals_dense_sdpa_when_context_fits():
+    rng = np.random.default_rng(10)
+    L = 300
+    q = rng.standard_normal((64, 576))
+    kv = rng.standard_normal((L, 576))
+    idx = np.full(2048, -1)
+    idx[:L] = rng.permutation(L)              # any order of the full set
+    p = L - 1
+    out, lse = O.sparse_mla(q, idx, kv[np.maximum(idx, 0)], p)
+    Q = torch.from_numpy(q)[None, :, None, :].transpose(1, 2)         # [1,1,64,576]
+    K = torch.from_numpy(kv)[None, None]                              # [1,1,L,576]
+    V = torch.from_numpy(kv[:, :512])[None, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, scale=1.0 / 16)[0, 0].numpy()
+    assert np.allclose(out, ref, rtol=1e-10, atol=1e-12)
+    ref_lse = torch.logsumexp(torch.from_numpy(q @ kv.T / 16.0), dim=1).numpy()
+    assert np.allclose(lse, ref_lse, rtol=1e-12)
+
+
+def test_sparse_mla_special_cases():
+    rng = np.random.default_rng(11)
+    kv = rng.standard_normal((5, 576))
+    q = rng.standard_normal((64, 576))
+    idx = np.array([3] + [-1] * 2047)
+    out, _ = O.sparse_mla(q, idx, kv[np.maximum(idx, 0)], 10)
+    assert np.allclose(out, np.broadcast_to(kv[3, :512], (64, 512)))       # one key: o = v
+    idx = np.array([0, 1, 2, 3, 4] + [-1] * 2043)
+    out, lse = O.sparse_mla(np.zeros((64, 576)), idx, kv[np.maximum(idx, 0)], 10)
+    assert np.allclose(out, np.broadcast_to(kv[:, :512].mean(0), (64, 512)))  # q = 0: mean of V
+    assert np.allclose(lse, np.log(5.0))
+    out, _ = O.sparse_mla(q, idx, kv[np.maximum(idx, 0)], 2)               # causal: j <= 2 only
+    ref, _ = O.sparse_mla(q, np.array([0, 1, 2]), kv[:3], 2)
+    assert np.allclose(out, ref)
