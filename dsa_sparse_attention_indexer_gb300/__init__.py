@@ -1,0 +1,359 @@
+"""Python binding of libdsa, the GB300 DSA attention-step library.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+PyTorch supplies device memory, streams and the output buffers.  If the shared
+library has not been built, every call raises ``DsaLibraryMissing`` - there is
+no fallback.
+
+The function names follow the C ABI in ``include/dsa.h``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint8, c_void_p
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libdsa.so")
+
+PAGE_TOKENS = 64
+INDEX_HEADS = 32
+INDEX_HEAD_DIM = 128
+IDXK_TOKEN_BYTES = 132
+IDXK_PAGE_BYTES = 8448
+MLA_HEADS = 64
+LATENT_DIM = 512
+ROPE_DIM = 64
+QK_DIM = 576
+KV_TOKEN_BYTES = 656
+KV_PAGE_BYTES = 41984
+TOPK = 2048
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+
+DEVERR_SLOT_RANGE = 1
+DEVERR_PAGE_RANGE = 2
+DEVERR_INDEX_RANGE = 4
+DEVERR_TIMEOUT = 8
+DEVERR_FP16_RANGE = 16
+
+ERR = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARGUMENT", 2: "DSA_ERR_ALIGNMENT", 3: "DSA_ERR_UNSUPPORTED",
+       4: "DSA_ERR_WORKSPACE_TOO_SMALL", 5: "DSA_ERR_NO_TOPK_SOURCE", 6: "DSA_ERR_CUDA", 7: "DSA_ERR_DEVICE"}
+
+
+class DsaLibraryMissing(ImportError):
+    pass
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        self.name = ERR.get(code, str(code))
+        super().__init__(f"{fn} -> {self.name} ({status_string(code)})")
+
+
+class DsaBatch(ctypes.Structure):
+    _fields_ = [("batch", c_int32), ("max_pages", c_int32), ("max_seq_len", c_int32),
+                ("max_q_len", c_int32), ("total_q", c_int64), ("num_pages", c_int64),
+                ("seq_len", c_void_p), ("q_start", c_void_p), ("page_table", c_void_p)]
+
+
+_lib = None
+
+_SIGS = {
+    "dsa_abi_version": (c_int32, []),
+    "dsa_status_string": (c_char_p, [c_int32]),
+    "dsa_device_status_reset": (c_int32, [c_void_p, c_void_p]),
+    "dsa_device_status_read": (c_int32, [c_void_p, c_void_p, POINTER(c_int32)]),
+    "dsa_index_k_store": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_float,
+                                    c_float, c_void_p, c_int64, c_void_p, c_void_p]),
+    "dsa_latent_kv_store": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64, c_void_p,
+                                      c_void_p]),
+    "dsa_indexer_topk_workspace_size": (c_int32, [POINTER(DsaBatch), POINTER(c_size_t)]),
+    "dsa_indexer_topk": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_void_p, c_void_p,
+                                   c_void_p, c_int32, c_void_p, c_size_t, c_void_p, c_void_p]),
+    "dsa_indexer_scores_workspace_size": (c_int32, [POINTER(DsaBatch), POINTER(c_size_t)]),
+    "dsa_indexer_scores": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_void_p, c_int64,
+                                     c_void_p, c_size_t, c_void_p, c_void_p]),
+    "dsa_topk_from_scores_workspace_size": (c_int32, [c_int32, c_int64, POINTER(c_size_t)]),
+    "dsa_topk_from_scores": (c_int32, [c_void_p, c_int64, c_void_p, c_int32, c_int64, c_void_p, c_void_p,
+                                       c_size_t, c_void_p]),
+    "dsa_sparse_mla_workspace_size": (c_int32, [POINTER(DsaBatch), POINTER(c_size_t)]),
+    "dsa_sparse_mla_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_float,
+                                        c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
+    "dsa_sparse_mla_prefill": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_float,
+                                         c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
+    "dsa_parse_indexer_types": (c_int32, [POINTER(c_char_p), c_int32, POINTER(c_uint8)]),
+    "dsa_schedule_from_freq": (c_int32, [c_int32, c_int32, c_int32, POINTER(c_uint8)]),
+    "dsa_topk_share_create": (c_int32, [POINTER(c_void_p)]),
+    "dsa_topk_share_destroy": (c_int32, [c_void_p]),
+    "dsa_topk_share_reset": (c_int32, [c_void_p]),
+    "dsa_topk_share_publish": (c_int32, [c_void_p, c_int32, c_void_p, c_int64]),
+    "dsa_topk_share_get": (c_int32, [c_void_p, POINTER(c_void_p), POINTER(c_int64), POINTER(c_int32)]),
+}
+
+
+def lib():
+    """The loaded libdsa (ctypes.CDLL); raises DsaLibraryMissing if not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise DsaLibraryMissing(
+                f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(h, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = h
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().dsa_status_string(code).decode()
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise DsaError(fn, code)
+
+
+def _ptr(t):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+# ---------------------------------------------------------------------------
+class Batch:
+    """Owns the device tensors of one batch and the dsa_batch struct over them.
+
+    seq_len int32 [B] and q_start int32 [B+1] (device), page_table int32
+    [B, max_pages] (device).  Host bounds default to the tensors' values
+    (read once, with a device sync).
+    """
+
+    def __init__(self, seq_len, q_start, page_table, num_pages: int, *, max_seq_len=None,
+                 max_q_len=None, total_q=None):
+        self.seq_len = _need(seq_len, torch.int32, "seq_len")
+        self.q_start = _need(q_start, torch.int32, "q_start")
+        self.page_table = _need(page_table, torch.int32, "page_table")
+        B = seq_len.numel()
+        if max_seq_len is None or max_q_len is None or total_q is None:
+            sl = seq_len.cpu()
+            qs = q_start.cpu()
+            max_seq_len = int(sl.max()) if max_seq_len is None else max_seq_len
+            max_q_len = int((qs[1:] - qs[:-1]).max()) if max_q_len is None else max_q_len
+            total_q = int(qs[-1]) if total_q is None else total_q
+        self.c = DsaBatch(B, page_table.shape[1], int(max_seq_len), int(max_q_len), int(total_q),
+                          int(num_pages), seq_len.data_ptr(), q_start.data_ptr(), page_table.data_ptr())
+
+    @property
+    def total_q(self) -> int:
+        return self.c.total_q
+
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def _ws_size(fn_name: str, batch: Batch) -> int:
+    n = c_size_t(0)
+    _check(fn_name, getattr(lib(), fn_name)(batch.ref(), ctypes.byref(n)))
+    return n.value
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def new_device_status(device) -> torch.Tensor:
+    return torch.zeros(4, dtype=torch.int32, device=device)
+
+
+def dsa_device_status_read(dev_status: torch.Tensor, stream=None):
+    out = (c_int32 * 4)()
+    code = lib().dsa_device_status_read(_ptr(dev_status), _stream(stream), out)
+    if code not in (0, 7):
+        _check("dsa_device_status_read", code)
+    return list(out)
+
+
+def dsa_device_status_reset(dev_status: torch.Tensor, stream=None):
+    _check("dsa_device_status_reset", lib().dsa_device_status_reset(_ptr(dev_status), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+def dsa_index_k_store(k, pos, slot, idxk_cache, *, gamma=None, beta=None, ln_eps=1e-6,
+                      rope_base=10000.0, num_pages=None, dev_status=None, stream=None):
+    _need(k, torch.bfloat16, "k")
+    _need(pos, torch.int32, "pos")
+    _need(slot, torch.int64, "slot")
+    _need(idxk_cache, torch.uint8, "idxk_cache")
+    n = k.shape[0]
+    if num_pages is None:
+        num_pages = idxk_cache.numel() // IDXK_PAGE_BYTES
+    _check("dsa_index_k_store", lib().dsa_index_k_store(
+        _ptr(k), _ptr(pos), _ptr(slot), n, _ptr(gamma), _ptr(beta), ln_eps, rope_base,
+        _ptr(idxk_cache), num_pages, _ptr(dev_status), _stream(stream)))
+
+
+def dsa_latent_kv_store(c, rope, slot, kv_cache, *, num_pages=None, dev_status=None, stream=None):
+    _need(c, torch.bfloat16, "c")
+    _need(rope, torch.bfloat16, "rope")
+    _need(slot, torch.int64, "slot")
+    _need(kv_cache, torch.uint8, "kv_cache")
+    if num_pages is None:
+        num_pages = kv_cache.numel() // KV_PAGE_BYTES
+    _check("dsa_latent_kv_store", lib().dsa_latent_kv_store(
+        _ptr(c), _ptr(rope), _ptr(slot), c.shape[0], _ptr(kv_cache), num_pages, _ptr(dev_status),
+        _stream(stream)))
+
+
+def dsa_indexer_topk_workspace_size(batch: Batch) -> int:
+    return _ws_size("dsa_indexer_topk_workspace_size", batch)
+
+
+def dsa_indexer_topk(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=None, share=None,
+                     layer_id: int = 0, ws=None, dev_status=None, stream=None):
+    """Indexer + top-2048.  Returns topk int32 [T, 2048] (allocated if not given)."""
+    _need(q, torch.bfloat16, "q")
+    _need(w, torch.float32, "w")
+    _need(idxk_cache, torch.uint8, "idxk_cache")
+    T = batch.total_q
+    if topk is None:
+        topk = torch.empty((T, TOPK), dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = workspace(dsa_indexer_topk_workspace_size(batch), q.device)
+    _check("dsa_indexer_topk", lib().dsa_indexer_topk(
+        _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
+        None if share is None else share.handle, layer_id, _ptr(ws), ws.numel(), _ptr(dev_status),
+        _stream(stream)))
+    return topk
+
+
+def dsa_indexer_scores(q, w, idxk_cache, batch: Batch, *, ld=None, scores=None, ws=None,
+                       dev_status=None, stream=None):
+    """Full fp32 score rows [T, ld] (debug / parity hook)."""
+    T = batch.total_q
+    ld = batch.c.max_seq_len if ld is None else ld
+    if scores is None:
+        scores = torch.empty((T, ld), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(_ws_size("dsa_indexer_scores_workspace_size", batch), q.device)
+    _check("dsa_indexer_scores", lib().dsa_indexer_scores(
+        _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(scores), ld, _ptr(ws), ws.numel(),
+        _ptr(dev_status), _stream(stream)))
+    return scores
+
+
+def dsa_topk_from_scores(scores, valid_len, *, max_len=None, topk=None, stream=None):
+    _need(scores, torch.float32, "scores")
+    _need(valid_len, torch.int32, "valid_len")
+    rows, ld = scores.shape
+    max_len = ld if max_len is None else max_len
+    if topk is None:
+        topk = torch.empty((rows, TOPK), dtype=torch.int32, device=scores.device)
+    n = c_size_t(0)
+    _check("dsa_topk_from_scores_workspace_size",
+           lib().dsa_topk_from_scores_workspace_size(rows, max_len, ctypes.byref(n)))
+    ws = workspace(n.value, scores.device)
+    _check("dsa_topk_from_scores", lib().dsa_topk_from_scores(
+        _ptr(scores), ld, _ptr(valid_len), rows, max_len, _ptr(topk), _ptr(ws), ws.numel(), _stream(stream)))
+    return topk
+
+
+def dsa_sparse_mla_workspace_size(batch: Batch) -> int:
+    return _ws_size("dsa_sparse_mla_workspace_size", batch)
+
+
+def _mla(fn, q, topk, kv_cache, batch, softmax_scale, out, out_dtype, lse, share, ws, dev_status, stream):
+    _need(q, torch.bfloat16, "q")
+    _need(kv_cache, torch.uint8, "kv_cache")
+    T = batch.total_q
+    if out is None:
+        out = torch.empty((T, MLA_HEADS, LATENT_DIM),
+                          dtype=torch.float32 if out_dtype == DTYPE_F32 else torch.bfloat16, device=q.device)
+    if ws is None:
+        ws = workspace(dsa_sparse_mla_workspace_size(batch), q.device)
+    _check(fn, getattr(lib(), fn)(
+        _ptr(q), _ptr(topk), None if share is None else share.handle, _ptr(kv_cache), batch.ref(),
+        softmax_scale, _ptr(out), out_dtype, _ptr(lse), _ptr(ws), ws.numel(), _ptr(dev_status),
+        _stream(stream)))
+    return out
+
+
+def dsa_sparse_mla_decode(q, topk, kv_cache, batch: Batch, *, softmax_scale=1.0 / 16, out=None,
+                          out_dtype=DTYPE_BF16, lse=None, share=None, ws=None, dev_status=None, stream=None):
+    return _mla("dsa_sparse_mla_decode", q, topk, kv_cache, batch, softmax_scale, out, out_dtype, lse,
+                share, ws, dev_status, stream)
+
+
+def dsa_sparse_mla_prefill(q, topk, kv_cache, batch: Batch, *, softmax_scale=1.0 / 16, out=None,
+                           out_dtype=DTYPE_BF16, lse=None, share=None, ws=None, dev_status=None, stream=None):
+    return _mla("dsa_sparse_mla_prefill", q, topk, kv_cache, batch, softmax_scale, out, out_dtype, lse,
+                share, ws, dev_status, stream)
+
+
+# ---------------------------------------------------------------------------
+def dsa_parse_indexer_types(types) -> list:
+    arr = (c_char_p * len(types))(*[t.encode() for t in types])
+    out = (c_uint8 * len(types))()
+    _check("dsa_parse_indexer_types", lib().dsa_parse_indexer_types(arr, len(types), out))
+    return [bool(v) for v in out]
+
+
+def dsa_schedule_from_freq(n_layers: int, freq: int, offset: int) -> list:
+    out = (c_uint8 * n_layers)()
+    _check("dsa_schedule_from_freq", lib().dsa_schedule_from_freq(n_layers, freq, offset, out))
+    return [bool(v) for v in out]
+
+
+class TopkShare:
+    """The share handle: the last full layer's indices, read by shared layers."""
+
+    def __init__(self):
+        h = c_void_p()
+        _check("dsa_topk_share_create", lib().dsa_topk_share_create(ctypes.byref(h)))
+        self.handle = h
+
+    def __del__(self):
+        if getattr(self, "handle", None) is not None and _lib is not None:
+            _lib.dsa_topk_share_destroy(self.handle)
+            self.handle = None
+
+    def reset(self):
+        _check("dsa_topk_share_reset", lib().dsa_topk_share_reset(self.handle))
+
+    def publish(self, layer_id: int, topk: torch.Tensor):
+        _check("dsa_topk_share_publish",
+               lib().dsa_topk_share_publish(self.handle, layer_id, _ptr(topk), topk.shape[0]))
+
+    def get(self):
+        """(device pointer, rows, layer_id); raises DsaError(DSA_ERR_NO_TOPK_SOURCE) if empty."""
+        p, rows, lid = c_void_p(), c_int64(), c_int32()
+        _check("dsa_topk_share_get", lib().dsa_topk_share_get(self.handle, ctypes.byref(p),
+                                                               ctypes.byref(rows), ctypes.byref(lid)))
+        return p.value, rows.value, lid.value
+
+
+def index_cache_scale_view(idxk_cache: torch.Tensor) -> torch.Tensor:
+    """fp32 [num_pages, 64] view of the per-token scales inside an index-K cache."""
+    pages = idxk_cache.view(-1, IDXK_PAGE_BYTES)
+    return pages[:, PAGE_TOKENS * INDEX_HEAD_DIM:].view(torch.float32)

@@ -1,0 +1,112 @@
+// Host-only parts of the C ABI: status strings, the device status block, the
+// full/shared layer schedule ("GLM-5.3 推理全链路(十一)", 配置里的 78 个字符)
+// and the share handle that carries a full layer's indices to the shared
+// layers after it ("GLM-5.3 推理全链路(十一)", 一次前向里 topk 只算一遍).
+#include <cstring>
+#include <new>
+
+#include "dsa_internal.cuh"
+
+struct dsa_topk_share {
+    const int32_t* topk;
+    int64_t rows;
+    int32_t layer_id;
+    bool valid;
+};
+
+extern "C" int32_t dsa_abi_version(void) { return 1; }
+
+extern "C" const char* dsa_status_string(dsa_status s) {
+    switch (s) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case DSA_ERR_ALIGNMENT: return "buffer not 16-byte aligned";
+        case DSA_ERR_UNSUPPORTED: return "unsupported shape";
+        case DSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case DSA_ERR_NO_TOPK_SOURCE: return "shared layer without a published full-layer top-k";
+        case DSA_ERR_CUDA: return "CUDA runtime error";
+        case DSA_ERR_DEVICE: return "device-side errors recorded in the status block";
+        default: return "unknown status";
+    }
+}
+
+extern "C" dsa_status dsa_device_status_reset(int32_t* dev_status, void* stream) {
+    if (!dev_status) return DSA_ERR_INVALID_ARGUMENT;
+    if (cudaMemsetAsync(dev_status, 0, DSA_DEVICE_STATUS_WORDS * sizeof(int32_t),
+                        dsa::as_stream(stream)) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_device_status_read(const int32_t* dev_status, void* stream, int32_t* host_out) {
+    if (!dev_status || !host_out) return DSA_ERR_INVALID_ARGUMENT;
+    cudaStream_t s = dsa::as_stream(stream);
+    if (cudaMemcpyAsync(host_out, dev_status, DSA_DEVICE_STATUS_WORDS * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DSA_ERR_CUDA;
+    return host_out[0] != 0 ? DSA_ERR_DEVICE : DSA_OK;
+}
+
+extern "C" dsa_status dsa_parse_indexer_types(const char* const* types, int32_t n_layers, uint8_t* is_full) {
+    if (!types || !is_full || n_layers < 0) return DSA_ERR_INVALID_ARGUMENT;
+    for (int32_t l = 0; l < n_layers; ++l) {
+        if (!types[l]) return DSA_ERR_INVALID_ARGUMENT;
+        if (std::strcmp(types[l], "full") == 0) is_full[l] = 1;
+        else if (std::strcmp(types[l], "shared") == 0) is_full[l] = 0;
+        else return DSA_ERR_INVALID_ARGUMENT;
+    }
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_schedule_from_freq(int32_t n_layers, int32_t freq, int32_t offset, uint8_t* is_full) {
+    if (!is_full || n_layers < 0 || freq < 1) return DSA_ERR_INVALID_ARGUMENT;
+    for (int32_t l = 0; l < n_layers; ++l) {
+        int32_t v = l - offset + 1;
+        if (v < 0) v = 0;
+        is_full[l] = (v % freq != 0) ? 0 : 1;
+    }
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_topk_share_create(dsa_topk_share** out) {
+    if (!out) return DSA_ERR_INVALID_ARGUMENT;
+    dsa_topk_share* s = new (std::nothrow) dsa_topk_share{nullptr, 0, -1, false};
+    if (!s) return DSA_ERR_INVALID_ARGUMENT;
+    *out = s;
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_topk_share_destroy(dsa_topk_share* s) {
+    delete s;
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_topk_share_reset(dsa_topk_share* s) {
+    if (!s) return DSA_ERR_INVALID_ARGUMENT;
+    s->topk = nullptr;
+    s->rows = 0;
+    s->layer_id = -1;
+    s->valid = false;
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_topk_share_publish(dsa_topk_share* s, int32_t layer_id, const int32_t* topk,
+                                             int64_t rows) {
+    if (!s || rows < 0 || (!topk && rows > 0)) return DSA_ERR_INVALID_ARGUMENT;
+    s->topk = topk;
+    s->rows = rows;
+    s->layer_id = layer_id;
+    s->valid = true;
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_topk_share_get(const dsa_topk_share* s, const int32_t** topk, int64_t* rows,
+                                         int32_t* layer_id) {
+    if (!s || !topk) return DSA_ERR_INVALID_ARGUMENT;
+    if (!s->valid) return DSA_ERR_NO_TOPK_SOURCE;
+    *topk = s->topk;
+    if (rows) *rows = s->rows;
+    if (layer_id) *layer_id = s->layer_id;
+    return DSA_OK;
+}

@@ -1,0 +1,86 @@
+// dsa_indexer_topk: index-Q quantisation -> indexer scores -> top-2048 per
+// query row ("vLLM 推理链路概览", DSA Indexer; "GLM-5.3 推理全链路(十一)",
+// 优化二 for the short-context rule).
+#include "dsa_internal.cuh"
+#include "indexer_common.cuh"
+#include "topk_common.cuh"
+
+namespace dsa {
+
+__global__ void __launch_bounds__(256)
+index_scores_ref_kernel(const uint8_t* __restrict__ q8, const float* __restrict__ wq,
+                        const uint8_t* __restrict__ cache, BatchDev b, float* __restrict__ scores,
+                        int64_t ld, int32_t* __restrict__ st);
+
+struct WsRowSource {
+    const float* row;
+    __device__ __forceinline__ uint32_t key(int64_t j) const { return score_key(row[j]); }
+    __device__ __forceinline__ float score(int64_t j) const { return row[j]; }
+};
+
+// One CTA per query row: select over the row's p + 1 visible scores.
+__global__ void __launch_bounds__(kSelThreads)
+indexer_select_kernel(const float* __restrict__ scores, int64_t ld, BatchDev b,
+                      int32_t* __restrict__ topk, float* __restrict__ topk_scores) {
+    __shared__ SelectSmem sm;
+    const int64_t row = blockIdx.x;
+    const int r = row_request(b.q_start, b.batch, row);
+    const int qn = b.q_start[r + 1] - b.q_start[r];
+    const int64_t t = row - b.q_start[r];
+    int64_t n = (int64_t)b.seq_len[r] - qn + t + 1;            // positions 0..p
+    if (n > ld) n = ld;                                          // seq_len beyond the declared bound
+    WsRowSource src{scores + row * ld};
+    select_topk_row(src, n, topk + row * kTopK, topk_scores ? topk_scores + row * kTopK : nullptr, sm);
+}
+
+inline int64_t score_ld(const dsa_batch* b) { return ((int64_t)b->max_seq_len + 3) / 4 * 4; }
+
+inline size_t indexer_ws_bytes(const dsa_batch* b) {
+    const size_t qbytes = (q8_workspace_bytes(b->total_q) + 255) / 256 * 256;
+    return qbytes + (size_t)b->total_q * (size_t)score_ld(b) * 4;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" dsa_status dsa_topk_share_publish(dsa_topk_share* s, int32_t layer_id, const int32_t* topk,
+                                             int64_t rows);
+
+extern "C" dsa_status dsa_indexer_topk_workspace_size(const dsa_batch* b, size_t* bytes) {
+    dsa_status vs = validate_batch(b);
+    if (vs != DSA_OK) return vs;
+    if (!bytes) return DSA_ERR_INVALID_ARGUMENT;
+    *bytes = indexer_ws_bytes(b);
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_cache,
+                                       const dsa_batch* b, int32_t* topk, float* topk_scores,
+                                       dsa_topk_share* share, int32_t layer_id, void* ws,
+                                       size_t ws_bytes, int32_t* dev_status, void* stream) {
+    dsa_status vs = validate_batch(b);
+    if (vs != DSA_OK) return vs;
+    if (!q || !w || !idxk_cache || !topk) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(idxk_cache) || !aligned16(topk)) return DSA_ERR_ALIGNMENT;
+    if (b->total_q > 0) {
+        if (!ws) return DSA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(ws)) return DSA_ERR_ALIGNMENT;
+        if (ws_bytes < indexer_ws_bytes(b)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+        cudaStream_t s = as_stream(stream);
+        uint8_t* q8 = static_cast<uint8_t*>(ws);
+        float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
+        float* sc = reinterpret_cast<float*>(q8 + (q8_workspace_bytes(b->total_q) + 255) / 256 * 256);
+        const int64_t ld = score_ld(b);
+        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, s);
+        if (rs != DSA_OK) return rs;
+        dim3 grid((unsigned)((b->max_seq_len + kPage - 1) / kPage), (unsigned)b->batch);
+        BatchDev bd = to_dev(b);
+        index_scores_ref_kernel<<<grid, 256, 0, s>>>(q8, wq, idxk_cache, bd, sc, ld, dev_status);
+        DSA_CHECK_LAUNCH();
+        indexer_select_kernel<<<(unsigned)b->total_q, kSelThreads, 0, s>>>(sc, ld, bd, topk, topk_scores);
+        DSA_CHECK_LAUNCH();
+    }
+    if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);
+    return DSA_OK;
+}

@@ -1,0 +1,53 @@
+// Batch descriptor handling shared by the indexer and sparse-MLA entry points.
+#pragma once
+#include "dsa_internal.cuh"
+
+namespace dsa {
+
+// By-value copy of dsa_batch passed to kernels.
+struct BatchDev {
+    int32_t batch;
+    int32_t max_pages;
+    int32_t max_seq_len;
+    int32_t max_q_len;
+    int64_t total_q;
+    int64_t num_pages;
+    const int32_t* seq_len;
+    const int32_t* q_start;
+    const int32_t* page_table;
+};
+
+inline BatchDev to_dev(const dsa_batch* b) {
+    BatchDev d;
+    d.batch = b->batch;
+    d.max_pages = b->max_pages;
+    d.max_seq_len = b->max_seq_len;
+    d.max_q_len = b->max_q_len;
+    d.total_q = b->total_q;
+    d.num_pages = b->num_pages;
+    d.seq_len = b->seq_len;
+    d.q_start = b->q_start;
+    d.page_table = b->page_table;
+    return d;
+}
+
+// Host-side checks of a batch descriptor (before any launch).
+inline dsa_status validate_batch(const dsa_batch* b) {
+    if (!b) return DSA_ERR_INVALID_ARGUMENT;
+    if (b->batch < 1 || b->max_pages < 1 || b->max_seq_len < 1 || b->max_q_len < 0 ||
+        b->total_q < 0 || b->num_pages < 1)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (!b->seq_len || !b->q_start || !b->page_table) return DSA_ERR_INVALID_ARGUMENT;
+    if ((int64_t)b->max_pages * DSA_PAGE_TOKENS < b->max_seq_len) return DSA_ERR_INVALID_ARGUMENT;
+    if (b->total_q > (int64_t)b->batch * b->max_q_len) return DSA_ERR_INVALID_ARGUMENT;
+    if (b->total_q > 0x7fffffffLL || b->batch > 65535) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+// Quantised index query + folded head weights: T * (4096 B codes + 128 B weights).
+inline size_t q8_workspace_bytes(int64_t total_q) { return (size_t)total_q * (4096 + 128); }
+
+dsa_status launch_index_q_quant(const void* q, const float* w, int64_t rows, uint8_t* q8, float* wq,
+                                cudaStream_t s);
+
+}  // namespace dsa

@@ -1,0 +1,143 @@
+// Lightning-indexer building blocks that materialise full score rows:
+//   * index-Q quantisation (FP8 E4M3 + one ue8m0 scale per head, folded into
+//     the head weight: w'_m = w_m * 2^e_m, exact) - "GLM-5.3 推理全链路(十一)",
+//     读取路径里的两条"非缓存"字节: Q is [tokens, 32, 128] FP8 plus a scale
+//     per 128 dims;
+//   * a CUDA-core scorer s_j = sk_j * sum_m w'_m ReLU(<q8_m, k8_j>) that writes
+//     every score ("vLLM 推理链路概览", DSA Indexer), used by the
+//     dsa_indexer_scores parity hook.  ReLU commutes with the positive scales,
+//     so this equals sum_m w_m ReLU(<q_m, k_j>) on the dequantised values.
+#include "dsa_internal.cuh"
+#include "indexer_common.cuh"
+
+namespace dsa {
+
+// One warp per (row, head): 128 bf16 -> 128 E4M3 codes + w * 2^e.
+__global__ void __launch_bounds__(256)
+index_q_quant_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w, int64_t rows,
+                     uint8_t* __restrict__ q8, float* __restrict__ wq) {
+    const int lane = threadIdx.x & 31;
+    const int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // row*32 + head
+    if (g >= rows * 32) return;
+    const uint2 raw = *reinterpret_cast<const uint2*>(q + g * 128 + lane * 4);
+    const float x0 = bf16_bits_to_f32(raw.x & 0xffffu), x1 = bf16_bits_to_f32(raw.x >> 16);
+    const float x2 = bf16_bits_to_f32(raw.y & 0xffffu), x3 = bf16_bits_to_f32(raw.y >> 16);
+    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+    amax = warp_max(amax);
+    const int e = ue8m0_exponent(amax);
+    const uint32_t lo = f32x2_to_e4m3x2(ldexpf(x0, -e), ldexpf(x1, -e));
+    const uint32_t hi = f32x2_to_e4m3x2(ldexpf(x2, -e), ldexpf(x3, -e));
+    *reinterpret_cast<uint32_t*>(q8 + g * 128 + lane * 4) = lo | (hi << 16);
+    if (lane == 0) wq[g] = w[g] * ldexpf(1.0f, e);
+}
+
+// One CTA per (logical page, request): the page's 64 keys against every query
+// row of the request.  Thread (j = tid/4, quarter = tid%4) handles token j and
+// heads 8*quarter .. 8*quarter+7.
+__global__ void __launch_bounds__(256)
+index_scores_ref_kernel(const uint8_t* __restrict__ q8, const float* __restrict__ wq,
+                        const uint8_t* __restrict__ cache, BatchDev b, float* __restrict__ scores,
+                        int64_t ld, int32_t* __restrict__ st) {
+    __shared__ float kf[64][129];
+    __shared__ float ksc[64];
+    __shared__ float qf[32][129];
+    __shared__ float wqs[32];
+    const int r = blockIdx.y;
+    const int pk = blockIdx.x;
+    const int L = b.seq_len[r];
+    if (pk * kPage >= L) return;
+    const int q0 = b.q_start[r];
+    const int qn = b.q_start[r + 1] - q0;
+    const int tid = threadIdx.x;
+    const int64_t page = b.page_table[(int64_t)r * b.max_pages + pk];
+    const bool page_ok = page >= 0 && page < b.num_pages;
+    if (!page_ok && tid == 0) record_error(st, DSA_DEVERR_PAGE_RANGE, page);
+    if (page_ok) {
+        const uint8_t* pg = cache + page * (int64_t)kIdxPageBytes;
+        for (int c = tid; c < 64 * 64; c += 256) {           // 2 codes per item
+            const int j = c >> 6, d = (c & 63) * 2;
+            const float2 v = e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(pg + j * 128 + d));
+            kf[j][d] = v.x;
+            kf[j][d + 1] = v.y;
+        }
+        if (tid < 64) ksc[tid] = reinterpret_cast<const float*>(pg + kIdxPayloadBytes)[tid];
+    }
+    const int j = tid >> 2, quarter = tid & 3;
+    for (int t = 0; t < qn; ++t) {
+        const int64_t row = q0 + t;
+        const int p = L - qn + t;
+        __syncthreads();
+        for (int c = tid; c < 32 * 64; c += 256) {
+            const int h = c >> 6, d = (c & 63) * 2;
+            const float2 v = e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(q8 + row * 4096 + h * 128 + d));
+            qf[h][d] = v.x;
+            qf[h][d + 1] = v.y;
+        }
+        if (tid < 32) wqs[tid] = wq[row * 32 + tid];
+        __syncthreads();
+        float acc = 0.f;
+        if (page_ok) {
+#pragma unroll 1
+            for (int hh = 0; hh < 8; ++hh) {
+                const int h = quarter * 8 + hh;
+                float dot = 0.f;
+#pragma unroll 8
+                for (int d = 0; d < 128; ++d) dot = fmaf(qf[h][d], kf[j][d], dot);
+                acc = fmaf(wqs[h], fmaxf(dot, 0.f), acc);
+            }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        const int pos = pk * kPage + j;
+        if (quarter == 0 && pos < ld) {
+            const bool valid = page_ok && pos <= p;
+            scores[row * ld + pos] = valid ? acc * ksc[j] : -INFINITY;
+        }
+    }
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+namespace dsa {
+dsa_status launch_index_q_quant(const void* q, const float* w, int64_t rows, uint8_t* q8, float* wq,
+                                cudaStream_t s) {
+    const int64_t warps = rows * 32;
+    const int64_t blocks = (warps + 7) / 8;
+    if (blocks == 0) return DSA_OK;
+    index_q_quant_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint16_t*>(q), w, rows, q8, wq);
+    DSA_CHECK_LAUNCH();
+    return DSA_OK;
+}
+}  // namespace dsa
+
+extern "C" dsa_status dsa_indexer_scores_workspace_size(const dsa_batch* b, size_t* bytes) {
+    dsa_status vs = validate_batch(b);
+    if (vs != DSA_OK) return vs;
+    if (!bytes) return DSA_ERR_INVALID_ARGUMENT;
+    *bytes = q8_workspace_bytes(b->total_q);
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_indexer_scores(const void* q, const float* w, const uint8_t* idxk_cache,
+                                         const dsa_batch* b, float* scores, int64_t ld, void* ws,
+                                         size_t ws_bytes, int32_t* dev_status, void* stream) {
+    dsa_status vs = validate_batch(b);
+    if (vs != DSA_OK) return vs;
+    if (!q || !w || !idxk_cache || !scores) return DSA_ERR_INVALID_ARGUMENT;
+    if (ld < b->max_seq_len) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(idxk_cache)) return DSA_ERR_ALIGNMENT;
+    if (b->total_q == 0) return DSA_OK;
+    if (!ws || !aligned16(ws)) return ws ? DSA_ERR_ALIGNMENT : DSA_ERR_INVALID_ARGUMENT;
+    if (ws_bytes < q8_workspace_bytes(b->total_q)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t* q8 = static_cast<uint8_t*>(ws);
+    float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
+    cudaStream_t s = as_stream(stream);
+    dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, s);
+    if (rs != DSA_OK) return rs;
+    dim3 grid((unsigned)((b->max_seq_len + kPage - 1) / kPage), (unsigned)b->batch);
+    index_scores_ref_kernel<<<grid, 256, 0, s>>>(q8, wq, idxk_cache, to_dev(b), scores, ld, dev_status);
+    DSA_CHECK_LAUNCH();
+    return DSA_OK;
+}

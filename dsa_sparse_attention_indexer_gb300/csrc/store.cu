@@ -1,0 +1,158 @@
+// Cache writers: the index-K store (k_norm LayerNorm -> interleaved RoPE on
+// dims 0..63 -> FP8 E4M3 with a ue8m0 scale; "GLM-5.3 推理全链路(十一)",
+// section 索引器缓存里存的是什么) and the latent-row store (512 FP8 + four
+// scales + 64 bf16 RoPE dims = 656 B; same page, section 主 KV 缓存里存的是什么).
+//
+// Both are tiny (n new tokens per step) and write-only; one warp per token,
+// every lane writes one contiguous 4- or 16-byte piece so the row leaves the
+// SM as full 128-byte segments.
+#include "dsa_internal.cuh"
+
+namespace dsa {
+
+// One warp per token; lane l owns dims [4l, 4l+4).  RoPE pairs (2i, 2i+1)
+// never straddle lanes.
+__global__ void __launch_bounds__(256)
+index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__ pos,
+                     const int64_t* __restrict__ slot, int64_t n,
+                     const float* __restrict__ gamma, const float* __restrict__ beta,
+                     float eps, double rope_base, uint8_t* __restrict__ cache,
+                     int64_t num_pages, int32_t* __restrict__ st) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= n) return;
+    const int64_t s = slot[t];
+    if (s < 0) return;                                   // padded row: K write skipped
+    if (s >= num_pages * kPage) {
+        if (lane == 0) record_error(st, DSA_DEVERR_SLOT_RANGE, s);
+        return;
+    }
+    const uint2 raw = *reinterpret_cast<const uint2*>(k + t * 128 + lane * 4);
+    float x[4] = {bf16_bits_to_f32(raw.x & 0xffffu), bf16_bits_to_f32(raw.x >> 16),
+                  bf16_bits_to_f32(raw.y & 0xffffu), bf16_bits_to_f32(raw.y >> 16)};
+    // LayerNorm over 128 dims, biased variance, fp32.
+    const float mean = warp_sum(x[0] + x[1] + x[2] + x[3]) * (1.0f / 128.0f);
+    float d2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { x[i] -= mean; d2 += x[i] * x[i]; }
+    const float var = warp_sum(d2) * (1.0f / 128.0f);
+    const float inv = 1.0f / sqrtf(var + eps);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float y = x[i] * inv;
+        if (gamma) y *= gamma[lane * 4 + i];
+        if (beta) y += beta[lane * 4 + i];
+        x[i] = y;
+    }
+    // Interleaved RoPE on dims 0..63: lanes 0..15 hold pairs i = 2l, 2l+1.
+    // The angle pos * base^(-2i/64) is formed in fp64: at positions near 2^20
+    // an fp32 angle would be off by ~0.1 rad.
+    if (lane < 16) {
+        const double p = (double)pos[t];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = 2 * lane + h;
+            const double ang = p * pow(rope_base, -2.0 * (double)i / 64.0);
+            double sn, cs;
+            sincos(ang, &sn, &cs);
+            const float c = (float)cs, si = (float)sn;
+            const float a = x[2 * h], b = x[2 * h + 1];
+            x[2 * h] = a * c - b * si;
+            x[2 * h + 1] = a * si + b * c;
+        }
+    }
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    amax = warp_max(amax);
+    const int e = ue8m0_exponent(amax);
+    const uint32_t lo = f32x2_to_e4m3x2(ldexpf(x[0], -e), ldexpf(x[1], -e));
+    const uint32_t hi = f32x2_to_e4m3x2(ldexpf(x[2], -e), ldexpf(x[3], -e));
+    const int64_t page = s / kPage;
+    const int row = (int)(s % kPage);
+    uint8_t* pg = cache + page * (int64_t)kIdxPageBytes;
+    *reinterpret_cast<uint32_t*>(pg + row * 128 + lane * 4) = lo | (hi << 16);
+    if (lane == 0) *reinterpret_cast<float*>(pg + kIdxPayloadBytes + row * 4) = ldexpf(1.0f, e);
+}
+
+// One warp per token; lane l owns latent dims [16l, 16l+16) (block l/8) and,
+// for l < 8, RoPE dims [8l, 8l+8).
+__global__ void __launch_bounds__(256)
+latent_store_kernel(const uint16_t* __restrict__ c, const uint16_t* __restrict__ rope,
+                    const int64_t* __restrict__ slot, int64_t n, uint8_t* __restrict__ cache,
+                    int64_t num_pages, int32_t* __restrict__ st) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= n) return;
+    const int64_t s = slot[t];
+    if (s < 0) return;
+    if (s >= num_pages * kPage) {
+        if (lane == 0) record_error(st, DSA_DEVERR_SLOT_RANGE, s);
+        return;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(c + t * 512 + lane * 16);
+    const uint4 r0 = src[0], r1 = src[1];
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    float x[16];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_bits_to_f32(w[i] & 0xffffu);
+        x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+        amax = fmaxf(amax, fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1])));
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int e = ue8m0_exponent(amax);
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = f32x2_to_e4m3x2(ldexpf(x[4 * i], -e), ldexpf(x[4 * i + 1], -e));
+        const uint32_t b = f32x2_to_e4m3x2(ldexpf(x[4 * i + 2], -e), ldexpf(x[4 * i + 3], -e));
+        q[i] = a | (b << 16);
+    }
+    uint8_t* row = cache + (s / kPage) * (int64_t)kKvPageBytes + (s % kPage) * kKvTokenBytes;
+    *reinterpret_cast<uint4*>(row + lane * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+    if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 512 + (lane >> 3) * 4) = ldexpf(1.0f, e);
+    if (lane < 8)
+        *reinterpret_cast<uint4*>(row + 528 + lane * 16) =
+            reinterpret_cast<const uint4*>(rope + t * 64)[lane];
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" dsa_status dsa_index_k_store(const void* k, const int32_t* pos, const int64_t* slot,
+                                        int64_t n, const float* gamma, const float* beta,
+                                        float ln_eps, float rope_base, uint8_t* idxk_cache,
+                                        int64_t num_pages, int32_t* dev_status, void* stream) {
+    if (n < 0 || num_pages < 0) return DSA_ERR_INVALID_ARGUMENT;
+    if (n == 0) return DSA_OK;
+    if (!k || !pos || !slot || !idxk_cache) return DSA_ERR_INVALID_ARGUMENT;
+    if (!(ln_eps >= 0.f) || !(rope_base > 0.f)) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(k) || !aligned16(idxk_cache)) return DSA_ERR_ALIGNMENT;
+    const int warps = 8;
+    const int64_t blocks = (n + warps - 1) / warps;
+    if (blocks > 0x7fffffff) return DSA_ERR_UNSUPPORTED;
+    index_k_store_kernel<<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
+        static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, (double)rope_base,
+        idxk_cache, num_pages, dev_status);
+    DSA_CHECK_LAUNCH();
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_latent_kv_store(const void* c, const void* rope, const int64_t* slot,
+                                          int64_t n, uint8_t* kv_cache, int64_t num_pages,
+                                          int32_t* dev_status, void* stream) {
+    if (n < 0 || num_pages < 0) return DSA_ERR_INVALID_ARGUMENT;
+    if (n == 0) return DSA_OK;
+    if (!c || !rope || !slot || !kv_cache) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(c) || !aligned16(rope) || !aligned16(kv_cache)) return DSA_ERR_ALIGNMENT;
+    const int warps = 8;
+    const int64_t blocks = (n + warps - 1) / warps;
+    if (blocks > 0x7fffffff) return DSA_ERR_UNSUPPORTED;
+    latent_store_kernel<<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
+        static_cast<const uint16_t*>(c), static_cast<const uint16_t*>(rope), slot, n, kv_cache,
+        num_pages, dev_status);
+    DSA_CHECK_LAUNCH();
+    return DSA_OK;
+}

@@ -1,0 +1,238 @@
+/*
+ * dsa.h - C ABI of the GB300 (sm_103a) DSA attention step library (libdsa.so).
+ *
+ * The step has three parts, all run on one GPU by hand-written CUDA kernels:
+ *   1. the lightning indexer: every cached token j gets the score
+ *        s_j = sum_{m<32} w_m * ReLU(<q_m, k_j>)
+ *      from 32 indexer query heads of 128 dims against one shared 128-d FP8
+ *      index key ("vLLM 推理链路概览：以 GLM-5.2 为例", section DSA Indexer);
+ *   2. top-2048 selection over those scores, I = TopK_{j,2048}(s_j) (same section);
+ *   3. sparse MLA in absorbed (MQA) form over the selected tokens:
+ *        alpha = softmax_{j in I, j <= i}(q k_j^T / sqrt(256)),  o = sum alpha c_j
+ *      with 64 query heads of 576 dims and a 512-d latent output per head
+ *      ("vLLM 推理链路概览", section Sparse MLA Attention; "GLM-5.3 推理全链路(一)",
+ *      section "decode: MQA 形态与吸收").
+ * Shared layers reuse the last full layer's indices ("GLM-5.3 推理全链路(一)",
+ * section 4.5; "GLM-5.3 推理全链路(十一)", section "配置里的 78 个字符").
+ *
+ * Conventions for every call:
+ *   - Every pointer documented "device" is caller-owned device memory; the
+ *     library allocates nothing on the device.  Scratch comes from a caller
+ *     workspace sized by the matching *_workspace_size call.
+ *   - Every compute call is asynchronous on the caller's CUDA stream, passed
+ *     as `void* stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - Argument errors (null pointers, sizes, alignment, unsupported shapes) are
+ *     detected on the host and returned before anything is launched.
+ *   - Errors that only the device can see (a page id outside the cache, a slot
+ *     outside the cache, an index outside the context, a wait that timed out)
+ *     never fault: the offending element is skipped and recorded in the
+ *     optional device status block `dev_status` (DSA_DEVICE_STATUS_WORDS int32,
+ *     device; NULL = do not record).  Read it with dsa_device_status_read().
+ *   - No call throws, exits or traps.
+ *   - "bf16" buffers hold IEEE bfloat16 bit patterns (uint16).
+ *
+ * Token positions: request r holds seq_len[r] cached tokens, INCLUDING its
+ * q_len[r] new query tokens; query token t (0-based within the request) sits at
+ * position p = seq_len[r] - q_len[r] + t and sees positions 0..p.
+ * Caches are paged: logical page k of request r is physical page
+ * page_table[r * max_pages + k]; one page table serves the index-K cache and
+ * every layer's latent cache ("GLM-5.3 推理全链路(一)", 细节二: page-interleaved
+ * pools share one logical-page plan).
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- Layout constants ("GLM-5.3 推理全链路(十一)", sections 索引器缓存里存的是什么
+ *      and 主 KV 缓存里存的是什么; page size 64 from 优化一: 按页分块打分). -------- */
+#define DSA_PAGE_TOKENS      64
+#define DSA_INDEX_HEADS      32
+#define DSA_INDEX_HEAD_DIM   128
+#define DSA_IDXK_TOKEN_BYTES 132    /* 128 B FP8 E4M3 key + 4 B scale             */
+#define DSA_IDXK_PAGE_BYTES  8448   /* [64 x 128 B payload | 64 x fp32 scale]     */
+#define DSA_MLA_HEADS        64
+#define DSA_LATENT_DIM       512
+#define DSA_ROPE_DIM         64
+#define DSA_QK_DIM           576
+#define DSA_KV_TOKEN_BYTES   656    /* [512 B FP8 | 4 x fp32 scale | 64 x bf16]   */
+#define DSA_KV_PAGE_BYTES    41984  /* 64 token rows of 656 B                     */
+#define DSA_TOPK             2048
+#define DSA_DEVICE_STATUS_WORDS 4
+
+/* ---- Status codes ------------------------------------------------------- */
+typedef int32_t dsa_status;
+#define DSA_OK                       0
+#define DSA_ERR_INVALID_ARGUMENT     1  /* null pointer, negative size, bad enum    */
+#define DSA_ERR_ALIGNMENT            2  /* a buffer is not 16-byte aligned          */
+#define DSA_ERR_UNSUPPORTED          3  /* a shape this build does not support      */
+#define DSA_ERR_WORKSPACE_TOO_SMALL  4
+#define DSA_ERR_NO_TOPK_SOURCE       5  /* shared layer with no full layer published*/
+#define DSA_ERR_CUDA                 6  /* a CUDA runtime call failed               */
+#define DSA_ERR_DEVICE               7  /* dsa_device_status_read saw device errors */
+
+/* Bits of dev_status[0]; dev_status[1] counts offending elements, dev_status[2]
+ * holds the low 32 bits of one offending value, dev_status[3] is reserved.      */
+#define DSA_DEVERR_SLOT_RANGE    1   /* store: slot >= 64 * num_pages              */
+#define DSA_DEVERR_PAGE_RANGE    2   /* page_table entry outside [0, num_pages)    */
+#define DSA_DEVERR_INDEX_RANGE   4   /* top-k index >= seq_len of its request      */
+#define DSA_DEVERR_TIMEOUT       8   /* a bounded wait inside a kernel gave up     */
+#define DSA_DEVERR_FP16_RANGE   16   /* latent scale outside [2^-15, 2^7]: the
+                                        sparse-MLA fp16 operands are inexact       */
+
+/* Output dtypes of the sparse MLA calls. */
+#define DSA_DTYPE_BF16 0
+#define DSA_DTYPE_F32  1
+
+/* Description of one batch of requests; the struct itself lives on the host. */
+typedef struct dsa_batch {
+    int32_t batch;              /* B >= 1 requests                                  */
+    int32_t max_pages;          /* entries per page-table row                       */
+    int32_t max_seq_len;        /* host upper bound on every seq_len[r]             */
+    int32_t max_q_len;          /* host upper bound on every q_len[r]               */
+    int64_t total_q;            /* T = q_start[B]: query rows in this batch         */
+    int64_t num_pages;          /* pages in each cache buffer (device bounds check) */
+    const int32_t* seq_len;     /* device [B]                                       */
+    const int32_t* q_start;     /* device [B+1], q_start[0] = 0, q_len = diff       */
+    const int32_t* page_table;  /* device [B * max_pages]                           */
+} dsa_batch;
+
+/* Host object that carries the last full layer's indices to the shared layers
+ * ("GLM-5.3 推理全链路(十一)", section 一次前向里 topk 只算一遍: the full layer
+ * updates the shared state, the following shared layers read the same tensor). */
+typedef struct dsa_topk_share dsa_topk_share;
+
+/* ---- General ------------------------------------------------------------ */
+int32_t     dsa_abi_version(void);                 /* 1 for this header */
+const char* dsa_status_string(dsa_status s);        /* static string, never NULL */
+
+/* Zero the device status block (async on stream). */
+dsa_status dsa_device_status_reset(int32_t* dev_status, void* stream);
+/* Synchronise `stream`, copy the block into host_out[4]; returns DSA_ERR_DEVICE
+ * when any error bit is set, DSA_OK otherwise. */
+dsa_status dsa_device_status_read(const int32_t* dev_status, void* stream, int32_t* host_out);
+
+/* ---- Index-K store ("GLM-5.3 推理全链路(一)", 4.5 闪电索引器; "GLM-5.3 推理全链路(十一)",
+ *      索引器缓存里存的是什么) -------------------------------------------------
+ * For each of n new tokens: LayerNorm over the 128 dims of k (eps, optional
+ * affine gamma/beta, fp32), interleaved RoPE on dims 0..63 (pairs (2i, 2i+1)
+ * rotated by pos * rope_base^(-2i/64)), then FP8 E4M3 (round to nearest even)
+ * with one scale 2^e per token, e the smallest integer with amax <= 448 * 2^e
+ * (amax == 0 -> 1.0), stored as fp32.  Token goes to cache slot `slot`
+ * (page slot/64, row slot%64); slot < 0 skips the token (padded rows).
+ *   k          device bf16 [n,128], row-major
+ *   pos        device int32 [n]
+ *   slot       device int64 [n]
+ *   gamma,beta device fp32 [128] or NULL (identity affine)
+ *   idxk_cache device uint8 [num_pages * 8448], 16-byte aligned
+ * A slot >= 64 * num_pages is skipped and recorded (DSA_DEVERR_SLOT_RANGE). */
+dsa_status dsa_index_k_store(const void* k, const int32_t* pos, const int64_t* slot, int64_t n,
+                             const float* gamma, const float* beta, float ln_eps, float rope_base,
+                             uint8_t* idxk_cache, int64_t num_pages,
+                             int32_t* dev_status, void* stream);
+
+/* ---- Latent KV store (writes the 656-B rows that sparse MLA gathers;
+ *      "GLM-5.3 推理全链路(十一)", 主 KV 缓存里存的是什么) --------------------------
+ * For each token: c (512 dims) -> four blocks of 128, each FP8 E4M3 with its own
+ * scale (same rule as above); the 64 RoPE dims are copied as bf16.
+ *   c        device bf16 [n,512];  rope  device bf16 [n,64]
+ *   slot     device int64 [n] (slot < 0 skips the token)
+ *   kv_cache device uint8 [num_pages * 41984], 16-byte aligned               */
+dsa_status dsa_latent_kv_store(const void* c, const void* rope, const int64_t* slot, int64_t n,
+                               uint8_t* kv_cache, int64_t num_pages,
+                               int32_t* dev_status, void* stream);
+
+/* ---- Indexer + top-2048 ("vLLM 推理链路概览", DSA Indexer; "GLM-5.3 推理全链路(十一)",
+ *      优化二: 短上下文直接跳过打分) ------------------------------------------------
+ * For every query row i (request r, position p): the query is quantised to
+ * FP8 E4M3 with one scale per head (the scale rule above), scores
+ * s_j = sum_m w_m ReLU(<q_m, k_j>) are formed on the dequantised values with
+ * fp32 accumulation for j = 0..p, and topk[i] receives the 2048 positions with
+ * the largest scores (ties -> lower position), in ascending order.  When
+ * p + 1 <= 2048 no score is computed and topk[i] = [0, 1, ..., p, -1, ...].
+ * Full score rows are never written to memory.
+ *   q           device bf16 [T,32,128];  w  device fp32 [T,32]
+ *   idxk_cache  device uint8 [num_pages * 8448], 16-byte aligned
+ *   topk        device int32 [T,2048]
+ *   topk_scores device fp32 [T,2048] or NULL: the score of each selected
+ *               position (0 for -1 entries and for short contexts)
+ *   share       NULL, or a share handle that receives (layer_id, topk, T)
+ *   ws          device workspace of at least dsa_indexer_topk_workspace_size() bytes */
+dsa_status dsa_indexer_topk_workspace_size(const dsa_batch* b, size_t* bytes);
+dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_cache,
+                            const dsa_batch* b, int32_t* topk, float* topk_scores,
+                            dsa_topk_share* share, int32_t layer_id,
+                            void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Debug / parity hook: the same scores as dsa_indexer_topk, written in full.
+ *   scores device fp32 [T, ld]; entries j > p of row i (and every entry of a
+ *   page whose id is out of range) are set to -inf.  Requires ld >= max_seq_len.
+ *   ws: device workspace of dsa_indexer_scores_workspace_size() bytes.        */
+dsa_status dsa_indexer_scores_workspace_size(const dsa_batch* b, size_t* bytes);
+dsa_status dsa_indexer_scores(const void* q, const float* w, const uint8_t* idxk_cache,
+                              const dsa_batch* b, float* scores, int64_t ld,
+                              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Parity hook: top-2048 of given fp32 score rows, same selection rule and
+ * output order as dsa_indexer_topk.  Row r uses scores[r*ld + 0 .. valid_len[r]-1].
+ *   scores device fp32 [rows, ld]; valid_len device int32 [rows] (<= max_len <= ld)
+ *   topk   device int32 [rows, 2048]                                          */
+dsa_status dsa_topk_from_scores_workspace_size(int32_t rows, int64_t max_len, size_t* bytes);
+dsa_status dsa_topk_from_scores(const float* scores, int64_t ld, const int32_t* valid_len,
+                                int32_t rows, int64_t max_len, int32_t* topk,
+                                void* ws, size_t ws_bytes, void* stream);
+
+/* ---- Sparse MLA ("vLLM 推理链路概览", Sparse MLA Attention) ---------------------
+ * For every query row i (request r, position p) and head h < 64:
+ *   S_hj = softmax_scale * <q_ih, k_j>,  k_j = [c_j * scale | rope_j] (576 dims)
+ *   out_ih = sum_j softmax_j(S_hj) c_j   over the valid entries j of topk[i]
+ * (entries -1 and entries > p are ignored; an entry >= seq_len[r] is skipped
+ * and recorded).  Softmax statistics and accumulation are fp32.
+ *   q        device bf16 [T,64,576]
+ *   topk     device int32 [T,2048], or NULL to take the indices published in
+ *            `share` (DSA_ERR_NO_TOPK_SOURCE when it holds none)
+ *   kv_cache device uint8 [num_pages * 41984] of THIS layer, 16-byte aligned
+ *   out      device [T,64,512], bf16 or fp32 per out_dtype
+ *   lse      device fp32 [T,64] or NULL: natural-log sum of exp(S) (-inf when
+ *            a row selects nothing, in which case out is 0)
+ * decode: suited to few query rows per request (splits each row's 2048 keys
+ * across CTAs); prefill: suited to many query rows.  Same results.           */
+dsa_status dsa_sparse_mla_workspace_size(const dsa_batch* b, size_t* bytes);
+dsa_status dsa_sparse_mla_decode(const void* q, const int32_t* topk, const dsa_topk_share* share,
+                                 const uint8_t* kv_cache, const dsa_batch* b, float softmax_scale,
+                                 void* out, int32_t out_dtype, float* lse,
+                                 void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+dsa_status dsa_sparse_mla_prefill(const void* q, const int32_t* topk, const dsa_topk_share* share,
+                                  const uint8_t* kv_cache, const dsa_batch* b, float softmax_scale,
+                                  void* out, int32_t out_dtype, float* lse,
+                                  void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ---- Full / shared layer schedule ("GLM-5.3 推理全链路(十一)", 配置里的 78 个字符) --
+ * dsa_parse_indexer_types: types[l] is "full" or "shared"; is_full[l] = 1/0.
+ *   An unknown string returns DSA_ERR_INVALID_ARGUMENT.
+ * dsa_schedule_from_freq: the parameterised form, layer l is shared iff
+ *   max(l - offset + 1, 0) % freq != 0 (GLM-5.3: freq 4, offset 3).           */
+dsa_status dsa_parse_indexer_types(const char* const* types, int32_t n_layers, uint8_t* is_full);
+dsa_status dsa_schedule_from_freq(int32_t n_layers, int32_t freq, int32_t offset, uint8_t* is_full);
+
+/* ---- Share handle ("GLM-5.3 推理全链路(十一)", 一次前向里 topk 只算一遍) ------------
+ * publish: record that `topk` (device int32 [rows,2048]) holds layer
+ *   `layer_id`'s indices; the pointer is borrowed, not copied.
+ * get: the last published indices; DSA_ERR_NO_TOPK_SOURCE if none.
+ * reset: forget the published indices (e.g. at the start of a forward pass). */
+dsa_status dsa_topk_share_create(dsa_topk_share** out);
+dsa_status dsa_topk_share_destroy(dsa_topk_share* s);
+dsa_status dsa_topk_share_reset(dsa_topk_share* s);
+dsa_status dsa_topk_share_publish(dsa_topk_share* s, int32_t layer_id, const int32_t* topk, int64_t rows);
+dsa_status dsa_topk_share_get(const dsa_topk_share* s, const int32_t** topk, int64_t* rows,
+                              int32_t* layer_id);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H_ */

@@ -1,0 +1,161 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function include/dsa.h declares, and
+reject bad arguments on the host before anything is launched.  Fake device
+addresses are never dereferenced on these paths.
+"""
+
+import ctypes
+import json
+import os
+import re
+import subprocess
+
+import pytest
+
+import dsa_sparse_attention_indexer_gb300 as D
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+GOLDEN = json.load(open(os.path.join(ROOT, "tests", "golden", "pages_constants.json")))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(D.LIB_PATH):
+        from dsa_sparse_attention_indexer_gb300 import build
+        build.build()
+    return D.lib()
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**\s*(dsa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_function_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only", D.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", out, flags=re.M))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(L, n)
+
+
+def test_constants_match_header_and_pages(L):
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    consts = dict(re.findall(r"#define\s+(DSA_\w+)\s+(\d+)", text))
+    assert int(consts["DSA_IDXK_TOKEN_BYTES"]) == GOLDEN["index_k_token_bytes"]["value"] == D.IDXK_TOKEN_BYTES
+    assert int(consts["DSA_IDXK_PAGE_BYTES"]) == GOLDEN["index_k_page_bytes"]["value"] == D.IDXK_PAGE_BYTES
+    assert int(consts["DSA_KV_TOKEN_BYTES"]) == GOLDEN["latent_token_bytes"]["value"] == D.KV_TOKEN_BYTES
+    assert int(consts["DSA_PAGE_TOKENS"]) == 64 and int(consts["DSA_TOPK"]) == 2048
+    assert int(consts["DSA_KV_PAGE_BYTES"]) == 64 * 656
+    assert L.dsa_abi_version() == 1
+
+
+def test_status_strings(L):
+    for code in range(0, 8):
+        assert len(D.status_string(code)) > 0
+    assert D.status_string(99) == "unknown status"
+
+
+def _fake_batch(B=2, T=2, max_seq=4096, max_q=1, pages=128):
+    fake = 0x10000000
+    return D.DsaBatch(B, (max_seq + 63) // 64, max_seq, max_q, T, pages, fake, fake + 256, fake + 512)
+
+
+def test_store_argument_errors(L):
+    s = None
+    fk = ctypes.c_void_p(0x20000000)
+    assert L.dsa_index_k_store(None, fk, fk, 1, None, None, 1e-6, 1e4, fk, 1, None, s) == 1
+    assert L.dsa_index_k_store(fk, fk, fk, -1, None, None, 1e-6, 1e4, fk, 1, None, s) == 1
+    assert L.dsa_index_k_store(fk, fk, fk, 0, None, None, 1e-6, 1e4, fk, 1, None, s) == 0   # nothing to do
+    odd = ctypes.c_void_p(0x20000001)
+    assert L.dsa_index_k_store(odd, fk, fk, 1, None, None, 1e-6, 1e4, fk, 1, None, s) == 2
+    assert L.dsa_index_k_store(fk, fk, fk, 1, None, None, 1e-6, -1.0, fk, 1, None, s) == 1
+    assert L.dsa_latent_kv_store(fk, None, fk, 1, fk, 1, None, s) == 1
+    assert L.dsa_latent_kv_store(fk, fk, fk, 1, odd, 1, None, s) == 2
+
+
+def test_batch_validation_and_workspace_sizes(L):
+    n = ctypes.c_size_t(0)
+    b = _fake_batch()
+    assert L.dsa_indexer_topk_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0 and n.value > 0
+    assert L.dsa_sparse_mla_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0
+    assert L.dsa_indexer_scores_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0 and n.value == 2 * (4096 + 128)
+    assert L.dsa_indexer_topk_workspace_size(None, ctypes.byref(n)) == 1
+    bad = _fake_batch()
+    bad.max_pages = 1                                   # 64 tokens cannot hold max_seq_len
+    assert L.dsa_indexer_topk_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
+    bad = _fake_batch(T=5, max_q=1)                     # T > B * max_q_len
+    assert L.dsa_indexer_topk_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
+    bad = _fake_batch()
+    bad.seq_len = None
+    assert L.dsa_indexer_topk_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
+
+
+def test_indexer_and_mla_argument_errors(L):
+    fk = ctypes.c_void_p(0x30000000)
+    odd = ctypes.c_void_p(0x30000004)
+    b = _fake_batch()
+    ws = ctypes.c_void_p(0x40000000)
+    # null query / unaligned cache / missing workspace
+    assert L.dsa_indexer_topk(None, fk, fk, ctypes.byref(b), fk, None, None, 0, ws, 1 << 30, None, None) == 1
+    assert L.dsa_indexer_topk(fk, fk, odd, ctypes.byref(b), fk, None, None, 0, ws, 1 << 30, None, None) == 2
+    assert L.dsa_indexer_topk(fk, fk, fk, ctypes.byref(b), fk, None, None, 0, ws, 16, None, None) == 4
+    # sparse MLA: bad dtype, bad scale, shared layer without a published top-k
+    assert L.dsa_sparse_mla_decode(fk, fk, None, fk, ctypes.byref(b), 0.0625, fk, 7, None, ws, 1 << 30, None, None) == 1
+    assert L.dsa_sparse_mla_decode(fk, fk, None, fk, ctypes.byref(b), -1.0, fk, 0, None, ws, 1 << 30, None, None) == 1
+    share = ctypes.c_void_p()
+    assert L.dsa_topk_share_create(ctypes.byref(share)) == 0
+    assert L.dsa_sparse_mla_decode(fk, None, share, fk, ctypes.byref(b), 0.0625, fk, 0, None, ws, 1 << 30,
+                                   None, None) == 5
+    assert L.dsa_sparse_mla_prefill(fk, None, None, fk, ctypes.byref(b), 0.0625, fk, 0, None, ws, 1 << 30,
+                                    None, None) == 1
+    assert L.dsa_topk_share_destroy(share) == 0
+    # top-k from scores: ld < max_len
+    assert L.dsa_topk_from_scores(fk, 10, fk, 1, 20, fk, None, 0, None) == 1
+    assert L.dsa_topk_from_scores(fk, 10, fk, 0, 10, fk, None, 0, None) == 0      # zero rows: no launch
+
+
+def test_schedule_parser_and_freq_rule(L):
+    full = GOLDEN["full_layers"]["value"]
+    types = ["full" if l in full else "shared" for l in range(78)]
+    is_full = D.dsa_parse_indexer_types(types)
+    assert sum(is_full) == 21 and len(is_full) - sum(is_full) == 57
+    assert [l for l in range(78) if is_full[l]] == full
+    assert D.dsa_schedule_from_freq(78, 4, 3) == is_full
+    # the vLLM default offset 2 differs at layers 2 and 3 (full/shared swap)
+    v = D.dsa_schedule_from_freq(78, 4, 2)
+    assert v[:4] == [True, True, False, False] or v[:4] == [True, True, False, True]
+    with pytest.raises(D.DsaError):
+        D.dsa_parse_indexer_types(["full", "sparse"])
+
+
+def test_share_handle_lifecycle(L):
+    s = D.TopkShare()
+    with pytest.raises(D.DsaError) as e:
+        s.get()
+    assert e.value.code == 5
+    class FakeT:
+        shape = (7, 2048)
+        def data_ptr(self):
+            return 0x50000000
+    s.publish(6, FakeT())
+    assert s.get() == (0x50000000, 7, 6)
+    s.reset()
+    with pytest.raises(D.DsaError):
+        s.get()
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(D, "_lib", None)
+    monkeypatch.setattr(D, "LIB_PATH", "/nonexistent/libdsa.so")
+    with pytest.raises(D.DsaLibraryMissing):
+        D.lib()

@@ -1,0 +1,356 @@
+"""GPU parity on small seeded cases: every CUDA call against the fp64 oracle.
+
+Sizes span several tiles / pages and ragged tails; edge cases include empty
+and short contexts (<= 2048 selects everything), exact multiples of the page
+and of the top-k, -1 padding, causal limits of multi-token rows, ties and
+signed zeros in the top-k, skipped and out-of-range cache slots.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import dsa_sparse_attention_indexer_gb300 as D
+from oracle import dsa_oracle as O
+from synth import Workload, page_table, batch_meta
+from tests.oracle_side import (bf16_bits, check_attention, check_scores, check_topk_row, f64,
+                               oracle_index_cache, oracle_latent_cache, round_bf16)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _gen(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+# ------------------------------------------------------------------ stores
+def _decode_index_cache(cache_u8: np.ndarray, slots: np.ndarray):
+    page, row = np.divmod(slots, 64)
+    codes = cache_u8[page[:, None], row[:, None] * 128 + np.arange(128)]
+    sc = np.ascontiguousarray(cache_u8[page[:, None], 8192 + 4 * row[:, None] + np.arange(4)]).view("<f4")
+    return codes, sc.reshape(-1).astype(np.float64)
+
+
+@pytest.mark.parametrize("affine", [False, True])
+def test_index_k_store_matches_oracle(affine):
+    g = _gen(11)
+    n, num_pages = 3000, 60
+    mag = torch.exp2(torch.randint(-6, 7, (n, 1), generator=g).float())
+    k = (torch.randn(n, 128, generator=g) * mag + torch.randn(n, 1, generator=g)).to(torch.bfloat16)
+    k[5] = 0.0                                          # constant row: LayerNorm output 0, scale 1
+    k[6] = 3.0
+    pos = torch.randint(0, 1 << 20, (n,), generator=g, dtype=torch.int32)
+    slots = torch.randperm(num_pages * 64, generator=g)[:n].to(torch.int64)
+    slots[::50] = -1                                    # padded rows: write skipped
+    gamma = (torch.rand(128, generator=g) + 0.5) if affine else None
+    beta = (torch.randn(128, generator=g) * 0.1) if affine else None
+    cache = torch.zeros(num_pages * 8448, dtype=torch.uint8, device=DEV)
+    st = D.new_device_status(DEV)
+    D.dsa_index_k_store(k.to(DEV), pos.to(DEV), slots.to(DEV), cache,
+                        gamma=None if gamma is None else gamma.to(DEV),
+                        beta=None if beta is None else beta.to(DEV), dev_status=st)
+    assert D.dsa_device_status_read(st)[0] == 0
+    gcache = cache.cpu().numpy().reshape(num_pages, 8448)
+    kf = f64(k)
+    y = O.rope_interleaved(O.layer_norm(kf, None if gamma is None else f64(gamma),
+                                        None if beta is None else f64(beta), 1e-6), pos.numpy(), 10000.0)
+    ocodes, oscales = O.quantize_blocks_128(y)
+    s = slots.numpy()
+    keep = s >= 0
+    gcodes, gscales = _decode_index_cache(gcache, s[keep])
+    oc, os_ = ocodes[keep], oscales[keep]
+    amax = np.max(np.abs(y[keep]), axis=1)
+    smis = gscales != os_
+    # scale differences only where amax / 448 sits on a power of two
+    if smis.any():
+        ratio = amax[smis] / 448.0
+        assert np.all(np.abs(ratio / np.exp2(np.round(np.log2(ratio))) - 1) < 1e-5)
+    assert smis.mean() < 1e-3
+    gd = O.e4m3_decode(gcodes) * gscales[:, None]
+    od = O.e4m3_decode(oc) * os_[:, None]
+    ulp = np.maximum(O.e4m3_ulp(od / os_[:, None]) * os_[:, None], O.e4m3_ulp(gd / gscales[:, None]) * gscales[:, None])
+    assert np.all(np.abs(gd - od) <= ulp * (1 + 1e-12))
+    assert (np.abs(gd - od) > 0).mean() < 1e-3
+    # untouched slots stay zero
+    written = np.zeros(num_pages * 64, bool)
+    written[s[keep]] = True
+    unw = np.nonzero(~written)[0]
+    c2, s2 = _decode_index_cache(gcache, unw)
+    assert not c2.any() and not s2.any()
+
+
+def test_latent_store_matches_oracle():
+    g = _gen(12)
+    n, num_pages = 700, 15
+    c = (torch.randn(n, 512, generator=g) * torch.exp2(torch.randint(-4, 5, (n, 4), generator=g).float())
+         .repeat_interleave(128, dim=1)).to(torch.bfloat16)
+    rope = torch.randn(n, 64, generator=g).to(torch.bfloat16)
+    slots = torch.randperm(num_pages * 64, generator=g)[:n].to(torch.int64)
+    slots[3] = -1
+    cache = torch.zeros(num_pages * 41984, dtype=torch.uint8, device=DEV)
+    D.dsa_latent_kv_store(c.to(DEV), rope.to(DEV), slots.to(DEV), cache)
+    gcache = cache.cpu().numpy().reshape(num_pages, 41984)
+    s = slots.numpy()
+    keep = s >= 0
+    ocache = np.zeros_like(gcache)
+    codes, scales = O.latent_quantize(f64(c))
+    O.latent_cache_write(ocache, s, codes, scales, bf16_bits(rope))
+    grows = O.latent_cache_read_rows(gcache, np.arange(num_pages), s[keep])
+    orows = O.latent_cache_read_rows(ocache, np.arange(num_pages), s[keep])
+    assert np.array_equal(grows[:, 512:], orows[:, 512:])             # RoPE copied bit-exactly
+    sc = np.repeat(scales[keep], 128, axis=1)
+    assert np.all(np.abs(grows[:, :512] - orows[:, :512]) <= O.e4m3_ulp(orows[:, :512] / sc) * sc)
+    written = np.zeros(num_pages * 64, bool)
+    written[s[keep]] = True
+    for sl in np.nonzero(~written)[0][:50]:                        # untouched rows stay zero
+        assert not gcache[sl // 64, (sl % 64) * 656:(sl % 64 + 1) * 656].any()
+
+
+def test_store_records_out_of_range_slot_without_fault():
+    cache = torch.zeros(2 * 8448, dtype=torch.uint8, device=DEV)
+    k = torch.randn(3, 128).to(torch.bfloat16).to(DEV)
+    pos = torch.zeros(3, dtype=torch.int32, device=DEV)
+    slots = torch.tensor([0, 128, 5], dtype=torch.int64, device=DEV)      # 128 >= 2 pages * 64
+    st = D.new_device_status(DEV)
+    D.dsa_index_k_store(k, pos, slots, cache, dev_status=st)
+    out = D.dsa_device_status_read(st)
+    assert out[0] & D.DEVERR_SLOT_RANGE and out[1] == 1 and out[2] == 128
+    assert cache.view(2, 8448)[0, 5 * 128:6 * 128].any()                 # the good rows were written
+
+
+# ------------------------------------------------------------------ top-k from scores
+def _score_rows(g):
+    rows = []
+    for n in [1, 63, 64, 65, 2047, 2048, 2049, 2050, 4097, 10000, 70001]:
+        rows.append(torch.randn(n, generator=g))
+    ties = torch.randint(-3, 4, (9000,), generator=g).float()
+    ties[torch.randint(0, 9000, (300,), generator=g)] = -0.0
+    rows.append(ties)
+    z = torch.zeros(5000)
+    z[::2] = -0.0                                      # only signed zeros: lowest positions win
+    rows.append(z)
+    w = torch.randn(3000, generator=g)
+    w[::3] = -math.inf
+    rows.append(w)
+    rows.append(torch.full((2500,), 7.0))              # all equal
+    return rows
+
+
+def test_topk_from_scores_bit_exact():
+    g = _gen(13)
+    rows = _score_rows(g)
+    ld = max(r.numel() for r in rows) + 3
+    S = torch.full((len(rows), ld), float("nan"))
+    for i, r in enumerate(rows):
+        S[i, :r.numel()] = r
+    vl = torch.tensor([r.numel() for r in rows], dtype=torch.int32)
+    topk = D.dsa_topk_from_scores(S.to(DEV), vl.to(DEV), max_len=ld).cpu().numpy()
+    for i, r in enumerate(rows):
+        ref = O.topk_positions(r.double().numpy(), r.numel())
+        assert np.array_equal(topk[i], ref), f"row {i} (n={r.numel()})"
+
+
+# ------------------------------------------------------------------ indexer
+def _small_workload(seq_len, q_len, seed):
+    return Workload("small", seed, list(seq_len), list(q_len), ["full"])
+
+
+SMALL_SEQ = [1, 63, 64, 65, 2047, 2048, 2049, 2100, 4097, 6000, 3000, 2051]
+SMALL_Q = [1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 6, 6]
+
+
+@pytest.fixture(scope="module")
+def indexer_case():
+    w = _small_workload(SMALL_SEQ, SMALL_Q, 777)
+    g = _gen(21)
+    pt = page_table(w, "cpu")
+    meta = batch_meta(w, "cpu")
+    raw, pos, slots = [], [], []
+    for r, L in enumerate(w.seq_len):
+        raw.append(torch.randn(L, 128, generator=g).to(torch.bfloat16))
+        p = np.arange(L)
+        pos.append(p)
+        slots.append(pt[r, p // 64].numpy().astype(np.int64) * 64 + p % 64)
+    boost = [np.zeros(L, bool) for L in w.seq_len]
+    boost[9][::97] = True                               # a few boosted keys
+    ocache = oracle_index_cache(w.num_pages, [f64(x) for x in raw], pos, slots, boost)
+    q = torch.randn(w.total_q, 32, 128, generator=g).to(torch.bfloat16)
+    wt = torch.randn(w.total_q, 32, generator=g) / math.sqrt(32)
+    # oracle: scores, magnitudes and top-k per row
+    rows = []
+    qs = meta["q_start"].numpy()
+    for r, L in enumerate(w.seq_len):
+        kc, ks = O.index_cache_read(ocache, pt[r].numpy(), L)
+        for t in range(w.q_len[r]):
+            i = qs[r] + t
+            n = L - w.q_len[r] + t + 1
+            qc, qsc = O.index_q_quantize(f64(q[i]))
+            s = O.indexer_scores(qc, qsc, f64(wt[i]), kc[:n], ks[:n])
+            m = O.score_magnitude(qc, qsc, f64(wt[i]), kc[:n], ks[:n])
+            rows.append(dict(r=r, i=i, n=n, s=s, mag=m, topk=O.topk_positions(s, n)))
+    batch = D.Batch(meta["seq_len"].to(DEV), meta["q_start"].to(DEV), pt.to(DEV), w.num_pages,
+                    max_seq_len=w.max_seq_len, max_q_len=w.max_q_len, total_q=w.total_q)
+    return dict(w=w, cache=torch.from_numpy(ocache.reshape(-1)).to(DEV), q=q.to(DEV), wt=wt.to(DEV),
+                batch=batch, rows=rows)
+
+
+def test_indexer_scores_match_oracle(indexer_case):
+    c = indexer_case
+    S = D.dsa_indexer_scores(c["q"], c["wt"], c["cache"], c["batch"]).cpu().numpy()
+    for row in c["rows"]:
+        i, n = row["i"], row["n"]
+        check_scores(S[i, :n], row["s"], row["mag"], what=f"row {i}")
+        assert np.all(np.isneginf(S[i, n:c["w"].seq_len[row["r"]]]))     # causal: j > p masked
+
+
+def test_indexer_topk_matches_oracle(indexer_case):
+    c = indexer_case
+    T = c["w"].total_q
+    sc = torch.empty(T, 2048, device=DEV)
+    st = D.new_device_status(DEV)
+    topk = D.dsa_indexer_topk(c["q"], c["wt"], c["cache"], c["batch"], topk_scores=sc, dev_status=st)
+    assert D.dsa_device_status_read(st)[0] == 0
+    topk, sc = topk.cpu().numpy(), sc.cpu().numpy()
+    ndiff = 0
+    for row in c["rows"]:
+        i = row["i"]
+        ndiff += check_topk_row(topk[i], row["topk"], row["s"], row["mag"], row["n"], what=f"row {i}")
+        if row["n"] > 2048:
+            check_scores(sc[i], row["s"][topk[i]], row["mag"][topk[i]], what=f"selected scores row {i}")
+        else:
+            assert not sc[i].any()
+    assert ndiff <= 2
+
+
+def test_indexer_topk_fed_oracle_fp32_scores_is_bit_exact(indexer_case):
+    c = indexer_case
+    rows = [r for r in c["rows"] if r["n"] > 0]
+    ld = max(r["n"] for r in rows)
+    S = torch.full((len(rows), ld), -math.inf)
+    for k, r in enumerate(rows):
+        S[k, :r["n"]] = torch.from_numpy(r["s"].astype(np.float32))
+    vl = torch.tensor([r["n"] for r in rows], dtype=torch.int32)
+    topk = D.dsa_topk_from_scores(S.to(DEV), vl.to(DEV)).cpu().numpy()
+    for k, r in enumerate(rows):
+        ref = O.topk_positions(r["s"].astype(np.float32).astype(np.float64), r["n"])
+        assert np.array_equal(topk[k], ref)
+
+
+def test_indexer_records_bad_page_without_fault(indexer_case):
+    c = indexer_case
+    b = c["batch"]
+    pt = b.page_table.clone()
+    pt[9, 3] = c["w"].num_pages + 5                        # request 9, logical page 3: out of range
+    bad = D.Batch(b.seq_len, b.q_start, pt, c["w"].num_pages, max_seq_len=b.c.max_seq_len,
+                  max_q_len=b.c.max_q_len, total_q=b.total_q)
+    st = D.new_device_status(DEV)
+    D.dsa_indexer_topk(c["q"], c["wt"], c["cache"], bad, dev_status=st)
+    out = D.dsa_device_status_read(st)
+    assert out[0] & D.DEVERR_PAGE_RANGE and out[2] == c["w"].num_pages + 5
+
+
+# ------------------------------------------------------------------ sparse MLA
+MLA_SEQ = [1, 100, 2048, 3000, 5000, 2500]
+MLA_Q = [1, 1, 1, 6, 2, 1]
+
+
+@pytest.fixture(scope="module")
+def mla_case():
+    w = _small_workload(MLA_SEQ, MLA_Q, 4242)
+    g = _gen(31)
+    pt = page_table(w, "cpu")
+    meta = batch_meta(w, "cpu")
+    cs, rs, slots = [], [], []
+    for r, L in enumerate(w.seq_len):
+        cs.append(f64(torch.randn(L, 512, generator=g).to(torch.bfloat16)))
+        rs.append(torch.randn(L, 64, generator=g).to(torch.bfloat16))
+        p = np.arange(L)
+        slots.append(pt[r, p // 64].numpy().astype(np.int64) * 64 + p % 64)
+    ocache = oracle_latent_cache(w.num_pages, cs, [bf16_bits(x) for x in rs], slots)
+    q = torch.randn(w.total_q, 64, 576, generator=g).to(torch.bfloat16)
+    qs = meta["q_start"].numpy()
+    topk = np.full((w.total_q, 2048), -1, np.int32)
+    for r, L in enumerate(w.seq_len):
+        for t in range(w.q_len[r]):
+            i = qs[r] + t
+            p = L - w.q_len[r] + t
+            if p + 1 <= 2048:
+                topk[i] = O.topk_positions(None, p + 1)
+            else:
+                sel = np.sort(np.random.default_rng(i).choice(p + 1, 2048, replace=False))
+                topk[i] = sel
+    topk[0, 5] = -1                                     # stray -1 inside a short row's list
+    topk[3][100:110] = -1                               # holes in a full row
+    # row 4 (request 3, t = 0 of 6) gets a few entries beyond its own position (causal mask)
+    p4 = MLA_SEQ[3] - 6
+    topk[4][-3:] = [p4 + 1, p4 + 2, p4 + 3]
+    topk[4] = np.sort(topk[4])
+    ref_out, ref_lse = [], []
+    for r, L in enumerate(w.seq_len):
+        for t in range(w.q_len[r]):
+            i = qs[r] + t
+            p = L - w.q_len[r] + t
+            idx = topk[i]
+            rows = O.latent_cache_read_rows(ocache, pt[r].numpy(), np.maximum(idx, 0))
+            o, lse = O.sparse_mla(f64(q[i]), idx, rows, p)
+            ref_out.append(o)
+            ref_lse.append(lse)
+    batch = D.Batch(meta["seq_len"].to(DEV), meta["q_start"].to(DEV), pt.to(DEV), w.num_pages,
+                    max_seq_len=w.max_seq_len, max_q_len=w.max_q_len, total_q=w.total_q)
+    return dict(w=w, cache=torch.from_numpy(ocache.reshape(-1)).to(DEV), q=q.to(DEV),
+                topk=torch.from_numpy(topk).to(DEV), batch=batch, out=np.stack(ref_out), lse=np.stack(ref_lse))
+
+
+@pytest.mark.parametrize("entry", ["decode", "prefill"])
+def test_sparse_mla_fp32_matches_oracle(mla_case, entry):
+    c = mla_case
+    fn = D.dsa_sparse_mla_decode if entry == "decode" else D.dsa_sparse_mla_prefill
+    lse = torch.empty(c["w"].total_q, 64, device=DEV)
+    st = D.new_device_status(DEV)
+    out = fn(c["q"], c["topk"], c["cache"], c["batch"], out_dtype=D.DTYPE_F32, lse=lse, dev_status=st)
+    assert D.dsa_device_status_read(st)[0] == 0
+    out = out.cpu().numpy()
+    for i in range(c["w"].total_q):
+        check_attention(out[i], c["out"][i], what=f"{entry} row {i}")
+    assert np.allclose(lse.cpu().numpy(), c["lse"], rtol=1e-5, atol=1e-4)
+
+
+def test_sparse_mla_bf16_matches_oracle_rounded(mla_case):
+    c = mla_case
+    out = D.dsa_sparse_mla_decode(c["q"], c["topk"], c["cache"], c["batch"], out_dtype=D.DTYPE_BF16)
+    out = out.float().cpu().numpy()
+    for i in range(c["w"].total_q):
+        check_attention(out[i], round_bf16(c["out"][i]), what=f"bf16 row {i}")
+
+
+def test_sparse_mla_empty_row_and_shared_layer_handle(mla_case):
+    c = mla_case
+    topk = c["topk"].clone()
+    topk[1] = -1                                       # nothing selected
+    share = D.TopkShare()
+    with pytest.raises(D.DsaError) as e:
+        D.dsa_sparse_mla_decode(c["q"], None, c["cache"], c["batch"], share=share)
+    assert e.value.code == 5                           # no full layer published yet
+    share.publish(0, topk)
+    lse = torch.empty(c["w"].total_q, 64, device=DEV)
+    a = D.dsa_sparse_mla_decode(c["q"], None, c["cache"], c["batch"], share=share, out_dtype=D.DTYPE_F32, lse=lse)
+    b = D.dsa_sparse_mla_decode(c["q"], topk, c["cache"], c["batch"], out_dtype=D.DTYPE_F32)
+    assert torch.equal(a, b)
+    assert not a[1].any() and torch.isneginf(lse[1]).all()
+
+
+def test_sparse_mla_records_bad_page_without_fault(mla_case):
+    c = mla_case
+    b = c["batch"]
+    pt = b.page_table.clone()
+    pt[4, 10] = -7                                     # request 4: logical page 10 corrupted
+    bad = D.Batch(b.seq_len, b.q_start, pt, c["w"].num_pages, max_seq_len=b.c.max_seq_len,
+                  max_q_len=b.c.max_q_len, total_q=b.total_q)
+    st = D.new_device_status(DEV)
+    out = D.dsa_sparse_mla_decode(c["q"], c["topk"], c["cache"], bad, out_dtype=D.DTYPE_F32, dev_status=st)
+    res = D.dsa_device_status_read(st)
+    assert res[0] & D.DEVERR_PAGE_RANGE and res[2] == -7
+    assert torch.isfinite(out).all()
