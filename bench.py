@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA attention step (index-K store -> indexer + top-2048 ->
+sparse MLA per layer of a full/shared group) through libdsa.
+
+One step = one pass of the whole path over one batch of synthetic decode
+input.  Default workload: 64 requests x 1 decode token, context 32768 +-25 %,
+layer group [full, shared, shared, shared].  Metric: query tokens per second
+through the group (and us per layer); the roofline is reported for the
+dominant call against the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+requests are independent; no collective on the data path) and rank 0 prints
+one JSON line with the whole-job throughput.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "DSA query-tokens/s at 32K-1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
+L2_BYTES = 129 * 1024 * 1024
+
+# DRAM traffic per launch from an ncu capture, keyed by call; valid only while
+# the kernel source it was taken on is unchanged (sha256 prefix of the file).
+NCU_TRAFFIC = {}
+
+
+def file_sha(path):
+    with open(os.path.join(ROOT, path), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        top = max(sm)
+        loaded = [s for s in sm if s >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+def workload_bytes(w):
+    """Algorithmic bytes of one step: index-K read once per request per full
+    layer, plus 656 B per selected token per query row per layer."""
+    n_full = sum(1 for t in w.layers if t == "full")
+    idx = 0
+    kv = 0
+    for L, q in zip(w.seq_len, w.q_len):
+        idx += 132 * L
+        for t in range(q):
+            kv += 656 * min(2048, L - q + t + 1)
+    return n_full * idx, kv * len(w.layers), idx, kv
+
+
+class Step:
+    """All device buffers of one step and the calls that make it up."""
+
+    def __init__(self, gw, D):
+        self.gw = gw
+        self.D = D
+        w = gw.w
+        dev = gw.device
+        self.share = D.TopkShare()
+        self.topk = torch.empty((w.total_q, 2048), dtype=torch.int32, device=dev)
+        self.idx_ws = D.workspace(D.dsa_indexer_topk_workspace_size(gw.batch), dev)
+        self.mla_ws = D.workspace(D.dsa_sparse_mla_workspace_size(gw.batch), dev)
+        self.out = {l: torch.empty((w.total_q, 64, 512), dtype=torch.bfloat16, device=dev) for l in gw.layers}
+        self.full = [t == "full" for t in w.layers]
+        self.launches_per_step = 0
+
+    def run(self, stream, timers=None):
+        D, gw = self.D, self.gw
+
+        def t(name, fn):
+            if timers is None:
+                fn()
+                return
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            timers.setdefault(name, []).append((e0, e1))
+
+        first_full = True
+        for li, l in enumerate(gw.layers):
+            if self.full[li]:
+                t("index_k_store", lambda: D.dsa_index_k_store(gw.new_k, gw.new_pos, gw.new_slot, gw.idx_cache,
+                                                                 dev_status=gw.dev_status, stream=stream))
+            t("latent_kv_store", lambda: D.dsa_latent_kv_store(gw.new_c[l], gw.new_r[l], gw.new_slot, gw.kv_cache[l],
+                                                                 dev_status=gw.dev_status, stream=stream))
+            if self.full[li]:
+                t("indexer_topk", lambda: D.dsa_indexer_topk(gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch,
+                                                             topk=self.topk, share=self.share, layer_id=l,
+                                                             ws=self.idx_ws, dev_status=gw.dev_status,
+                                                             stream=stream))
+                first_full = False
+            t("sparse_mla_decode", lambda: D.dsa_sparse_mla_decode(
+                gw.q_mla[l], None, gw.kv_cache[l], gw.batch, share=self.share, out=self.out[l], ws=self.mla_ws,
+                dev_status=gw.dev_status, stream=stream))
+        return first_full
+
+
+KERNELS_PER_CALL = {"index_k_store": 1, "latent_kv_store": 1, "indexer_topk": 3, "sparse_mla_decode": 2}
+
+
+def call_bytes(name, w):
+    """Algorithmic bytes of one launch of a call."""
+    _, _, idx, kv = workload_bytes(w)
+    if name == "indexer_topk":
+        return idx
+    if name == "sparse_mla_decode":
+        return kv
+    if name == "index_k_store":
+        return w.total_q * (256 + 132)
+    if name == "latent_kv_store":
+        return w.total_q * (1152 + 656)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    import dsa_sparse_attention_indexer_gb300 as D
+    import synth
+    from synth.gpu import GpuWorkload
+
+    dev = f"cuda:{torch.cuda.current_device()}"
+    w = synth.workload(args.workload)
+    gw = GpuWorkload(w, dev)
+    step = Step(gw, D)
+    stream = torch.cuda.current_stream()
+    total_bytes = sum(workload_bytes(w)[:2])
+    flush = total_bytes < 4 * L2_BYTES
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
+
+    for _ in range(args.warmup):
+        step.run(stream)
+    torch.cuda.synchronize()
+    st = D.dsa_device_status_read(gw.dev_status)
+    if st[0] != 0:
+        raise RuntimeError(f"device errors during warm-up: {st}")
+
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    gpu_id = str(getattr(props, "uuid", "0"))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) >= 32:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.start()
+    time.sleep(0.3)
+    timers = {}
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    if flush:
+        tot = 0.0
+        for _ in range(args.steps):
+            flush_buf.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step.run(stream, timers)
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        ms = tot / args.steps
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step.run(stream, timers)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    per_call = {k: sum(a.elapsed_time(b) for a, b in v) / args.steps * 1000.0 for k, v in timers.items()}
+    per_launch = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) * 1000.0 for k, v in timers.items()}
+
+    # ---- end to end: host buffers in, host buffers out, through the same calls
+    pinned_in = {
+        "q_idx": gw.q_idx.cpu().pin_memory(), "w_idx": gw.w_idx.cpu().pin_memory(),
+        "new_k": gw.new_k.cpu().pin_memory(), "new_pos": gw.new_pos.cpu().pin_memory(),
+        "new_slot": gw.new_slot.cpu().pin_memory()}
+    for l in gw.layers:
+        pinned_in[f"c{l}"] = gw.new_c[l].cpu().pin_memory()
+        pinned_in[f"r{l}"] = gw.new_r[l].cpu().pin_memory()
+        pinned_in[f"q{l}"] = gw.q_mla[l].cpu().pin_memory()
+    dev_of = {"q_idx": gw.q_idx, "w_idx": gw.w_idx, "new_k": gw.new_k, "new_pos": gw.new_pos,
+              "new_slot": gw.new_slot}
+    for l in gw.layers:
+        dev_of[f"c{l}"] = gw.new_c[l]
+        dev_of[f"r{l}"] = gw.new_r[l]
+        dev_of[f"q{l}"] = gw.q_mla[l]
+    pinned_out = {l: torch.empty(step.out[l].shape, dtype=step.out[l].dtype).pin_memory() for l in gw.layers}
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in pinned_out.values())
+    e2e_steps = max(3, min(args.steps, 50))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for k, h in pinned_in.items():
+            dev_of[k].copy_(h, non_blocking=True)
+        step.run(stream)
+        for l in gw.layers:
+            pinned_out[l].copy_(step.out[l], non_blocking=True)
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1000.0 / e2e_steps
+
+    if world > 1:
+        t_ = torch.tensor([ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t_, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t_[0]), float(t_[1])
+    return dict(w=w, ms=ms, e2e_ms=e2e_ms, per_call=per_call, per_launch=per_launch, clocks=clocks,
+                h2d=h2d, d2h=d2h, launches=sum(KERNELS_PER_CALL[k] * len(v) for k, v in timers.items()) // args.steps)
+
+
+# ----------------------------------------------------------------------------
+def oracle_sample(w, budget_s: float, max_requests: int = 64):
+    """Time the fp64 oracle on whole requests of the workload until ~budget_s.
+
+    Per request, the inputs are drawn with the same distributions (request-
+    scoped seeds); the index cache is built outside the timing (it is resident
+    state), and so are the latent rows of the positions the step selects.
+    Timed: index-Q quantisation, scoring of every visible position, top-2048,
+    and sparse MLA for every layer of the group.  Returns (requests, seconds).
+    """
+    import synth
+    from oracle import dsa_oracle as O
+
+    done, spent = 0, 0.0
+    for r in range(min(w.batch, max_requests)):
+        L, qn = w.seq_len[r], w.q_len[r]
+        npg = (L + 63) // 64
+        g = torch.Generator().manual_seed(w.seed * 7919 + r)
+        pt = torch.randperm(npg, generator=g).numpy().astype(np.int32)
+        pos = np.arange(L)
+        slots = pt[pos // 64].astype(np.int64) * 64 + pos % 64
+        idx_cache = np.zeros((npg, O.INDEX_PAGE_BYTES), np.uint8)
+        k = synth.normal_bf16(w, f"idx_k/req{r}", (L, 128), "cpu")
+        codes, scales = O.index_k_prepare(k.double().numpy(), pos)
+        O.index_cache_write(idx_cache, slots, codes, scales)
+        q_rows = synth.normal_bf16(w, f"idx_q/req{r}", (qn, 32, 128), "cpu").double().numpy()
+        wr = (torch.randn((qn, 32), generator=g) / math.sqrt(32.0)).double().numpy()
+        t0 = time.perf_counter()
+        topk, _ = O.request_topk(q_rows, wr, idx_cache, pt, L, qn)
+        spent += time.perf_counter() - t0
+        sel = np.unique(topk[topk >= 0])
+        for l in range(len(w.layers)):
+            c = synth.normal_bf16(w, f"lat_c/{l}/req{r}", (L, 512), "cpu")[sel].double().numpy()
+            rp = synth.normal_bf16(w, f"lat_r/{l}/req{r}", (L, 64), "cpu")[sel].contiguous()
+            lc, ls = O.latent_quantize(c)
+            cache = np.zeros((npg, O.LATENT_PAGE_BYTES), np.uint8)
+            O.latent_cache_write(cache, slots[sel], lc, ls, rp.view(torch.int16).numpy().view(np.uint16))
+            qm = synth.normal_bf16(w, f"mla_q/{l}/req{r}", (qn, 64, 576), "cpu").double().numpy()
+            t0 = time.perf_counter()
+            for t in range(qn):
+                rows = O.latent_cache_read_rows(cache, pt, np.maximum(topk[t], 0))
+                O.sparse_mla(qm[t], topk[t], rows, L - qn + t)
+            spent += time.perf_counter() - t0
+        done += 1
+        if spent >= budget_s:
+            break
+    return done, spent
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle, on the host cores, on a bounded
+    sample of the same workload."""
+    import synth
+    w = synth.workload(args.workload)
+    total_q = 0
+    t_all = 0.0
+    steps_done = 0
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        pass
+    for _ in range(max(1, args.steps if args.steps <= 3 else 3)):
+        n, sec = oracle_sample(w, args.ref_budget)
+        total_q += sum(w.q_len[:n])
+        t_all += sec
+        steps_done += 1
+    return dict(w=w, value=total_q / t_all, sample=f"{total_q} query rows ({total_q // steps_done} per pass) "
+                f"of {w.name}, full indexer + top-k + {len(w.layers)} sparse-MLA layers each", seconds=t_all)
+
+
+# ----------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode32k",
+                    choices=["tiny", "decode32k", "decode1m", "verify64k", "prefill128k"])
+    ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per reference pass")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        res = run_reference(args, rank, world)
+        w = res["w"]
+        line = {
+            "impl": "reference", "metric": METRIC, "value": res["value"], "unit": "query_tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len[0], "layers": w.layers,
+                       "mean_ctx": float(np.mean(w.seq_len))},
+            "cpu_baseline": {"value": res["value"], "unit": "query_tokens/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": res["sample"]},
+            "e2e": {"value": res["value"], "unit": "query_tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    w = res["w"]
+    pk = peaks()
+    ms = res["ms"]
+    idx_b, kv_b, _, _ = workload_bytes(w)
+    step_bytes = idx_b + kv_b
+    value = w.total_q * world / (ms / 1000.0)
+    dom = max(res["per_call"], key=lambda k: res["per_call"][k])
+    dom_us = res["per_launch"][dom]
+    dom_bytes = call_bytes(dom, w)
+    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+    src = {"indexer_topk": "dsa_sparse_attention_indexer_gb300/csrc/indexer.cu",
+           "sparse_mla_decode": "dsa_sparse_attention_indexer_gb300/csrc/mla.cu"}.get(dom)
+    traffic = None
+    if dom in NCU_TRAFFIC and src and NCU_TRAFFIC[dom][1] == file_sha(src):
+        traffic = NCU_TRAFFIC[dom][0]
+    line = {
+        "metric": METRIC, "value": value, "unit": "query_tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8-e4m3 cache, fp32/fp16 compute", "data": "synthetic (seeded)",
+        "config": {
+            "workload": w.name, "description": w.description, "batch": w.batch, "q_len": w.q_len[0],
+            "mean_ctx": float(np.mean(w.seq_len)), "layers": w.layers,
+            "us_per_layer": ms * 1000.0 / len(w.layers),
+            "l2": ("flushed (256 MB write) between timed steps" if step_bytes < 4 * L2_BYTES else
+                   f"inputs larger than L2 ({step_bytes / 1e6:.0f} MB algorithmic bytes per step), no flush"),
+            "algorithmic_bytes_per_step": step_bytes,
+            "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
+            "step_frac_of_measured_hbm": step_bytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "step_frac_of_8tbs": step_bytes / (ms * 1e-3) / 1e9 / 8000.0,
+            "us_per_call": {k: round(v, 2) for k, v in res["per_call"].items()},
+        },
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"],
+                     "algorithmic_bytes_per_launch": dom_bytes, "us_per_launch": dom_us},
+        "clocks": res["clocks"],
+        "e2e": {"value": w.total_q * world / (res["e2e_ms"] / 1000.0), "unit": "query_tokens/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"], "ms_per_step": res["e2e_ms"]},
+        "gpu_launches": res["launches"] * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        n, sec = oracle_sample(w, args.ref_budget)
+        qrows = sum(w.q_len[:n])
+        line["cpu_baseline"] = {"value": qrows / sec, "unit": "query_tokens/s", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{n} of {w.batch} requests ({qrows} query rows): indexer over the full "
+                                          f"context + top-2048 + {len(w.layers)} sparse-MLA layers, fp64 numpy"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
