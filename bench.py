@@ -201,7 +201,7 @@ def run_ours(args, rank, world):
     from synth.gpu import GpuWorkload
 
     dev = f"cuda:{torch.cuda.current_device()}"
-    w = synth.workload(args.workload)
+    w = synth.workload(args.workload, batch=args.batch, ctx=args.ctx)
     gw = GpuWorkload(w, dev)
     step = Step(gw, D)
     stream = torch.cuda.current_stream()
@@ -345,7 +345,7 @@ def run_reference(args, rank, world):
     """The reference arm: the fp64 CPU oracle, on the host cores, on a bounded
     sample of the same workload."""
     import synth
-    w = synth.workload(args.workload)
+    w = synth.workload(args.workload, batch=args.batch, ctx=args.ctx)
     total_q = 0
     t_all = 0.0
     steps_done = 0
@@ -369,6 +369,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode32k",
                     choices=["tiny", "decode32k", "decode1m", "verify64k", "prefill128k"])
+    ap.add_argument("--batch", type=int, default=None, help="shrink the workload to its first N requests (profiling)")
+    ap.add_argument("--ctx", type=int, default=None, help="shrink every context proportionally (profiling)")
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per reference pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

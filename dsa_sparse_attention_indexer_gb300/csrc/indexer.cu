@@ -4,6 +4,7 @@
 #include "dsa_internal.cuh"
 #include "indexer_common.cuh"
 #include "topk_common.cuh"
+#include "indexer_tc.cuh"
 
 namespace dsa {
 
@@ -35,8 +36,14 @@ indexer_select_kernel(const float* __restrict__ scores, int64_t ld, BatchDev b,
 
 inline int64_t score_ld(const dsa_batch* b) { return ((int64_t)b->max_seq_len + 3) / 4 * 4; }
 
+// Decode batches (one query row per request) take the fused tensor-core path;
+// other batches score into full rows and select from them.
+inline bool use_tc_path(const dsa_batch* b) { return b->max_q_len == 1 && b->total_q == b->batch; }
+
 inline size_t indexer_ws_bytes(const dsa_batch* b) {
     const size_t qbytes = (q8_workspace_bytes(b->total_q) + 255) / 256 * 256;
+    if (use_tc_path(b))   // row histograms + plan, for any GPU of up to 1024 SMs
+        return qbytes + (size_t)b->total_q * 4096 * 4 + tc_plan_bytes(b->batch, 1024);
     return qbytes + (size_t)b->total_q * (size_t)score_ld(b) * 4;
 }
 
@@ -72,8 +79,19 @@ extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint
         float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
         float* sc = reinterpret_cast<float*>(q8 + (q8_workspace_bytes(b->total_q) + 255) / 256 * 256);
         const int64_t ld = score_ld(b);
-        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, s);
+        if (b->num_pages * 66 > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+        const bool tc = use_tc_path(b);
+        uint32_t* hist = tc ? reinterpret_cast<uint32_t*>(sc) : nullptr;
+        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, hist, s);
         if (rs != DSA_OK) return rs;
+        if (tc) {
+            const int G = device_sm_count();
+            void* plan = reinterpret_cast<uint8_t*>(sc) + (size_t)b->total_q * 4096 * 4;
+            rs = launch_indexer_tc(q8, wq, hist, idxk_cache, b, topk, topk_scores, plan, G, dev_status, s);
+            if (rs != DSA_OK) return rs;
+            if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);
+            return DSA_OK;
+        }
         dim3 grid((unsigned)((b->max_seq_len + kPage - 1) / kPage), (unsigned)b->batch);
         BatchDev bd = to_dev(b);
         index_scores_ref_kernel<<<grid, 256, 0, s>>>(q8, wq, idxk_cache, bd, sc, ld, dev_status);

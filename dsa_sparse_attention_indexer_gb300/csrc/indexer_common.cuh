@@ -48,6 +48,6 @@ inline dsa_status validate_batch(const dsa_batch* b) {
 inline size_t q8_workspace_bytes(int64_t total_q) { return (size_t)total_q * (4096 + 128); }
 
 dsa_status launch_index_q_quant(const void* q, const float* w, int64_t rows, uint8_t* q8, float* wq,
-                                cudaStream_t s);
+                                uint32_t* hist, cudaStream_t s);
 
 }  // namespace dsa

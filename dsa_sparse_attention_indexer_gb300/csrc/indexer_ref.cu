@@ -15,10 +15,11 @@ namespace dsa {
 // One warp per (row, head): 128 bf16 -> 128 E4M3 codes + w * 2^e.
 __global__ void __launch_bounds__(256)
 index_q_quant_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w, int64_t rows,
-                     uint8_t* __restrict__ q8, float* __restrict__ wq) {
+                     uint8_t* __restrict__ q8, float* __restrict__ wq, uint32_t* __restrict__ hist) {
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // row*32 + head
     if (g >= rows * 32) return;
+    if (hist) reinterpret_cast<uint4*>(hist + g * 128)[lane] = make_uint4(0, 0, 0, 0);   // row histogram reset
     const uint2 raw = *reinterpret_cast<const uint2*>(q + g * 128 + lane * 4);
     const float x0 = bf16_bits_to_f32(raw.x & 0xffffu), x1 = bf16_bits_to_f32(raw.x >> 16);
     const float x2 = bf16_bits_to_f32(raw.y & 0xffffu), x3 = bf16_bits_to_f32(raw.y >> 16);
@@ -102,11 +103,11 @@ using namespace dsa;
 
 namespace dsa {
 dsa_status launch_index_q_quant(const void* q, const float* w, int64_t rows, uint8_t* q8, float* wq,
-                                cudaStream_t s) {
+                                uint32_t* hist, cudaStream_t s) {
     const int64_t warps = rows * 32;
     const int64_t blocks = (warps + 7) / 8;
     if (blocks == 0) return DSA_OK;
-    index_q_quant_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint16_t*>(q), w, rows, q8, wq);
+    index_q_quant_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint16_t*>(q), w, rows, q8, wq, hist);
     DSA_CHECK_LAUNCH();
     return DSA_OK;
 }
@@ -134,7 +135,7 @@ extern "C" dsa_status dsa_indexer_scores(const void* q, const float* w, const ui
     uint8_t* q8 = static_cast<uint8_t*>(ws);
     float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
     cudaStream_t s = as_stream(stream);
-    dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, s);
+    dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, nullptr, s);
     if (rs != DSA_OK) return rs;
     dim3 grid((unsigned)((b->max_seq_len + kPage - 1) / kPage), (unsigned)b->batch);
     index_scores_ref_kernel<<<grid, 256, 0, s>>>(q8, wq, idxk_cache, to_dev(b), scores, ld, dev_status);

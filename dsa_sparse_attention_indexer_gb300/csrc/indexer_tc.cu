@@ -1,0 +1,891 @@
+// Fused lightning indexer + top-2048 for decode rows (one query token per
+// request) on the 5th-generation tensor cores ("vLLM 推理链路概览", DSA
+// Indexer: s_j = sum_m w_m ReLU(<q_m, k_j>), I = TopK_{j,2048}(s_j);
+// "GLM-5.3 推理全链路(十一)", 优化一: the index-K cache is read page by page).
+//
+// Per request the score is a dense contraction [L tokens x 128] x [128 x 32
+// heads] in FP8: the index-K tile (128 tokens = two 64-token pages) is the A
+// operand (M = 128), the request's quantised query the B operand (N = 32).
+//
+//  1. plan kernel: cuts the concatenated tiles of all requests that need
+//     scoring (context > 2048) into one contiguous, equal share per CTA; a
+//     share is split at request boundaries into segments.
+//  2. score kernel (persistent, one CTA per SM, warp-specialised):
+//       warp 0     TMA producer: per tile, two 8 KB payload boxes through a
+//                  128-byte-swizzled tensor map + the two 256-B scale rows,
+//                  into a 4-stage ring;
+//       warp 1     tcgen05.mma issuer (kind::f8f6f4, M=128, N=32, K=4x32) into
+//                  a double-buffered TMEM accumulator;
+//       warps 2-5  epilogue: tcgen05.ld of a token's 32 head dots, ReLU, head-
+//                  weighted sum, times the token's key scale; keys above the
+//                  running threshold are appended to a shared-memory candidate
+//                  buffer, which is compacted to its exact top-2048 (radix
+//                  select) whenever it fills; the threshold rises to the
+//                  2048th key.  A segment ends with its exact local top-2048.
+//     No full score row is ever written to memory.
+//  3. merge kernel: per query row, radix select over the union of the row's
+//     segment candidates (ties -> lower position), sorted by position.
+// The global top-2048 is inside the union of the segment top-2048s, and the
+// shared (key desc, position asc) order makes ties consistent.
+#include "dsa_internal.cuh"
+#include "indexer_common.cuh"
+#include "indexer_tc.cuh"
+#include "select_common.cuh"
+#include "sm100.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace dsa {
+namespace itc {
+
+using namespace sm100;
+
+constexpr int kStages = 8;
+constexpr int kStageBytes = 16384;              // 2 x 8192 FP8 payload (two 64-token pages)
+constexpr int kPidChunk = 128;                  // tiles whose page ids the producer fetches at once
+constexpr int kCheckEvery = 4;                  // tiles between epilogue-wide checks
+constexpr int kMinTiles = 16;                   // smallest per-CTA share of tiles
+constexpr int kCap = 6144;                      // candidate buffer entries
+constexpr int kEpiThreads = 256;                // two epilogue groups of 4 warps, alternating tiles
+constexpr int kThreads = 64 + kEpiThreads;      // + producer warp + MMA warp
+constexpr int kEpiBar = 1;
+constexpr int kTmemCols = 64;
+constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 32);
+
+constexpr int kOffStages = 0;
+constexpr int kOffScales = kOffStages + kStages * kStageBytes;   // 2 x 256 B of key scales per stage
+constexpr int kOffB = (kOffScales + kStages * 512 + 1023) / 1024 * 1024;   // quantised query, 2 x 4 KB
+constexpr int kOffCbKey = kOffB + 2 * 4096;                      // candidate keys
+constexpr int kOffCbPos = kOffCbKey + kCap * 4;                  // candidate positions
+constexpr int kOffHist = kOffCbPos + kCap * 4;                   // top-12-bit histogram of the candidates
+constexpr int kOffHist2 = kOffHist + 4096 * 4;                   // compaction scratch histogram
+constexpr int kOffSideKey = kOffHist2;                           // survivors (reuse the scratch histogram)
+constexpr int kOffSidePos = kOffSideKey + kTopK * 4;
+constexpr int kOffBars = kOffHist2 + 4096 * 4;
+constexpr int kOffPid = kOffBars + (2 * kStages + 4) * 8;
+constexpr int kOffMisc = kOffPid + kPidChunk * 2 * 8;
+constexpr int kSmemUsed = kOffMisc + 256;
+constexpr int kSmemAlloc = kSmemUsed + 1024;                     // slack for 1 KB alignment
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
+
+struct Misc {
+    int32_t stage_valid[kStages];
+    uint32_t tmem_base;
+    int32_t cb_count;
+    uint32_t theta;
+    int32_t abort;
+    sel::Found found;
+    int32_t scratch[32];
+    int32_t wtot[8];
+};
+static_assert(sizeof(Misc) <= 256, "misc block");
+static_assert(kCap % kEpiThreads == 0 && kCap / kEpiThreads <= 32, "per-thread candidate slice");
+
+__device__ __forceinline__ int64_t cta_start(int64_t g, int64_t N, int64_t G) { return g * N / G; }
+__device__ __forceinline__ int64_t cta_of_tile(int64_t x, int64_t N, int64_t G) { return ((x + 1) * G + N - 1) / N - 1; }
+
+// Single CTA of 1024 threads.
+__global__ void __launch_bounds__(1024)
+plan_kernel(BatchDev b, int G_launch, Plan p) {
+    __shared__ int32_t scratch[32];
+    int G = G_launch;                                  // CTAs that get a share (<= G_launch)
+    const int gt = threadIdx.x;
+    // pass 1: tile prefix over requests that need scoring
+    int64_t run = 0;
+    for (int base = 0; base < b.batch; base += 1024) {
+        const int r = base + gt;
+        int tiles = 0;
+        if (r < b.batch) {
+            const int L = b.seq_len[r];
+            const int qn = b.q_start[r + 1] - b.q_start[r];
+            tiles = (qn > 0 && L > kTopK) ? (L + 127) / 128 : 0;
+        }
+        int total;
+        const int ex = sel::excl_scan<1024, 0>(tiles, gt, scratch, &total);
+        if (r < b.batch) p.tile_start[r] = run + ex;
+        run += total;
+    }
+    const int64_t N = run;
+    if (gt == 0) p.tile_start[b.batch] = N;
+    // no CTA share below kMinTiles tiles: small batches use fewer CTAs
+    if (N > 0 && N < (int64_t)G * kMinTiles) G = (int)max((int64_t)1, (N + kMinTiles - 1) / kMinTiles);
+    __syncthreads();
+    // pass 2: pieces per request (CTA boundaries inside it) and their prefix
+    int32_t srun = 0;
+    for (int base = 0; base < b.batch; base += 1024) {
+        const int r = base + gt;
+        int np = 0;
+        if (r < b.batch) {
+            const int64_t s0 = p.tile_start[r], s1 = p.tile_start[r + 1];
+            if (s1 > s0) np = (int)(cta_of_tile(s1 - 1, N, G) - cta_of_tile(s0, N, G) + 1);
+        }
+        int total;
+        const int ex = sel::excl_scan<1024, 0>(np, gt, scratch, &total);
+        if (r < b.batch) p.seg_first[r] = srun + ex;
+        srun += total;
+    }
+    if (gt == 0) p.seg_first[b.batch] = srun;
+    for (int g = gt; g < G_launch; g += 1024) {          // every launched CTA, also the idle ones
+        p.cta_range[2 * g] = 0;
+        p.cta_range[2 * g + 1] = 0;
+    }
+    __syncthreads();
+    // pass 3: segment records, one thread per segment
+    const int32_t ns_total = srun;
+    for (int s = gt; s < ns_total; s += 1024) {
+        int lo = 0, hi = b.batch - 1;                  // request r: seg_first[r] <= s < seg_first[r+1]
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.seg_first[mid] <= s) lo = mid; else hi = mid - 1;
+        }
+        const int r = lo;
+        const int64_t s0 = p.tile_start[r], s1 = p.tile_start[r + 1];
+        const int64_t g0 = cta_of_tile(s0, N, G), g1 = cta_of_tile(s1 - 1, N, G);
+        const int64_t g = g0 + (s - p.seg_first[r]);
+        const int64_t tlo = (g == g0) ? s0 : cta_start(g, N, G);
+        const int64_t thi = (g == g1) ? s1 : cta_start(g + 1, N, G);
+        p.segs[s] = Seg{r, (int32_t)(tlo - s0), (int32_t)(thi - s0), (int32_t)g};
+    }
+    __syncthreads();
+    // pass 4: each CTA's contiguous run of segments
+    const int32_t ns = srun;
+    for (int s = gt; s < ns; s += 1024) {
+        const int32_t g = p.segs[s].cta;
+        if (s == 0 || p.segs[s - 1].cta != g) p.cta_range[2 * g] = s;
+        if (s == ns - 1 || p.segs[s + 1].cta != g) p.cta_range[2 * g + 1] = s + 1;
+    }
+}
+
+__device__ __forceinline__ void epi_sync() { sel::gsync<kEpiThreads, kEpiBar>(); }
+
+// Barrier over the epilogue threads that also returns the OR of `pred`:
+// every epilogue thread gets the same answer.
+__device__ __forceinline__ bool epi_any(bool pred) {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+                 " selp.u32 %0, 1, 0, q;\n}"
+                 : "=r"(r) : "r"((uint32_t)pred), "n"(kEpiBar), "n"(kEpiThreads) : "memory");
+    return r != 0;
+}
+
+
+// Crossing bin of a 4096-bin histogram read from the top: count(bins > b) <
+// k <= count(bins >= b).  Thread et owns the 16 bins 4095-16et .. 4080-16et
+// (four 16-byte loads); the prefix over threads is a warp scan plus one
+// exchange of warp totals.
+__device__ __forceinline__ void crossing_bin_4096(const uint32_t* h, int k, int et, Misc* misc) {
+    const int lane = et & 31, wid = et >> 5;
+    const uint4* h4 = reinterpret_cast<const uint4*>(h);
+    uint32_t c[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 v = h4[1023 - (et * 4 + q)];          // bins 4095-16et-4q-3 .. 4095-16et-4q
+        c[4 * q + 0] = v.w;
+        c[4 * q + 1] = v.z;
+        c[4 * q + 2] = v.y;
+        c[4 * q + 3] = v.x;
+    }
+    int mine = 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) mine += (int)c[q];
+    int x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) misc->wtot[wid] = x;
+    epi_sync();
+    int above = x - mine;
+    for (int v = 0; v < wid; ++v) above += misc->wtot[v];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        if (above < k && above + (int)c[q] >= k) {
+            misc->found.bin = (uint32_t)(4095 - (et * 16 + q));
+            misc->found.above = above;
+        }
+        above += (int)c[q];
+    }
+    epi_sync();
+}
+
+// Same for a 256-bin histogram: one bin per thread.
+__device__ __forceinline__ void crossing_bin_256(const uint32_t* h, int k, int et, Misc* misc) {
+    const int lane = et & 31, wid = et >> 5;
+    const int mine = (int)h[255 - et];
+    int x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) misc->wtot[wid] = x;
+    epi_sync();
+    int above = x - mine;
+    for (int v = 0; v < wid; ++v) above += misc->wtot[v];
+    if (above < k && above + mine >= k) {
+        misc->found.bin = (uint32_t)(255 - et);
+        misc->found.above = above;
+    }
+    epi_sync();
+}
+
+// Keep the exact top-2048 (key desc, position asc) of the candidate buffer.
+// hist holds the top-12-bit histogram of the buffer on entry and of the
+// survivors on exit.  Called by all epilogue threads with cb_count > 2048.
+// The survivors' order in the buffer is not preserved (it does not matter:
+// ties are resolved by position values and the merge sorts by position).
+__device__ void compact_candidates(uint32_t* cb_key, int32_t* cb_pos, uint32_t* hist, uint32_t* hist2,
+                                   uint32_t* side_key, int32_t* side_pos, Misc* misc, int et) {
+    constexpr int NT = kEpiThreads;
+    const int n = misc->cb_count;
+    constexpr int kPer = kCap / NT;                // entries per thread (strided by NT)
+    crossing_bin_4096(hist, kTopK, et, misc);
+    const uint32_t b1 = misc->found.bin;
+    const int above1 = misc->found.above;            // candidates in bins above b1: all survive
+    int krem = kTopK - above1;
+    for (int i = et; i < 4096; i += NT) hist2[i] = 0u;
+    epi_sync();
+    uint32_t k[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) k[u] = (et + u * NT < n) ? cb_key[et + u * NT] : 0u;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)                   // second digit among bin b1
+        if (et + u * NT < n && (k[u] >> 20) == b1) atomicAdd(&hist2[(k[u] >> 8) & 0xfffu], 1u);
+    epi_sync();
+    crossing_bin_4096(hist2, krem, et, misc);
+    const uint32_t b2 = misc->found.bin;
+    krem -= misc->found.above;
+    epi_sync();
+    hist2[et] = 0u;                                    // 256 bins, one per thread
+    epi_sync();
+    const uint32_t pre = (b1 << 12) | b2;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)                   // third digit among prefix (b1, b2)
+        if (et + u * NT < n && (k[u] >> 8) == pre) atomicAdd(&hist2[k[u] & 0xffu], 1u);
+    epi_sync();
+    crossing_bin_256(hist2, krem, et, misc);
+    const uint32_t b3 = misc->found.bin;
+    const int need_eq = krem - misc->found.above;
+    const int n_eq = (int)hist2[b3];
+    epi_sync();
+    const uint32_t kth = (b1 << 20) | (b2 << 8) | b3;
+    int32_t pmax = 0x7fffffff;
+    if (n_eq > need_eq) {                          // exact ties at the cut: lowest positions win
+        sel::SmemSrc<NT> src{cb_key, cb_pos, n};
+        sel::TieSrc<sel::SmemSrc<NT>> ts{src, kth};
+        uint32_t tk;
+        int ne2;
+        sel::radix_kth<NT, kEpiBar>(ts, need_eq, et, hist2, misc->scratch, &misc->found, &tk, &ne2, nullptr);
+        pmax = (int32_t)(0x7fffffffu - tk);
+    }
+    // survivors into the side buffer (which reuses hist2): count, scan, write
+    uint32_t keepm = 0;
+    int cnt = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = et + u * NT;
+        const bool keep = i < n && (k[u] > kth || (k[u] == kth && cb_pos[i] <= pmax));
+        keepm |= (keep ? 1u : 0u) << u;
+        cnt += keep ? 1 : 0;
+    }
+    const int lane = et & 31, wid = et >> 5;
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) misc->wtot[wid] = x;
+    epi_sync();
+    int off = x - cnt;
+    for (int v = 0; v < wid; ++v) off += misc->wtot[v];
+    int total = 0;
+    for (int v = 0; v < NT / 32; ++v) total += misc->wtot[v];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        if ((keepm >> u) & 1u) {
+            if (off < kTopK) {
+                side_key[off] = k[u];
+                side_pos[off] = cb_pos[et + u * NT];
+            }
+            ++off;
+        }
+    }
+    // survivors' histogram: bins above b1 keep their counts, b1 keeps the rest
+    for (int i = et; i < 4096; i += NT) {
+        if ((uint32_t)i < b1) hist[i] = 0u;
+        else if ((uint32_t)i == b1) hist[i] = (uint32_t)(kTopK - above1);
+    }
+    epi_sync();
+    total = min(total, kTopK);
+    for (int i = et; i < total; i += NT) {
+        cb_key[i] = side_key[i];
+        cb_pos[i] = side_pos[i];
+    }
+    if (et == 0) {
+        misc->cb_count = total;
+        misc->theta = kth;
+    }
+    epi_sync();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ cache,
+                  const uint8_t* __restrict__ q8, const float* __restrict__ wq, BatchDev b, Plan p,
+                  int32_t* __restrict__ st) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1 KB alignment by offset (not through an integer cast) so that every
+    // access below stays a shared-memory access.
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
+    uint64_t* empty = full + kStages;
+    uint64_t* accf = empty + kStages;
+    uint64_t* acce = accf + 2;
+    int64_t* pid = reinterpret_cast<int64_t*>(smem + kOffPid);
+    Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
+    uint32_t* cb_key = reinterpret_cast<uint32_t*>(smem + kOffCbKey);
+    int32_t* cb_pos = reinterpret_cast<int32_t*>(smem + kOffCbPos);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
+    uint32_t* hist2 = reinterpret_cast<uint32_t*>(smem + kOffHist2);
+    uint32_t* side_key = reinterpret_cast<uint32_t*>(smem + kOffSideKey);
+    int32_t* side_pos = reinterpret_cast<int32_t*>(smem + kOffSidePos);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1 + 4);          // MMA commit + one arrive per warp of the epilogue group
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&accf[a], 1);
+            mbar_init(&acce[a], 4);
+        }
+        misc->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&misc->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc->tmem_base;
+    int s_begin = p.cta_range[2 * blockIdx.x], s_end = p.cta_range[2 * blockIdx.x + 1];
+    const int nseg_max = (int)gridDim.x + b.batch;    // segment slots in the workspace
+    if (s_begin < 0 || s_end > nseg_max || s_begin > s_end) {   // never for a plan from plan_kernel
+        if (threadIdx.x == 0) record_error(st, DSA_DEVERR_INDEX_RANGE, s_begin);
+        s_begin = s_end = 0;
+    }
+    volatile int32_t* abort_flag = &misc->abort;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        // The warp fetches the page ids of up to kPidChunk tiles at once; lane 0
+        // then issues the copies without waiting on global loads.
+        int stage = 0;
+        uint32_t phase = 0;
+        int inflight = 0;
+        bool stop = false;
+        for (int s = s_begin; s < s_end && !stop; ++s) {
+            const Seg sg = p.segs[s];
+            const int L = b.seq_len[sg.r];
+            const int32_t* pt = b.page_table + (int64_t)sg.r * b.max_pages;
+            for (int c0 = sg.lo; c0 < sg.hi && !stop; c0 += kPidChunk) {
+                const int nt = min(kPidChunk, sg.hi - c0);
+                for (int k = lane; k < 2 * nt; k += 32) {
+                    const int idx = c0 * 2 + k;
+                    pid[k] = idx < b.max_pages ? (int64_t)pt[idx] : (int64_t)-2;
+                }
+                __syncwarp();
+                int ok = 1;
+                if (lane == 0) {
+                    for (int tile = c0; tile < c0 + nt; ++tile) {
+                        if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) {
+                            ok = 0;
+                            break;
+                        }
+                        const int t0 = tile * 128;
+                        const int pages = (L - t0 > 64) ? 2 : 1;
+                        uint32_t bytes = 0;
+                        int vmask = 0;
+                        int64_t pg[2];
+                        for (int j = 0; j < pages; ++j) {
+                            pg[j] = pid[(tile - c0) * 2 + j];
+                            if (pg[j] >= 0 && pg[j] < b.num_pages) {
+                                vmask |= 1 << j;
+                                bytes += 8192 + 256;
+                            } else if (pg[j] == -2) {
+                                record_error(st, DSA_DEVERR_INDEX_RANGE, t0 + j * 64);   // beyond the page table row
+                            } else {
+                                record_error(st, DSA_DEVERR_PAGE_RANGE, pg[j]);
+                            }
+                        }
+                        misc->stage_valid[stage] = vmask;
+                        uint8_t* sb = smem + kOffStages + stage * kStageBytes;
+                        mbar_arrive_expect_tx(&full[stage], bytes);
+                        for (int j = 0; j < pages; ++j) {
+                            if (!(vmask & (1 << j))) continue;
+                            tma_load_2d(sb + j * 8192, &tmap, 0, (int32_t)(pg[j] * 66), &full[stage]);
+                            bulk_load(smem + kOffScales + stage * 512 + j * 256,
+                                      cache + pg[j] * (int64_t)kIdxPageBytes + kIdxPayloadBytes, 256, &full[stage]);
+                        }
+                        ++inflight;
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) stop = true;
+                __syncwarp();
+            }
+        }
+        if (lane == 0 && stop) {
+            if (!*abort_flag) record_error(st, DSA_DEVERR_TIMEOUT, 1);
+            *abort_flag = 1;
+            // let the copies already issued land before the CTA winds down
+            for (int i = 0; i < kStages && inflight > 0; ++i, --inflight) {
+                stage = (stage + kStages - 1) % kStages;
+                if (stage == kStages - 1) phase ^= 1;
+                mbar_wait(&full[stage], phase, 500000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // Lane 0 waits and issues; every decision is broadcast so the warp
+        // never diverges around its __syncwarp / shuffles.
+        int stage = 0, acc = 0, bbuf = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool issued_any = false, stop = false;
+        int last_acc = 0;
+        uint32_t last_acc_phase = 0;
+        for (int s = s_begin; s < s_end && !stop; ++s) {
+            const Seg sg = p.segs[s];
+            const int64_t row = b.q_start[sg.r];
+            uint8_t* bq = smem + kOffB + bbuf * 4096;
+            for (int tile = sg.lo; tile < sg.hi; ++tile) {
+                int ok = 1;
+                if (lane == 0) ok = (!*abort_flag && mbar_wait(&acce[acc], acc_phase ^ 1)) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) { stop = true; break; }
+                if (tile == sg.lo) {
+                    // B operand: head `lane` row of the quantised query, 128-byte swizzled
+                    const uint4* src = reinterpret_cast<const uint4*>(q8 + row * 4096 + lane * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(bq + lane * 128 + ((c ^ (lane & 7)) * 16)) = src[c];
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    ok = mbar_wait(&full[stage], phase) ? 1 : 0;
+                    if (ok) {
+                        tc_fence_after();
+                        const uint32_t a0 = smem_addr(smem + kOffStages + stage * kStageBytes);
+                        const uint32_t b0 = smem_addr(bq);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_f8f6f4(tmem + acc * 32, desc_kmajor_sw128(a0 + 32 * k), desc_kmajor_sw128(b0 + 32 * k),
+                                       kIdesc, k > 0 ? 1u : 0u);
+                        mma_commit(&empty[stage]);
+                        mma_commit(&accf[acc]);
+                        issued_any = true;
+                        last_acc = acc;
+                        last_acc_phase = acc_phase;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) { stop = true; break; }
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            bbuf ^= 1;
+        }
+        if (lane == 0 && stop) {
+            record_error(st, DSA_DEVERR_TIMEOUT, 2);
+            *abort_flag = 1;
+            if (issued_any) mbar_wait(&accf[last_acc], last_acc_phase, 500000000ull);   // MMAs in flight
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        // Two groups of 4 warps; group g takes the tiles whose running index
+        // has parity g (= its TMEM accumulator).  Warp w may read TMEM lanes
+        // 32*(w%4) .. 32*(w%4)+31, i.e. tokens 32*(w%4) .. of the tile.
+        const int et = threadIdx.x - 64;
+        const int grp = (warp - 2) >> 2;
+        const int quarter = warp & 3;
+        const int tok = quarter * 32 + lane;
+        int64_t gidx = 0;                              // running tile index of this CTA
+        for (int s = s_begin; s < s_end; ++s) {
+            if (epi_any(*abort_flag != 0)) break;
+            const Seg sg = p.segs[s];
+            const int L = b.seq_len[sg.r];
+            const int64_t row = b.q_start[sg.r];
+            const int n_valid = L;                     // one decode row: positions 0..L-1
+            float w[32];
+#pragma unroll
+            for (int m = 0; m < 32; ++m) w[m] = __ldg(wq + row * 32 + m);
+            if (et == 0) {
+                misc->cb_count = 0;
+                misc->theta = 0u;
+            }
+            for (int i = et; i < 4096; i += kEpiThreads) hist[i] = 0u;
+            epi_sync();
+            bool aborted = false;
+            bool warp_bad = false;                     // this warp saw a timeout
+            for (int tile = sg.lo; tile < sg.hi; ++tile, ++gidx) {
+                if ((int)(gidx & 1) == grp && !warp_bad) {
+                    const int stage = (int)(gidx % kStages);
+                    const uint32_t phase = (uint32_t)((gidx / kStages) & 1);
+                    const int acc = (int)(gidx & 1);
+                    const uint32_t acc_phase = (uint32_t)((gidx >> 1) & 1);
+                    int ok = __all_sync(0xffffffffu, mbar_wait(&accf[acc], acc_phase));
+                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase));   // scales + page mask
+                    if (ok) {
+                        uint32_t v[32];
+                        tc_fence_after();
+                        tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 32, v);
+                        tmem_ld_wait();
+                        const int vmask = misc->stage_valid[stage];
+                        const float sk = reinterpret_cast<const float*>(smem + kOffScales + stage * 512)[tok];
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&acce[acc]);
+                            mbar_arrive(&empty[stage]);
+                        }
+                        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+                        for (int m = 0; m < 32; m += 4) {
+                            a0 = fmaf(w[m], fmaxf(__uint_as_float(v[m]), 0.f), a0);
+                            a1 = fmaf(w[m + 1], fmaxf(__uint_as_float(v[m + 1]), 0.f), a1);
+                            a2 = fmaf(w[m + 2], fmaxf(__uint_as_float(v[m + 2]), 0.f), a2);
+                            a3 = fmaf(w[m + 3], fmaxf(__uint_as_float(v[m + 3]), 0.f), a3);
+                        }
+                        const float score = ((a0 + a1) + (a2 + a3)) * sk;
+                        const int pos = tile * 128 + tok;
+                        const bool valid = ((vmask >> (tok >> 6)) & 1) && pos < n_valid;
+                        const uint32_t key = score_key(score);
+                        const bool pass = valid && key > misc->theta;
+                        const unsigned m = __ballot_sync(0xffffffffu, pass);
+                        if (m) {
+                            int base = 0;
+                            if (lane == __ffs(m) - 1) base = atomicAdd(&misc->cb_count, __popc(m));
+                            base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+                            if (pass) {
+                                const int idx = base + __popc(m & ((1u << lane) - 1u));
+                                cb_key[idx] = key;
+                                cb_pos[idx] = pos;
+                                atomicAdd(&hist[key >> 20], 1u);
+                            }
+                        }
+                    } else {
+                        warp_bad = true;
+                        if (lane == 0) {
+                            record_error(st, DSA_DEVERR_TIMEOUT, 4);
+                            *abort_flag = 1;
+                        }
+                    }
+                }
+                // epilogue-wide decisions (abort, buffer room) every few tiles and at the segment end
+                if (((tile - sg.lo + 1) % kCheckEvery) == 0 || tile + 1 == sg.hi) {
+                    if (epi_any(warp_bad)) { aborted = true; break; }
+                    if (misc->cb_count > kCap - kCheckEvery * 128)
+                        compact_candidates(cb_key, cb_pos, hist, hist2, side_key, side_pos, misc, et);
+                }
+            }
+            if (aborted) break;
+            // segment end: exact local top-2048 and its histogram, written out
+            if (misc->cb_count > kTopK) compact_candidates(cb_key, cb_pos, hist, hist2, side_key, side_pos, misc, et);
+            const int cnt = misc->cb_count;
+            for (int i = et; i < cnt; i += kEpiThreads) {
+                p.cand_key[(int64_t)s * kTopK + i] = cb_key[i];
+                p.cand_pos[(int64_t)s * kTopK + i] = cb_pos[i];
+            }
+            if (et == 0) p.cand_cnt[s] = cnt;
+            uint32_t* gh = p.hist + row * 4096;
+            for (int i = et; i < 4096; i += kEpiThreads)
+                if (hist[i]) atomicAdd(&gh[i], hist[i]);
+            epi_sync();
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- merge
+// Per query row.  The row histogram (top 12 key bits of every visible score)
+// gives the bin b* holding the 2048th score and the count A above it; one flat
+// pass over the row's segment candidates keeps bins > b* and gathers bin b*
+// into shared memory, where the remaining 2048 - A are selected exactly.
+constexpr int kMergeThreads = 1024;
+constexpr int kBndCap = 16384;
+constexpr int kMaxSegs = 1024;
+constexpr int kMOffHist = 0;
+constexpr int kMOffSelPos = kMOffHist + 4096 * 4;
+constexpr int kMOffSelKey = kMOffSelPos + kTopK * 4;
+constexpr int kMOffSegOff = kMOffSelKey + kTopK * 4;
+constexpr int kMOffBndKey = kMOffSegOff + (kMaxSegs + 1) * 4 + 12;
+constexpr int kMOffBndPos = kMOffBndKey + kBndCap * 4;
+constexpr int kMOffMisc = kMOffBndPos + kBndCap * 4;
+constexpr int kMergeSmem = kMOffMisc + 256;
+
+struct MergeMisc {
+    int32_t n_sel, n_bnd, above;
+    uint32_t bstar;
+    sel::Found found;
+    int32_t scratch[32];
+};
+
+// A row's candidates in their physical slots: segment s0 + j holds
+// cnt[j] <= 2048 entries at [(s0 + j) * 2048, ...).  Threads walk the slots
+// with several independent loads in flight; empty slots are skipped.
+struct PhysSrc {
+    const uint32_t* key;
+    const int32_t* pos;
+    const int32_t* cnt;         // [nseg] in shared memory
+    int s0, nseg;
+    template <class F>
+    __device__ __forceinline__ void visit(int gt, F&& f) const {
+        constexpr int U = 8;
+        const int64_t nslots = (int64_t)nseg * kTopK;
+        const int64_t base0 = (int64_t)s0 * kTopK;
+        for (int64_t v0 = gt; v0 < nslots; v0 += (int64_t)kMergeThreads * U) {
+            uint32_t k[U];
+            int32_t p[U];
+            bool a[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + (int64_t)u * kMergeThreads;
+                a[u] = v < nslots && (int)(v % kTopK) < cnt[v / kTopK];
+                k[u] = a[u] ? key[base0 + v] : 0u;
+                p[u] = a[u] ? pos[base0 + v] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) f(a[u], k[u], p[u]);
+        }
+    }
+};
+
+__global__ void __launch_bounds__(kMergeThreads)
+merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__ topk_scores) {
+    extern __shared__ __align__(16) uint8_t msm[];
+    uint32_t* hist = reinterpret_cast<uint32_t*>(msm + kMOffHist);
+    int32_t* sel_pos = reinterpret_cast<int32_t*>(msm + kMOffSelPos);
+    uint32_t* sel_key = reinterpret_cast<uint32_t*>(msm + kMOffSelKey);
+    int32_t* seg_off = reinterpret_cast<int32_t*>(msm + kMOffSegOff);
+    uint32_t* bnd_key = reinterpret_cast<uint32_t*>(msm + kMOffBndKey);
+    int32_t* bnd_pos = reinterpret_cast<int32_t*>(msm + kMOffBndPos);
+    MergeMisc* mm = reinterpret_cast<MergeMisc*>(msm + kMOffMisc);
+    const int64_t row = blockIdx.x;
+    const int gt = threadIdx.x;
+    const int r = row_request(b.q_start, b.batch, row);
+    const int qn = b.q_start[r + 1] - b.q_start[r];
+    const int64_t n_valid = (int64_t)b.seq_len[r] - qn + (row - b.q_start[r]) + 1;
+    int32_t* out = topk + row * kTopK;
+    float* outs = topk_scores ? topk_scores + row * kTopK : nullptr;
+    if (n_valid <= kTopK) {
+        for (int i = gt; i < kTopK; i += kMergeThreads) {
+            out[i] = i < n_valid ? i : -1;
+            if (outs) outs[i] = 0.f;
+        }
+        return;
+    }
+    // candidate counts of the row's segments
+    const int s0 = p.seg_first[r], nseg = p.seg_first[r + 1] - s0;    // nseg <= number of CTAs <= 1024
+    if (gt < nseg) seg_off[gt] = p.cand_cnt[s0 + gt];
+    // threshold bin from the row histogram
+    const uint32_t* gh = p.hist + row * 4096;
+    for (int i = gt; i < 4096; i += kMergeThreads) hist[i] = gh[i];
+    if (gt == 0) { mm->n_sel = 0; mm->n_bnd = 0; }
+    __syncthreads();
+    {
+        constexpr int per = 4096 / kMergeThreads;
+        int mine = 0;
+        for (int q = 0; q < per; ++q) mine += (int)hist[4095 - (gt * per + q)];
+        int tot;
+        int above = sel::excl_scan<kMergeThreads, 0>(mine, gt, mm->scratch, &tot);
+        for (int q = 0; q < per; ++q) {
+            const int bb = 4095 - (gt * per + q);
+            const int cc = (int)hist[bb];
+            if (above < kTopK && above + cc >= kTopK) { mm->bstar = (uint32_t)bb; mm->above = above; }
+            above += cc;
+        }
+    }
+    __syncthreads();
+    const uint32_t bstar = mm->bstar;
+    PhysSrc src{p.cand_key, p.cand_pos, seg_off, s0, nseg};
+    // one pass: bins above b* are in; bin b* goes to the boundary buffer
+    src.visit(gt, [&](bool a, uint32_t key, int32_t pos) {
+        if (!a) return;
+        const uint32_t bin = key >> 20;
+        if (bin > bstar) {
+            const int i = atomicAdd(&mm->n_sel, 1);
+            if (i < kTopK) { sel_pos[i] = pos; sel_key[i] = key; }
+        } else if (bin == bstar) {
+            const int i = atomicAdd(&mm->n_bnd, 1);
+            if (i < kBndCap) { bnd_key[i] = key; bnd_pos[i] = pos; }
+        }
+    });
+    __syncthreads();
+    const int n_sure = mm->n_sel, n_bnd = mm->n_bnd;
+    const int need = kTopK - n_sure;
+    __syncthreads();
+    if (n_bnd <= kBndCap && n_sure == mm->above && need <= n_bnd) {
+        if (need > 0 && n_bnd > need) {
+            sel::SmemSrc<kMergeThreads> bs{bnd_key, bnd_pos, n_bnd};
+            const sel::Threshold th = sel::topk_threshold<kMergeThreads, 0>(bs, need, gt, hist, mm->scratch,
+                                                                            &mm->found);
+            for (int i = gt; i < n_bnd; i += kMergeThreads) {
+                if (th.keep(bnd_key[i], bnd_pos[i])) {
+                    const int j = atomicAdd(&mm->n_sel, 1);
+                    if (j < kTopK) { sel_pos[j] = bnd_pos[i]; sel_key[j] = bnd_key[i]; }
+                }
+            }
+        } else if (need > 0) {
+            for (int i = gt; i < n_bnd; i += kMergeThreads) { sel_pos[n_sure + i] = bnd_pos[i]; sel_key[n_sure + i] = bnd_key[i]; }
+            if (gt == 0) mm->n_sel = n_sure + n_bnd;
+        }
+    } else {
+        // boundary bin too large for shared memory: exact selection over all candidates
+        const sel::Threshold th = sel::topk_threshold<kMergeThreads, 0>(src, kTopK, gt, hist, mm->scratch, &mm->found);
+        if (gt == 0) mm->n_sel = 0;
+        __syncthreads();
+        src.visit(gt, [&](bool a, uint32_t key, int32_t pos) {
+            if (a && th.keep(key, pos)) {
+                const int i = atomicAdd(&mm->n_sel, 1);
+                if (i < kTopK) { sel_pos[i] = pos; sel_key[i] = key; }
+            }
+        });
+    }
+    __syncthreads();
+    const int ns = min(mm->n_sel, kTopK);
+    for (int i = ns + gt; i < kTopK; i += kMergeThreads) {    // only if candidates were missing
+        sel_pos[i] = 0x7fffffff;
+        sel_key[i] = 0u;
+    }
+    __syncthreads();
+    sel::bitonic_sort_by_pos<kMergeThreads, 0>(sel_pos, sel_key, kTopK, gt);
+    for (int i = gt; i < kTopK; i += kMergeThreads) {
+        const bool have = i < ns;
+        out[i] = have ? sel_pos[i] : -1;
+        if (outs) outs[i] = have ? key_score(sel_key[i]) : 0.f;
+    }
+}
+
+}  // namespace itc
+
+// ---------------------------------------------------------------- host side
+namespace {
+struct MapCache {
+    const void* ptr = nullptr;
+    int64_t pages = -1;
+    CUtensorMap map;
+};
+}  // namespace
+
+bool make_index_tmap(const uint8_t* cache, int64_t num_pages, CUtensorMap* out) {
+    static MapCache mc;
+    if (mc.ptr == cache && mc.pages == num_pages) {
+        *out = mc.map;
+        return true;
+    }
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    // The cache viewed as a [num_pages * 66, 128] byte matrix: page p's 64
+    // payload rows are rows 66p .. 66p+63 (its scales fill rows 66p+64, +65).
+    cuuint64_t dims[2] = {128, (cuuint64_t)num_pages * 66};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, 64};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS) return false;
+    mc.ptr = cache;
+    mc.pages = num_pages;
+    mc.map = *out;
+    return true;
+}
+
+size_t tc_plan_bytes(int64_t batch, int G) {
+    const size_t nseg = (size_t)G + (size_t)batch;
+    size_t b = 0;
+    b += (size_t)(batch + 1) * 8;                   // tile_start
+    b += (size_t)(batch + 1) * 4;                   // seg_first
+    b += (size_t)G * 2 * 4;                         // cta_range
+    b = (b + 15) / 16 * 16;
+    b += nseg * sizeof(Seg);                        // segs
+    b = (b + 255) / 256 * 256;
+    b += nseg * kTopK * 4 * 2;                      // cand_key, cand_pos
+    b += nseg * 4;                                  // cand_cnt
+    b = (b + 255) / 256 * 256;
+    return b;
+}
+
+Plan carve_plan(void* base, int64_t batch, int G) {
+    const size_t nseg = (size_t)G + (size_t)batch;
+    uint8_t* q = static_cast<uint8_t*>(base);
+    Plan p;
+    p.tile_start = reinterpret_cast<int64_t*>(q);
+    q += (size_t)(batch + 1) * 8;
+    p.seg_first = reinterpret_cast<int32_t*>(q);
+    q += (size_t)(batch + 1) * 4;
+    p.cta_range = reinterpret_cast<int32_t*>(q);
+    q += (size_t)G * 2 * 4;
+    q = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q) + 15) & ~uintptr_t(15));
+    p.segs = reinterpret_cast<Seg*>(q);
+    q += nseg * sizeof(Seg);
+    q = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q) + 255) & ~uintptr_t(255));
+    p.cand_key = reinterpret_cast<uint32_t*>(q);
+    q += nseg * kTopK * 4;
+    p.cand_pos = reinterpret_cast<int32_t*>(q);
+    q += nseg * kTopK * 4;
+    p.cand_cnt = reinterpret_cast<int32_t*>(q);
+    p.hist = nullptr;
+    return p;
+}
+
+dsa_status launch_indexer_tc(const uint8_t* q8, const float* wq, uint32_t* hist, const uint8_t* cache,
+                             const dsa_batch* b, int32_t* topk, float* topk_scores, void* plan_ws, int G, int32_t* st,
+                             cudaStream_t s) {
+    CUtensorMap map;
+    if (!make_index_tmap(cache, b->num_pages, &map)) return DSA_ERR_CUDA;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(itc::score_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 itc::kSmemAlloc) != cudaSuccess ||
+            cudaFuncSetAttribute(itc::merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 itc::kMergeSmem) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        attr = true;
+    }
+    BatchDev bd = to_dev(b);
+    Plan p = carve_plan(plan_ws, b->batch, G);
+    p.hist = hist;
+    itc::plan_kernel<<<1, 1024, 0, s>>>(bd, G, p);
+    DSA_CHECK_LAUNCH();
+    itc::score_topk_kernel<<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
+    DSA_CHECK_LAUNCH();
+    itc::merge_kernel<<<(unsigned)b->total_q, itc::kMergeThreads, itc::kMergeSmem, s>>>(bd, p, topk, topk_scores);
+    DSA_CHECK_LAUNCH();
+    return DSA_OK;
+}
+
+}  // namespace dsa

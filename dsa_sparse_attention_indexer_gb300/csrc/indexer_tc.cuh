@@ -1,0 +1,32 @@
+// Work plan of the fused tensor-core indexer (device buffers in the caller's
+// workspace) and its host entry points.
+#pragma once
+#include <cuda.h>
+#include "indexer_common.cuh"
+
+namespace dsa {
+
+// Tiles [lo, hi) (128 tokens each, relative to the request) of request r,
+// scored by CTA `cta`; its candidates go to slot = segment index.
+struct Seg {
+    int32_t r, lo, hi, cta;
+};
+
+struct Plan {
+    int64_t* tile_start;   // [B+1] tile prefix over requests that need scoring
+    int32_t* seg_first;    // [B+1] first segment of each request
+    int32_t* cta_range;    // [2G] segment range of each CTA
+    Seg* segs;             // [G+B]
+    uint32_t* cand_key;    // [G+B, 2048]
+    int32_t* cand_pos;     // [G+B, 2048]
+    int32_t* cand_cnt;     // [G+B]
+    uint32_t* hist;        // [T, 4096] top-12-bit key histogram of every visible score, per query row
+};
+
+size_t tc_plan_bytes(int64_t batch, int G);
+dsa_status launch_indexer_tc(const uint8_t* q8, const float* wq, uint32_t* hist, const uint8_t* cache,
+                             const dsa_batch* b, int32_t* topk, float* topk_scores, void* plan_ws, int G, int32_t* st,
+                             cudaStream_t s);
+int device_sm_count();
+
+}  // namespace dsa

@@ -473,7 +473,7 @@ inline size_t mla_ws_bytes(int64_t total_q, int nsplit) {
 int device_sm_count() {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    return sms;
+    return sms > 1024 ? 1024 : sms;
 }
 
 dsa_status sparse_mla_launch(const void* q, const int32_t* topk, const dsa_topk_share* share,

@@ -6,9 +6,16 @@
 // Both are tiny (n new tokens per step) and write-only; one warp per token,
 // every lane writes one contiguous 4- or 16-byte piece so the row leaves the
 // SM as full 128-byte segments.
+#include <cmath>
+
 #include "dsa_internal.cuh"
 
 namespace dsa {
+
+// Rotation frequencies base^(-2i/64), i < 32, computed once on the host in fp64.
+struct RopeFreqs {
+    double theta[32];
+};
 
 // One warp per token; lane l owns dims [4l, 4l+4).  RoPE pairs (2i, 2i+1)
 // never straddle lanes.
@@ -16,7 +23,7 @@ __global__ void __launch_bounds__(256)
 index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__ pos,
                      const int64_t* __restrict__ slot, int64_t n,
                      const float* __restrict__ gamma, const float* __restrict__ beta,
-                     float eps, double rope_base, uint8_t* __restrict__ cache,
+                     float eps, RopeFreqs fr, uint8_t* __restrict__ cache,
                      int64_t num_pages, int32_t* __restrict__ st) {
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -45,17 +52,18 @@ index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__
         x[i] = y;
     }
     // Interleaved RoPE on dims 0..63: lanes 0..15 hold pairs i = 2l, 2l+1.
-    // The angle pos * base^(-2i/64) is formed in fp64: at positions near 2^20
-    // an fp32 angle would be off by ~0.1 rad.
+    // The angle pos * theta_i and its reduction modulo 2*pi are formed in
+    // fp64 (at positions near 2^20 an fp32 angle would be off by ~0.1 rad);
+    // the reduced angle, |r| <= pi, goes through fp32 sincos.
     if (lane < 16) {
         const double p = (double)pos[t];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int i = 2 * lane + h;
-            const double ang = p * pow(rope_base, -2.0 * (double)i / 64.0);
-            double sn, cs;
-            sincos(ang, &sn, &cs);
-            const float c = (float)cs, si = (float)sn;
+            const double ang = p * fr.theta[i];
+            const double red = fma(-6.283185307179586, rint(ang * 0.15915494309189535), ang);
+            float si, c;
+            sincosf((float)red, &si, &c);
             const float a = x[2 * h], b = x[2 * h + 1];
             x[2 * h] = a * c - b * si;
             x[2 * h + 1] = a * si + b * c;
@@ -133,8 +141,10 @@ extern "C" dsa_status dsa_index_k_store(const void* k, const int32_t* pos, const
     const int warps = 8;
     const int64_t blocks = (n + warps - 1) / warps;
     if (blocks > 0x7fffffff) return DSA_ERR_UNSUPPORTED;
+    RopeFreqs fr;
+    for (int i = 0; i < 32; ++i) fr.theta[i] = std::pow((double)rope_base, -2.0 * (double)i / 64.0);
     index_k_store_kernel<<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
-        static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, (double)rope_base,
+        static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, fr,
         idxk_cache, num_pages, dev_status);
     DSA_CHECK_LAUNCH();
     return DSA_OK;

@@ -162,10 +162,9 @@ SMALL_SEQ = [1, 63, 64, 65, 2047, 2048, 2049, 2100, 4097, 6000, 3000, 2051]
 SMALL_Q = [1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 6, 6]
 
 
-@pytest.fixture(scope="module")
-def indexer_case():
-    w = _small_workload(SMALL_SEQ, SMALL_Q, 777)
-    g = _gen(21)
+def _build_indexer_case(seq, qlen, seed, boost_req=None):
+    w = _small_workload(seq, qlen, seed)
+    g = _gen(seed)
     pt = page_table(w, "cpu")
     meta = batch_meta(w, "cpu")
     raw, pos, slots = [], [], []
@@ -175,7 +174,8 @@ def indexer_case():
         pos.append(p)
         slots.append(pt[r, p // 64].numpy().astype(np.int64) * 64 + p % 64)
     boost = [np.zeros(L, bool) for L in w.seq_len]
-    boost[9][::97] = True                               # a few boosted keys
+    if boost_req is not None:
+        boost[boost_req][::97] = True                   # a few boosted keys
     ocache = oracle_index_cache(w.num_pages, [f64(x) for x in raw], pos, slots, boost)
     q = torch.randn(w.total_q, 32, 128, generator=g).to(torch.bfloat16)
     wt = torch.randn(w.total_q, 32, generator=g) / math.sqrt(32)
@@ -197,17 +197,28 @@ def indexer_case():
                 batch=batch, rows=rows)
 
 
-def test_indexer_scores_match_oracle(indexer_case):
-    c = indexer_case
-    S = D.dsa_indexer_scores(c["q"], c["wt"], c["cache"], c["batch"]).cpu().numpy()
-    for row in c["rows"]:
-        i, n = row["i"], row["n"]
-        check_scores(S[i, :n], row["s"], row["mag"], what=f"row {i}")
-        assert np.all(np.isneginf(S[i, n:c["w"].seq_len[row["r"]]]))     # causal: j > p masked
+@pytest.fixture(scope="module")
+def indexer_case():
+    return _build_indexer_case(SMALL_SEQ, SMALL_Q, 777, boost_req=9)
 
 
-def test_indexer_topk_matches_oracle(indexer_case):
-    c = indexer_case
+# Decode batches (one query row per request) take the fused tensor-core path.
+DECODE_SEQ = [2049, 1, 100, 2048, 4097, 6000, 2100, 33000, 10000, 70000, 128 * 40, 128 * 40 + 1, 8191]
+
+
+@pytest.fixture(scope="module")
+def decode_case():
+    return _build_indexer_case(DECODE_SEQ, [1] * len(DECODE_SEQ), 991, boost_req=7)
+
+
+@pytest.fixture(scope="module")
+def decode_many_case():
+    rng = np.random.default_rng(5)
+    seq = rng.integers(1, 9000, 300).tolist()           # more requests than CTAs, many short ones
+    return _build_indexer_case(seq, [1] * len(seq), 992)
+
+
+def _check_indexer_topk(c, max_diff):
     T = c["w"].total_q
     sc = torch.empty(T, 2048, device=DEV)
     st = D.new_device_status(DEV)
@@ -222,7 +233,48 @@ def test_indexer_topk_matches_oracle(indexer_case):
             check_scores(sc[i], row["s"][topk[i]], row["mag"][topk[i]], what=f"selected scores row {i}")
         else:
             assert not sc[i].any()
-    assert ndiff <= 2
+    assert ndiff <= max_diff
+
+
+def test_indexer_topk_decode_tensor_core_path(decode_case):
+    _check_indexer_topk(decode_case, 2)
+
+
+def test_indexer_topk_decode_many_requests(decode_many_case):
+    _check_indexer_topk(decode_many_case, 4)
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xAB, 0xFF])
+def test_indexer_topk_decode_dirty_workspace(decode_case, fill):
+    """The workspace content on entry must not matter (it is caller memory)."""
+    c = decode_case
+    nbytes = D.dsa_indexer_topk_workspace_size(c["batch"])
+    ws = torch.full((nbytes,), fill, dtype=torch.uint8, device=DEV)
+    st = D.new_device_status(DEV)
+    got = D.dsa_indexer_topk(c["q"], c["wt"], c["cache"], c["batch"], ws=ws, dev_status=st).cpu().numpy()
+    assert D.dsa_device_status_read(st)[0] == 0
+    for row in c["rows"]:
+        check_topk_row(got[row["i"]], row["topk"], row["s"], row["mag"], row["n"], what=f"row {row['i']}")
+
+
+def test_indexer_topk_decode_repeatable(decode_case):
+    c = decode_case
+    a = D.dsa_indexer_topk(c["q"], c["wt"], c["cache"], c["batch"])
+    b = D.dsa_indexer_topk(c["q"], c["wt"], c["cache"], c["batch"])
+    assert torch.equal(a, b)
+
+
+def test_indexer_scores_match_oracle(indexer_case):
+    c = indexer_case
+    S = D.dsa_indexer_scores(c["q"], c["wt"], c["cache"], c["batch"]).cpu().numpy()
+    for row in c["rows"]:
+        i, n = row["i"], row["n"]
+        check_scores(S[i, :n], row["s"], row["mag"], what=f"row {i}")
+        assert np.all(np.isneginf(S[i, n:c["w"].seq_len[row["r"]]]))     # causal: j > p masked
+
+
+def test_indexer_topk_matches_oracle(indexer_case):
+    _check_indexer_topk(indexer_case, 2)
 
 
 def test_indexer_topk_fed_oracle_fp32_scores_is_bit_exact(indexer_case):
@@ -239,8 +291,9 @@ def test_indexer_topk_fed_oracle_fp32_scores_is_bit_exact(indexer_case):
         assert np.array_equal(topk[k], ref)
 
 
-def test_indexer_records_bad_page_without_fault(indexer_case):
-    c = indexer_case
+@pytest.mark.parametrize("case", ["indexer_case", "decode_case"])
+def test_indexer_records_bad_page_without_fault(case, request):
+    c = request.getfixturevalue(case)
     b = c["batch"]
     pt = b.page_table.clone()
     pt[9, 3] = c["w"].num_pages + 5                        # request 9, logical page 3: out of range
