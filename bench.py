@@ -176,8 +176,30 @@ class Step:
                 dev_status=gw.dev_status, stream=stream))
         return first_full
 
+    def calls(self):
+        """(name, fn) for every call of one step, in order (for per-call timing)."""
+        out = []
 
-KERNELS_PER_CALL = {"index_k_store": 1, "latent_kv_store": 1, "indexer_topk": 3, "sparse_mla_decode": 2}
+        D, gw = self.D, self.gw
+        stream = torch.cuda.current_stream()
+        for li, l in enumerate(gw.layers):
+            if self.full[li]:
+                out.append(("index_k_store", lambda: D.dsa_index_k_store(
+                    gw.new_k, gw.new_pos, gw.new_slot, gw.idx_cache, dev_status=gw.dev_status, stream=stream)))
+            out.append(("latent_kv_store", (lambda l=l: D.dsa_latent_kv_store(
+                gw.new_c[l], gw.new_r[l], gw.new_slot, gw.kv_cache[l], dev_status=gw.dev_status, stream=stream))))
+            if self.full[li]:
+                out.append(("indexer_topk", (lambda l=l: D.dsa_indexer_topk(
+                    gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch, topk=self.topk, share=self.share, layer_id=l,
+                    ws=self.idx_ws, dev_status=gw.dev_status, stream=stream))))
+            out.append(("sparse_mla_decode", (lambda l=l: D.dsa_sparse_mla_decode(
+                gw.q_mla[l], None, gw.kv_cache[l], gw.batch, share=self.share, out=self.out[l], ws=self.mla_ws,
+                dev_status=gw.dev_status, stream=stream))))
+        return out
+
+
+# our kernels per call (the sparse-MLA call also issues one memset of its row counters)
+KERNELS_PER_CALL = {"index_k_store": 1, "latent_kv_store": 1, "indexer_topk": 4, "sparse_mla_decode": 1}
 
 
 def call_bytes(name, w):
@@ -204,13 +226,31 @@ def run_ours(args, rank, world):
     w = synth.workload(args.workload, batch=args.batch, ctx=args.ctx)
     gw = GpuWorkload(w, dev)
     step = Step(gw, D)
-    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()                      # graphs are captured on a non-default stream
+    torch.cuda.set_stream(stream)
     total_bytes = sum(workload_bytes(w)[:2])
     flush = total_bytes < 4 * L2_BYTES
     flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
 
-    for _ in range(args.warmup):
+    # Capture one step (and, separately, each call) into CUDA graphs: decode
+    # steps are replayed as graphs, which keeps host launch overhead out of
+    # the device timeline.  Two eager runs first do the one-time set-up.
+    for _ in range(2):
         step.run(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step.run(stream)
+    call_graphs = {}
+    for name, fn in step.calls():
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_, stream=stream):
+            fn()
+        call_graphs.setdefault(name, []).append(g_)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
     torch.cuda.synchronize()
     st = D.dsa_device_status_read(gw.dev_status)
     if st[0] != 0:
@@ -225,7 +265,6 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     sampler.start()
     time.sleep(0.3)
-    timers = {}
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -235,7 +274,7 @@ def run_ours(args, rank, world):
             flush_buf.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            step.run(stream, timers)
+            graph.replay()
             e1.record(stream)
             e1.synchronize()
             tot += e0.elapsed_time(e1)
@@ -244,15 +283,31 @@ def run_ours(args, rank, world):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
-            step.run(stream, timers)
+            graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / args.steps
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    per_call = {k: sum(a.elapsed_time(b) for a, b in v) / args.steps * 1000.0 for k, v in timers.items()}
-    per_launch = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) * 1000.0 for k, v in timers.items()}
+    # per-call device time: each call's own graph, replayed back to back
+    per_call, per_launch = {}, {}
+    reps = max(3, min(args.steps, 20))
+    for name, graphs in call_graphs.items():
+        tot = 0.0
+        for g_ in graphs:
+            if flush:
+                flush_buf.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g_.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1) / reps
+        per_call[name] = tot * 1000.0
+        per_launch[name] = tot * 1000.0 / len(graphs)
+    timers = {k: [None] * len(v) for k, v in call_graphs.items()}
 
     # ---- end to end: host buffers in, host buffers out, through the same calls
     pinned_in = {
@@ -278,7 +333,7 @@ def run_ours(args, rank, world):
     for _ in range(e2e_steps):
         for k, h in pinned_in.items():
             dev_of[k].copy_(h, non_blocking=True)
-        step.run(stream)
+        graph.replay()
         for l in gw.layers:
             pinned_out[l].copy_(step.out[l], non_blocking=True)
         stream.synchronize()
@@ -289,7 +344,7 @@ def run_ours(args, rank, world):
         torch.distributed.all_reduce(t_, op=torch.distributed.ReduceOp.MAX)
         ms, e2e_ms = float(t_[0]), float(t_[1])
     return dict(w=w, ms=ms, e2e_ms=e2e_ms, per_call=per_call, per_launch=per_launch, clocks=clocks,
-                h2d=h2d, d2h=d2h, launches=sum(KERNELS_PER_CALL[k] * len(v) for k, v in timers.items()) // args.steps)
+                h2d=h2d, d2h=d2h, launches=sum(KERNELS_PER_CALL[k] * len(v) for k, v in timers.items()))
 
 
 # ----------------------------------------------------------------------------

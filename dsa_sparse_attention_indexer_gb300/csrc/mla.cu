@@ -3,8 +3,9 @@
 //   S_hj = scale * <q_h, [c_j * s_j | r_j]>,  out_h = sum_j softmax_j(S_hj) c_j
 // over the selected positions j of each query row (j <= p).
 //
-// Work unit: (query row, split of its 2048 selected entries).  A CTA gathers the
-// valid entries of its split, streams them in tiles of 64 tokens (656-B rows
+// Work split: the T x 2048 (row, entry) slots are cut into one contiguous,
+// equal share per CTA (at least 256 slots each).  For each row piece in its
+// share a CTA gathers the valid entries, streams them in tiles of 64 tokens (656-B rows
 // copied with cp.async into a staging buffer while the previous tile computes),
 // dequantises each tile into fp16 (c * scale is exact in fp16 for scales in
 // [2^-15, 2^7]; the RoPE part converts from bf16), and runs
@@ -12,7 +13,9 @@
 //   O^T += V^T P^T   (M = 512 latent dims, N = 64 heads, K = 64 tokens)
 // on warp-level fp16 tensor-core MMAs with fp32 accumulation and an online
 // softmax in fp32 (P is rounded to fp16 for the second product).
-// Splits of one row are merged by a log-sum-exp combine kernel.
+// A row covered by several CTAs is merged by log-sum-exp: each piece writes a
+// partial (unnormalised O, max, sum) and the last CTA to finish the row (an
+// atomic counter per row) combines them.
 #include "dsa_internal.cuh"
 #include "indexer_common.cuh"
 
@@ -99,14 +102,24 @@ struct MlaArgs {
     const uint8_t* kv;          // latent cache
     BatchDev b;
     float scale_log2;           // softmax_scale * log2(e)
-    int nsplit;
-    void* out;                  // final output (nsplit == 1)
+    int64_t n_slots;            // T * 2048
+    int G;                      // CTAs sharing the slots
+    void* out;
     int out_f32;
     float* lse;
-    float* part_o;              // [T*nsplit, 64, 512] (nsplit > 1)
-    float* part_ml;             // [T*nsplit, 64, 2]
+    float* part_o;              // [2G, 64, 512]: a CTA's first / last row piece
+    float* part_ml;             // [2G, 64, 2]
+    int32_t* row_done;          // [T] pieces finished per row (zero on entry, reset to zero)
     int32_t* st;
 };
+
+__device__ __forceinline__ int64_t mla_cta_start(int64_t g, int64_t N, int64_t G) { return g * N / G; }
+__device__ __forceinline__ int64_t mla_cta_of(int64_t x, int64_t N, int64_t G) { return ((x + 1) * G + N - 1) / N - 1; }
+
+// Partial slot of CTA g's piece of row r: 2g for the CTA's first row, 2g+1 otherwise.
+__device__ __forceinline__ int64_t mla_slot(int64_t g, int64_t r, int64_t N, int64_t G) {
+    return 2 * g + ((mla_cta_start(g, N, G) / kTopK == r) ? 0 : 1);
+}
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
 sparse_mla_kernel(MlaArgs a) {
@@ -124,17 +137,22 @@ sparse_mla_kernel(MlaArgs a) {
     int* misc = reinterpret_cast<int*>(smem + kOffMisc);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t row = blockIdx.x / a.nsplit;
-    const int split = blockIdx.x % a.nsplit;
     const BatchDev& b = a.b;
+    const int64_t N = a.n_slots, G = a.G, g = blockIdx.x;
+    const int64_t e_begin = mla_cta_start(g, N, G), e_end = mla_cta_start(g + 1, N, G);
+    for (int64_t row = e_begin / kTopK; row * kTopK < e_end; ++row) {
+    const int64_t lo_e = max(e_begin, row * kTopK) - row * kTopK;
+    const int64_t hi_e = min(e_end, (row + 1) * kTopK) - row * kTopK;
+    const int64_t g0 = mla_cta_of(row * kTopK, N, G), g1 = mla_cta_of(row * kTopK + kTopK - 1, N, G);
     const int r = row_request(b.q_start, b.batch, row);
     const int qn = b.q_start[r + 1] - b.q_start[r];
     const int L = b.seq_len[r];
     const int p = L - qn + (int)(row - b.q_start[r]);
+    __syncthreads();                                   // shared state of the previous piece is free
 
-    // ---- 1. collect this split's valid entries (ordered) ------------------
-    const int chunk = kTopK / a.nsplit;
-    const int e0 = split * chunk;
+    // ---- 1. collect the piece's valid entries (ordered) ------------------
+    const int chunk = (int)(hi_e - lo_e);
+    const int e0 = (int)lo_e;
     int ntok = 0;
     for (int base = 0; base < chunk; base += kMlaThreads * 8) {
         int64_t sl[8];
@@ -207,7 +225,7 @@ sparse_mla_kernel(MlaArgs a) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) oacc[i][n][k] = 0.f;
 
-    const int g = lane >> 2, cq = lane & 3;
+    const int g8 = lane >> 2, cq = lane & 3;
     for (int tile = 0; tile < ntiles; ++tile) {
         const int n_in = min(kTile, ntok - tile * kTile);
         cp_async_wait_all();
@@ -279,7 +297,7 @@ sparse_mla_kernel(MlaArgs a) {
             }
         }
         // ---- online softmax over the tile (columns = heads) -----------------
-        const int tok0 = mt * 16 + g, tok1 = tok0 + 8;
+        const int tok0 = mt * 16 + g8, tok1 = tok0 + 8;
         const bool v0 = tok0 < n_in, v1 = tok1 < n_in;
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
@@ -293,7 +311,7 @@ sparse_mla_kernel(MlaArgs a) {
                 m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
                 m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
             }
-            if (g == 0) {
+            if (g8 == 0) {
                 red_max[mt * 64 + nh * 32 + n * 8 + 2 * cq] = m0;
                 red_max[mt * 64 + nh * 32 + n * 8 + 2 * cq + 1] = m1;
             }
@@ -325,7 +343,7 @@ sparse_mla_kernel(MlaArgs a) {
                 s0 += __shfl_xor_sync(0xffffffffu, s0, o);
                 s1 += __shfl_xor_sync(0xffffffffu, s1, o);
             }
-            if (g == 0) {
+            if (g8 == 0) {
                 red_sum[mt * 64 + h0] = s0;
                 red_sum[mt * 64 + h0 + 1] = s1;
             }
@@ -372,7 +390,7 @@ sparse_mla_kernel(MlaArgs a) {
 
     // ---- 3. write the result ---------------------------------------------
     __syncthreads();
-    if (a.nsplit == 1) {
+    if (g0 == g1) {
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
             const int h0 = n * 8 + 2 * cq;
@@ -380,7 +398,7 @@ sparse_mla_kernel(MlaArgs a) {
             const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int d0 = warp * 64 + i * 16 + g, d1 = d0 + 8;
+                const int d0 = warp * 64 + i * 16 + g8, d1 = d0 + 8;
                 const int64_t o00 = (row * 64 + h0) * 512, o01 = (row * 64 + h0 + 1) * 512;
                 const float v00 = oacc[i][n][0] * i0, v01 = oacc[i][n][1] * i1;
                 const float v10 = oacc[i][n][2] * i0, v11 = oacc[i][n][3] * i1;
@@ -398,15 +416,18 @@ sparse_mla_kernel(MlaArgs a) {
             const float l = l_run[tid];
             a.lse[row * 64 + tid] = l > 0.f ? (m_run[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
-    } else {
-        const int64_t unit = row * a.nsplit + split;
+        continue;
+    }
+    // several CTAs share the row: write this piece's partial
+    {
+        const int64_t unit = mla_slot(g, row, N, G);
         float* po = a.part_o + unit * 64 * 512;
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
             const int h0 = n * 8 + 2 * cq;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int d0 = warp * 64 + i * 16 + g, d1 = d0 + 8;
+                const int d0 = warp * 64 + i * 16 + g8, d1 = d0 + 8;
                 po[h0 * 512 + d0] = oacc[i][n][0];
                 po[(h0 + 1) * 512 + d0] = oacc[i][n][1];
                 po[h0 * 512 + d1] = oacc[i][n][2];
@@ -418,56 +439,75 @@ sparse_mla_kernel(MlaArgs a) {
             a.part_ml[(unit * 64 + tid) * 2 + 1] = l_run[tid];
         }
     }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) misc[8] = (atomicAdd(&a.row_done[row], 1) == (int)(g1 - g0)) ? 1 : 0;
+    __syncthreads();
+    if (misc[8]) {
+        // last piece of the row: combine all partials by log-sum-exp
+        __threadfence();
+        for (int h = warp; h < 64; h += 8) {
+            float M = -INFINITY;
+            for (int64_t gg = g0; gg <= g1; ++gg) {
+                const int64_t u = mla_slot(gg, row, N, G);
+                const float m = __ldcg(&a.part_ml[(u * 64 + h) * 2]), l = __ldcg(&a.part_ml[(u * 64 + h) * 2 + 1]);
+                if (l > 0.f) M = fmaxf(M, m);
+            }
+            float acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+            float Ltot = 0.f;
+            for (int64_t gg = g0; gg <= g1; ++gg) {
+                const int64_t u = mla_slot(gg, row, N, G);
+                const float m = __ldcg(&a.part_ml[(u * 64 + h) * 2]), l = __ldcg(&a.part_ml[(u * 64 + h) * 2 + 1]);
+                if (!(l > 0.f)) continue;
+                const float wgt = exp2f(m - M);
+                Ltot += wgt * l;
+                const float4* src = reinterpret_cast<const float4*>(a.part_o + (u * 64 + h) * 512) + lane;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 v = __ldcg(src + j * 32);
+                    acc[4 * j] += wgt * v.x; acc[4 * j + 1] += wgt * v.y;
+                    acc[4 * j + 2] += wgt * v.z; acc[4 * j + 3] += wgt * v.w;
+                }
+            }
+            const float inv = Ltot > 0.f ? 1.f / Ltot : 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t o = (row * 64 + h) * 512 + (lane + j * 32) * 4;
+                if (a.out_f32) {
+                    reinterpret_cast<float4*>(static_cast<float*>(a.out) + o)[0] =
+                        make_float4(acc[4 * j] * inv, acc[4 * j + 1] * inv, acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
+                } else {
+                    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + o;
+                    ob[0] = __float2bfloat16_rn(acc[4 * j] * inv); ob[1] = __float2bfloat16_rn(acc[4 * j + 1] * inv);
+                    ob[2] = __float2bfloat16_rn(acc[4 * j + 2] * inv); ob[3] = __float2bfloat16_rn(acc[4 * j + 3] * inv);
+                }
+            }
+            if (a.lse && lane == 0)
+                a.lse[row * 64 + h] = Ltot > 0.f ? (M + log2f(Ltot)) * 0.69314718055994531f : -INFINITY;
+        }
+        if (tid == 0) a.row_done[row] = 0;             // ready for the next call
+    }
+    }   // row pieces
 }
 
-// One CTA of 128 threads per (row, head): merge the splits by log-sum-exp.
-__global__ void __launch_bounds__(128)
-mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int nsplit,
-                   void* out, int out_f32, float* lse) {
-    const int64_t rh = blockIdx.x;            // row * 64 + head
-    const int64_t row = rh / 64;
-    const int h = (int)(rh % 64);
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) {
-        const float l = part_ml[((row * nsplit + s) * 64 + h) * 2 + 1];
-        if (l > 0.f) M = fmaxf(M, part_ml[((row * nsplit + s) * 64 + h) * 2]);
-    }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float Ltot = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-        const int64_t unit = row * nsplit + s;
-        const float m = part_ml[(unit * 64 + h) * 2], l = part_ml[(unit * 64 + h) * 2 + 1];
-        if (!(l > 0.f)) continue;
-        const float wgt = exp2f(m - M);
-        Ltot += wgt * l;
-        const float4 v = reinterpret_cast<const float4*>(part_o + (unit * 64 + h) * 512)[threadIdx.x];
-        acc[0] += wgt * v.x; acc[1] += wgt * v.y; acc[2] += wgt * v.z; acc[3] += wgt * v.w;
-    }
-    const float inv = Ltot > 0.f ? 1.f / Ltot : 0.f;
-    const int64_t o = rh * 512 + threadIdx.x * 4;
-    if (out_f32) {
-        reinterpret_cast<float4*>(static_cast<float*>(out) + o)[0] =
-            make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-    } else {
-        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out) + o;
-        ob[0] = __float2bfloat16_rn(acc[0] * inv); ob[1] = __float2bfloat16_rn(acc[1] * inv);
-        ob[2] = __float2bfloat16_rn(acc[2] * inv); ob[3] = __float2bfloat16_rn(acc[3] * inv);
-    }
-    if (lse && threadIdx.x == 0)
-        lse[rh] = Ltot > 0.f ? (M + log2f(Ltot)) * 0.69314718055994531f : -INFINITY;
+// CTAs sharing the T x 2048 slots: at most one per SM, and at least 256 slots
+// (four 64-token tiles) per CTA.
+inline int mla_ctas(int64_t total_q, int sms) {
+    const int64_t n = total_q * kTopK;
+    int64_t gcount = n / 256;
+    if (gcount < 1) gcount = 1;
+    if (gcount > sms) gcount = sms;
+    return (int)gcount;
 }
 
-// Splits per row: enough CTAs to cover the GPU twice, 64 to 2048 entries each.
-inline int mla_splits(int64_t total_q, bool decode, int sms) {
-    if (!decode) return 1;
-    int ns = 1;
-    while (ns < 32 && total_q * ns < 2 * (int64_t)sms) ns *= 2;
-    return ns;
-}
-
-inline size_t mla_ws_bytes(int64_t total_q, int nsplit) {
-    if (nsplit <= 1) return 0;
-    return (size_t)total_q * nsplit * 64 * (512 + 2) * sizeof(float);
+// Workspace: partials for two row pieces per CTA, their (max, sum), and the
+// per-row counters.
+inline size_t mla_ws_bytes(int64_t total_q, int G) {
+    size_t b = (size_t)2 * G * 64 * 512 * 4 + (size_t)2 * G * 64 * 2 * 4;
+    b = (b + 255) / 256 * 256;
+    return b + (size_t)total_q * 4;
 }
 
 int device_sm_count() {
@@ -506,10 +546,12 @@ dsa_status dsa::sparse_mla_launch(const void* q, const int32_t* topk, const dsa_
     }
     if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || !aligned16(topk)) return DSA_ERR_ALIGNMENT;
     if (b->total_q == 0) return DSA_OK;
-    const int nsplit = mla_splits(b->total_q, decode, device_sm_count());
-    if (ws_bytes < mla_ws_bytes(b->total_q, nsplit) || (nsplit > 1 && !ws)) return DSA_ERR_WORKSPACE_TOO_SMALL;
-    if (nsplit > 1 && !aligned16(ws)) return DSA_ERR_ALIGNMENT;
-    if (b->total_q * nsplit > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    (void)decode;
+    const int G = mla_ctas(b->total_q, device_sm_count());
+    if (!ws) return DSA_ERR_INVALID_ARGUMENT;
+    if (ws_bytes < mla_ws_bytes(b->total_q, G)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(ws)) return DSA_ERR_ALIGNMENT;
+    if (b->total_q > 0x3fffffffLL / 2048) return DSA_ERR_UNSUPPORTED;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmem) !=
@@ -523,21 +565,20 @@ dsa_status dsa::sparse_mla_launch(const void* q, const int32_t* topk, const dsa_
     a.kv = kv;
     a.b = to_dev(b);
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
-    a.nsplit = nsplit;
+    a.n_slots = b->total_q * kTopK;
+    a.G = G;
     a.out = out;
     a.out_f32 = out_dtype == DSA_DTYPE_F32;
     a.lse = lse;
-    a.part_o = nsplit > 1 ? static_cast<float*>(ws) : nullptr;
-    a.part_ml = nsplit > 1 ? static_cast<float*>(ws) + (size_t)b->total_q * nsplit * 64 * 512 : nullptr;
+    a.part_o = static_cast<float*>(ws);
+    a.part_ml = a.part_o + (size_t)2 * G * 64 * 512;
+    const size_t cnt_off = ((size_t)2 * G * 64 * 512 * 4 + (size_t)2 * G * 64 * 2 * 4 + 255) / 256 * 256;
+    a.row_done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + cnt_off);
     a.st = st;
     cudaStream_t s = as_stream(stream);
-    sparse_mla_kernel<<<(unsigned)(b->total_q * nsplit), kMlaThreads, kMlaSmem, s>>>(a);
+    if (cudaMemsetAsync(a.row_done, 0, (size_t)b->total_q * 4, s) != cudaSuccess) return DSA_ERR_CUDA;
+    sparse_mla_kernel<<<(unsigned)G, kMlaThreads, kMlaSmem, s>>>(a);
     DSA_CHECK_LAUNCH();
-    if (nsplit > 1) {
-        mla_combine_kernel<<<(unsigned)(b->total_q * 64), 128, 0, s>>>(a.part_o, a.part_ml, nsplit, out,
-                                                                       a.out_f32, lse);
-        DSA_CHECK_LAUNCH();
-    }
     return DSA_OK;
 }
 
@@ -545,8 +586,8 @@ extern "C" dsa_status dsa_sparse_mla_workspace_size(const dsa_batch* b, size_t* 
     dsa_status vs = validate_batch(b);
     if (vs != DSA_OK) return vs;
     if (!bytes) return DSA_ERR_INVALID_ARGUMENT;
-    // Enough for the decode split count on any GPU of up to 1024 SMs.
-    *bytes = mla_ws_bytes(b->total_q, mla_splits(b->total_q, true, 1024));
+    // Enough for any GPU of up to 1024 SMs.
+    *bytes = mla_ws_bytes(b->total_q, mla_ctas(b->total_q, 1024));
     return DSA_OK;
 }
 
