@@ -1,0 +1,776 @@
+// Sparse MLA on the 5th-generation tensor cores ("vLLM 推理链路概览", Sparse
+// MLA Attention; "GLM-5.3 推理全链路(一)", decode: MQA 形态与吸收):
+//   S_hj = scale * <q_h, [c_j * s_j | r_j]>,  out_h = sum_j softmax_j(S_hj) c_j
+// over the selected positions j of each query row (j <= p), 64 heads of 576
+// dims, 512-d latent output per head.
+//
+// Work split: the T x 2048 (row, entry) slots are cut into one contiguous,
+// equal share per CTA; a row covered by several CTAs is merged by
+// log-sum-exp (partials + last-CTA combine through a per-row counter).
+//
+// Per CTA, per tile of 96 selected tokens (the M = 128 MMA rows 96..127 are
+// padding), in transposed form so that tokens are the MMA rows:
+//   S^T = K Q^T      tcgen05.mma kind::f16, M=128 tokens, N=64 heads, K=576,
+//                    A = fp16 KV tile (K-major), B = Q (K-major), D in TMEM;
+//   O^T += V^T P^T   M = 4 x 128 latent dims, N = 64 heads, K = 96 tokens,
+//                    A = the same KV tile read MN-major, B = P^T (MN-major),
+//                    D = 256 TMEM columns that stay resident for the row piece.
+// Shared memory holds one fp16 KV tile (110.6 KB) next to the fp16 Q of the
+// row (73.7 KB), so tiles cannot be double-buffered.  Instead the tile is
+// recycled group by group: its five 128-byte column groups (latent dims
+// 128g..128g+127 for g < 4, the RoPE dims for g = 4) are released by
+// separate MMA commits (the RoPE group when S^T is done, group g when the
+// P.V MMAs of latent block g are done) and the next tile's group is written
+// as soon as its predecessor is released, so dequantisation overlaps the
+// tensor pipe and the next S^T starts right behind the last P.V.
+// Warp roles (512 threads):
+//   warps 0-7   softmax: each thread owns one token (TMEM lane) and 32 of the
+//               64 heads; per-head max and sum by a transposing warp
+//               reduction, online softmax with lazy rescaling (O^T in TMEM is
+//               rescaled only when a head's max grows by more than 2^8), P
+//               written as fp16 P^T rows.  Thread 0 also issues the MMAs and
+//               warp 0 owns the TMEM allocation.
+//   warps 8-15  loaders: build the row piece's list of cache slots, convert
+//               Q to fp16, and gather each tile's 656-B latent rows into
+//               registers one tile ahead (all 18 16-byte pieces of a lane in
+//               flight at once), then dequantise group by group into the
+//               128-byte-swizzled fp16 tile (c * scale is exact in fp16 for
+//               scales in [2^-15, 2^7]; the RoPE dims convert from bf16).
+// Every wait is time-bounded; a timeout is recorded and the CTA winds down.
+#include "dsa_internal.cuh"
+#include "indexer_common.cuh"
+#include "sm100.cuh"
+
+namespace dsa {
+namespace mtc {
+
+using namespace sm100;
+
+constexpr int kTok = 96;                                   // tokens per tile
+constexpr int kBlk = kTok * 128;                           // one 64-dim K-block of the KV tile
+constexpr int kSoftWarps = 8;                              // two per TMEM lane quarter, 32 heads each
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kLoadWarp0 = kSoftWarps;
+constexpr int kLoadWarps = 8;
+constexpr int kThreads = (kSoftWarps + kLoadWarps) * 32;
+constexpr int kLoadThreads = kLoadWarps * 32;
+constexpr int kTokPerLoadWarp = kTok / kLoadWarps;         // 12: four tokens per step, three steps
+constexpr int kSoftBar = 1;
+constexpr int kLoadBar = 2;
+constexpr float kTau = 8.0f;                               // lazy-rescale threshold, log2 units
+constexpr int kMaxPieces = 64;
+constexpr int kMaxParts = 16;                              // CTAs one row can span (shares >= 256 slots: <= 10)
+constexpr uint32_t kIdescQK = idesc_f16_f32(128, 64, false, false);
+constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, true, true);
+constexpr uint32_t kColS = 0;                              // TMEM: S^T [128 x 64]
+constexpr uint32_t kColO = 64;                             // TMEM: O^T 4 x [128 x 64]
+
+constexpr int kOffKV = 0;                                  // 9 K-blocks of [96 tokens x 128 B]
+constexpr int kOffQ = kOffKV + 9 * kBlk;                   // 9 K-blocks of [64 heads x 128 B]
+constexpr int kOffP = kOffQ + 9 * 8192;                    // P^T: 96 token rows x 64 heads fp16
+constexpr int kOffSlots = kOffP + kTok * 128;              // int32 cache slots of the row piece
+constexpr int kOffRed = kOffSlots + 2048 * 4;              // [2][4 lane quarters][64 heads] fp32
+constexpr int kOffStat = kOffRed + 2 * 4 * 64 * 4;         // m_ref, l_acc, alpha [64]
+constexpr int kOffBars = kOffStat + 3 * 64 * 4;
+constexpr int kOffMisc = kOffBars + 16 * 8;
+constexpr int kSmemUsed = kOffMisc + 512;
+constexpr int kSmemAlloc = kSmemUsed + 1024;
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kBlk % 1024 == 0, "swizzle atoms need 1 KB alignment");
+// S^T rows 96..127 read 32 rows past each K-block: still inside the tile / Q.
+static_assert(8 * kBlk + 128 * 128 <= kOffQ + 9 * 8192, "padding rows stay in shared memory");
+
+enum { B_QFULL = 0, B_QEMPTY, B_FULL0, B_FULL4 = B_FULL0 + 4, B_SFULL, B_PV0, B_PV3 = B_PV0 + 3, B_DRAIN, B_COUNT };
+static_assert(B_COUNT <= 16, "barrier block");
+
+struct Misc {
+    uint32_t tmem_base;
+    int32_t abort;
+    int32_t last;
+    int32_t scratch[8];
+    int32_t ntok[kMaxPieces];
+};
+static_assert(sizeof(Misc) <= 512, "misc block");
+
+struct Args {
+    const uint16_t* q;          // [T,64,576] bf16
+    const int32_t* topk;        // [T,2048]
+    const uint8_t* kv;          // latent cache
+    BatchDev b;
+    float scale_log2;
+    int64_t n_slots;            // T * 2048
+    int G;
+    void* out;
+    int out_f32;
+    float* lse;
+    float* part_o;              // [2G, 64, 512]
+    float* part_ml;             // [2G, 64, 2]
+    int32_t* row_done;          // [T]
+    int32_t* st;
+};
+
+__device__ __forceinline__ int64_t cta_start(int64_t g, int64_t N, int64_t G) { return g * N / G; }
+__device__ __forceinline__ int64_t cta_of(int64_t x, int64_t N, int64_t G) { return ((x + 1) * G + N - 1) / N - 1; }
+__device__ __forceinline__ int64_t slot_of(int64_t g, int64_t r, int64_t N, int64_t G) {
+    return 2 * g + ((cta_start(g, N, G) / kTopK == r) ? 0 : 1);
+}
+
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync %0, %1;" ::"n"(kSoftBar), "n"(kSoftThreads) : "memory"); }
+__device__ __forceinline__ void load_sync() { asm volatile("bar.sync %0, %1;" ::"n"(kLoadBar), "n"(kLoadThreads) : "memory"); }
+__device__ __forceinline__ bool soft_any(bool pred) {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+                 " selp.u32 %0, 1, 0, q;\n}"
+                 : "=r"(r) : "r"((uint32_t)pred), "n"(kSoftBar), "n"(kSoftThreads) : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool load_any(bool pred) {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+                 " selp.u32 %0, 1, 0, q;\n}"
+                 : "=r"(r) : "r"((uint32_t)pred), "n"(kLoadBar), "n"(kLoadThreads) : "memory");
+    return r != 0;
+}
+
+// mbarrier wait that also gives up when another role has set the abort flag.
+__device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, const volatile int32_t* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u && (*abort_flag || globaltimer_ns() - t0 > 2000000000ull)) return false;
+    }
+}
+
+// 16-byte read-only load that stays where it is written (a prefetch a tile
+// ahead must not be sunk to its first use).
+__device__ __forceinline__ uint4 ldg_pinned(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t e4m3x2_scaled_h2(uint32_t two, __half2 sc2) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);   // exact
+    const __half2 p = __hmul2(*reinterpret_cast<__half2*>(&h), sc2);                     // * 2^e: exact
+    return *reinterpret_cast<const uint32_t*>(&p);
+}
+__device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t w) {
+    return pack_h2(bf16_bits_to_f32(w & 0xffffu), bf16_bits_to_f32(w >> 16));
+}
+
+// Reduce 32 values across the 32 lanes of a warp: afterwards lane l holds the
+// result for index l in v[0] (31 shuffles instead of 160).
+template <bool kMax>
+__device__ __forceinline__ void xreduce32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16, n = 16; s >= 1; s >>= 1, n >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float send = up ? v[i] : v[i + n];
+            const float keep = up ? v[i + n] : v[i];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+            v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+}
+
+// S^T += K-blocks [B0, B0 + NB) of the KV tile x the same blocks of Q, four
+// K = 16 steps per 64-dim block; the first MMA of a tile overwrites.
+template <int B0, int NB>
+__device__ __forceinline__ void qk_blocks(uint32_t d_tmem, uint64_t d_kv, uint64_t d_q, bool first) {
+#pragma unroll
+    for (int bk = B0; bk < B0 + NB; ++bk)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_f16(d_tmem, d_kv + (uint64_t)((bk * kBlk + kk * 32) >> 4), d_q + (uint64_t)((bk * 8192 + kk * 32) >> 4),
+                    kIdescQK, (first && bk == B0 && kk == 0) ? 0u : 1u);
+}
+// O^T rows of latent block MB (dims 128 MB ..) += V^T P^T over the tile's six
+// 16-token steps, then a commit that releases the block's KV group.
+template <int MB>
+__device__ __forceinline__ void pv_block(uint32_t o_tmem, uint64_t d_v, uint64_t d_p, bool acc0, uint64_t* bar) {
+#pragma unroll
+    for (int kt = 0; kt < kTok / 16; ++kt)
+        mma_f16(o_tmem + MB * 64, d_v + (uint64_t)((2 * MB * kBlk + kt * 2048) >> 4), d_p + (uint64_t)((kt * 2048) >> 4),
+                kIdescPV, (acc0 || kt > 0) ? 1u : 0u);
+    mma_commit(bar);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_mla_tc_kernel(Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+    Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
+    int32_t* slots = reinterpret_cast<int32_t*>(smem + kOffSlots);
+    float* red = reinterpret_cast<float*>(smem + kOffRed);
+    float* m_ref = reinterpret_cast<float*>(smem + kOffStat);
+    float* l_acc = m_ref + 64;
+    float* alpha = l_acc + 64;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const BatchDev& b = a.b;
+    const int64_t N = a.n_slots, G = a.G, g = blockIdx.x;
+    const int64_t e_begin = cta_start(g, N, G), e_end = cta_start(g + 1, N, G);
+    volatile int32_t* abort_flag = &misc->abort;
+
+    if (tid == 0) {
+        mbar_init(&bars[B_QFULL], kLoadWarps);
+        mbar_init(&bars[B_QEMPTY], kSoftWarps);
+        for (int i = 0; i < 5; ++i) mbar_init(&bars[B_FULL0 + i], kLoadWarps);
+        mbar_init(&bars[B_SFULL], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[B_PV0 + i], 1);
+        mbar_init(&bars[B_DRAIN], 1);
+        misc->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&misc->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc->tmem_base;
+
+    auto timeout = [&](int where) {
+        record_error(a.st, DSA_DEVERR_TIMEOUT, where);
+        *abort_flag = 1;
+    };
+
+    if (warp >= kLoadWarp0) {
+        // ================================================================ loaders
+        const int lt = tid - kLoadWarp0 * 32;            // 0..255
+        const int lw = lt >> 5;                            // 0..7
+        const int c8 = lane & 7;                           // 16-byte piece of a 128-byte group
+        int64_t gt = 0;                                    // tiles dequantised so far by this CTA
+        int k = 0;
+        uint4 raw[4][3], rope[3], scv[3];                  // [group][step]: the next tile, in flight
+        bool ok = true;
+        for (int64_t row = e_begin / kTopK; row * kTopK < e_end; ++row, ++k) {
+            if (load_any(!ok || *abort_flag)) break;      // one decision for all loader warps
+            const int64_t lo_e = max(e_begin, row * kTopK) - row * kTopK;
+            const int64_t hi_e = min(e_end, (row + 1) * kTopK) - row * kTopK;
+            const int r = row_request(b.q_start, b.batch, row);
+            const int qn = b.q_start[r + 1] - b.q_start[r];
+            const int L = b.seq_len[r];
+            const int p = L - qn + (int)(row - b.q_start[r]);
+            // ---- valid entries of the piece -> cache slots, in order
+            int ntok = 0;
+            for (int base = (int)lo_e; base < (int)hi_e; base += kLoadThreads * 8) {
+                int32_t sl[8];
+                int cnt = 0;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int e = base + lt * 8 + u;
+                    sl[u] = -1;
+                    if (e < (int)hi_e) {
+                        const int j = a.topk[row * kTopK + e];
+                        if (j >= 0 && j <= p) {
+                            if (j >= L || j / kPage >= b.max_pages) {
+                                record_error(a.st, DSA_DEVERR_INDEX_RANGE, j);
+                            } else {
+                                const int64_t pg = b.page_table[(int64_t)r * b.max_pages + j / kPage];
+                                if (pg < 0 || pg >= b.num_pages) record_error(a.st, DSA_DEVERR_PAGE_RANGE, pg);
+                                else sl[u] = (int32_t)(pg * kPage + (j % kPage));
+                            }
+                        }
+                    }
+                    cnt += sl[u] >= 0;
+                }
+                int x = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (lane == 31) misc->scratch[lw] = x;
+                load_sync();
+                int off = ntok + x - cnt, tot = 0;
+                for (int v = 0; v < kLoadWarps; ++v) {
+                    if (v < lw) off += misc->scratch[v];
+                    tot += misc->scratch[v];
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (sl[u] >= 0) slots[off++] = sl[u];
+                ntok += tot;
+                load_sync();
+            }
+            const int ntiles = (ntok + kTok - 1) / kTok;
+            // ---- gather of tile t into registers: step i covers tokens
+            //      12 lw + 4 i + lane / 8, lane % 8 picks the 16-byte piece of each group
+            // Part `what` of the gather of tile t into registers: 0..3 = latent group,
+            // 4 = RoPE dims, 5 = scales.  Each part of tile t + 1 is issued as soon as the
+            // same part of tile t has been consumed, so every load has a whole tile
+            // period to arrive.
+            auto prefetch = [&](int t, int what) {
+                const int n_in = min(kTok, ntok - t * kTok);
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    const int tk = lw * kTokPerLoadWarp + 4 * i + (lane >> 3);
+                    if (tk < n_in) {
+                        const int32_t sl = slots[t * kTok + tk];
+                        const uint4* rowp = reinterpret_cast<const uint4*>(
+                            a.kv + (int64_t)(sl >> 6) * kKvPageBytes + (sl & 63) * kKvTokenBytes);
+                        if (what == 0) raw[0][i] = ldg_pinned(rowp + 0 * 8 + c8);
+                        if (what == 1) raw[1][i] = ldg_pinned(rowp + 1 * 8 + c8);
+                        if (what == 2) raw[2][i] = ldg_pinned(rowp + 2 * 8 + c8);
+                        if (what == 3) raw[3][i] = ldg_pinned(rowp + 3 * 8 + c8);
+                        if (what == 4) rope[i] = ldg_pinned(rowp + 33 + c8);
+                        if (what == 5) scv[i] = ldg_pinned(rowp + 32);
+                    } else {                               // no token: zero row (P is 0 there, V must be finite)
+                        if (what == 0) raw[0][i] = make_uint4(0, 0, 0, 0);
+                        if (what == 1) raw[1][i] = make_uint4(0, 0, 0, 0);
+                        if (what == 2) raw[2][i] = make_uint4(0, 0, 0, 0);
+                        if (what == 3) raw[3][i] = make_uint4(0, 0, 0, 0);
+                        if (what == 4) rope[i] = make_uint4(0, 0, 0, 0);
+                        if (what == 5) scv[i] = make_uint4(0x3f800000u, 0x3f800000u, 0x3f800000u, 0x3f800000u);
+                    }
+                }
+            };
+            if (ntiles > 0) {
+                prefetch(0, 4);
+                prefetch(0, 5);
+                prefetch(0, 0);
+                prefetch(0, 1);
+                prefetch(0, 2);
+                prefetch(0, 3);
+            }
+            // ---- Q of the row, once the softmax group has taken the previous piece
+            //      (so QFULL never runs two phases ahead) and its last S^T MMA is done
+            if (k > 0) ok = wait_ab(&bars[B_QEMPTY], (uint32_t)((k - 1) & 1), abort_flag);
+            if (ok && gt > 0) ok = wait_ab(&bars[B_SFULL], (uint32_t)((gt - 1) & 1), abort_flag);
+            if (!ok) {
+                if (lane == 0) timeout(11);
+                continue;                                  // the decision is taken at the loop top
+            }
+            const uint16_t* qrow = a.q + row * (64 * 576);
+#pragma unroll 1
+            for (int c0 = lt; c0 < 64 * 72; c0 += 6 * kLoadThreads) {   // 18 pieces per thread, 6 in flight
+                uint4 qv[6];
+#pragma unroll
+                for (int u = 0; u < 6; ++u) {
+                    const int c = c0 + u * kLoadThreads;
+                    qv[u] = c < 64 * 72 ? __ldg(reinterpret_cast<const uint4*>(qrow) + c) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 6; ++u) {
+                    const int c = c0 + u * kLoadThreads;
+                    if (c >= 64 * 72) continue;
+                    const int h = c / 72, cq = c % 72;
+                    const int blk = cq >> 3, ch = cq & 7;
+                    *reinterpret_cast<uint4*>(smem + kOffQ + blk * 8192 + h * 128 + ((ch ^ (h & 7)) * 16)) =
+                        make_uint4(bf16x2_to_h2(qv[u].x), bf16x2_to_h2(qv[u].y), bf16x2_to_h2(qv[u].z),
+                                   bf16x2_to_h2(qv[u].w));
+                }
+            }
+            if (lt == 0) misc->ntok[k % kMaxPieces] = ntok;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_QFULL]);
+            // ---- tiles: RoPE group first (free once S^T of the previous tile is done), then
+            //      latent groups 0..3 (free once that tile's P.V of block g is done)
+            for (int t = 0; t < ntiles && ok; ++t, ++gt) {
+                const uint32_t ph = (uint32_t)((gt - 1) & 1);
+                uint32_t bad_scale = 0;
+                if (gt > 0 && !(ok = wait_ab(&bars[B_SFULL], ph, abort_flag))) break;
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    const int tk = lw * kTokPerLoadWarp + 4 * i + (lane >> 3);
+                    *reinterpret_cast<uint4*>(smem + kOffKV + 8 * kBlk + tk * 128 + ((c8 ^ (tk & 7)) * 16)) =
+                        make_uint4(bf16x2_to_h2(rope[i].x), bf16x2_to_h2(rope[i].y), bf16x2_to_h2(rope[i].z),
+                                   bf16x2_to_h2(rope[i].w));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_FULL4]);
+                const bool more = t + 1 < ntiles;
+                if (more) prefetch(t + 1, 4);
+#pragma unroll
+                for (int gg = 0; gg < 4; ++gg) {
+                    if (gt > 0 && !(ok = wait_ab(&bars[B_PV0 + gg], ph, abort_flag))) break;
+#pragma unroll
+                    for (int i = 0; i < 3; ++i) {
+                        const int tk = lw * kTokPerLoadWarp + 4 * i + (lane >> 3);
+                        const uint32_t scb = gg == 0 ? scv[i].x : gg == 1 ? scv[i].y : gg == 2 ? scv[i].z : scv[i].w;
+                        const float sc = __uint_as_float(scb);
+                        bad_scale |= (sc < 0x1p-15f || sc > 0x1p7f) ? 1u : 0u;
+                        const __half2 sc2 = __float2half2_rn(sc);           // a power of two: exact
+                        const uint4 w = raw[gg][i];
+                        // 16 FP8 dims 128 gg + 16 c8 .. -> K-block 2 gg + c8 / 4, 16-byte chunks 2 (c8 % 4), +1
+                        uint8_t* blkp = smem + kOffKV + (2 * gg + (c8 >> 2)) * kBlk + tk * 128;
+                        const int ch = 2 * (c8 & 3), sw = tk & 7;
+                        *reinterpret_cast<uint4*>(blkp + ((ch ^ sw) * 16)) =
+                            make_uint4(e4m3x2_scaled_h2(w.x & 0xffffu, sc2), e4m3x2_scaled_h2(w.x >> 16, sc2),
+                                       e4m3x2_scaled_h2(w.y & 0xffffu, sc2), e4m3x2_scaled_h2(w.y >> 16, sc2));
+                        *reinterpret_cast<uint4*>(blkp + (((ch + 1) ^ sw) * 16)) =
+                            make_uint4(e4m3x2_scaled_h2(w.z & 0xffffu, sc2), e4m3x2_scaled_h2(w.z >> 16, sc2),
+                                       e4m3x2_scaled_h2(w.w & 0xffffu, sc2), e4m3x2_scaled_h2(w.w >> 16, sc2));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[B_FULL0 + gg]);
+                    if (more) prefetch(t + 1, gg);
+                }
+                if (!ok) break;
+                if (bad_scale) record_error(a.st, DSA_DEVERR_FP16_RANGE, lane);
+                if (more) prefetch(t + 1, 5);
+            }
+            if (!ok && lane == 0) timeout(12);
+        }
+    } else {
+        // ================================================================ softmax + MMA issue + epilogue
+        // Warp w reads TMEM lane quarter w % 4 (token / latent row st) and
+        // heads [32 hh, 32 hh + 32), hh = w / 4.
+        const int q4 = warp & 3, hh = warp >> 2;
+        const int st = q4 * 32 + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
+        const uint32_t kv0 = smem_addr(smem + kOffKV), q0 = smem_addr(smem + kOffQ), p0 = smem_addr(smem + kOffP);
+        bool issued = false;
+        // Shared-memory descriptors of the operand bases; an MMA's descriptor is
+        // base + offset / 16 with a compile-time offset, so the issuing thread
+        // spends a few instructions per MMA (a dependent descriptor computation
+        // per MMA would make the issuer, not the tensor pipe, the bottleneck).
+        const uint64_t d_kv = desc_kmajor_sw128(kv0), d_q = desc_kmajor_sw128(q0);
+        const uint64_t d_v = desc_mnmajor_sw128(kv0, kBlk), d_p = desc_mnmajor_sw128(p0, 8192);
+        // S^T of tile gt_ (thread 0): groups in the order the loaders release them
+        auto issue_qk = [&](int64_t gt_) -> bool {
+            const uint32_t ph = (uint32_t)(gt_ & 1);
+            if (!wait_ab(&bars[B_FULL4], ph, abort_flag)) return false;
+            tc_fence_after();
+            qk_blocks<8, 1>(tmem + kColS, d_kv, d_q, true);
+            if (!wait_ab(&bars[B_FULL0], ph, abort_flag)) return false;
+            tc_fence_after();
+            qk_blocks<0, 2>(tmem + kColS, d_kv, d_q, false);
+            if (!wait_ab(&bars[B_FULL0 + 1], ph, abort_flag)) return false;
+            tc_fence_after();
+            qk_blocks<2, 2>(tmem + kColS, d_kv, d_q, false);
+            if (!wait_ab(&bars[B_FULL0 + 2], ph, abort_flag)) return false;
+            tc_fence_after();
+            qk_blocks<4, 2>(tmem + kColS, d_kv, d_q, false);
+            if (!wait_ab(&bars[B_FULL0 + 3], ph, abort_flag)) return false;
+            tc_fence_after();
+            qk_blocks<6, 2>(tmem + kColS, d_kv, d_q, false);
+            mma_commit(&bars[B_SFULL]);
+            issued = true;
+            return true;
+        };
+        // O^T += V^T P^T of a tile (thread 0); block g's commit releases KV group g
+        auto issue_pv = [&](bool acc0) {
+            tc_fence_after();
+            pv_block<0>(tmem + kColO, d_v, d_p, acc0, &bars[B_PV0]);
+            pv_block<1>(tmem + kColO, d_v, d_p, acc0, &bars[B_PV0 + 1]);
+            pv_block<2>(tmem + kColO, d_v, d_p, acc0, &bars[B_PV0 + 2]);
+            pv_block<3>(tmem + kColO, d_v, d_p, acc0, &bars[B_PV0 + 3]);
+        };
+        int64_t gt = 0;
+        int k = 0;
+        for (int64_t row = e_begin / kTopK; row * kTopK < e_end; ++row, ++k) {
+            int ok = mbar_wait(&bars[B_QFULL], (uint32_t)(k & 1)) ? 1 : 0;
+            if (soft_any(!ok || *abort_flag)) {
+                if (tid == 0 && !ok) timeout(31);
+                break;
+            }
+            const int ntok = misc->ntok[k % kMaxPieces];
+            const int ntiles = (ntok + kTok - 1) / kTok;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_QEMPTY]);
+            if (tid < 64) {
+                m_ref[tid] = -INFINITY;
+                l_acc[tid] = 0.f;
+            }
+            if (tid == 0 && ntiles > 0 && !issue_qk(gt)) timeout(34);
+            soft_sync();
+            bool failed = false;
+            for (int t = 0; t < ntiles; ++t, ++gt) {
+                ok = wait_ab(&bars[B_SFULL], (uint32_t)(gt & 1), abort_flag) ? 1 : 0;
+                if (soft_any(!ok)) { failed = true; break; }
+                const int n_in = min(kTok, ntok - t * kTok);
+                const bool valid = st < n_in;
+                // S^T row of this token for the warp's 32 heads, in log2 units; absent tokens -> -inf
+                auto load_s = [&](float (&v)[32]) {
+                    uint32_t u[32];
+                    tmem_ld_32x32b_x32(lane_addr + kColS + hh * 32, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) v[h] = valid ? __uint_as_float(u[h]) * a.scale_log2 : -INFINITY;
+                };
+                float v[32];
+                tc_fence_after();
+                load_s(v);
+                // ---- per-head tile max, lazy rescale decision
+                xreduce32<true>(v, lane);
+                red[q4 * 64 + hh * 32 + lane] = v[0];
+                soft_sync();
+                bool need = false;
+                if (tid < 64) {
+                    const float tm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+                    const float mo = m_ref[tid];
+                    need = (tm > mo + kTau) || (mo == -INFINITY && tm > -INFINITY);
+                    alpha[tid] = need ? (mo == -INFINITY ? 0.f : exp2f(mo - tm)) : 1.f;
+                    if (need) {
+                        m_ref[tid] = tm;
+                        l_acc[tid] *= alpha[tid];
+                    }
+                }
+                // S^T of tile gt is complete, and it was issued after the P.V of tile gt - 1:
+                // O^T is stable and P^T is free.
+                const bool resc = soft_any(need);
+                if (resc && t > 0) {                        // rescale the resident O^T columns of these heads
+#pragma unroll 1
+                    for (int mb = 0; mb < 4; ++mb) {
+                        uint32_t o[32];
+                        const uint32_t addr = lane_addr + kColO + mb * 64 + hh * 32;
+                        tmem_ld_32x32b_x32(addr, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[hh * 32 + c]);
+                        tmem_st_32x32b_x32(addr, o);
+                    }
+                    tmem_st_wait();
+                }
+                // ---- probabilities (S reloaded from TMEM) and their per-head sums
+                load_s(v);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float mr = m_ref[hh * 32 + c];
+                    v[c] = (v[c] == -INFINITY) ? 0.f : exp2f(v[c] - mr);
+                }
+                // ---- P^T row of this token: heads 32 hh.. as fp16, MN-major 128-byte swizzle
+                if (st < kTok) {
+                    uint8_t* prow = smem + kOffP + st * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = hh * 4 + cc;
+                        *reinterpret_cast<uint4*>(prow + ((c ^ (st & 7)) * 16)) =
+                            make_uint4(pack_h2(v[8 * cc], v[8 * cc + 1]), pack_h2(v[8 * cc + 2], v[8 * cc + 3]),
+                                       pack_h2(v[8 * cc + 4], v[8 * cc + 5]), pack_h2(v[8 * cc + 6], v[8 * cc + 7]));
+                    }
+                }
+                xreduce32<false>(v, lane);
+                red[256 + q4 * 64 + hh * 32 + lane] = v[0];
+                fence_proxy_async_smem();
+                tc_fence_before();
+                soft_sync();                                // P^T written, S^T and O^T reads / writes done
+                if (tid < 64) l_acc[tid] += red[256 + tid] + red[320 + tid] + red[384 + tid] + red[448 + tid];
+                if (tid == 0) {
+                    issue_pv(t > 0);
+                    if (t + 1 < ntiles && !issue_qk(gt + 1)) timeout(35);
+                }
+            }
+            if (failed) {
+                if (tid == 0) timeout(32);
+                break;
+            }
+            // ---- piece end: O^T is final once the last P.V completes
+            if (ntiles > 0) {
+                ok = wait_ab(&bars[B_PV3], (uint32_t)((gt - 1) & 1), abort_flag) ? 1 : 0;
+                if (soft_any(!ok)) {
+                    if (tid == 0) timeout(33);
+                    break;
+                }
+                tc_fence_after();
+            }
+            const int64_t g0 = cta_of(row * kTopK, N, G), g1 = cta_of(row * kTopK + kTopK - 1, N, G);
+            const bool whole = g0 == g1;
+            const int64_t unit = whole ? 0 : slot_of(g, row, N, G);
+#pragma unroll 1
+            for (int mb = 0; mb < 4; ++mb) {
+                uint32_t o[32];
+                if (ntiles > 0) {
+                    tmem_ld_32x32b_x32(lane_addr + kColO + mb * 64 + hh * 32, o);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = 0u;
+                }
+                const int d = mb * 128 + st;                           // latent dim of this TMEM lane
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {                         // a warp stores 32 consecutive dims
+                    const int h = hh * 32 + c;
+                    const float ov = __uint_as_float(o[c]);
+                    if (whole) {
+                        const float l = l_acc[h];
+                        const float val = l > 0.f ? ov / l : 0.f;
+                        const int64_t oi = (row * 64 + h) * 512 + d;
+                        if (a.out_f32) static_cast<float*>(a.out)[oi] = val;
+                        else static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(val);
+                    } else {
+                        a.part_o[(unit * 64 + h) * 512 + d] = ov;
+                    }
+                }
+            }
+            tc_fence_before();
+            if (whole) {
+                if (a.lse && tid < 64) {
+                    const float l = l_acc[tid];
+                    a.lse[row * 64 + tid] = l > 0.f ? (m_ref[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                }
+            } else {
+                if (tid < 64) {
+                    a.part_ml[(unit * 64 + tid) * 2] = m_ref[tid];
+                    a.part_ml[(unit * 64 + tid) * 2 + 1] = l_acc[tid];
+                }
+                __threadfence();
+                soft_sync();
+                if (tid == 0) misc->last = (atomicAdd(&a.row_done[row], 1) == (int)(g1 - g0)) ? 1 : 0;
+                soft_sync();
+                if (misc->last) {
+                    // last piece of the row: log-sum-exp combine of the row's np partials.
+                    // P^T is free here (the next P.V waits for this group): it holds the
+                    // per-partial weights and units.
+                    __threadfence();
+                    const int np = (int)(g1 - g0 + 1);
+                    float* wsm = reinterpret_cast<float*>(smem + kOffP);            // [kMaxParts][64]
+                    float* inv_s = wsm + kMaxParts * 64;                            // [64]
+                    int64_t* usm = reinterpret_cast<int64_t*>(inv_s + 64);          // [kMaxParts]
+                    if (tid < kMaxParts) usm[tid] = tid < np ? slot_of(g0 + tid, row, N, G) : 0;
+                    soft_sync();
+                    if (tid < 64) {
+                        float mm[kMaxParts], ll[kMaxParts];
+#pragma unroll
+                        for (int q = 0; q < kMaxParts; ++q) {
+                            mm[q] = -INFINITY;
+                            ll[q] = 0.f;
+                            if (q < np) {
+                                mm[q] = __ldcg(&a.part_ml[(usm[q] * 64 + tid) * 2]);
+                                ll[q] = __ldcg(&a.part_ml[(usm[q] * 64 + tid) * 2 + 1]);
+                            }
+                        }
+                        float M = -INFINITY;
+#pragma unroll
+                        for (int q = 0; q < kMaxParts; ++q)
+                            if (ll[q] > 0.f) M = fmaxf(M, mm[q]);
+                        float Ltot = 0.f;
+#pragma unroll
+                        for (int q = 0; q < kMaxParts; ++q) {
+                            const float w = ll[q] > 0.f ? exp2f(mm[q] - M) : 0.f;
+                            wsm[q * 64 + tid] = w;
+                            Ltot += w * ll[q];
+                        }
+                        inv_s[tid] = Ltot > 0.f ? 1.f / Ltot : 0.f;
+                        if (a.lse) a.lse[row * 64 + tid] = Ltot > 0.f ? (M + log2f(Ltot)) * 0.69314718055994531f : -INFINITY;
+                    }
+                    soft_sync();
+                    // thread tid owns float4 f = i * 256 + tid of the [64 x 512] row (head 2 i + tid / 128)
+#pragma unroll 1
+                    for (int ig = 0; ig < 4; ++ig) {
+                        float4 acc[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                        for (int q = 0; q < np; q += 2) {          // two partials' loads in flight
+                            const bool two = q + 1 < np;
+                            const float4* s0 = reinterpret_cast<const float4*>(a.part_o + usm[q] * 32768) + tid;
+                            const float4* s1 = reinterpret_cast<const float4*>(a.part_o + usm[two ? q + 1 : q] * 32768) + tid;
+                            float4 x0[8], x1[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                x0[j] = __ldcg(s0 + (ig * 8 + j) * 256);
+                                x1[j] = __ldcg(s1 + (ig * 8 + j) * 256);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int h = 2 * (ig * 8 + j) + (tid >> 7);
+                                const float w0 = wsm[q * 64 + h], w1 = two ? wsm[(q + 1) * 64 + h] : 0.f;
+                                acc[j].x += w0 * x0[j].x + w1 * x1[j].x;
+                                acc[j].y += w0 * x0[j].y + w1 * x1[j].y;
+                                acc[j].z += w0 * x0[j].z + w1 * x1[j].z;
+                                acc[j].w += w0 * x0[j].w + w1 * x1[j].w;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int i = ig * 8 + j;
+                            const float inv = inv_s[2 * i + (tid >> 7)];
+                            const int64_t o = row * 32768 + (int64_t)(i * 256 + tid) * 4;
+                            if (a.out_f32) {
+                                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) =
+                                    make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
+                            } else {
+                                __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
+                                __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
+                                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o) =
+                                    make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
+                            }
+                        }
+                    }
+                    if (tid == 0) a.row_done[row] = 0;
+                }
+            }
+            soft_sync();                                    // O^T and the combine scratch may be reused
+        }
+        // no MMA may be in flight when the TMEM is released
+        if (tid == 0 && issued) {
+            mma_commit(&bars[B_DRAIN]);
+            mbar_wait(&bars[B_DRAIN], 0, 500000000ull);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace mtc
+
+// CTAs sharing the T x 2048 slots: at most one per SM, at least 256 slots
+// each, and no more than ~60 row pieces per CTA.
+int mla_tc_ctas(int64_t total_q, int sms) {
+    const int64_t n = total_q * kTopK;
+    int64_t gcount = n / 256;
+    if (gcount < 1) gcount = 1;
+    if (gcount > sms) gcount = sms;
+    const int64_t min_g = (total_q + 59) / 60;
+    if (gcount < min_g) gcount = min_g;
+    return (int)gcount;
+}
+
+size_t mla_tc_ws_bytes(int64_t total_q, int G) {
+    size_t b = (size_t)2 * G * 64 * 512 * 4 + (size_t)2 * G * 64 * 2 * 4;
+    b = (b + 255) / 256 * 256;
+    return b + (size_t)total_q * 4;
+}
+
+dsa_status launch_sparse_mla_tc(const void* q, const int32_t* topk, const uint8_t* kv, const dsa_batch* b,
+                                float softmax_scale, void* out, int32_t out_dtype, float* lse, void* ws,
+                                int G, int32_t* st, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(mtc::sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mtc::kSmemAlloc) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        attr = true;
+    }
+    mtc::Args a;
+    a.q = static_cast<const uint16_t*>(q);
+    a.topk = topk;
+    a.kv = kv;
+    a.b = to_dev(b);
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.n_slots = b->total_q * kTopK;
+    a.G = G;
+    a.out = out;
+    a.out_f32 = out_dtype == DSA_DTYPE_F32;
+    a.lse = lse;
+    a.part_o = static_cast<float*>(ws);
+    a.part_ml = a.part_o + (size_t)2 * G * 64 * 512;
+    const size_t cnt_off = ((size_t)2 * G * 64 * 512 * 4 + (size_t)2 * G * 64 * 2 * 4 + 255) / 256 * 256;
+    a.row_done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + cnt_off);
+    a.st = st;
+    if (cudaMemsetAsync(a.row_done, 0, (size_t)b->total_q * 4, s) != cudaSuccess) return DSA_ERR_CUDA;
+    mtc::sparse_mla_tc_kernel<<<(unsigned)G, mtc::kThreads, mtc::kSmemAlloc, s>>>(a);
+    DSA_CHECK_LAUNCH();
+    return DSA_OK;
+}
+
+}  // namespace dsa
