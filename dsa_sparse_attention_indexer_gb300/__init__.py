@@ -41,7 +41,9 @@ DEVERR_TIMEOUT = 8
 DEVERR_FP16_RANGE = 16
 
 ERR = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARGUMENT", 2: "DSA_ERR_ALIGNMENT", 3: "DSA_ERR_UNSUPPORTED",
-       4: "DSA_ERR_WORKSPACE_TOO_SMALL", 5: "DSA_ERR_NO_TOPK_SOURCE", 6: "DSA_ERR_CUDA", 7: "DSA_ERR_DEVICE"}
+       4: "DSA_ERR_WORKSPACE_TOO_SMALL", 5: "DSA_ERR_NO_TOPK_SOURCE", 6: "DSA_ERR_CUDA", 7: "DSA_ERR_DEVICE",
+       8: "DSA_ERR_SCRATCH_LIMIT"}
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class DsaLibraryMissing(ImportError):
@@ -75,6 +77,8 @@ _SIGS = {
     "dsa_indexer_topk_workspace_size": (c_int32, [POINTER(DsaBatch), POINTER(c_size_t)]),
     "dsa_indexer_topk": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_void_p, c_void_p,
                                    c_void_p, c_int32, c_void_p, c_size_t, c_void_p, c_void_p]),
+    "dsa_indexer_topk_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_void_p, c_void_p,
+                                           c_void_p, c_int32, c_void_p, c_void_p]),
     "dsa_indexer_scores_workspace_size": (c_int32, [POINTER(DsaBatch), POINTER(c_size_t)]),
     "dsa_indexer_scores": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_void_p, c_int64,
                                      c_void_p, c_size_t, c_void_p, c_void_p]),
@@ -245,6 +249,21 @@ def dsa_indexer_topk(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=N
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
         None if share is None else share.handle, layer_id, _ptr(ws), ws.numel(), _ptr(dev_status),
         _stream(stream)))
+    return topk
+
+
+def dsa_indexer_topk_noalloc(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=None, share=None,
+                             layer_id: int = 0, dev_status=None, stream=None):
+    """dsa_indexer_topk for decode batches on the library's fixed scratch (no workspace)."""
+    _need(q, torch.bfloat16, "q")
+    _need(w, torch.float32, "w")
+    _need(idxk_cache, torch.uint8, "idxk_cache")
+    T = batch.total_q
+    if topk is None:
+        topk = torch.empty((T, TOPK), dtype=torch.int32, device=q.device)
+    _check("dsa_indexer_topk_noalloc", lib().dsa_indexer_topk_noalloc(
+        _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
+        None if share is None else share.handle, layer_id, _ptr(dev_status), _stream(stream)))
     return topk
 
 

@@ -26,6 +26,7 @@ extern "C" const char* dsa_status_string(dsa_status s) {
         case DSA_ERR_NO_TOPK_SOURCE: return "shared layer without a published full-layer top-k";
         case DSA_ERR_CUDA: return "CUDA runtime error";
         case DSA_ERR_DEVICE: return "device-side errors recorded in the status block";
+        case DSA_ERR_SCRATCH_LIMIT: return "batch too large for the fixed no-alloc scratch";
         default: return "unknown status";
     }
 }

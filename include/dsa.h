@@ -75,6 +75,8 @@ typedef int32_t dsa_status;
 #define DSA_ERR_NO_TOPK_SOURCE       5  /* shared layer with no full layer published*/
 #define DSA_ERR_CUDA                 6  /* a CUDA runtime call failed               */
 #define DSA_ERR_DEVICE               7  /* dsa_device_status_read saw device errors */
+#define DSA_ERR_SCRATCH_LIMIT        8  /* batch too large for the fixed scratch of
+                                           dsa_indexer_topk_noalloc                 */
 
 /* Bits of dev_status[0]; dev_status[1] counts offending elements, dev_status[2]
  * holds the low 32 bits of one offending value, dev_status[3] is reserved.      */
@@ -168,6 +170,32 @@ dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_c
                             const dsa_batch* b, int32_t* topk, float* topk_scores,
                             dsa_topk_share* share, int32_t layer_id,
                             void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ---- Indexer + top-2048 without a workspace argument --------------------
+ * The pages have no counterpart of this call.  It serves callers that cannot
+ * allocate device memory per call and keep no workspace of their own: a plain
+ * C host loop that owns no device allocator, or a runtime whose device memory
+ * is fully reserved up front and forbids allocation on the serving path.
+ * Inputs, outputs and kernels are those of dsa_indexer_topk, for decode
+ * batches only (every request has q_len == 1; other shapes return
+ * DSA_ERR_UNSUPPORTED).  The scratch is a fixed array of
+ * DSA_NOALLOC_SCRATCH_BYTES inside this library, so no call allocates.  A batch
+ * of T = B rows needs, on a GPU with S SMs,
+ *   round_up(4224 T, 256) + 16384 T + (S + B) * 16404 + 12 (B + 1) + 8 S
+ * bytes, plus up to 768 bytes of alignment (150 rows fit at S = 152, 160 do
+ * not); a larger batch returns
+ * DSA_ERR_SCRATCH_LIMIT and launches nothing.  Nothing in the scratch needs
+ * to start at zero: the kernels clear the histogram bins and plan entries
+ * before they read them.  The first call on a device performs set-up (it looks
+ * up the scratch's device address); make that call before any stream capture
+ * begins.  There is one scratch per device: calls that overlap in time (on
+ * other streams or from other host threads) race on it, and the caller must
+ * serialise them. */
+#define DSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+dsa_status dsa_indexer_topk_noalloc(const void* q, const float* w, const uint8_t* idxk_cache,
+                                    const dsa_batch* b, int32_t* topk, float* topk_scores,
+                                    dsa_topk_share* share, int32_t layer_id,
+                                    int32_t* dev_status, void* stream);
 
 /* Debug / parity hook: the same scores as dsa_indexer_topk, written in full.
  *   scores device fp32 [T, ld]; entries j > p of row i (and every entry of a
