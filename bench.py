@@ -39,7 +39,10 @@ L2_BYTES = 129 * 1024 * 1024
 
 # DRAM traffic per launch from an ncu capture, keyed by call; valid only while
 # the kernel source it was taken on is unchanged (sha256 prefix of the file).
-NCU_TRAFFIC = {}
+# Scaled to a full launch by the units processed: sparse_mla_decode from an ncu
+# capture of 16 requests (x4 rows), indexer_topk from a 256K-context decode1m
+# capture (x4 context).
+NCU_TRAFFIC = {"sparse_mla_decode": (105.6e6, "8c98073db5c500d9"), "indexer_topk": (554.5e6, "2a1005e9b5960edd")}
 
 
 def file_sha(path):
@@ -467,8 +470,8 @@ def main():
     dom_us = res["per_launch"][dom]
     dom_bytes = call_bytes(dom, w)
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
-    src = {"indexer_topk": "dsa_sparse_attention_indexer_gb300/csrc/indexer.cu",
-           "sparse_mla_decode": "dsa_sparse_attention_indexer_gb300/csrc/mla.cu"}.get(dom)
+    src = {"indexer_topk": "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
+           "sparse_mla_decode": "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu"}.get(dom)
     traffic = None
     if dom in NCU_TRAFFIC and src and NCU_TRAFFIC[dom][1] == file_sha(src):
         traffic = NCU_TRAFFIC[dom][0]
