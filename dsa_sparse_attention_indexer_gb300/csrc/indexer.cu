@@ -44,7 +44,8 @@ inline size_t indexer_ws_bytes(const dsa_batch* b) {
     const size_t qbytes = (q8_workspace_bytes(b->total_q) + 255) / 256 * 256;
     if (use_tc_path(b))   // row histograms + plan, for any GPU of up to 1024 SMs
         return qbytes + (size_t)b->total_q * 4096 * 4 + tc_plan_bytes(b->batch, 1024);
-    return qbytes + (size_t)b->total_q * (size_t)score_ld(b) * 4;
+    const size_t sbytes = ((size_t)b->total_q * (size_t)score_ld(b) * 4 + 255) / 256 * 256;
+    return qbytes + sbytes + mt_plan_bytes(b->batch, b->total_q);
 }
 
 }  // namespace dsa
@@ -92,10 +93,10 @@ extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint
             if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);
             return DSA_OK;
         }
-        dim3 grid((unsigned)((b->max_seq_len + kPage - 1) / kPage), (unsigned)b->batch);
+        void* plan = reinterpret_cast<uint8_t*>(sc) + ((size_t)b->total_q * (size_t)ld * 4 + 255) / 256 * 256;
+        rs = launch_indexer_rows(q8, wq, idxk_cache, b, sc, ld, true, false, plan, device_sm_count(), dev_status, s);
+        if (rs != DSA_OK) return rs;
         BatchDev bd = to_dev(b);
-        index_scores_ref_kernel<<<grid, 256, 0, s>>>(q8, wq, idxk_cache, bd, sc, ld, dev_status);
-        DSA_CHECK_LAUNCH();
         indexer_select_kernel<<<(unsigned)b->total_q, kSelThreads, 0, s>>>(sc, ld, bd, topk, topk_scores);
         DSA_CHECK_LAUNCH();
     }

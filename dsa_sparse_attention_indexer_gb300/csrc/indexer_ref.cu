@@ -9,6 +9,7 @@
 //     so this equals sum_m w_m ReLU(<q_m, k_j>) on the dequantised values.
 #include "dsa_internal.cuh"
 #include "indexer_common.cuh"
+#include "indexer_tc.cuh"
 
 namespace dsa {
 
@@ -32,71 +33,6 @@ index_q_quant_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w
     if (lane == 0) wq[g] = w[g] * ldexpf(1.0f, e);
 }
 
-// One CTA per (logical page, request): the page's 64 keys against every query
-// row of the request.  Thread (j = tid/4, quarter = tid%4) handles token j and
-// heads 8*quarter .. 8*quarter+7.
-__global__ void __launch_bounds__(256)
-index_scores_ref_kernel(const uint8_t* __restrict__ q8, const float* __restrict__ wq,
-                        const uint8_t* __restrict__ cache, BatchDev b, float* __restrict__ scores,
-                        int64_t ld, int32_t* __restrict__ st) {
-    __shared__ float kf[64][129];
-    __shared__ float ksc[64];
-    __shared__ float qf[32][129];
-    __shared__ float wqs[32];
-    const int r = blockIdx.y;
-    const int pk = blockIdx.x;
-    const int L = b.seq_len[r];
-    if (pk * kPage >= L) return;
-    const int q0 = b.q_start[r];
-    const int qn = b.q_start[r + 1] - q0;
-    const int tid = threadIdx.x;
-    const int64_t page = b.page_table[(int64_t)r * b.max_pages + pk];
-    const bool page_ok = page >= 0 && page < b.num_pages;
-    if (!page_ok && tid == 0) record_error(st, DSA_DEVERR_PAGE_RANGE, page);
-    if (page_ok) {
-        const uint8_t* pg = cache + page * (int64_t)kIdxPageBytes;
-        for (int c = tid; c < 64 * 64; c += 256) {           // 2 codes per item
-            const int j = c >> 6, d = (c & 63) * 2;
-            const float2 v = e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(pg + j * 128 + d));
-            kf[j][d] = v.x;
-            kf[j][d + 1] = v.y;
-        }
-        if (tid < 64) ksc[tid] = reinterpret_cast<const float*>(pg + kIdxPayloadBytes)[tid];
-    }
-    const int j = tid >> 2, quarter = tid & 3;
-    for (int t = 0; t < qn; ++t) {
-        const int64_t row = q0 + t;
-        const int p = L - qn + t;
-        __syncthreads();
-        for (int c = tid; c < 32 * 64; c += 256) {
-            const int h = c >> 6, d = (c & 63) * 2;
-            const float2 v = e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(q8 + row * 4096 + h * 128 + d));
-            qf[h][d] = v.x;
-            qf[h][d + 1] = v.y;
-        }
-        if (tid < 32) wqs[tid] = wq[row * 32 + tid];
-        __syncthreads();
-        float acc = 0.f;
-        if (page_ok) {
-#pragma unroll 1
-            for (int hh = 0; hh < 8; ++hh) {
-                const int h = quarter * 8 + hh;
-                float dot = 0.f;
-#pragma unroll 8
-                for (int d = 0; d < 128; ++d) dot = fmaf(qf[h][d], kf[j][d], dot);
-                acc = fmaf(wqs[h], fmaxf(dot, 0.f), acc);
-            }
-        }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        const int pos = pk * kPage + j;
-        if (quarter == 0 && pos < ld) {
-            const bool valid = page_ok && pos <= p;
-            scores[row * ld + pos] = valid ? acc * ksc[j] : -INFINITY;
-        }
-    }
-}
-
 }  // namespace dsa
 
 using namespace dsa;
@@ -117,7 +53,7 @@ extern "C" dsa_status dsa_indexer_scores_workspace_size(const dsa_batch* b, size
     dsa_status vs = validate_batch(b);
     if (vs != DSA_OK) return vs;
     if (!bytes) return DSA_ERR_INVALID_ARGUMENT;
-    *bytes = q8_workspace_bytes(b->total_q);
+    *bytes = (q8_workspace_bytes(b->total_q) + 255) / 256 * 256 + mt_plan_bytes(b->batch, b->total_q);
     return DSA_OK;
 }
 
@@ -131,14 +67,14 @@ extern "C" dsa_status dsa_indexer_scores(const void* q, const float* w, const ui
     if (!aligned16(q) || !aligned16(idxk_cache)) return DSA_ERR_ALIGNMENT;
     if (b->total_q == 0) return DSA_OK;
     if (!ws || !aligned16(ws)) return ws ? DSA_ERR_ALIGNMENT : DSA_ERR_INVALID_ARGUMENT;
-    if (ws_bytes < q8_workspace_bytes(b->total_q)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t qbytes = (q8_workspace_bytes(b->total_q) + 255) / 256 * 256;
+    if (ws_bytes < qbytes + mt_plan_bytes(b->batch, b->total_q)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+    if (b->num_pages * 66 > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
     uint8_t* q8 = static_cast<uint8_t*>(ws);
     float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
     cudaStream_t s = as_stream(stream);
     dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, nullptr, s);
     if (rs != DSA_OK) return rs;
-    dim3 grid((unsigned)((b->max_seq_len + kPage - 1) / kPage), (unsigned)b->batch);
-    index_scores_ref_kernel<<<grid, 256, 0, s>>>(q8, wq, idxk_cache, to_dev(b), scores, ld, dev_status);
-    DSA_CHECK_LAUNCH();
-    return DSA_OK;
+    return launch_indexer_rows(q8, wq, idxk_cache, b, scores, ld, false, true, q8 + qbytes, device_sm_count(),
+                               dev_status, s);
 }

@@ -29,4 +29,9 @@ dsa_status launch_indexer_tc(const uint8_t* q8, const float* wq, uint32_t* hist,
                              cudaStream_t s);
 int device_sm_count();
 
+size_t mt_plan_bytes(int64_t batch, int64_t total_q);
+dsa_status launch_indexer_rows(const uint8_t* q8, const float* wq, const uint8_t* cache, const dsa_batch* b,
+                               float* scores, int64_t ld, bool skip_short, bool full_rows, void* plan_ws, int G,
+                               int32_t* st, cudaStream_t s);
+
 }  // namespace dsa

@@ -88,7 +88,8 @@ def test_batch_validation_and_workspace_sizes(L):
     b = _fake_batch()
     assert L.dsa_indexer_topk_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0 and n.value > 0
     assert L.dsa_sparse_mla_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0
-    assert L.dsa_indexer_scores_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0 and n.value == 2 * (4096 + 128)
+    assert L.dsa_indexer_scores_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0
+    assert n.value >= 2 * (4096 + 128) and n.value % 256 == 0      # quantised q + the row-block plan
     assert L.dsa_indexer_topk_workspace_size(None, ctypes.byref(n)) == 1
     bad = _fake_batch()
     bad.max_pages = 1                                   # 64 tokens cannot hold max_seq_len

@@ -266,7 +266,9 @@ def test_indexer_topk_decode_repeatable(decode_case):
 
 def test_indexer_scores_match_oracle(indexer_case):
     c = indexer_case
-    S = D.dsa_indexer_scores(c["q"], c["wt"], c["cache"], c["batch"]).cpu().numpy()
+    st = D.new_device_status(DEV)
+    S = D.dsa_indexer_scores(c["q"], c["wt"], c["cache"], c["batch"], dev_status=st).cpu().numpy()
+    assert D.dsa_device_status_read(st)[0] == 0
     for row in c["rows"]:
         i, n = row["i"], row["n"]
         check_scores(S[i, :n], row["s"], row["mag"], what=f"row {i}")
