@@ -219,6 +219,19 @@ def call_bytes(name, w):
     return 0
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings over every rank of the job."""
+    t_ = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t_, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t_.tolist()]
+
+
+def job_throughput(rows_per_rank, world, ms):
+    """Query rows per second of the whole job: every rank runs its own replica
+    of the workload, and the step takes as long as the slowest rank."""
+    return rows_per_rank * world / (ms / 1000.0)
+
+
 # ----------------------------------------------------------------------------
 def run_ours(args, rank, world):
     import dsa_sparse_attention_indexer_gb300 as D
@@ -343,9 +356,7 @@ def run_ours(args, rank, world):
     e2e_ms = (time.perf_counter() - t0) * 1000.0 / e2e_steps
 
     if world > 1:
-        t_ = torch.tensor([ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t_, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t_[0]), float(t_[1])
+        ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
     return dict(w=w, ms=ms, e2e_ms=e2e_ms, per_call=per_call, per_launch=per_launch, clocks=clocks,
                 h2d=h2d, d2h=d2h, launches=sum(KERNELS_PER_CALL[k] * len(v) for k, v in timers.items()))
 
@@ -465,7 +476,7 @@ def main():
     ms = res["ms"]
     idx_b, kv_b, _, _ = workload_bytes(w)
     step_bytes = idx_b + kv_b
-    value = w.total_q * world / (ms / 1000.0)
+    value = job_throughput(w.total_q, world, ms)
     dom = max(res["per_call"], key=lambda k: res["per_call"][k])
     dom_us = res["per_launch"][dom]
     dom_bytes = call_bytes(dom, w)
@@ -495,7 +506,7 @@ def main():
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"],
                      "algorithmic_bytes_per_launch": dom_bytes, "us_per_launch": dom_us},
         "clocks": res["clocks"],
-        "e2e": {"value": w.total_q * world / (res["e2e_ms"] / 1000.0), "unit": "query_tokens/s",
+        "e2e": {"value": job_throughput(w.total_q, world, res["e2e_ms"]), "unit": "query_tokens/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"], "ms_per_step": res["e2e_ms"]},
         "gpu_launches": res["launches"] * args.steps,
     }
