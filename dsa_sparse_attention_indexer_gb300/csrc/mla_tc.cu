@@ -4,9 +4,16 @@
 // over the selected positions j of each query row (j <= p), 64 heads of 576
 // dims, 512-d latent output per head.
 //
-// Work split: the T x 2048 (row, entry) slots are cut into one contiguous,
-// equal share per CTA; a row covered by several CTAs is merged by
-// log-sum-exp (partials + last-CTA combine through a per-row counter).
+// Work split: each CTA takes one contiguous range of the T x 2048 (row, entry)
+// slots, cut one of three ways:
+//   T < SMs       each row gets c or c + 1 CTAs, cut on whole 96-token tiles,
+//                 so no CTA crosses a row (a crossing costs a second O store,
+//                 Q load and pipeline refill on that CTA's critical path);
+//   T < 8 x SMs   equal slot shares (rows at share edges are split);
+//   otherwise     whole rows per CTA (at most 1/8 imbalance, nothing split).
+// A row covered by several CTAs leaves one unnormalised partial (O, running
+// max, sum) per CTA; a second kernel merges them by log-sum-exp, spread over
+// (row, head group) CTAs.
 //
 // Per CTA, per tile of 96 selected tokens (the M = 128 MMA rows 96..127 are
 // padding), in transposed form so that tokens are the MMA rows:
@@ -28,10 +35,12 @@
 //               64 heads; per-head max and sum by a transposing warp
 //               reduction, online softmax with lazy rescaling (O^T in TMEM is
 //               rescaled only when a head's max grows by more than 2^8), P
-//               written as fp16 P^T rows.  Thread 0 also issues the MMAs and
+//               written as fp16 P^T rows.  At a piece start they convert the
+//               row's Q to fp16 while the loaders build the slot list and
+//               gather the first tile.  Thread 0 also issues the MMAs and
 //               warp 0 owns the TMEM allocation.
-//   warps 8-15  loaders: build the row piece's list of cache slots, convert
-//               Q to fp16, and gather each tile's 656-B latent rows into
+//   warps 8-15  loaders: build the row piece's list of cache slots and gather
+//               each tile's 656-B latent rows into
 //               registers one tile ahead (all 18 16-byte pieces of a lane in
 //               flight at once), then dequantise group by group into the
 //               128-byte-swizzled fp16 tile (c * scale is exact in fp16 for
@@ -59,7 +68,9 @@ constexpr int kSoftBar = 1;
 constexpr int kLoadBar = 2;
 constexpr float kTau = 8.0f;                               // lazy-rescale threshold, log2 units
 constexpr int kMaxPieces = 64;
-constexpr int kMaxParts = 16;                              // CTAs one row can span (shares >= 256 slots: <= 10)
+constexpr int kTilesPerRow = (kTopK + kTok - 1) / kTok;    // 22
+constexpr int kMaxParts = 24;                              // CTAs one row can span
+static_assert(kMaxParts >= kTilesPerRow, "a row is cut into at most one piece per tile");
 constexpr uint32_t kIdescQK = idesc_f16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, true, true);
 constexpr uint32_t kColS = 0;                              // TMEM: S^T [128 x 64]
@@ -86,11 +97,20 @@ static_assert(B_COUNT <= 16, "barrier block");
 struct Misc {
     uint32_t tmem_base;
     int32_t abort;
-    int32_t last;
     int32_t scratch[8];
     int32_t ntok[kMaxPieces];
 };
 static_assert(sizeof(Misc) <= 512, "misc block");
+
+// How the T x 2048 slots are cut into CTA ranges (see the file comment).
+enum { SPLIT_WHOLE_ROWS = 0, SPLIT_ROW_CTAS = 1, SPLIT_EQUAL = 2 };
+struct Split {
+    int64_t T;                  // query rows
+    int64_t N;                  // T * 2048 slots
+    int32_t G;                  // CTAs
+    int32_t mode;
+    int32_t c, extra;           // SPLIT_ROW_CTAS: rows < extra get c + 1 CTAs, the others c
+};
 
 struct Args {
     const uint16_t* q;          // [T,64,576] bf16
@@ -98,21 +118,42 @@ struct Args {
     const uint8_t* kv;          // latent cache
     BatchDev b;
     float scale_log2;
-    int64_t n_slots;            // T * 2048
-    int G;
+    Split sp;
     void* out;
     int out_f32;
     float* lse;
     float* part_o;              // [2G, 64, 512]
-    float* part_ml;             // [2G, 64, 2]
-    int32_t* row_done;          // [T]
+    float* part_ml;             // [2G, 64, 2]: running max (log2 units), sum
     int32_t* st;
 };
 
-__device__ __forceinline__ int64_t cta_start(int64_t g, int64_t N, int64_t G) { return g * N / G; }
-__device__ __forceinline__ int64_t cta_of(int64_t x, int64_t N, int64_t G) { return ((x + 1) * G + N - 1) / N - 1; }
-__device__ __forceinline__ int64_t slot_of(int64_t g, int64_t r, int64_t N, int64_t G) {
-    return 2 * g + ((cta_start(g, N, G) / kTopK == r) ? 0 : 1);
+// First slot of CTA g's range (g = G gives T x 2048).
+__device__ __forceinline__ int64_t split_begin(int64_t g, const Split& sp) {
+    if (g >= sp.G) return sp.N;
+    if (sp.mode == SPLIT_WHOLE_ROWS) return (g * sp.T / sp.G) * kTopK;
+    if (sp.mode == SPLIT_EQUAL) return g * sp.N / sp.G;
+    const int64_t big = (int64_t)sp.extra * (sp.c + 1);
+    int64_t r, j, n;
+    if (g < big) {
+        r = g / (sp.c + 1), j = g % (sp.c + 1), n = sp.c + 1;
+    } else {
+        r = sp.extra + (g - big) / sp.c, j = (g - big) % sp.c, n = sp.c;
+    }
+    return r * kTopK + min((int64_t)kTopK, (j * kTilesPerRow / n) * kTok);
+}
+// The CTA whose range holds slot x (the inverse of split_begin).
+__device__ __forceinline__ int64_t split_owner(int64_t x, const Split& sp) {
+    if (sp.mode == SPLIT_WHOLE_ROWS) return ((x / kTopK + 1) * sp.G - 1) / sp.T;
+    if (sp.mode == SPLIT_EQUAL) return ((x + 1) * sp.G + sp.N - 1) / sp.N - 1;
+    const int64_t r = x / kTopK, tile = (x % kTopK) / kTok;
+    const int64_t big = (int64_t)sp.extra * (sp.c + 1);
+    const int64_t gf = r < sp.extra ? r * (sp.c + 1) : big + (r - sp.extra) * sp.c;
+    const int64_t n = r < sp.extra ? sp.c + 1 : sp.c;
+    return gf + ((tile + 1) * n - 1) / kTilesPerRow;
+}
+// Partial slot of CTA g's piece of row r: its first row uses 2g, its last 2g + 1.
+__device__ __forceinline__ int64_t slot_of(int64_t g, int64_t r, const Split& sp) {
+    return 2 * g + ((split_begin(g, sp) / kTopK == r) ? 0 : 1);
 }
 
 __device__ __forceinline__ void soft_sync() { asm volatile("bar.sync %0, %1;" ::"n"(kSoftBar), "n"(kSoftThreads) : "memory"); }
@@ -216,8 +257,8 @@ sparse_mla_tc_kernel(Args a) {
     float* alpha = l_acc + 64;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const BatchDev& b = a.b;
-    const int64_t N = a.n_slots, G = a.G, g = blockIdx.x;
-    const int64_t e_begin = cta_start(g, N, G), e_end = cta_start(g + 1, N, G);
+    const int64_t g = blockIdx.x;
+    const int64_t e_begin = split_begin(g, a.sp), e_end = split_begin(g + 1, a.sp);
     volatile int32_t* abort_flag = &misc->abort;
 
     if (tid == 0) {
@@ -343,36 +384,13 @@ sparse_mla_tc_kernel(Args a) {
                 prefetch(0, 2);
                 prefetch(0, 3);
             }
-            // ---- Q of the row, once the softmax group has taken the previous piece
-            //      (so QFULL never runs two phases ahead) and its last S^T MMA is done
-            if (k > 0) ok = wait_ab(&bars[B_QEMPTY], (uint32_t)((k - 1) & 1), abort_flag);
-            if (ok && gt > 0) ok = wait_ab(&bars[B_SFULL], (uint32_t)((gt - 1) & 1), abort_flag);
-            if (!ok) {
+            // ---- the piece's token count, once the softmax group has taken the
+            //      previous one (so QFULL never runs two phases ahead)
+            if (k > 0 && !(ok = wait_ab(&bars[B_QEMPTY], (uint32_t)((k - 1) & 1), abort_flag))) {
                 if (lane == 0) timeout(11);
                 continue;                                  // the decision is taken at the loop top
             }
-            const uint16_t* qrow = a.q + row * (64 * 576);
-#pragma unroll 1
-            for (int c0 = lt; c0 < 64 * 72; c0 += 6 * kLoadThreads) {   // 18 pieces per thread, 6 in flight
-                uint4 qv[6];
-#pragma unroll
-                for (int u = 0; u < 6; ++u) {
-                    const int c = c0 + u * kLoadThreads;
-                    qv[u] = c < 64 * 72 ? __ldg(reinterpret_cast<const uint4*>(qrow) + c) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int u = 0; u < 6; ++u) {
-                    const int c = c0 + u * kLoadThreads;
-                    if (c >= 64 * 72) continue;
-                    const int h = c / 72, cq = c % 72;
-                    const int blk = cq >> 3, ch = cq & 7;
-                    *reinterpret_cast<uint4*>(smem + kOffQ + blk * 8192 + h * 128 + ((ch ^ (h & 7)) * 16)) =
-                        make_uint4(bf16x2_to_h2(qv[u].x), bf16x2_to_h2(qv[u].y), bf16x2_to_h2(qv[u].z),
-                                   bf16x2_to_h2(qv[u].w));
-                }
-            }
             if (lt == 0) misc->ntok[k % kMaxPieces] = ntok;
-            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_QFULL]);
             // ---- tiles: RoPE group first (free once S^T of the previous tile is done), then
@@ -417,6 +435,8 @@ sparse_mla_tc_kernel(Args a) {
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[B_FULL0 + gg]);
+                    // spread over the tile: a whole tile's requests at once fill the
+                    // SM's outstanding-miss capacity and stall every memory instruction
                     if (more) prefetch(t + 1, gg);
                 }
                 if (!ok) break;
@@ -473,6 +493,32 @@ sparse_mla_tc_kernel(Args a) {
         int64_t gt = 0;
         int k = 0;
         for (int64_t row = e_begin / kTopK; row * kTopK < e_end; ++row, ++k) {
+            // ---- Q of the row -> fp16, K-major, 128-byte swizzle.  Every S^T MMA of the
+            //      previous piece has completed (each was waited for), so Q is free; the
+            //      loaders meanwhile build the slot list and gather the first tile.
+            {
+                const uint16_t* qrow = a.q + row * (64 * 576);
+#pragma unroll 1
+                for (int c0 = tid; c0 < 64 * 72; c0 += 6 * kSoftThreads) {   // 18 pieces per thread, 6 in flight
+                    uint4 qv[6];
+#pragma unroll
+                    for (int u = 0; u < 6; ++u) {
+                        const int c = c0 + u * kSoftThreads;
+                        qv[u] = c < 64 * 72 ? __ldg(reinterpret_cast<const uint4*>(qrow) + c) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 6; ++u) {
+                        const int c = c0 + u * kSoftThreads;
+                        if (c >= 64 * 72) continue;
+                        const int h = c / 72, cq = c % 72;
+                        const int blk = cq >> 3, ch = cq & 7;
+                        *reinterpret_cast<uint4*>(smem + kOffQ + blk * 8192 + h * 128 + ((ch ^ (h & 7)) * 16)) =
+                            make_uint4(bf16x2_to_h2(qv[u].x), bf16x2_to_h2(qv[u].y), bf16x2_to_h2(qv[u].z),
+                                       bf16x2_to_h2(qv[u].w));
+                    }
+                }
+                fence_proxy_async_smem();
+            }
             int ok = mbar_wait(&bars[B_QFULL], (uint32_t)(k & 1)) ? 1 : 0;
             if (soft_any(!ok || *abort_flag)) {
                 if (tid == 0 && !ok) timeout(31);
@@ -486,8 +532,11 @@ sparse_mla_tc_kernel(Args a) {
                 m_ref[tid] = -INFINITY;
                 l_acc[tid] = 0.f;
             }
+            soft_sync();                                    // Q and the statistics are in place
+            float lsum[32];                                 // this token lane's running sums of its 32 heads
+#pragma unroll
+            for (int c = 0; c < 32; ++c) lsum[c] = 0.f;
             if (tid == 0 && ntiles > 0 && !issue_qk(gt)) timeout(34);
-            soft_sync();
             bool failed = false;
             for (int t = 0; t < ntiles; ++t, ++gt) {
                 ok = wait_ab(&bars[B_SFULL], (uint32_t)(gt & 1), abort_flag) ? 1 : 0;
@@ -505,45 +554,51 @@ sparse_mla_tc_kernel(Args a) {
                 float v[32];
                 tc_fence_after();
                 load_s(v);
-                // ---- per-head tile max, lazy rescale decision
-                xreduce32<true>(v, lane);
-                red[q4 * 64 + hh * 32 + lane] = v[0];
-                soft_sync();
-                bool need = false;
-                if (tid < 64) {
-                    const float tm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
-                    const float mo = m_ref[tid];
-                    need = (tm > mo + kTau) || (mo == -INFINITY && tm > -INFINITY);
-                    alpha[tid] = need ? (mo == -INFINITY ? 0.f : exp2f(mo - tm)) : 1.f;
-                    if (need) {
-                        m_ref[tid] = tm;
-                        l_acc[tid] *= alpha[tid];
-                    }
-                }
+                // ---- lazy rescale: the exact tile max is needed only when a score
+                //      exceeds its head's reference max by more than 2^kTau (always on
+                //      the piece's first tile, where the reference is -inf)
+                bool over = false;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) over |= v[c] > m_ref[hh * 32 + c] + kTau;
                 // S^T of tile gt is complete, and it was issued after the P.V of tile gt - 1:
                 // O^T is stable and P^T is free.
-                const bool resc = soft_any(need);
-                if (resc && t > 0) {                        // rescale the resident O^T columns of these heads
-#pragma unroll 1
-                    for (int mb = 0; mb < 4; ++mb) {
-                        uint32_t o[32];
-                        const uint32_t addr = lane_addr + kColO + mb * 64 + hh * 32;
-                        tmem_ld_32x32b_x32(addr, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[hh * 32 + c]);
-                        tmem_st_32x32b_x32(addr, o);
+                if (soft_any(over)) {
+                    xreduce32<true>(v, lane);                   // per-head tile max (consumes v)
+                    red[q4 * 64 + hh * 32 + lane] = v[0];
+                    soft_sync();
+                    if (tid < 64) {
+                        const float tm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+                        const float mo = m_ref[tid];
+                        const bool need = tm > mo + kTau;
+                        alpha[tid] = need ? (mo == -INFINITY ? 0.f : exp2f(mo - tm)) : 1.f;
+                        if (need) m_ref[tid] = tm;
                     }
-                    tmem_st_wait();
+                    soft_sync();
+                    if (t > 0) {                                // rescale the resident O^T columns of these heads
+#pragma unroll 1
+                        for (int mb = 0; mb < 4; ++mb) {
+                            uint32_t o[32];
+                            const uint32_t addr = lane_addr + kColO + mb * 64 + hh * 32;
+                            tmem_ld_32x32b_x32(addr, o);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[hh * 32 + c]);
+                            tmem_st_32x32b_x32(addr, o);
+                        }
+                        tmem_st_wait();
+                    }
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) lsum[c] *= alpha[hh * 32 + c];
+                    load_s(v);
                 }
-                // ---- probabilities (S reloaded from TMEM) and their per-head sums
-                load_s(v);
+                // ---- probabilities, this token's running sums, and its P^T row
+                //      (heads 32 hh.. as fp16, MN-major 128-byte swizzle)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const float mr = m_ref[hh * 32 + c];
                     v[c] = (v[c] == -INFINITY) ? 0.f : exp2f(v[c] - mr);
+                    lsum[c] += v[c];
                 }
-                // ---- P^T row of this token: heads 32 hh.. as fp16, MN-major 128-byte swizzle
                 if (st < kTok) {
                     uint8_t* prow = smem + kOffP + st * 128;
 #pragma unroll
@@ -554,12 +609,9 @@ sparse_mla_tc_kernel(Args a) {
                                        pack_h2(v[8 * cc + 4], v[8 * cc + 5]), pack_h2(v[8 * cc + 6], v[8 * cc + 7]));
                     }
                 }
-                xreduce32<false>(v, lane);
-                red[256 + q4 * 64 + hh * 32 + lane] = v[0];
                 fence_proxy_async_smem();
                 tc_fence_before();
                 soft_sync();                                // P^T written, S^T and O^T reads / writes done
-                if (tid < 64) l_acc[tid] += red[256 + tid] + red[320 + tid] + red[384 + tid] + red[448 + tid];
                 if (tid == 0) {
                     issue_pv(t > 0);
                     if (t + 1 < ntiles && !issue_qk(gt + 1)) timeout(35);
@@ -578,9 +630,15 @@ sparse_mla_tc_kernel(Args a) {
                 }
                 tc_fence_after();
             }
-            const int64_t g0 = cta_of(row * kTopK, N, G), g1 = cta_of(row * kTopK + kTopK - 1, N, G);
+            // ---- per-head sums over the piece: the lanes' running sums reduced
+            xreduce32<false>(lsum, lane);
+            red[256 + q4 * 64 + hh * 32 + lane] = lsum[0];
+            soft_sync();
+            if (tid < 64) l_acc[tid] = red[256 + tid] + red[320 + tid] + red[384 + tid] + red[448 + tid];
+            soft_sync();
+            const int64_t g0 = split_owner(row * kTopK, a.sp), g1 = split_owner(row * kTopK + kTopK - 1, a.sp);
             const bool whole = g0 == g1;
-            const int64_t unit = whole ? 0 : slot_of(g, row, N, G);
+            const int64_t unit = whole ? 0 : slot_of(g, row, a.sp);
 #pragma unroll 1
             for (int mb = 0; mb < 4; ++mb) {
                 uint32_t o[32];
@@ -618,94 +676,8 @@ sparse_mla_tc_kernel(Args a) {
                     a.part_ml[(unit * 64 + tid) * 2] = m_ref[tid];
                     a.part_ml[(unit * 64 + tid) * 2 + 1] = l_acc[tid];
                 }
-                __threadfence();
-                soft_sync();
-                if (tid == 0) misc->last = (atomicAdd(&a.row_done[row], 1) == (int)(g1 - g0)) ? 1 : 0;
-                soft_sync();
-                if (misc->last) {
-                    // last piece of the row: log-sum-exp combine of the row's np partials.
-                    // P^T is free here (the next P.V waits for this group): it holds the
-                    // per-partial weights and units.
-                    __threadfence();
-                    const int np = (int)(g1 - g0 + 1);
-                    float* wsm = reinterpret_cast<float*>(smem + kOffP);            // [kMaxParts][64]
-                    float* inv_s = wsm + kMaxParts * 64;                            // [64]
-                    int64_t* usm = reinterpret_cast<int64_t*>(inv_s + 64);          // [kMaxParts]
-                    if (tid < kMaxParts) usm[tid] = tid < np ? slot_of(g0 + tid, row, N, G) : 0;
-                    soft_sync();
-                    if (tid < 64) {
-                        float mm[kMaxParts], ll[kMaxParts];
-#pragma unroll
-                        for (int q = 0; q < kMaxParts; ++q) {
-                            mm[q] = -INFINITY;
-                            ll[q] = 0.f;
-                            if (q < np) {
-                                mm[q] = __ldcg(&a.part_ml[(usm[q] * 64 + tid) * 2]);
-                                ll[q] = __ldcg(&a.part_ml[(usm[q] * 64 + tid) * 2 + 1]);
-                            }
-                        }
-                        float M = -INFINITY;
-#pragma unroll
-                        for (int q = 0; q < kMaxParts; ++q)
-                            if (ll[q] > 0.f) M = fmaxf(M, mm[q]);
-                        float Ltot = 0.f;
-#pragma unroll
-                        for (int q = 0; q < kMaxParts; ++q) {
-                            const float w = ll[q] > 0.f ? exp2f(mm[q] - M) : 0.f;
-                            wsm[q * 64 + tid] = w;
-                            Ltot += w * ll[q];
-                        }
-                        inv_s[tid] = Ltot > 0.f ? 1.f / Ltot : 0.f;
-                        if (a.lse) a.lse[row * 64 + tid] = Ltot > 0.f ? (M + log2f(Ltot)) * 0.69314718055994531f : -INFINITY;
-                    }
-                    soft_sync();
-                    // thread tid owns float4 f = i * 256 + tid of the [64 x 512] row (head 2 i + tid / 128)
-#pragma unroll 1
-                    for (int ig = 0; ig < 4; ++ig) {
-                        float4 acc[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-                        for (int q = 0; q < np; q += 2) {          // two partials' loads in flight
-                            const bool two = q + 1 < np;
-                            const float4* s0 = reinterpret_cast<const float4*>(a.part_o + usm[q] * 32768) + tid;
-                            const float4* s1 = reinterpret_cast<const float4*>(a.part_o + usm[two ? q + 1 : q] * 32768) + tid;
-                            float4 x0[8], x1[8];
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                x0[j] = __ldcg(s0 + (ig * 8 + j) * 256);
-                                x1[j] = __ldcg(s1 + (ig * 8 + j) * 256);
-                            }
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int h = 2 * (ig * 8 + j) + (tid >> 7);
-                                const float w0 = wsm[q * 64 + h], w1 = two ? wsm[(q + 1) * 64 + h] : 0.f;
-                                acc[j].x += w0 * x0[j].x + w1 * x1[j].x;
-                                acc[j].y += w0 * x0[j].y + w1 * x1[j].y;
-                                acc[j].z += w0 * x0[j].z + w1 * x1[j].z;
-                                acc[j].w += w0 * x0[j].w + w1 * x1[j].w;
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int i = ig * 8 + j;
-                            const float inv = inv_s[2 * i + (tid >> 7)];
-                            const int64_t o = row * 32768 + (int64_t)(i * 256 + tid) * 4;
-                            if (a.out_f32) {
-                                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) =
-                                    make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
-                            } else {
-                                __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
-                                __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
-                                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o) =
-                                    make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
-                            }
-                        }
-                    }
-                    if (tid == 0) a.row_done[row] = 0;
-                }
             }
-            soft_sync();                                    // O^T and the combine scratch may be reused
+            soft_sync();                                    // O^T may be reused
         }
         // no MMA may be in flight when the TMEM is released
         if (tid == 0 && issued) {
@@ -721,24 +693,139 @@ sparse_mla_tc_kernel(Args a) {
     }
 }
 
+// ---------------------------------------------------------------- combine
+// Rows cut across CTAs.  With CTAs per row, block x merges row x when that row
+// has several CTAs.  With equal shares, block x looks at CTA boundary
+// bd = x + 1: the row holding slot split_begin(bd) is split when that slot is
+// not the row's first, and the row's first such boundary merges it.  Per head h of the row
+// over its partials u:  M = max m_u,  w_u = 2^(m_u - M),  L = sum w_u l_u,
+//   out_h = sum_u w_u O_u,h / L,   lse_h = (M + log2 L) ln 2.
+constexpr int kCombHeads = 4;                              // heads per combine CTA
+constexpr int kCombThreads = 256;                          // 4 heads x 512 dims, 8 dims per thread
+
+__global__ void __launch_bounds__(kCombThreads)
+combine_kernel(Args a) {
+    __shared__ float w_s[kMaxParts][kCombHeads];
+    __shared__ float inv_s[kCombHeads];
+    __shared__ int64_t u_s[kMaxParts];
+    int64_t row;
+    if (a.sp.mode == SPLIT_ROW_CTAS) {
+        row = blockIdx.x;
+    } else {
+        const int64_t bd = (int64_t)blockIdx.x + 1;
+        const int64_t x = split_begin(bd, a.sp);
+        row = x / kTopK;
+        if (x % kTopK == 0) return;                         // a row boundary: nothing split here
+        if (bd >= 2) {
+            const int64_t px = split_begin(bd - 1, a.sp);
+            if (px / kTopK == row && px % kTopK != 0) return;   // an earlier boundary merges this row
+        }
+    }
+    const int64_t g0 = split_owner(row * kTopK, a.sp), g1 = split_owner(row * kTopK + kTopK - 1, a.sp);
+    if (g0 == g1) return;                                   // written whole by its CTA
+    const int np = (int)min(g1 - g0 + 1, (int64_t)kMaxParts);   // at most one CTA per tile of the row
+    const int tid = threadIdx.x;
+    const int h0 = blockIdx.y * kCombHeads;
+    if (tid < kMaxParts) u_s[tid] = tid < np ? slot_of(g0 + tid, row, a.sp) : 0;
+    __syncthreads();
+    if (tid < kCombHeads) {
+        const int h = h0 + tid;
+        float M = -INFINITY;
+        for (int q = 0; q < np; ++q) {
+            const float m = __ldcg(&a.part_ml[(u_s[q] * 64 + h) * 2]);
+            const float l = __ldcg(&a.part_ml[(u_s[q] * 64 + h) * 2 + 1]);
+            if (l > 0.f) M = fmaxf(M, m);
+        }
+        float Lt = 0.f;
+        for (int q = 0; q < np; ++q) {
+            const float m = __ldcg(&a.part_ml[(u_s[q] * 64 + h) * 2]);
+            const float l = __ldcg(&a.part_ml[(u_s[q] * 64 + h) * 2 + 1]);
+            const float w = l > 0.f ? exp2f(m - M) : 0.f;
+            w_s[q][tid] = w;
+            Lt += w * l;
+        }
+        inv_s[tid] = Lt > 0.f ? 1.f / Lt : 0.f;
+        if (a.lse) a.lse[row * 64 + h] = Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
+    }
+    __syncthreads();
+    const int hl = tid >> 6, d0 = (tid & 63) * 8;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int q0 = 0; q0 < np; q0 += 4) {                    // four partials' loads in flight
+        float4 v[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (q0 + j < np) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(a.part_o + (u_s[q0 + j] * 64 + h0 + hl) * 512 + d0);
+                v[j][0] = __ldcg(src);
+                v[j][1] = __ldcg(src + 1);
+            } else {
+                v[j][0] = v[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float w = q0 + j < np ? w_s[q0 + j][hl] : 0.f;
+            acc[0] += w * v[j][0].x;
+            acc[1] += w * v[j][0].y;
+            acc[2] += w * v[j][0].z;
+            acc[3] += w * v[j][0].w;
+            acc[4] += w * v[j][1].x;
+            acc[5] += w * v[j][1].y;
+            acc[6] += w * v[j][1].z;
+            acc[7] += w * v[j][1].w;
+        }
+    }
+    const float inv = inv_s[hl];
+    const int64_t o = (row * 64 + h0 + hl) * 512 + d0;
+    if (a.out_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o);
+        dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+        dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+    } else {
+        uint32_t wv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+            wv[j] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + o) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+}
+
 }  // namespace mtc
 
-// CTAs sharing the T x 2048 slots: at most one per SM, at least 256 slots
-// each, and no more than ~60 row pieces per CTA.
+// CTAs sharing the T x 2048 slots: one per SM, and with fewer rows than SMs
+// no more than one per 96-token tile of each row.
 int mla_tc_ctas(int64_t total_q, int sms) {
-    const int64_t n = total_q * kTopK;
-    int64_t gcount = n / 256;
-    if (gcount < 1) gcount = 1;
-    if (gcount > sms) gcount = sms;
-    const int64_t min_g = (total_q + 59) / 60;
-    if (gcount < min_g) gcount = min_g;
-    return (int)gcount;
+    if (total_q < sms) return (int)std::min<int64_t>(sms, total_q * mtc::kTilesPerRow);
+    return sms;
+}
+
+static mtc::Split make_split(int64_t T, int G) {
+    mtc::Split sp;
+    sp.T = T;
+    sp.N = T * kTopK;
+    sp.G = G;
+    sp.c = sp.extra = 0;
+    if (T < G) {
+        sp.mode = mtc::SPLIT_ROW_CTAS;
+        sp.c = (int32_t)(G / T);
+        sp.extra = (int32_t)(G % T);
+    } else if (T < (int64_t)8 * G) {
+        sp.mode = mtc::SPLIT_EQUAL;
+    } else {
+        sp.mode = mtc::SPLIT_WHOLE_ROWS;
+    }
+    return sp;
 }
 
 size_t mla_tc_ws_bytes(int64_t total_q, int G) {
-    size_t b = (size_t)2 * G * 64 * 512 * 4 + (size_t)2 * G * 64 * 2 * 4;
-    b = (b + 255) / 256 * 256;
-    return b + (size_t)total_q * 4;
+    (void)total_q;
+    const size_t b = (size_t)2 * G * 64 * 512 * 4 + (size_t)2 * G * 64 * 2 * 4;
+    return (b + 255) / 256 * 256;
 }
 
 dsa_status launch_sparse_mla_tc(const void* q, const int32_t* topk, const uint8_t* kv, const dsa_batch* b,
@@ -757,19 +844,22 @@ dsa_status launch_sparse_mla_tc(const void* q, const int32_t* topk, const uint8_
     a.kv = kv;
     a.b = to_dev(b);
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
-    a.n_slots = b->total_q * kTopK;
-    a.G = G;
+    a.sp = make_split(b->total_q, G);
     a.out = out;
     a.out_f32 = out_dtype == DSA_DTYPE_F32;
     a.lse = lse;
     a.part_o = static_cast<float*>(ws);
     a.part_ml = a.part_o + (size_t)2 * G * 64 * 512;
-    const size_t cnt_off = ((size_t)2 * G * 64 * 512 * 4 + (size_t)2 * G * 64 * 2 * 4 + 255) / 256 * 256;
-    a.row_done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + cnt_off);
     a.st = st;
-    if (cudaMemsetAsync(a.row_done, 0, (size_t)b->total_q * 4, s) != cudaSuccess) return DSA_ERR_CUDA;
     mtc::sparse_mla_tc_kernel<<<(unsigned)G, mtc::kThreads, mtc::kSmemAlloc, s>>>(a);
     DSA_CHECK_LAUNCH();
+    unsigned nx = 0;                                        // combine blocks: candidate rows
+    if (a.sp.mode == mtc::SPLIT_ROW_CTAS) nx = (unsigned)b->total_q;
+    else if (a.sp.mode == mtc::SPLIT_EQUAL) nx = (unsigned)(G - 1);
+    if (nx > 0) {
+        mtc::combine_kernel<<<dim3(nx, 64 / mtc::kCombHeads), mtc::kCombThreads, 0, s>>>(a);
+        DSA_CHECK_LAUNCH();
+    }
     return DSA_OK;
 }
 
