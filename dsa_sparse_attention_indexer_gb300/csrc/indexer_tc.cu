@@ -23,8 +23,11 @@
 //                  select) whenever it fills; the threshold rises to the
 //                  2048th key.  A segment ends with its exact local top-2048.
 //     No full score row is ever written to memory.
-//  3. merge kernel: per query row, radix select over the union of the row's
-//     segment candidates (ties -> lower position), sorted by position.
+//  3. merge: one block per segment keeps the candidates at or above the bin
+//     of its row's 2048th key (the row histogram of all segment candidates
+//     gives that bin); one block per query row then selects the rest of the
+//     2048 inside that bin exactly (ties -> lower position) and sorts by
+//     position.
 // The global top-2048 is inside the union of the segment top-2048s, and the
 // shared (key desc, position asc) order makes ties consistent.
 #include "dsa_internal.cuh"
@@ -622,57 +625,187 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
 }
 
 // ---------------------------------------------------------------- merge
-// Per query row.  The row histogram (top 12 key bits of every visible score)
-// gives the bin b* holding the 2048th score and the count A above it; one flat
-// pass over the row's segment candidates keeps bins > b* and gathers bin b*
-// into shared memory, where the remaining 2048 - A are selected exactly.
+// Two kernels after the score kernel.
+//  merge_filter_kernel, one block per segment: the row histogram (top 12 key
+//    bits of every segment candidate of the row) gives the bin b* that holds
+//    the row's 2048th key.  The block compacts its segment's candidates in
+//    place to [bins > b* | bin b*] and packs the two counts into cand_cnt
+//    (sure | boundary << 16); lower bins cannot reach the row's top-2048.
+//  merge_kernel, one block per query row: gathers the row's sure entries,
+//    selects the remaining 2048 - sure among the bin-b* entries exactly (ties
+//    -> lower position), sorts the 2048 by position and writes them out.
+constexpr int kFiltThreads = 256;
+constexpr int kFiltPer = kTopK / kFiltThreads;     // candidates per thread
+
+__global__ void __launch_bounds__(kFiltThreads)
+merge_filter_kernel(BatchDev b, Plan p) {
+    __shared__ int32_t scratch[32];
+    __shared__ uint32_t s_bstar;
+    const int s = blockIdx.x;
+    if (s >= p.seg_first[b.batch]) return;             // launched for the most segments a plan can hold
+    const int tid = threadIdx.x;
+    const Seg sg = p.segs[s];
+    const int64_t row = b.q_start[sg.r];
+    // b*: thread tid owns the 16 bins 4095 - 16 tid .. 4080 - 16 tid
+    const uint4* h4 = reinterpret_cast<const uint4*>(p.hist + row * 4096);
+    uint32_t c[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 v = __ldcg(h4 + 1023 - (tid * 4 + q));
+        c[4 * q + 0] = v.w;
+        c[4 * q + 1] = v.z;
+        c[4 * q + 2] = v.y;
+        c[4 * q + 3] = v.x;
+    }
+    int mine = 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) mine += (int)c[q];
+    if (tid == 0) s_bstar = 0u;                        // fewer than 2048 candidates: keep them all
+    int tot;
+    int above = sel::excl_scan<kFiltThreads, 0>(mine, tid, scratch, &tot);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        if (above < kTopK && above + (int)c[q] >= kTopK) s_bstar = (uint32_t)(4095 - (tid * 16 + q));
+        above += (int)c[q];
+    }
+    __syncthreads();
+    const uint32_t bstar = s_bstar;
+    const int cnt = min(p.cand_cnt[s], kTopK);
+    uint32_t* key = p.cand_key + (int64_t)s * kTopK;
+    int32_t* pos = p.cand_pos + (int64_t)s * kTopK;
+    uint32_t k[kFiltPer];
+    int32_t ps[kFiltPer];
+    uint32_t cls = 0;                                  // 2 bits per entry: 1 sure, 2 boundary
+    int n_s = 0, n_b = 0;
+#pragma unroll
+    for (int u = 0; u < kFiltPer; ++u) {
+        const int i = tid + u * kFiltThreads;
+        const bool have = i < cnt;
+        k[u] = have ? key[i] : 0u;
+        ps[u] = have ? pos[i] : 0;
+        const uint32_t bin = k[u] >> 20;
+        const uint32_t cu = !have ? 0u : bin > bstar ? 1u : bin == bstar ? 2u : 0u;
+        cls |= cu << (2 * u);
+        n_s += cu == 1u;
+        n_b += cu == 2u;
+    }
+    int tot_s, tot_b;
+    int off_s = sel::excl_scan<kFiltThreads, 0>(n_s, tid, scratch, &tot_s);   // every read is done past here
+    int off_b = tot_s + sel::excl_scan<kFiltThreads, 0>(n_b, tid, scratch, &tot_b);
+#pragma unroll
+    for (int u = 0; u < kFiltPer; ++u) {
+        const uint32_t cu = (cls >> (2 * u)) & 3u;
+        if (cu == 1u) {
+            key[off_s] = k[u];
+            pos[off_s] = ps[u];
+            ++off_s;
+        } else if (cu == 2u) {
+            key[off_b] = k[u];
+            pos[off_b] = ps[u];
+            ++off_b;
+        }
+    }
+    if (tid == 0) p.cand_cnt[s] = tot_s | (tot_b << 16);
+}
+
+// Largest j < n with pre[j] <= i (pre non-decreasing, pre[0] = 0 <= i).
+__device__ __forceinline__ int seg_lookup(const int32_t* pre, int n, int i) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// The bin-b* entries of a row's filtered segment slots, as a selection source
+// (slot j: sure entries [0, ns_j), then nb_j boundary entries).
+struct BndSrc {
+    const uint32_t* key;        // the row's first segment slot
+    const int32_t* pos;
+    const int32_t* ns_pre;      // [nseg + 1] prefix of sure counts (shared memory)
+    const int32_t* nb_pre;      // [nseg + 1] prefix of boundary counts (shared memory)
+    int nseg, n;
+    __device__ __forceinline__ int64_t at(int i) const {
+        const int j = seg_lookup(nb_pre, nseg, i);
+        return (int64_t)j * kTopK + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
+    }
+    template <class F>
+    __device__ __forceinline__ void visit(int gt, F&& f) const {
+        const int nr = (n + 1023) / 1024 * 1024;
+        for (int i = gt; i < nr; i += 1024) {
+            const bool a = i < n;
+            const int64_t x = a ? at(i) : 0;
+            f(a, a ? key[x] : 0u, a ? pos[x] : 0);
+        }
+    }
+};
+
+// Ascending bitonic sort of 2048 packed (position << 32 | key) values by 1024
+// threads.  Thread t holds elements i0 = 64 (t / 32) + 2 (t % 32) and i0 + 1
+// in registers; partner distances up to 32 are exchanged by warp shuffles and
+// only distances >= 64 go through shared memory (v64, 2048 words).
+__device__ __forceinline__ void sort2048_regs(uint64_t& a, uint64_t& c, uint64_t* v64, int gt) {
+    const int i0 = 64 * (gt >> 5) + 2 * (gt & 31);
+    auto reg_stages = [&](int size, int smax) {
+        const bool up = (i0 & size) == 0;
+        for (int stride = smax; stride >= 1; stride >>= 1) {
+            if (stride == 1) {
+                if ((a > c) == up) {
+                    const uint64_t t = a;
+                    a = c;
+                    c = t;
+                }
+            } else {
+                const int m = stride >> 1;
+                const uint64_t pa = __shfl_xor_sync(0xffffffffu, a, m);
+                const uint64_t pc = __shfl_xor_sync(0xffffffffu, c, m);
+                const bool take_min = ((i0 & stride) == 0) == up;
+                a = take_min ? min(a, pa) : max(a, pa);
+                c = take_min ? min(c, pc) : max(c, pc);
+            }
+        }
+    };
+    for (int size = 2; size <= 64; size <<= 1) reg_stages(size, size >> 1);
+    for (int size = 128; size <= kTopK; size <<= 1) {
+        v64[i0] = a;
+        v64[i0 + 1] = c;
+        __syncthreads();
+        for (int stride = size >> 1; stride >= 64; stride >>= 1) {
+            const int lo = 2 * gt - (gt & (stride - 1)), hi = lo + stride;
+            const bool up = (lo & size) == 0;
+            const uint64_t x = v64[lo], y = v64[hi];
+            if ((x > y) == up) {
+                v64[lo] = y;
+                v64[hi] = x;
+            }
+            __syncthreads();
+        }
+        a = v64[i0];                                   // only this thread reads or writes i0, i0 + 1 until the next barrier
+        c = v64[i0 + 1];
+        reg_stages(size, 32);
+    }
+}
+
 constexpr int kMergeThreads = 1024;
 constexpr int kBndCap = 16384;
 constexpr int kMaxSegs = 1024;
 constexpr int kMOffHist = 0;
-constexpr int kMOffSelPos = kMOffHist + 4096 * 4;
+constexpr int kMOffSelPos = kMOffHist + 4096 * 4;                 // selected positions, then keys: 2048 x u64 for the sort
 constexpr int kMOffSelKey = kMOffSelPos + kTopK * 4;
-constexpr int kMOffSegOff = kMOffSelKey + kTopK * 4;
-constexpr int kMOffBndKey = kMOffSegOff + (kMaxSegs + 1) * 4 + 12;
+constexpr int kMOffNs = kMOffSelKey + kTopK * 4;
+constexpr int kMOffNb = kMOffNs + (kMaxSegs + 1) * 4;
+constexpr int kMOffBndKey = (kMOffNb + (kMaxSegs + 1) * 4 + 15) / 16 * 16;
 constexpr int kMOffBndPos = kMOffBndKey + kBndCap * 4;
 constexpr int kMOffMisc = kMOffBndPos + kBndCap * 4;
 constexpr int kMergeSmem = kMOffMisc + 256;
+static_assert(kMergeThreads * 2 == kTopK, "the sort holds two elements per thread");
+static_assert(kMOffSelPos % 8 == 0, "the sort reuses the selection as 64-bit words");
 
 struct MergeMisc {
-    int32_t n_sel, n_bnd, above;
-    uint32_t bstar;
+    int32_t n_sel, n_sure, n_bnd;
     sel::Found found;
     int32_t scratch[32];
-};
-
-// A row's candidates in their physical slots: segment s0 + j holds
-// cnt[j] <= 2048 entries at [(s0 + j) * 2048, ...).  Threads walk the slots
-// with several independent loads in flight; empty slots are skipped.
-struct PhysSrc {
-    const uint32_t* key;
-    const int32_t* pos;
-    const int32_t* cnt;         // [nseg] in shared memory
-    int s0, nseg;
-    template <class F>
-    __device__ __forceinline__ void visit(int gt, F&& f) const {
-        constexpr int U = 8;
-        const int64_t nslots = (int64_t)nseg * kTopK;
-        const int64_t base0 = (int64_t)s0 * kTopK;
-        for (int64_t v0 = gt; v0 < nslots; v0 += (int64_t)kMergeThreads * U) {
-            uint32_t k[U];
-            int32_t p[U];
-            bool a[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + (int64_t)u * kMergeThreads;
-                a[u] = v < nslots && (int)(v % kTopK) < cnt[v / kTopK];
-                k[u] = a[u] ? key[base0 + v] : 0u;
-                p[u] = a[u] ? pos[base0 + v] : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) f(a[u], k[u], p[u]);
-        }
-    }
 };
 
 __global__ void __launch_bounds__(kMergeThreads)
@@ -681,7 +814,8 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     uint32_t* hist = reinterpret_cast<uint32_t*>(msm + kMOffHist);
     int32_t* sel_pos = reinterpret_cast<int32_t*>(msm + kMOffSelPos);
     uint32_t* sel_key = reinterpret_cast<uint32_t*>(msm + kMOffSelKey);
-    int32_t* seg_off = reinterpret_cast<int32_t*>(msm + kMOffSegOff);
+    int32_t* ns_pre = reinterpret_cast<int32_t*>(msm + kMOffNs);
+    int32_t* nb_pre = reinterpret_cast<int32_t*>(msm + kMOffNb);
     uint32_t* bnd_key = reinterpret_cast<uint32_t*>(msm + kMOffBndKey);
     int32_t* bnd_pos = reinterpret_cast<int32_t*>(msm + kMOffBndPos);
     MergeMisc* mm = reinterpret_cast<MergeMisc*>(msm + kMOffMisc);
@@ -699,85 +833,141 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
         }
         return;
     }
-    // candidate counts of the row's segments
-    const int s0 = p.seg_first[r], nseg = p.seg_first[r + 1] - s0;    // nseg <= number of CTAs <= 1024
-    if (gt < nseg) seg_off[gt] = p.cand_cnt[s0 + gt];
-    // threshold bin from the row histogram
-    const uint32_t* gh = p.hist + row * 4096;
-    for (int i = gt; i < 4096; i += kMergeThreads) hist[i] = gh[i];
-    if (gt == 0) { mm->n_sel = 0; mm->n_bnd = 0; }
-    __syncthreads();
-    {
-        constexpr int per = 4096 / kMergeThreads;
-        int mine = 0;
-        for (int q = 0; q < per; ++q) mine += (int)hist[4095 - (gt * per + q)];
-        int tot;
-        int above = sel::excl_scan<kMergeThreads, 0>(mine, gt, mm->scratch, &tot);
-        for (int q = 0; q < per; ++q) {
-            const int bb = 4095 - (gt * per + q);
-            const int cc = (int)hist[bb];
-            if (above < kTopK && above + cc >= kTopK) { mm->bstar = (uint32_t)bb; mm->above = above; }
-            above += cc;
-        }
+    // filtered counts of the row's segments (nseg <= number of CTAs <= 1024)
+    const int s0 = p.seg_first[r], nseg = p.seg_first[r + 1] - s0;
+    const int packed = gt < nseg ? p.cand_cnt[s0 + gt] : 0;
+    int n_sure, n_bnd;
+    const int es = sel::excl_scan<kMergeThreads, 0>(packed & 0xffff, gt, mm->scratch, &n_sure);
+    const int eb = sel::excl_scan<kMergeThreads, 0>(packed >> 16, gt, mm->scratch, &n_bnd);
+    if (gt <= nseg) {
+        ns_pre[gt] = gt < nseg ? es : n_sure;
+        nb_pre[gt] = gt < nseg ? eb : n_bnd;
     }
+    if (gt == 0) mm->n_sel = 0;
     __syncthreads();
-    const uint32_t bstar = mm->bstar;
-    PhysSrc src{p.cand_key, p.cand_pos, seg_off, s0, nseg};
-    // one pass: bins above b* are in; bin b* goes to the boundary buffer
-    src.visit(gt, [&](bool a, uint32_t key, int32_t pos) {
-        if (!a) return;
-        const uint32_t bin = key >> 20;
-        if (bin > bstar) {
-            const int i = atomicAdd(&mm->n_sel, 1);
-            if (i < kTopK) { sel_pos[i] = pos; sel_key[i] = key; }
-        } else if (bin == bstar) {
-            const int i = atomicAdd(&mm->n_bnd, 1);
-            if (i < kBndCap) { bnd_key[i] = key; bnd_pos[i] = pos; }
-        }
-    });
-    __syncthreads();
-    const int n_sure = mm->n_sel, n_bnd = mm->n_bnd;
+    const uint32_t* ckey = p.cand_key + (int64_t)s0 * kTopK;
+    const int32_t* cpos = p.cand_pos + (int64_t)s0 * kTopK;
+    n_sure = min(n_sure, kTopK);
+    for (int i = gt; i < n_sure; i += kMergeThreads) {           // entries above the boundary bin: all in
+        const int j = seg_lookup(ns_pre, nseg, i);
+        const int64_t x = (int64_t)j * kTopK + (i - ns_pre[j]);
+        sel_pos[i] = cpos[x];
+        sel_key[i] = ckey[x];
+    }
     const int need = kTopK - n_sure;
-    __syncthreads();
-    if (n_bnd <= kBndCap && n_sure == mm->above && need <= n_bnd) {
-        if (need > 0 && n_bnd > need) {
-            sel::SmemSrc<kMergeThreads> bs{bnd_key, bnd_pos, n_bnd};
-            const sel::Threshold th = sel::topk_threshold<kMergeThreads, 0>(bs, need, gt, hist, mm->scratch,
-                                                                            &mm->found);
-            for (int i = gt; i < n_bnd; i += kMergeThreads) {
-                if (th.keep(bnd_key[i], bnd_pos[i])) {
-                    const int j = atomicAdd(&mm->n_sel, 1);
-                    if (j < kTopK) { sel_pos[j] = bnd_pos[i]; sel_key[j] = bnd_key[i]; }
-                }
-            }
-        } else if (need > 0) {
-            for (int i = gt; i < n_bnd; i += kMergeThreads) { sel_pos[n_sure + i] = bnd_pos[i]; sel_key[n_sure + i] = bnd_key[i]; }
-            if (gt == 0) mm->n_sel = n_sure + n_bnd;
+    int ns = n_sure;
+    if (need > 0 && n_bnd <= need) {                             // the whole boundary bin fits
+        for (int i = gt; i < n_bnd; i += kMergeThreads) {
+            const int j = seg_lookup(nb_pre, nseg, i);
+            const int64_t x = (int64_t)j * kTopK + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
+            sel_pos[n_sure + i] = cpos[x];
+            sel_key[n_sure + i] = ckey[x];
         }
-    } else {
-        // boundary bin too large for shared memory: exact selection over all candidates
-        const sel::Threshold th = sel::topk_threshold<kMergeThreads, 0>(src, kTopK, gt, hist, mm->scratch, &mm->found);
-        if (gt == 0) mm->n_sel = 0;
+        ns = n_sure + n_bnd;
+    } else if (need > 0 && n_bnd <= kBndCap) {                   // exact selection in shared memory
+        for (int i = gt; i < n_bnd; i += kMergeThreads) {
+            const int j = seg_lookup(nb_pre, nseg, i);
+            const int64_t x = (int64_t)j * kTopK + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
+            bnd_pos[i] = cpos[x];
+            bnd_key[i] = ckey[x];
+        }
+        if (gt == 0) mm->n_sel = n_sure;
         __syncthreads();
+        sel::SmemSrc<kMergeThreads> bs{bnd_key, bnd_pos, n_bnd};
+        const sel::Threshold th = sel::topk_threshold<kMergeThreads, 0>(bs, need, gt, hist, mm->scratch, &mm->found,
+                                                                        1, bnd_key[0] >> 20);   // one bin: skip it
+        for (int i = gt; i < n_bnd; i += kMergeThreads) {
+            if (th.keep(bnd_key[i], bnd_pos[i])) {
+                const int jj = atomicAdd(&mm->n_sel, 1);
+                if (jj < kTopK) { sel_pos[jj] = bnd_pos[i]; sel_key[jj] = bnd_key[i]; }
+            }
+        }
+        __syncthreads();
+        ns = min(mm->n_sel, kTopK);
+    } else if (need > 0) {                                       // boundary bin too large: select in place
+        if (gt == 0) mm->n_sel = n_sure;
+        __syncthreads();
+        BndSrc src{ckey, cpos, ns_pre, nb_pre, nseg, n_bnd};
+        const sel::Threshold th = sel::topk_threshold<kMergeThreads, 0>(src, need, gt, hist, mm->scratch, &mm->found,
+                                                                        1, ckey[src.at(0)] >> 20);
         src.visit(gt, [&](bool a, uint32_t key, int32_t pos) {
             if (a && th.keep(key, pos)) {
-                const int i = atomicAdd(&mm->n_sel, 1);
-                if (i < kTopK) { sel_pos[i] = pos; sel_key[i] = key; }
+                const int jj = atomicAdd(&mm->n_sel, 1);
+                if (jj < kTopK) { sel_pos[jj] = pos; sel_key[jj] = key; }
             }
         });
+        __syncthreads();
+        ns = min(mm->n_sel, kTopK);
     }
-    __syncthreads();
-    const int ns = min(mm->n_sel, kTopK);
+    if (n_valid <= (int64_t)kBndCap * 64) {
+        // Positions are distinct, so the output index of position p is the number
+        // of selected positions below it: a bitmap of the row (the boundary
+        // buffers, free now) and its popcount prefix give it without a sort.
+        uint32_t* bm = reinterpret_cast<uint32_t*>(msm + kMOffBndKey);
+        int32_t* chunk_pre = ns_pre;                                // free now: one entry per 32-word chunk
+        const int nwords = (int)((n_valid + 31) >> 5);
+        const int nchunks = (nwords + 31) >> 5;                     // <= 1024
+        for (int w = gt; w < nchunks * 32; w += kMergeThreads) bm[w] = 0u;
+        __syncthreads();
+        for (int i = gt; i < ns; i += kMergeThreads) {
+            const int32_t pp = sel_pos[i];
+            atomicOr(&bm[pp >> 5], 1u << (pp & 31));
+        }
+        __syncthreads();
+        // in-chunk prefix of every 2^gsh-word sub-chunk (16-bit, in the histogram
+        // space, free now): a rank then adds at most 2^gsh - 1 words
+        uint16_t* sub_pre = reinterpret_cast<uint16_t*>(hist);
+        int gsh = 0;
+        while ((nwords >> gsh) > 8192) ++gsh;                        // <= 2 for nwords <= 32768
+        const int lane = gt & 31, wid = gt >> 5;
+        for (int c = wid; c < nchunks; c += kMergeThreads / 32) {  // a warp counts a chunk, a lane a word
+            const int pc = __popc(bm[c * 32 + lane]);
+            int x = pc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if ((lane & ((1 << gsh) - 1)) == 0) sub_pre[(c * 32 + lane) >> gsh] = (uint16_t)(x - pc);
+            if (lane == 31) chunk_pre[c] = x;
+        }
+        __syncthreads();
+        const int ccount = gt < nchunks ? chunk_pre[gt] : 0;
+        int total;
+        const int cpre = sel::excl_scan<kMergeThreads, 0>(ccount, gt, mm->scratch, &total);   // reads done
+        if (gt < nchunks) chunk_pre[gt] = cpre;
+        __syncthreads();
+        for (int i = gt; i < ns; i += kMergeThreads) {
+            const int32_t pp = sel_pos[i];
+            const int w = pp >> 5, sub = w >> gsh;
+            int rank = chunk_pre[w >> 5] + sub_pre[sub];
+            for (int v = sub << gsh; v < w; ++v) rank += __popc(bm[v]);
+            rank += __popc(bm[w] & ((1u << (pp & 31)) - 1u));
+            out[rank] = pp;
+            if (outs) outs[rank] = key_score(sel_key[i]);
+        }
+        for (int i = ns + gt; i < kTopK; i += kMergeThreads) {   // only if candidates were missing
+            out[i] = -1;
+            if (outs) outs[i] = 0.f;
+        }
+        return;
+    }
     for (int i = ns + gt; i < kTopK; i += kMergeThreads) {    // only if candidates were missing
         sel_pos[i] = 0x7fffffff;
         sel_key[i] = 0u;
     }
     __syncthreads();
-    sel::bitonic_sort_by_pos<kMergeThreads, 0>(sel_pos, sel_key, kTopK, gt);
-    for (int i = gt; i < kTopK; i += kMergeThreads) {
-        const bool have = i < ns;
-        out[i] = have ? sel_pos[i] : -1;
-        if (outs) outs[i] = have ? key_score(sel_key[i]) : 0.f;
+    // sort by position: registers from the two arrays, then the arrays' 16 KB as 2048 64-bit words
+    const int i0 = 64 * (gt >> 5) + 2 * (gt & 31);
+    uint64_t va = ((uint64_t)(uint32_t)sel_pos[i0] << 32) | sel_key[i0];
+    uint64_t vc = ((uint64_t)(uint32_t)sel_pos[i0 + 1] << 32) | sel_key[i0 + 1];
+    __syncthreads();
+    sort2048_regs(va, vc, reinterpret_cast<uint64_t*>(msm + kMOffSelPos), gt);
+    const bool ha = i0 < ns, hc = i0 + 1 < ns;
+    *reinterpret_cast<int2*>(out + i0) = make_int2(ha ? (int32_t)(va >> 32) : -1, hc ? (int32_t)(vc >> 32) : -1);
+    if (outs) {                                        // 4-byte aligned only
+        outs[i0] = ha ? key_score((uint32_t)va) : 0.f;
+        outs[i0 + 1] = hc ? key_score((uint32_t)vc) : 0.f;
     }
 }
 
@@ -882,6 +1072,8 @@ dsa_status launch_indexer_tc(const uint8_t* q8, const float* wq, uint32_t* hist,
     itc::plan_kernel<<<1, 1024, 0, s>>>(bd, G, p);
     DSA_CHECK_LAUNCH();
     itc::score_topk_kernel<<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
+    DSA_CHECK_LAUNCH();
+    itc::merge_filter_kernel<<<(unsigned)(G + b->batch), itc::kFiltThreads, 0, s>>>(bd, p);
     DSA_CHECK_LAUNCH();
     itc::merge_kernel<<<(unsigned)b->total_q, itc::kMergeThreads, itc::kMergeSmem, s>>>(bd, p, topk, topk_scores);
     DSA_CHECK_LAUNCH();

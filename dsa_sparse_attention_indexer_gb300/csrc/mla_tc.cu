@@ -6,14 +6,21 @@
 //
 // Work split: each CTA takes one contiguous range of the T x 2048 (row, entry)
 // slots, cut one of three ways:
-//   T < SMs       each row gets c or c + 1 CTAs, cut on whole 96-token tiles,
-//                 so no CTA crosses a row (a crossing costs a second O store,
-//                 Q load and pipeline refill on that CTA's critical path);
+//   T < SMs       each row gets c CTAs, cut on whole 96-token tiles, so no CTA
+//                 crosses a row (a crossing costs a second O store, Q load and
+//                 pipeline refill on that CTA's critical path).  With c = 2 or
+//                 4 the row is one thread-block cluster whose CTAs merge their
+//                 results through distributed shared memory: each publishes its
+//                 per-head (max, sum), scales its O^T by its log-sum-exp weight,
+//                 and bulk-copies every head's columns to the CTA that owns the
+//                 head (64 / c heads each), which adds them up and writes the
+//                 output.  Tiny batches (SMs / T >= 8) take up to one CTA per
+//                 tile and merge through global partials (below);
 //   T < 8 x SMs   equal slot shares (rows at share edges are split);
 //   otherwise     whole rows per CTA (at most 1/8 imbalance, nothing split).
-// A row covered by several CTAs leaves one unnormalised partial (O, running
-// max, sum) per CTA; a second kernel merges them by log-sum-exp, spread over
-// (row, head group) CTAs.
+// Otherwise a row covered by several CTAs leaves one unnormalised
+// partial (O, running max, sum) per CTA in global memory; a second kernel
+// merges them by log-sum-exp, spread over (row, head) blocks.
 //
 // Per CTA, per tile of 96 selected tokens (the M = 128 MMA rows 96..127 are
 // padding), in transposed form so that tokens are the MMA rows:
@@ -46,6 +53,8 @@
 //               128-byte-swizzled fp16 tile (c * scale is exact in fp16 for
 //               scales in [2^-15, 2^7]; the RoPE dims convert from bf16).
 // Every wait is time-bounded; a timeout is recorded and the CTA winds down.
+#include <type_traits>
+
 #include "dsa_internal.cuh"
 #include "indexer_common.cuh"
 #include "sm100.cuh"
@@ -71,6 +80,7 @@ constexpr int kMaxPieces = 64;
 constexpr int kTilesPerRow = (kTopK + kTok - 1) / kTok;    // 22
 constexpr int kMaxParts = 24;                              // CTAs one row can span
 static_assert(kMaxParts >= kTilesPerRow, "a row is cut into at most one piece per tile");
+static_assert(kMaxParts <= 32, "one warp forms the combine weights");
 constexpr uint32_t kIdescQK = idesc_f16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, true, true);
 constexpr uint32_t kColS = 0;                              // TMEM: S^T [128 x 64]
@@ -82,16 +92,22 @@ constexpr int kOffP = kOffQ + 9 * 8192;                    // P^T: 96 token rows
 constexpr int kOffSlots = kOffP + kTok * 128;              // int32 cache slots of the row piece
 constexpr int kOffRed = kOffSlots + 2048 * 4;              // [2][4 lane quarters][64 heads] fp32
 constexpr int kOffStat = kOffRed + 2 * 4 * 64 * 4;         // m_ref, l_acc, alpha [64]
-constexpr int kOffBars = kOffStat + 3 * 64 * 4;
+constexpr int kOffXstat = kOffStat + 3 * 64 * 4;          // [8][64] (max, sum) of a row's cluster
+constexpr int kOffBars = kOffXstat + 8 * 64 * 2 * 4;
 constexpr int kOffMisc = kOffBars + 16 * 8;
 constexpr int kSmemUsed = kOffMisc + 512;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
+// in-cluster merge (c = 2 or 4): (c - 1) x 64 / c heads x 512 fp32 received plus as many staged for
+// the other CTAs (2 x 48 heads at most, c = 4) fit in the tile, Q, P and slot space, all free once
+// the last MMA has completed
+static_assert(2 * 48 * 512 * 4 <= kOffRed, "cluster exchange area");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kBlk % 1024 == 0, "swizzle atoms need 1 KB alignment");
 // S^T rows 96..127 read 32 rows past each K-block: still inside the tile / Q.
 static_assert(8 * kBlk + 128 * 128 <= kOffQ + 9 * 8192, "padding rows stay in shared memory");
 
-enum { B_QFULL = 0, B_QEMPTY, B_FULL0, B_FULL4 = B_FULL0 + 4, B_SFULL, B_PV0, B_PV3 = B_PV0 + 3, B_DRAIN, B_COUNT };
+enum { B_QFULL = 0, B_QEMPTY, B_FULL0, B_FULL4 = B_FULL0 + 4, B_SFULL, B_PV0, B_PV3 = B_PV0 + 3, B_DRAIN, B_XCHG,
+       B_COUNT };
 static_assert(B_COUNT <= 16, "barrier block");
 
 struct Misc {
@@ -110,6 +126,7 @@ struct Split {
     int32_t G;                  // CTAs
     int32_t mode;
     int32_t c, extra;           // SPLIT_ROW_CTAS: rows < extra get c + 1 CTAs, the others c
+    int32_t cluster;            // CTAs per thread-block cluster (one row each), 1 = no cluster
 };
 
 struct Args {
@@ -261,6 +278,10 @@ sparse_mla_tc_kernel(Args a) {
     const int64_t e_begin = split_begin(g, a.sp), e_end = split_begin(g + 1, a.sp);
     volatile int32_t* abort_flag = &misc->abort;
 
+    if (tid < 64) {
+        m_ref[tid] = -INFINITY;
+        l_acc[tid] = 0.f;
+    }
     if (tid == 0) {
         mbar_init(&bars[B_QFULL], kLoadWarps);
         mbar_init(&bars[B_QEMPTY], kSoftWarps);
@@ -268,6 +289,7 @@ sparse_mla_tc_kernel(Args a) {
         mbar_init(&bars[B_SFULL], 1);
         for (int i = 0; i < 4; ++i) mbar_init(&bars[B_PV0 + i], 1);
         mbar_init(&bars[B_DRAIN], 1);
+        mbar_init(&bars[B_XCHG], 1);
         misc->abort = 0;
         fence_barrier_init();
     }
@@ -636,6 +658,7 @@ sparse_mla_tc_kernel(Args a) {
             soft_sync();
             if (tid < 64) l_acc[tid] = red[256 + tid] + red[320 + tid] + red[384 + tid] + red[448 + tid];
             soft_sync();
+            if (a.sp.cluster > 1) break;                    // the row's only piece: merged in the cluster below
             const int64_t g0 = split_owner(row * kTopK, a.sp), g1 = split_owner(row * kTopK + kTopK - 1, a.sp);
             const bool whole = g0 == g1;
             const int64_t unit = whole ? 0 : slot_of(g, row, a.sp);
@@ -687,6 +710,107 @@ sparse_mla_tc_kernel(Args a) {
     }
     tc_fence_before();
     __syncthreads();
+    // ---- merge of the row inside its cluster (all 16 warps).  Every CTA
+    //      reaches both cluster barriers and sends its full share, whatever
+    //      happened above; a CTA that gave up contributes zeros (sum 0).  The
+    //      cluster size is a compile-time constant so head -> owner is a shift.
+    auto cluster_merge = [&](auto csize) {
+        constexpr int c = decltype(csize)::value;            // 2 or 4
+        tc_fence_after();
+        const int j = (int)cluster_ctarank();
+        const int64_t row = e_begin / kTopK;
+        constexpr int hpc = 64 / c;                          // heads per CTA
+        constexpr uint32_t blk = (uint32_t)hpc * 512 * 4;    // one CTA's share of one owner's heads, fp32
+        float* recv = reinterpret_cast<float*>(smem + kOffKV);   // [c - 1 senders][hpc][512]
+        float* stage = recv + (c - 1) * hpc * 512;               // [c - 1 owners][hpc][512]
+        float* xstat = reinterpret_cast<float*>(smem + kOffXstat);   // [rank][head] (max, sum)
+        if (tid == 0) mbar_arrive_expect_tx(&bars[B_XCHG], (uint32_t)(c - 1) * blk);   // armed before any send
+        if (tid < 64) {                                      // this CTA's statistics to every CTA of the row
+            const float ms = m_ref[tid], ls = *abort_flag ? 0.f : l_acc[tid];
+            const uint32_t dst = smem_addr(xstat + (j * 64 + tid) * 2);
+            for (int r = 0; r < c; ++r) {
+                st_cluster_f32(mapa_shared(dst, (uint32_t)r), ms);
+                st_cluster_f32(mapa_shared(dst + 4, (uint32_t)r), ls);
+            }
+        }
+        cluster_sync();                                     // #1: statistics everywhere, MMAs drained, barriers armed
+        float* scale = alpha;                               // [64]: this CTA's weight per head
+        if (tid < 64) {
+            float M = -INFINITY;
+            for (int r = 0; r < c; ++r)
+                if (xstat[(r * 64 + tid) * 2 + 1] > 0.f) M = fmaxf(M, xstat[(r * 64 + tid) * 2]);
+            float L = 0.f;
+            for (int r = 0; r < c; ++r) {
+                const float lr = xstat[(r * 64 + tid) * 2 + 1];
+                if (lr > 0.f) L += lr * exp2f(xstat[(r * 64 + tid) * 2] - M);
+            }
+            const float ls = xstat[(j * 64 + tid) * 2 + 1];
+            scale[tid] = (ls > 0.f && L > 0.f) ? exp2f(xstat[(j * 64 + tid) * 2] - M) / L : 0.f;
+            if (a.lse && tid / hpc == j)
+                a.lse[row * 64 + tid] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        }
+        __syncthreads();
+        // the other owners' heads, scaled, staged as [owner slot][head - first head][dim]
+        const int q4 = warp & 3, mb = warp >> 2;
+        const int dim = mb * 128 + q4 * 32 + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + kColO + mb * 64;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            if (half * 32 / hpc == j && hpc >= 32) continue;    // all own heads
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(taddr + half * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const int h = half * 32 + cc;
+                const int owner = h / hpc;
+                if (owner == j) continue;
+                const int slot = owner < j ? owner : owner - 1;
+                const float sc = scale[h];
+                stage[(slot * hpc + (h - owner * hpc)) * 512 + dim] = sc != 0.f ? __uint_as_float(o[cc]) * sc : 0.f;
+            }
+        }
+        fence_proxy_async_smem();                           // staged by plain stores, read by the copy engine
+        __syncthreads();
+        if (tid < c - 1) {                                   // one bulk copy per other owner
+            const int owner = tid < j ? tid : tid + 1;
+            const int slot_there = j < owner ? j : j - 1;
+            bulk_s2cluster(mapa_shared(smem_addr(recv + slot_there * hpc * 512), (uint32_t)owner), stage + tid * hpc * 512,
+                           blk, mapa_shared(smem_addr(&bars[B_XCHG]), (uint32_t)owner));
+        }
+        if (!mbar_wait(&bars[B_XCHG], 0) && tid == 0) timeout(41);   // the other CTAs' shares of my heads
+        cluster_sync();                                     // #2: every copy has landed: staging is free everywhere
+        // own heads: this CTA's scaled columns plus the c - 1 received shares, staged
+        // as the output block [head - h0][dim], then one bulk store
+        {
+            const int h0 = j * hpc, half = h0 >> 5;
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(taddr + half * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const int h = half * 32 + cc;
+                if (h < h0 || h >= h0 + hpc) continue;
+                const int hl = h - h0;
+                const float sc = scale[h];
+                float acc = sc != 0.f ? __uint_as_float(o[cc]) * sc : 0.f;
+                for (int sl = 0; sl < c - 1; ++sl) acc += recv[(sl * hpc + hl) * 512 + dim];
+                if (a.out_f32) stage[hl * 512 + dim] = acc;
+                else reinterpret_cast<__nv_bfloat16*>(stage)[hl * 512 + dim] = __float2bfloat16_rn(acc);
+            }
+        }
+        __syncthreads();
+        // the block of rows row * 64 + h0 .. + hpc is contiguous in the output: 16-byte stores
+        const int eb = a.out_f32 ? 4 : 2;
+        const int n16 = hpc * 512 * eb / 16;
+        const uint4* src = reinterpret_cast<const uint4*>(stage);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + (size_t)(row * 64 + j * hpc) * 512 * eb);
+        for (int e = tid; e < n16; e += kThreads) dst[e] = src[e];
+        tc_fence_before();
+        __syncthreads();
+    };
+    if (a.sp.cluster == 2) cluster_merge(std::integral_constant<int, 2>{});
+    else if (a.sp.cluster == 4) cluster_merge(std::integral_constant<int, 4>{});
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -700,13 +824,12 @@ sparse_mla_tc_kernel(Args a) {
 // not the row's first, and the row's first such boundary merges it.  Per head h of the row
 // over its partials u:  M = max m_u,  w_u = 2^(m_u - M),  L = sum w_u l_u,
 //   out_h = sum_u w_u O_u,h / L,   lse_h = (M + log2 L) ln 2.
-constexpr int kCombHeads = 4;                              // heads per combine CTA
-constexpr int kCombThreads = 256;                          // 4 heads x 512 dims, 8 dims per thread
+constexpr int kCombThreads = 128;                          // one head: 512 dims, 4 per thread
 
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(Args a) {
-    __shared__ float w_s[kMaxParts][kCombHeads];
-    __shared__ float inv_s[kCombHeads];
+    __shared__ float w_s[kMaxParts];
+    __shared__ float inv_s;
     __shared__ int64_t u_s[kMaxParts];
     int64_t row;
     if (a.sp.mode == SPLIT_ROW_CTAS) {
@@ -725,82 +848,71 @@ combine_kernel(Args a) {
     if (g0 == g1) return;                                   // written whole by its CTA
     const int np = (int)min(g1 - g0 + 1, (int64_t)kMaxParts);   // at most one CTA per tile of the row
     const int tid = threadIdx.x;
-    const int h0 = blockIdx.y * kCombHeads;
+    const int h = blockIdx.y;
     if (tid < kMaxParts) u_s[tid] = tid < np ? slot_of(g0 + tid, row, a.sp) : 0;
     __syncthreads();
-    if (tid < kCombHeads) {
-        const int h = h0 + tid;
-        float M = -INFINITY;
-        for (int q = 0; q < np; ++q) {
-            const float m = __ldcg(&a.part_ml[(u_s[q] * 64 + h) * 2]);
-            const float l = __ldcg(&a.part_ml[(u_s[q] * 64 + h) * 2 + 1]);
-            if (l > 0.f) M = fmaxf(M, m);
+    // partial q's (max, sum) of head h, one thread each; then warp 0 forms the weights
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (tid < np) ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + u_s[tid] * 64 + h);
+    if (tid < 32) {
+        float M = ml.y > 0.f ? ml.x : -INFINITY;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float w = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
+        float Lt = w * ml.y;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) Lt += __shfl_xor_sync(0xffffffffu, Lt, o);
+        if (tid < kMaxParts) w_s[tid] = w;
+        if (tid == 0) {
+            inv_s = Lt > 0.f ? 1.f / Lt : 0.f;
+            if (a.lse) a.lse[row * 64 + h] = Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
         }
-        float Lt = 0.f;
-        for (int q = 0; q < np; ++q) {
-            const float m = __ldcg(&a.part_ml[(u_s[q] * 64 + h) * 2]);
-            const float l = __ldcg(&a.part_ml[(u_s[q] * 64 + h) * 2 + 1]);
-            const float w = l > 0.f ? exp2f(m - M) : 0.f;
-            w_s[q][tid] = w;
-            Lt += w * l;
-        }
-        inv_s[tid] = Lt > 0.f ? 1.f / Lt : 0.f;
-        if (a.lse) a.lse[row * 64 + h] = Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
-    const int hl = tid >> 6, d0 = (tid & 63) * 8;
-    float acc[8];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < np; q0 += 8) {                    // eight partials' loads in flight
+        float4 v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-    for (int q0 = 0; q0 < np; q0 += 4) {                    // four partials' loads in flight
-        float4 v[4][2];
+        for (int j = 0; j < 8; ++j)
+            v[j] = q0 + j < np ? __ldcg(reinterpret_cast<const float4*>(a.part_o + (u_s[q0 + j] * 64 + h) * 512) + tid)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (q0 + j < np) {
-                const float4* src =
-                    reinterpret_cast<const float4*>(a.part_o + (u_s[q0 + j] * 64 + h0 + hl) * 512 + d0);
-                v[j][0] = __ldcg(src);
-                v[j][1] = __ldcg(src + 1);
-            } else {
-                v[j][0] = v[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float w = q0 + j < np ? w_s[q0 + j][hl] : 0.f;
-            acc[0] += w * v[j][0].x;
-            acc[1] += w * v[j][0].y;
-            acc[2] += w * v[j][0].z;
-            acc[3] += w * v[j][0].w;
-            acc[4] += w * v[j][1].x;
-            acc[5] += w * v[j][1].y;
-            acc[6] += w * v[j][1].z;
-            acc[7] += w * v[j][1].w;
+        for (int j = 0; j < 8; ++j) {
+            const float w = q0 + j < np ? w_s[q0 + j] : 0.f;
+            acc.x += w * v[j].x;
+            acc.y += w * v[j].y;
+            acc.z += w * v[j].z;
+            acc.w += w * v[j].w;
         }
     }
-    const float inv = inv_s[hl];
-    const int64_t o = (row * 64 + h0 + hl) * 512 + d0;
+    const float inv = inv_s;
+    const int64_t o = (row * 64 + h) * 512 + tid * 4;
     if (a.out_f32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o);
-        dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-        dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     } else {
-        uint32_t wv[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * j] * inv, acc[2 * j + 1] * inv);
-            wv[j] = *reinterpret_cast<uint32_t*>(&h2);
-        }
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + o) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
     }
 }
 
 }  // namespace mtc
 
-// CTAs sharing the T x 2048 slots: one per SM, and with fewer rows than SMs
-// no more than one per 96-token tile of each row.
+// CTAs per row when rows are fewer than SMs: a cluster of at most 8.
+// CTAs per row when rows are fewer than SMs: a cluster of 2 or 4 when that
+// fills the GPU best, else (tiny batches) up to one CTA per tile of the row,
+// merged through global partials.
+static int row_ctas(int64_t total_q, int sms) {
+    const int64_t per = sms / total_q;
+    if (per >= 8) return (int)std::min<int64_t>(per, mtc::kTilesPerRow);
+    return per >= 4 ? 4 : per >= 2 ? 2 : 1;
+}
+
+// CTAs sharing the T x 2048 slots: one per SM at most.
 int mla_tc_ctas(int64_t total_q, int sms) {
-    if (total_q < sms) return (int)std::min<int64_t>(sms, total_q * mtc::kTilesPerRow);
+    if (total_q < sms) return (int)(total_q * row_ctas(total_q, sms));
     return sms;
 }
 
@@ -810,10 +922,12 @@ static mtc::Split make_split(int64_t T, int G) {
     sp.N = T * kTopK;
     sp.G = G;
     sp.c = sp.extra = 0;
-    if (T < G) {
+    sp.cluster = 1;
+    if (T <= G) {
         sp.mode = mtc::SPLIT_ROW_CTAS;
         sp.c = (int32_t)(G / T);
         sp.extra = (int32_t)(G % T);
+        if (sp.extra == 0 && (sp.c == 2 || sp.c == 4)) sp.cluster = sp.c;
     } else if (T < (int64_t)8 * G) {
         sp.mode = mtc::SPLIT_EQUAL;
     } else {
@@ -851,13 +965,29 @@ dsa_status launch_sparse_mla_tc(const void* q, const int32_t* topk, const uint8_
     a.part_o = static_cast<float*>(ws);
     a.part_ml = a.part_o + (size_t)2 * G * 64 * 512;
     a.st = st;
+    if (a.sp.cluster > 1) {                                 // one cluster per row
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)G);
+        cfg.blockDim = dim3(mtc::kThreads);
+        cfg.dynamicSmemBytes = mtc::kSmemAlloc;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)a.sp.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, mtc::sparse_mla_tc_kernel, a) != cudaSuccess) return DSA_ERR_CUDA;
+        return DSA_OK;                                      // merged inside the clusters
+    }
     mtc::sparse_mla_tc_kernel<<<(unsigned)G, mtc::kThreads, mtc::kSmemAlloc, s>>>(a);
     DSA_CHECK_LAUNCH();
     unsigned nx = 0;                                        // combine blocks: candidate rows
     if (a.sp.mode == mtc::SPLIT_ROW_CTAS) nx = (unsigned)b->total_q;
     else if (a.sp.mode == mtc::SPLIT_EQUAL) nx = (unsigned)(G - 1);
     if (nx > 0) {
-        mtc::combine_kernel<<<dim3(nx, 64 / mtc::kCombHeads), mtc::kCombThreads, 0, s>>>(a);
+        mtc::combine_kernel<<<dim3(nx, 64), mtc::kCombThreads, 0, s>>>(a);
         DSA_CHECK_LAUNCH();
     }
     return DSA_OK;

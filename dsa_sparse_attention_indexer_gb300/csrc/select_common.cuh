@@ -63,16 +63,19 @@ struct Found {
 // The k-th largest key (k >= 1) among the active elements a source visits, and
 // how many elements equal to it belong to the top k.  Three passes of
 // 12 + 12 + 8 bits over the source.  hist: 4096 words of shared memory.
+// A caller that knows every active key shares the top 12 bits `top12` passes
+// pass0 = 1 and skips the first pass.
 //
 // Src::visit(gt, f) calls f(active, key, pos) for its elements with the same
 // trip count on every thread of the group.
 template <int NT, int BAR, class Src>
 __device__ void radix_kth(const Src& src, int k, int gt, uint32_t* hist, int* scratch, Found* found,
-                          uint32_t* kth_out, int* need_eq_out, int* n_eq_out) {
-    uint32_t prefix = 0, pmask = 0;
+                          uint32_t* kth_out, int* need_eq_out, int* n_eq_out, int pass0 = 0,
+                          uint32_t top12 = 0) {
+    uint32_t prefix = pass0 ? top12 << 20 : 0u, pmask = pass0 ? 0xfff00000u : 0u;
     int krem = k;
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
+    for (int pass = pass0; pass < 3; ++pass) {
         const int shift = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
         const int nb = pass < 2 ? 4096 : 256;
         for (int i = gt; i < nb; i += NT) hist[i] = 0;
@@ -154,10 +157,11 @@ struct Threshold {
 };
 
 template <int NT, int BAR, class Src>
-__device__ Threshold topk_threshold(const Src& src, int k, int gt, uint32_t* hist, int* scratch, Found* found) {
+__device__ Threshold topk_threshold(const Src& src, int k, int gt, uint32_t* hist, int* scratch, Found* found,
+                                    int pass0 = 0, uint32_t top12 = 0) {
     uint32_t kth;
     int need_eq, n_eq = 0;
-    radix_kth<NT, BAR>(src, k, gt, hist, scratch, found, &kth, &need_eq, &n_eq);
+    radix_kth<NT, BAR>(src, k, gt, hist, scratch, found, &kth, &need_eq, &n_eq, pass0, top12);
     Threshold t{kth, 0x7fffffff};
     if (n_eq > need_eq) {
         TieSrc<Src> ts{src, kth};
