@@ -37,12 +37,18 @@ import torch  # noqa: E402
 METRIC = "DSA query-tokens/s at 32K-1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
 L2_BYTES = 129 * 1024 * 1024
 
-# DRAM traffic per launch from an ncu capture, keyed by call; valid only while
-# the kernel source it was taken on is unchanged (sha256 prefix of the file).
-# Scaled to a full launch by the units processed: sparse_mla_decode from an ncu
-# capture of 16 requests (x4 rows), indexer_topk from a 256K-context decode1m
-# capture (x4 context).
-NCU_TRAFFIC = {"sparse_mla_decode": (105.6e6, "8c98073db5c500d9"), "indexer_topk": (554.5e6, "2a1005e9b5960edd")}
+# DRAM traffic per launch from an ncu capture, keyed by (workload, call), with the
+# kernel source it was taken on; valid only while that source is unchanged
+# (sha256 prefix).  decode32k sparse_mla_decode: a capture of its 64 decode rows
+# on 16K contexts (the same 2048 selected rows each, so the same launch);
+# decode1m indexer_topk: a 256K-context capture scaled by the context (x4).
+NCU_TRAFFIC = {
+    ("decode32k", "sparse_mla_decode"): (106.5e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
+                                         "68ebbdee426302f0"),
+    ("decode1m", "indexer_topk"): (569.0e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
+                                   "2144dd31fe20df87"),
+}
+FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s)
 
 
 def file_sha(path):
@@ -203,6 +209,21 @@ class Step:
 
 # our kernels per call (the sparse-MLA call also issues one memset of its row counters)
 KERNELS_PER_CALL = {"index_k_store": 1, "latent_kv_store": 1, "indexer_topk": 4, "sparse_mla_decode": 1}
+
+
+def call_flops(name, w):
+    """Tensor-core FLOPs of one launch of a call: the indexer's FP8 scoring
+    (32 heads x 128 dims x 2 per visible token and query row) and sparse MLA's
+    fp16 S and P.V (64 heads x (576 + 512) x 2 per selected token and row)."""
+    f = 0
+    for L, q in zip(w.seq_len, w.q_len):
+        for t in range(q):
+            n = L - q + t + 1
+            if name == "indexer_topk" and n > 2048:
+                f += n * 32 * 128 * 2
+            elif name == "sparse_mla_decode":
+                f += min(2048, n) * 64 * (576 + 512) * 2
+    return f
 
 
 def call_bytes(name, w):
@@ -480,12 +501,21 @@ def main():
     dom = max(res["per_call"], key=lambda k: res["per_call"][k])
     dom_us = res["per_launch"][dom]
     dom_bytes = call_bytes(dom, w)
-    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
-    src = {"indexer_topk": "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
-           "sparse_mla_decode": "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu"}.get(dom)
+    dom_flops = call_flops(dom, w)
+    tensor_peak = pk["bf16_tflops"] * (FP8_OVER_BF16 if dom == "indexer_topk" else 1.0)
+    tensor_bound = dom_flops / (tensor_peak * 1e12) > dom_bytes / (pk["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": dom_flops / (dom_us * 1e-6) / 1e12, "peak": tensor_peak,
+                "unit": "TFLOP/s",
+                "peak_note": ("FP8: measured bf16 burst x the nominal FP8/BF16 ratio" if dom == "indexer_topk"
+                              else "fp16: measured bf16 burst")}
+    else:
+        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_us * 1e-6) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
     traffic = None
-    if dom in NCU_TRAFFIC and src and NCU_TRAFFIC[dom][1] == file_sha(src):
-        traffic = NCU_TRAFFIC[dom][0]
+    rec = NCU_TRAFFIC.get((w.name, dom))
+    if rec and file_sha(rec[1]) == rec[2]:
+        traffic = rec[0]
     line = {
         "metric": METRIC, "value": value, "unit": "query_tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -502,9 +532,9 @@ def main():
             "step_frac_of_8tbs": step_bytes / (ms * 1e-3) / 1e9 / 8000.0,
             "us_per_call": {k: round(v, 2) for k, v in res["per_call"].items()},
         },
-        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"],
-                     "algorithmic_bytes_per_launch": dom_bytes, "us_per_launch": dom_us},
+        "roofline": {"kernel": dom, **roof, "traffic": traffic, "peak_source": pk["source"],
+                     "algorithmic_bytes_per_launch": dom_bytes, "algorithmic_flops_per_launch": dom_flops,
+                     "us_per_launch": dom_us},
         "clocks": res["clocks"],
         "e2e": {"value": job_throughput(w.total_q, world, res["e2e_ms"]), "unit": "query_tokens/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"], "ms_per_step": res["e2e_ms"]},
