@@ -91,7 +91,7 @@ constexpr int kOffQ = kOffKV + 9 * kBlk;                   // 9 K-blocks of [64 
 constexpr int kOffP = kOffQ + 9 * 8192;                    // P^T: 96 token rows x 64 heads fp16
 constexpr int kOffSlots = kOffP + kTok * 128;              // int32 cache slots of the row piece
 constexpr int kOffRed = kOffSlots + 2048 * 4;              // [2][4 lane quarters][64 heads] fp32
-constexpr int kOffStat = kOffRed + 2 * 4 * 64 * 4;         // m_ref, l_acc, alpha [64]
+constexpr int kOffStat = kOffRed + 2 * 4 * 64 * 4;         // m_ref, l_acc, alpha [64] (16-byte aligned)
 constexpr int kOffXstat = kOffStat + 3 * 64 * 4;          // [8][64] (max, sum) of a row's cluster
 constexpr int kOffBars = kOffXstat + 8 * 64 * 2 * 4;
 constexpr int kOffMisc = kOffBars + 16 * 8;
@@ -103,6 +103,7 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 // the last MMA has completed
 static_assert(2 * 48 * 512 * 4 <= kOffRed, "cluster exchange area");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kBlk % 1024 == 0, "swizzle atoms need 1 KB alignment");
+static_assert(kOffStat % 16 == 0, "reference maxima are read as float4");
 // S^T rows 96..127 read 32 rows past each K-block: still inside the tile / Q.
 static_assert(8 * kBlk + 128 * 128 <= kOffQ + 9 * 8192, "padding rows stay in shared memory");
 
@@ -207,6 +208,14 @@ __device__ __forceinline__ uint4 ldg_pinned(const uint4* p) {
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
     return r;
+}
+
+// 2^x by the hardware approximation (subnormal results flush to 0): its error
+// is far below the fp16 rounding that P gets next.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -580,8 +589,13 @@ sparse_mla_tc_kernel(Args a) {
                 //      exceeds its head's reference max by more than 2^kTau (always on
                 //      the piece's first tile, where the reference is -inf)
                 bool over = false;
+                const float4* mr4 = reinterpret_cast<const float4*>(m_ref + hh * 32);   // 16-byte reads
 #pragma unroll
-                for (int c = 0; c < 32; ++c) over |= v[c] > m_ref[hh * 32 + c] + kTau;
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 m = mr4[c4];
+                    over |= v[4 * c4] > m.x + kTau || v[4 * c4 + 1] > m.y + kTau || v[4 * c4 + 2] > m.z + kTau ||
+                            v[4 * c4 + 3] > m.w + kTau;
+                }
                 // S^T of tile gt is complete, and it was issued after the P.V of tile gt - 1:
                 // O^T is stable and P^T is free.
                 if (soft_any(over)) {
@@ -610,16 +624,21 @@ sparse_mla_tc_kernel(Args a) {
                         tmem_st_wait();
                     }
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) lsum[c] *= alpha[hh * 32 + c];
+                    for (int c = 0; c < 32; ++c) lsum[c] *= alpha[hh * 32 + c];   // rare: first tile of a piece
                     load_s(v);
                 }
                 // ---- probabilities, this token's running sums, and its P^T row
                 //      (heads 32 hh.. as fp16, MN-major 128-byte swizzle)
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float mr = m_ref[hh * 32 + c];
-                    v[c] = (v[c] == -INFINITY) ? 0.f : exp2f(v[c] - mr);
-                    lsum[c] += v[c];
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 m = mr4[c4];
+                    const float mr[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 4 * c4 + e;
+                        v[c] = (v[c] == -INFINITY) ? 0.f : ex2_approx(v[c] - mr[e]);
+                        lsum[c] += v[c];
+                    }
                 }
                 if (st < kTok) {
                     uint8_t* prow = smem + kOffP + st * 128;
