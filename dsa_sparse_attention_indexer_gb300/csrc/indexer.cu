@@ -13,25 +13,19 @@ index_scores_ref_kernel(const uint8_t* __restrict__ q8, const float* __restrict_
                         const uint8_t* __restrict__ cache, BatchDev b, float* __restrict__ scores,
                         int64_t ld, int32_t* __restrict__ st);
 
-struct WsRowSource {
-    const float* row;
-    __device__ __forceinline__ uint32_t key(int64_t j) const { return score_key(row[j]); }
-    __device__ __forceinline__ float score(int64_t j) const { return row[j]; }
-};
-
 // One CTA per query row: select over the row's p + 1 visible scores.
 __global__ void __launch_bounds__(kSelThreads)
 indexer_select_kernel(const float* __restrict__ scores, int64_t ld, BatchDev b,
                       int32_t* __restrict__ topk, float* __restrict__ topk_scores) {
-    __shared__ SelectSmem sm;
+    extern __shared__ __align__(16) uint8_t sel_smem[];
     const int64_t row = blockIdx.x;
     const int r = row_request(b.q_start, b.batch, row);
     const int qn = b.q_start[r + 1] - b.q_start[r];
     const int64_t t = row - b.q_start[r];
     int64_t n = (int64_t)b.seq_len[r] - qn + t + 1;            // positions 0..p
     if (n > ld) n = ld;                                          // seq_len beyond the declared bound
-    WsRowSource src{scores + row * ld};
-    select_topk_row(src, n, topk + row * kTopK, topk_scores ? topk_scores + row * kTopK : nullptr, sm);
+    select_topk_row(scores + row * ld, n, topk + row * kTopK, topk_scores ? topk_scores + row * kTopK : nullptr,
+                    sel_smem);
 }
 
 inline int64_t score_ld(const dsa_batch* b) { return ((int64_t)b->max_seq_len + 3) / 4 * 4; }
@@ -97,7 +91,14 @@ extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint
         rs = launch_indexer_rows(q8, wq, idxk_cache, b, sc, ld, true, false, plan, device_sm_count(), dev_status, s);
         if (rs != DSA_OK) return rs;
         BatchDev bd = to_dev(b);
-        indexer_select_kernel<<<(unsigned)b->total_q, kSelThreads, 0, s>>>(sc, ld, bd, topk, topk_scores);
+        static bool attr = false;
+        if (!attr) {
+            if (cudaFuncSetAttribute(indexer_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem) !=
+                cudaSuccess)
+                return DSA_ERR_CUDA;
+            attr = true;
+        }
+        indexer_select_kernel<<<(unsigned)b->total_q, kSelThreads, kSelSmem, s>>>(sc, ld, bd, topk, topk_scores);
         DSA_CHECK_LAUNCH();
     }
     if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);

@@ -899,57 +899,9 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
         __syncthreads();
         ns = min(mm->n_sel, kTopK);
     }
-    if (n_valid <= (int64_t)kBndCap * 64) {
-        // Positions are distinct, so the output index of position p is the number
-        // of selected positions below it: a bitmap of the row (the boundary
-        // buffers, free now) and its popcount prefix give it without a sort.
-        uint32_t* bm = reinterpret_cast<uint32_t*>(msm + kMOffBndKey);
-        int32_t* chunk_pre = ns_pre;                                // free now: one entry per 32-word chunk
-        const int nwords = (int)((n_valid + 31) >> 5);
-        const int nchunks = (nwords + 31) >> 5;                     // <= 1024
-        for (int w = gt; w < nchunks * 32; w += kMergeThreads) bm[w] = 0u;
-        __syncthreads();
-        for (int i = gt; i < ns; i += kMergeThreads) {
-            const int32_t pp = sel_pos[i];
-            atomicOr(&bm[pp >> 5], 1u << (pp & 31));
-        }
-        __syncthreads();
-        // in-chunk prefix of every 2^gsh-word sub-chunk (16-bit, in the histogram
-        // space, free now): a rank then adds at most 2^gsh - 1 words
-        uint16_t* sub_pre = reinterpret_cast<uint16_t*>(hist);
-        int gsh = 0;
-        while ((nwords >> gsh) > 8192) ++gsh;                        // <= 2 for nwords <= 32768
-        const int lane = gt & 31, wid = gt >> 5;
-        for (int c = wid; c < nchunks; c += kMergeThreads / 32) {  // a warp counts a chunk, a lane a word
-            const int pc = __popc(bm[c * 32 + lane]);
-            int x = pc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            if ((lane & ((1 << gsh) - 1)) == 0) sub_pre[(c * 32 + lane) >> gsh] = (uint16_t)(x - pc);
-            if (lane == 31) chunk_pre[c] = x;
-        }
-        __syncthreads();
-        const int ccount = gt < nchunks ? chunk_pre[gt] : 0;
-        int total;
-        const int cpre = sel::excl_scan<kMergeThreads, 0>(ccount, gt, mm->scratch, &total);   // reads done
-        if (gt < nchunks) chunk_pre[gt] = cpre;
-        __syncthreads();
-        for (int i = gt; i < ns; i += kMergeThreads) {
-            const int32_t pp = sel_pos[i];
-            const int w = pp >> 5, sub = w >> gsh;
-            int rank = chunk_pre[w >> 5] + sub_pre[sub];
-            for (int v = sub << gsh; v < w; ++v) rank += __popc(bm[v]);
-            rank += __popc(bm[w] & ((1u << (pp & 31)) - 1u));
-            out[rank] = pp;
-            if (outs) outs[rank] = key_score(sel_key[i]);
-        }
-        for (int i = ns + gt; i < kTopK; i += kMergeThreads) {   // only if candidates were missing
-            out[i] = -1;
-            if (outs) outs[i] = 0.f;
-        }
+    if (n_valid <= (int64_t)kBndCap * 64) {                     // the boundary buffers, free now, hold its bitmap
+        sel::write_ranked<kMergeThreads>(sel_pos, sel_key, ns, n_valid, reinterpret_cast<uint32_t*>(msm + kMOffBndKey),
+                                         ns_pre, reinterpret_cast<uint16_t*>(hist), mm->scratch, out, outs, gt);
         return;
     }
     for (int i = ns + gt; i < kTopK; i += kMergeThreads) {    // only if candidates were missing

@@ -225,5 +225,59 @@ __device__ void bitonic_sort_by_pos(int32_t* pos, uint32_t* key, int n, int gt) 
     }
 }
 
+// Writes the ns selected (position, key) pairs to out / outs in ascending
+// position order, then -1 (score 0) up to 2048.  Positions are distinct and
+// below n_valid (<= 2^20), so the output index of p is the number of selected
+// positions below p: a bitmap of the row and its popcount prefix give it
+// without a sort.  Shared memory: bm, 32 * ceil(n_valid / 1024) words;
+// chunk_pre, 1024 ints; sub_pre, 8192 uint16 (the in-chunk prefix of every
+// 2^gsh-word sub-chunk, so a rank adds at most 3 words).  The whole CTA of
+// 1024 threads calls it.
+template <int NT>
+__device__ void write_ranked(const int32_t* pos, const uint32_t* key, int ns, int64_t n_valid, uint32_t* bm,
+                             int32_t* chunk_pre, uint16_t* sub_pre, int* scratch, int32_t* out, float* outs,
+                             int gt) {
+    static_assert(NT == 1024, "one 32-word chunk prefix per thread");
+    const int nwords = (int)((n_valid + 31) >> 5);
+    const int nchunks = (nwords + 31) >> 5;                         // <= 1024
+    for (int w = gt; w < nchunks * 32; w += NT) bm[w] = 0u;
+    __syncthreads();
+    for (int i = gt; i < ns; i += NT) atomicOr(&bm[pos[i] >> 5], 1u << (pos[i] & 31));
+    __syncthreads();
+    int gsh = 0;
+    while ((nwords >> gsh) > 8192) ++gsh;                            // <= 2
+    const int lane = gt & 31, wid = gt >> 5;
+    for (int c = wid; c < nchunks; c += NT / 32) {                  // a warp counts a chunk, a lane a word
+        const int pc = __popc(bm[c * 32 + lane]);
+        int x = pc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if ((lane & ((1 << gsh) - 1)) == 0) sub_pre[(c * 32 + lane) >> gsh] = (uint16_t)(x - pc);
+        if (lane == 31) chunk_pre[c] = x;
+    }
+    __syncthreads();
+    const int ccount = gt < nchunks ? chunk_pre[gt] : 0;
+    int total;
+    const int cpre = excl_scan<NT, 0>(ccount, gt, scratch, &total);   // every read is done
+    if (gt < nchunks) chunk_pre[gt] = cpre;
+    __syncthreads();
+    for (int i = gt; i < ns; i += NT) {
+        const int32_t pp = pos[i];
+        const int w = pp >> 5, sub = w >> gsh;
+        int rank = chunk_pre[w >> 5] + sub_pre[sub];
+        for (int v = sub << gsh; v < w; ++v) rank += __popc(bm[v]);
+        rank += __popc(bm[w] & ((1u << (pp & 31)) - 1u));
+        out[rank] = pp;
+        if (outs) outs[rank] = key_score(key[i]);
+    }
+    for (int i = ns + gt; i < 2048; i += NT) {                      // only if candidates were missing
+        out[i] = -1;
+        if (outs) outs[i] = 0.f;
+    }
+}
+
 }  // namespace sel
 }  // namespace dsa

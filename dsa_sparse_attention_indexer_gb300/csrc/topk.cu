@@ -3,29 +3,22 @@
 // at most 2048 tokens selects [0, 1, ..., L-1, -1, ...]).
 //
 // One CTA per row.  Scores become order-preserving uint32 keys (-0 folded onto
-// +0).  A three-pass radix select (11 + 11 + 10 bits) finds the 2048th largest
-// key K* and how many keys equal to K* are needed; a final ordered pass keeps
-// key > K*, plus the first `need` keys == K* in position order (ties -> lower
-// position), and writes the kept positions in ascending order.
+// +0); select_topk_row reads the row twice (a histogram of the top 12 key
+// bits, then the keys at or above the bin of the 2048th) and selects the rest
+// exactly inside that bin (ties -> lower position), writing the kept positions
+// in ascending order.
 #include "dsa_internal.cuh"
 #include "topk_common.cuh"
 
 namespace dsa {
 
-struct ScoreRowSource {
-    const float* row;
-    __device__ __forceinline__ uint32_t key(int64_t j) const { return score_key(__ldg(row + j)); }
-    __device__ __forceinline__ float score(int64_t j) const { return __ldg(row + j); }
-};
-
 __global__ void __launch_bounds__(kSelThreads)
-topk_from_scores_kernel(const float* __restrict__ scores, int64_t ld,
-                        const int32_t* __restrict__ valid_len, int32_t* __restrict__ topk) {
-    __shared__ SelectSmem sm;
+topk_from_scores_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ valid_len,
+                        int64_t max_len, int32_t* __restrict__ topk) {
+    extern __shared__ __align__(16) uint8_t sel_smem[];
     const int64_t r = blockIdx.x;
-    const int64_t n = valid_len[r];
-    ScoreRowSource src{scores + r * ld};
-    select_topk_row(src, n, topk + r * kTopK, (float*)nullptr, sm);
+    const int64_t n = max((int64_t)0, min((int64_t)valid_len[r], max_len));   // never past the row
+    select_topk_row(scores + r * ld, n, topk + r * kTopK, nullptr, sel_smem);
 }
 
 }  // namespace dsa
@@ -47,7 +40,14 @@ extern "C" dsa_status dsa_topk_from_scores(const float* scores, int64_t ld, cons
     if (rows == 0) return DSA_OK;
     if (!scores || !valid_len || !topk) return DSA_ERR_INVALID_ARGUMENT;
     if (max_len > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
-    topk_from_scores_kernel<<<rows, kSelThreads, 0, as_stream(stream)>>>(scores, ld, valid_len, topk);
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(topk_from_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem) !=
+            cudaSuccess)
+            return DSA_ERR_CUDA;
+        attr = true;
+    }
+    topk_from_scores_kernel<<<rows, kSelThreads, kSelSmem, as_stream(stream)>>>(scores, ld, valid_len, max_len, topk);
     DSA_CHECK_LAUNCH();
     return DSA_OK;
 }

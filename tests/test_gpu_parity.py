@@ -153,6 +153,26 @@ def test_topk_from_scores_bit_exact():
         assert np.array_equal(topk[i], ref), f"row {i} (n={r.numel()})"
 
 
+def test_topk_from_scores_fallback_paths():
+    # a boundary bin larger than the shared-memory buffer (40000 equal keys), a
+    # row longer than the position bitmap (sorted instead), and rows that are not
+    # 16-byte aligned (ld odd: scalar loads)
+    g = _gen(17)
+    rows = [torch.full((40000,), 3.0), torch.randn(1_100_000, generator=g), torch.randn(9001, generator=g)]
+    eq = torch.randn(30000, generator=g)
+    eq[5000:25000] = 0.25                               # 20000 equal keys around the cut
+    rows.append(eq)
+    ld = max(r.numel() for r in rows) + 1               # odd: rows 1.. start off 16-byte alignment
+    S = torch.full((len(rows), ld), float("nan"))
+    for i, r in enumerate(rows):
+        S[i, :r.numel()] = r
+    vl = torch.tensor([r.numel() for r in rows], dtype=torch.int32)
+    topk = D.dsa_topk_from_scores(S.to(DEV), vl.to(DEV), max_len=ld).cpu().numpy()
+    for i, r in enumerate(rows):
+        ref = O.topk_positions(r.double().numpy(), r.numel())
+        assert np.array_equal(topk[i], ref), f"row {i} (n={r.numel()})"
+
+
 # ------------------------------------------------------------------ indexer
 def _small_workload(seq_len, q_len, seed):
     return Workload("small", seed, list(seq_len), list(q_len), ["full"])
