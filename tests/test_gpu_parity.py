@@ -379,6 +379,55 @@ def mla_case():
                 topk=torch.from_numpy(topk).to(DEV), batch=batch, out=np.stack(ref_out), lse=np.stack(ref_lse))
 
 
+def _mla_decode_rows_case(T, seed):
+    """T decode requests (one row each) of 2200.. tokens with 2048 random selected
+    positions (a few holes), built and evaluated as in mla_case."""
+    seq = [2200 + 37 * r for r in range(T)]
+    w = _small_workload(seq, [1] * T, seed)
+    g = _gen(seed)
+    pt = page_table(w, "cpu")
+    meta = batch_meta(w, "cpu")
+    cs, rs, slots = [], [], []
+    for r, L in enumerate(w.seq_len):
+        cs.append(f64(torch.randn(L, 512, generator=g).to(torch.bfloat16)))
+        rs.append(torch.randn(L, 64, generator=g).to(torch.bfloat16))
+        pp = np.arange(L)
+        slots.append(pt[r, pp // 64].numpy().astype(np.int64) * 64 + pp % 64)
+    ocache = oracle_latent_cache(w.num_pages, cs, [bf16_bits(x) for x in rs], slots)
+    q = torch.randn(T, 64, 576, generator=g).to(torch.bfloat16)
+    topk = np.stack([np.sort(np.random.default_rng(seed * 1000 + i).choice(L, 2048, replace=False))
+                     for i, L in enumerate(w.seq_len)]).astype(np.int32)
+    topk[::7, 300:305] = -1                              # holes
+    ref_out, ref_lse = [], []
+    for i, L in enumerate(w.seq_len):
+        rows = O.latent_cache_read_rows(ocache, pt[i].numpy(), np.maximum(topk[i], 0))
+        o, lse = O.sparse_mla(f64(q[i]), topk[i], rows, L - 1)
+        ref_out.append(o)
+        ref_lse.append(lse)
+    batch = D.Batch(meta["seq_len"].to(DEV), meta["q_start"].to(DEV), pt.to(DEV), w.num_pages,
+                    max_seq_len=w.max_seq_len, max_q_len=1, total_q=T)
+    return dict(cache=torch.from_numpy(ocache.reshape(-1)).to(DEV), q=q.to(DEV), topk=torch.from_numpy(topk).to(DEV),
+                batch=batch, out=np.stack(ref_out), lse=np.stack(ref_lse))
+
+
+# With 152 SMs: 24 rows run as clusters of 4 CTAs per row, 48 as clusters of 2,
+# 100 as one CTA per row (the 12-row case above takes global partials).
+@pytest.mark.parametrize("T", [24, 48, 100])
+def test_sparse_mla_row_splits_match_oracle(T):
+    c = _mla_decode_rows_case(T, 500 + T)
+    lse = torch.empty(T, 64, device=DEV)
+    st = D.new_device_status(DEV)
+    out = D.dsa_sparse_mla_decode(c["q"], c["topk"], c["cache"], c["batch"], out_dtype=D.DTYPE_F32, lse=lse,
+                                  dev_status=st)
+    outb = D.dsa_sparse_mla_decode(c["q"], c["topk"], c["cache"], c["batch"], out_dtype=D.DTYPE_BF16)
+    assert D.dsa_device_status_read(st)[0] == 0
+    out, outb = out.cpu().numpy(), outb.float().cpu().numpy()
+    for i in range(T):
+        check_attention(out[i], c["out"][i], what=f"T={T} row {i}")
+        check_attention(outb[i], round_bf16(c["out"][i]), what=f"T={T} bf16 row {i}")
+    assert np.allclose(lse.cpu().numpy(), c["lse"], rtol=1e-5, atol=1e-4)
+
+
 @pytest.mark.parametrize("entry", ["decode", "prefill"])
 def test_sparse_mla_fp32_matches_oracle(mla_case, entry):
     c = mla_case
