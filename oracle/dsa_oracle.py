@@ -20,6 +20,10 @@ Sources (the four web pages collected for dsa_sparse_attention_indexer):
   Section "配置里的 78 个字符": the indexer_types list and the freq/offset rule.
 * "GLM-5.3 推理全链路(一)", section 4.5: indexer_rope_interleave=True, and the
   full layers 0, 1, 2, 6, 10, ..., 74 (21 full, 57 shared).
+* "GLM-5.3 推理全链路(十一)", sections "优化三: MTP 迭代内复用 topk" and "优化四":
+  the draft steps of one MTP iteration reuse the first step's top-k (only with
+  one draft candidate per step), a carried seed row of index_topk +
+  index_kpool - 1 int32 is a plain copy of a selected top-k row.
 
 Readings where the pages are silent (each also listed in the design notes):
 LayerNorm eps 1e-6 with optional affine; interleaved RoPE pairs (2i, 2i+1),
@@ -33,8 +37,11 @@ positions are listed in ascending order followed by -1 padding.
 Parity pins: every function here is pinned by tests under ``-m "not gpu"``
 (codec vs the format definition and torch's float8 casts, layout constants the
 pages print, the 21/57 schedule, brute-force top-k, sparse == dense attention
-when the context fits in the top-k, closed forms).  The LayerNorm eps, RoPE base
-and RoPE pairing are NOT fixed by the pages: "parity unpinned" for those three
+when the context fits in the top-k, closed forms, the MTP seed width and
+draft-step read counts the pages print, brute-force top-k per draft position).
+The MTP reading where the pages are silent: a draft step with a context of at
+most 2048 publishes its all-positions row like any other step.  The LayerNorm
+eps, RoPE base and RoPE pairing are NOT fixed by the pages: "parity unpinned" for those three
 parameters - the tests check only self-consistency (moments, pair norms, the
 rotation group law) for them.
 """
@@ -389,3 +396,91 @@ def request_topk(q_idx, w, idx_cache, page_table_row, seq_len, q_len):
         out[t] = topk_positions(s, n_valid)
         all_scores.append(s)
     return out, all_scores
+
+
+# ----------------------------------------------------------------------------
+# Top-k reuse across the draft steps of one MTP iteration ("GLM-5.3 推理全链路
+# (十一)", sections 优化三: MTP 迭代内复用 topk, 优化四: PD 分离下的 seed 传输,
+# 乘法二: 投机草稿步数 × full 层数, and 误解四).
+# ----------------------------------------------------------------------------
+def mtp_topk_width(index_topk: int = TOPK, index_kpool: int = 1) -> int:
+    """Width of a seed row: index_topk + index_kpool - 1 (2048 for GLM-5.3,
+    whose index_kpool is 1; the extra kpool - 1 slots are tail slots)."""
+    if index_topk < 1 or index_kpool < 1:
+        raise ValueError("index_topk and index_kpool must be >= 1")
+    return index_topk + index_kpool - 1
+
+
+def mtp_seed_write(topk: np.ndarray, src_rows: np.ndarray, width: int) -> np.ndarray:
+    """Seed buffer [n, width] int32: row r is a plain copy of the selected
+    top-k row topk[src_rows[r]] (2048 int32), the tail slots are -1.  A source
+    row outside topk gives a row of -1."""
+    topk = np.asarray(topk, dtype=np.int32)
+    src_rows = np.asarray(src_rows, dtype=np.int64)
+    if width < TOPK:
+        raise ValueError("seed width below index_topk")
+    seed = np.full((len(src_rows), width), -1, dtype=np.int32)
+    for r, s in enumerate(src_rows):
+        if 0 <= s < topk.shape[0]:
+            seed[r, :TOPK] = topk[s]
+    return seed
+
+
+class MtpShareState:
+    """The shared top-k state across the draft steps of one MTP iteration.
+
+    begin(): reuse is on only when it is enabled AND the draft keeps one
+    candidate per step (eagle topk == 1: with more, the draft's rows are
+    reordered and a carried row no longer matches its request).  With reuse on,
+    a carried seed is kept when keep_carry_seed is set and one is given;
+    otherwise the state starts empty.  While reuse is on, the first step that
+    has no indices runs the indexer and publishes; every later step takes the
+    published indices.  end() forgets everything.  With reuse off every draft
+    step runs its own indexer.
+    """
+
+    def __init__(self):
+        self.reuse = False
+        self.indices = None
+
+    def begin(self, enabled: bool, eagle_topk: int, keep_carry_seed: bool = False, seed=None) -> bool:
+        self.reuse = bool(enabled) and eagle_topk == 1
+        self.indices = None
+        if self.reuse and keep_carry_seed and seed is not None:
+            self.indices = np.asarray(seed, dtype=np.int32)
+        return self.reuse
+
+    def needs_scoring(self) -> bool:
+        return not (self.reuse and self.indices is not None)
+
+    def publish(self, topk: np.ndarray):
+        self.indices = np.asarray(topk, dtype=np.int32)
+
+    def end(self):
+        self.reuse = False
+        self.indices = None
+
+
+def mtp_draft_topk(q_idx, w, idx_cache, page_table_row, seq_len0, n_steps, state: MtpShareState):
+    """The indices every draft step of one request attends with.
+
+    Draft step k (k = 0 .. n_steps-1) holds seq_len0 + k tokens and queries the
+    last one, at position seq_len0 - 1 + k, with q_idx[k] [32,128] and w[k] [32].
+    A step that needs scoring runs the indexer + top-2048 on its whole visible
+    context and publishes; the others reuse the published row as it is.
+    Returns (topk int32 [n_steps, 2048], index-cache tokens read), the read
+    count being 0 for a reused step, and the context for a scored one (a
+    context <= 2048 takes every position without scores and reads nothing)."""
+    out = np.empty((n_steps, TOPK), dtype=np.int32)
+    read = 0
+    for k in range(n_steps):
+        L = seq_len0 + k
+        if state.needs_scoring():
+            row, _ = request_topk(q_idx[k:k + 1], w[k:k + 1], idx_cache, page_table_row, L, 1)
+            if state.reuse:
+                state.publish(row[0])
+            out[k] = row[0]
+            read += L if L > TOPK else 0
+        else:
+            out[k] = state.indices
+    return out, read

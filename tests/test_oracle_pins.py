@@ -306,3 +306,106 @@ def test_sparse_mla_special_cases():
     out, _ = O.sparse_mla(q, idx, kv[np.maximum(idx, 0)], 2)               # causal: j <= 2 only
     ref, _ = O.sparse_mla(q, np.array([0, 1, 2]), kv[:3], 2)
     assert np.allclose(out, ref)
+
+
+# ------------------------------------------------------------------ MTP top-k reuse
+def _mtp_request(rng, L0, n_steps):
+    """Index cache of one request that grows to L0 + n_steps - 1 tokens, and
+    the indexer query of each draft step."""
+    L = L0 + n_steps - 1
+    pages = (L + 63) // 64
+    cache = np.zeros((pages + 2, O.INDEX_PAGE_BYTES), np.uint8)
+    pt = rng.permutation(pages + 2)[:pages].astype(np.int32)
+    kc, ks = O.index_k_prepare(rng.standard_normal((L, 128)), np.arange(L))
+    O.index_cache_write(cache, pt[np.arange(L) // 64] * 64 + np.arange(L) % 64, kc, ks)
+    qi = rng.standard_normal((n_steps, 32, 128))
+    w = rng.standard_normal((n_steps, 32)) / math.sqrt(32)
+    return cache, pt, kc, ks, qi, w
+
+
+def test_mtp_seed_width_and_draft_reads_printed_on_the_pages():
+    assert O.mtp_topk_width() == g("mtp_seed_width") == g("index_topk")
+    assert O.mtp_topk_width(2048, 3) == 2050                      # kpool - 1 tail slots
+    assert O.mtp_topk_width() * 4 == g("mtp_seed_bytes_per_request")
+    # the oracle's read count at a small context: one scored step with reuse,
+    # every step without
+    rng = np.random.default_rng(21)
+    n = g("mtp_draft_steps")
+    L0 = 2100
+    cache, pt, _, _, qi, w = _mtp_request(rng, L0, n)
+    st = O.MtpShareState()
+    assert st.begin(True, 1)
+    _, read_reuse = O.mtp_draft_topk(qi, w, cache, pt, L0, n, st)
+    st.end()
+    assert not st.begin(False, 1)
+    _, read_plain = O.mtp_draft_topk(qi, w, cache, pt, L0, n, st)
+    assert read_reuse == L0 and read_plain == sum(L0 + k for k in range(n))
+    # the same counts at a 1M context give the byte figures the pages print
+    L = 10 ** 6
+    assert abs(O.INDEX_TOKEN_BYTES * L - g("mtp_draft_reads_reuse_L1e6")) <= 0.01 * 132e6
+    assert abs(O.INDEX_TOKEN_BYTES * sum(L + k for k in range(n)) - g("mtp_draft_reads_no_reuse_L1e6")) <= 0.01 * 660e6
+
+
+def test_mtp_steps_without_reuse_match_brute_force_per_position():
+    rng = np.random.default_rng(22)
+    n, L0 = 3, 2050
+    cache, pt, kc, ks, qi, w = _mtp_request(rng, L0, n)
+    st = O.MtpShareState()
+    assert not st.begin(True, eagle_topk=4)                       # several draft candidates: reuse off
+    topk, read = O.mtp_draft_topk(qi, w, cache, pt, L0, n, st)
+    assert read == sum(L0 + k for k in range(n))
+    kd = O.e4m3_decode(kc) * ks[:, None]
+    for k in range(n):
+        L = L0 + k                                                # step k queries position L0 - 1 + k
+        qc, qs = O.index_q_quantize(qi[k])
+        qd = O.e4m3_decode(qc) * qs[:, None]
+        s = np.maximum(kd[:L] @ qd.T, 0.0) @ w[k]
+        best = np.lexsort((np.arange(L), -s))[:2048]              # score desc, then position asc
+        assert topk[k].tolist() == sorted(best.tolist())
+
+
+def test_mtp_reuse_carries_the_first_step_and_keep_carry_seed():
+    rng = np.random.default_rng(23)
+    n, L0 = 4, 2060
+    cache, pt, kc, ks, qi, w = _mtp_request(rng, L0, n)
+    st = O.MtpShareState()
+    st.begin(False, 1)
+    plain, _ = O.mtp_draft_topk(qi, w, cache, pt, L0, n, st)
+    st.end()
+    assert st.begin(True, 1) and st.needs_scoring()
+    reuse, read = O.mtp_draft_topk(qi, w, cache, pt, L0, n, st)
+    assert not st.needs_scoring()
+    assert read == L0 and all(np.array_equal(reuse[k], plain[0]) for k in range(n))
+    assert any(not np.array_equal(plain[k], plain[0]) for k in range(1, n))   # reuse is an approximation
+    st.end()
+    assert st.needs_scoring() and st.indices is None
+    # a carried seed is used from the first draft step on, and nothing is read
+    seed = O.mtp_seed_write(plain, np.array([2]), O.mtp_topk_width())
+    assert st.begin(True, 1, keep_carry_seed=True, seed=seed[0])
+    got, read = O.mtp_draft_topk(qi, w, cache, pt, L0, n, st)
+    assert read == 0 and all(np.array_equal(got[k], plain[2]) for k in range(n))
+    st.end()
+    # without keep_carry_seed the seed is dropped and the first step scores
+    assert st.begin(True, 1, keep_carry_seed=False, seed=seed[0]) and st.needs_scoring()
+    st.end()
+
+
+def test_mtp_short_context_step_publishes_every_position():
+    rng = np.random.default_rng(24)
+    n, L0 = 3, 2047                                               # steps at contexts 2047, 2048, 2049
+    cache, pt, _, _, qi, w = _mtp_request(rng, L0, n)
+    st = O.MtpShareState()
+    st.begin(True, 1)
+    got, read = O.mtp_draft_topk(qi, w, cache, pt, L0, n, st)
+    assert read == 0
+    assert all(got[k].tolist() == list(range(L0)) + [-1] for k in range(n))
+
+
+def test_mtp_seed_write_copies_rows_and_pads_the_tail():
+    topk = np.arange(3 * 2048, dtype=np.int32).reshape(3, 2048)
+    seed = O.mtp_seed_write(topk, np.array([2, 0, 5, -1]), 2050)
+    assert seed.shape == (4, 2050)
+    assert np.array_equal(seed[0, :2048], topk[2]) and np.array_equal(seed[1, :2048], topk[0])
+    assert (seed[:, 2048:] == -1).all() and (seed[2] == -1).all() and (seed[3] == -1).all()
+    with pytest.raises(ValueError):
+        O.mtp_seed_write(topk, np.array([0]), 2047)
