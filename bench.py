@@ -124,14 +124,19 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
-def workload_bytes(w):
+def workload_bytes(w, mtp_reuse=True):
     """Algorithmic bytes of one step: index-K read once per request per full
-    layer, plus 656 B per selected token per query row per layer."""
+    layer, plus 656 B per selected token per query row per layer.  An MTP
+    draft iteration reads index-K in its first step only when the steps reuse
+    the top-k, in every step otherwise."""
     n_full = sum(1 for t in w.layers if t == "full")
     idx = 0
     kv = 0
     for L, q in zip(w.seq_len, w.q_len):
-        idx += 132 * L
+        if w.draft_steps and not mtp_reuse:
+            idx += sum(132 * (L - q + t + 1) for t in range(q))
+        else:
+            idx += 132 * (L - q + 1 if w.draft_steps else L)
         for t in range(q):
             kv += 656 * min(2048, L - q + t + 1)
     return n_full * idx, kv * len(w.layers), idx, kv
@@ -192,6 +197,14 @@ class Step:
                 after_layer(l)
         return first_full
 
+    def e2e_io(self):
+        """(inputs copied first, inputs per layer, output per layer) of the e2e step."""
+        gw = self.gw
+        first = {"q_idx": gw.q_idx, "w_idx": gw.w_idx, "new_k": gw.new_k, "new_pos": gw.new_pos,
+                 "new_slot": gw.new_slot}
+        per = {l: {f"c{l}": gw.new_c[l], f"r{l}": gw.new_r[l], f"q{l}": gw.q_mla[l]} for l in gw.layers}
+        return first, per, self.out
+
     def calls(self):
         """(name, fn) for every call of one step, in order (for per-call timing)."""
         out = []
@@ -214,6 +227,105 @@ class Step:
         return out
 
 
+class MtpStep:
+    """One MTP draft iteration: the MTP layer runs `draft_steps` times, step k
+    on a batch whose requests hold k more tokens than at step 0.  Every step
+    stores its draft token's index key and latent row; with reuse on only the
+    first step runs the indexer and every step attends with its top-k (the
+    share handle's MTP iteration), with reuse off every step scores."""
+
+    def __init__(self, gw, D, reuse=True):
+        self.gw = gw
+        self.D = D
+        self.reuse = reuse
+        w = gw.w
+        dev = gw.device
+        n, B = w.draft_steps, w.batch
+        self.n = n
+        self.share = D.TopkShare()
+        self.topk = torch.empty((B, 2048), dtype=torch.int32, device=dev)
+        q0 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+        self.batches = []
+        for k in range(n):
+            seq = gw.seq_len - (n - 1 - k)
+            self.batches.append(D.Batch(seq.contiguous(), q0, gw.pt, w.num_pages, max_seq_len=w.max_seq_len - (n - 1 - k),
+                                        max_q_len=1, total_q=B))
+        self.idx_ws = D.workspace(max(D.dsa_indexer_topk_workspace_size(b) for b in self.batches), dev)
+        self.mla_ws = D.workspace(max(D.dsa_sparse_mla_workspace_size(b) for b in self.batches), dev)
+
+        def rows(t, k):                      # draft token k of every request (request-major rows)
+            return t.view(B, n, *t.shape[1:])[:, k].contiguous()
+
+        l0 = gw.layers[0]
+        self.inp = [{"q_idx": rows(gw.q_idx, k), "w_idx": rows(gw.w_idx, k), "new_k": rows(gw.new_k, k),
+                     "new_pos": rows(gw.new_pos, k), "new_slot": rows(gw.new_slot, k), "c": rows(gw.new_c[l0], k),
+                     "r": rows(gw.new_r[l0], k), "q_mla": rows(gw.q_mla[l0], k)} for k in range(n)]
+        self.kv = gw.kv_cache[l0]
+        self.out = {k: torch.empty((B, 64, 512), dtype=torch.bfloat16, device=dev) for k in range(n)}
+        self.launches_per_step = 0
+
+    def _store_k(self, k, stream):
+        x = self.inp[k]
+        self.D.dsa_index_k_store(x["new_k"], x["new_pos"], x["new_slot"], self.gw.idx_cache,
+                                 dev_status=self.gw.dev_status, stream=stream)
+
+    def _store_c(self, k, stream):
+        x = self.inp[k]
+        self.D.dsa_latent_kv_store(x["c"], x["r"], x["new_slot"], self.kv, dev_status=self.gw.dev_status,
+                                   stream=stream)
+
+    def _indexer(self, k, stream):
+        x = self.inp[k]
+        self.D.dsa_indexer_topk(x["q_idx"], x["w_idx"], self.gw.idx_cache, self.batches[k], topk=self.topk,
+                                share=self.share, layer_id=0, ws=self.idx_ws, dev_status=self.gw.dev_status,
+                                stream=stream)
+
+    def _mla(self, k, stream, topk=None):
+        x = self.inp[k]
+        self.D.dsa_sparse_mla_decode(x["q_mla"], topk, self.kv, self.batches[k],
+                                     share=None if topk is not None else self.share, out=self.out[k],
+                                     ws=self.mla_ws, dev_status=self.gw.dev_status, stream=stream)
+
+    def run(self, stream, timers=None, before_layer=None, after_layer=None):
+        def t(name, fn):
+            if timers is None:
+                fn()
+                return
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            timers.setdefault(name, []).append((e0, e1))
+
+        with self.share.mtp_iteration(enabled=self.reuse, eagle_topk=1):
+            for k in range(self.n):
+                if before_layer is not None:
+                    before_layer(k)
+                t("index_k_store", lambda: self._store_k(k, stream))
+                t("latent_kv_store", lambda: self._store_c(k, stream))
+                if self.share.needs_scoring():
+                    t("indexer_topk", lambda: self._indexer(k, stream))
+                t("sparse_mla_decode", lambda: self._mla(k, stream))
+                if after_layer is not None:
+                    after_layer(k)
+
+    def e2e_io(self):
+        per = {k: {f"{name}{k}": v for name, v in self.inp[k].items()} for k in range(self.n)}
+        return {}, per, self.out
+
+    def calls(self):
+        stream = torch.cuda.current_stream()
+        out = []
+        for k in range(self.n):
+            out.append(("index_k_store", (lambda k=k: self._store_k(k, stream))))
+            out.append(("latent_kv_store", (lambda k=k: self._store_c(k, stream))))
+            if k == 0 or not self.reuse:
+                out.append(("indexer_topk", (lambda k=k: self._indexer(k, stream))))
+            out.append(("sparse_mla_decode", (lambda k=k: self._mla(k, stream, topk=self.topk))))
+        return out
+
+
 # our kernels per call (the sparse-MLA call also issues one memset of its row counters)
 KERNELS_PER_CALL = {"index_k_store": 1, "latent_kv_store": 1, "indexer_topk": 4, "sparse_mla_decode": 1}
 
@@ -224,7 +336,7 @@ def call_flops(name, w):
     fp16 S and P.V (64 heads x (576 + 512) x 2 per selected token and row)."""
     f = 0
     for L, q in zip(w.seq_len, w.q_len):
-        for t in range(q):
+        for t in range(1 if w.draft_steps else q):          # a draft step's launch has one row per request
             n = L - q + t + 1
             if name == "indexer_topk" and n > 2048:
                 f += n * 32 * 128 * 2
@@ -234,16 +346,18 @@ def call_flops(name, w):
 
 
 def call_bytes(name, w):
-    """Algorithmic bytes of one launch of a call."""
+    """Algorithmic bytes of one launch of a call (a draft step's launch covers
+    one of the draft_steps rows of every request)."""
     _, _, idx, kv = workload_bytes(w)
+    per = w.draft_steps or 1
     if name == "indexer_topk":
         return idx
     if name == "sparse_mla_decode":
-        return kv
+        return kv / per
     if name == "index_k_store":
-        return w.total_q * (256 + 132)
+        return w.total_q * (256 + 132) / per
     if name == "latent_kv_store":
-        return w.total_q * (1152 + 656)
+        return w.total_q * (1152 + 656) / per
     return 0
 
 
@@ -269,11 +383,11 @@ def run_ours(args, rank, world):
     dev = f"cuda:{torch.cuda.current_device()}"
     w = synth.workload(args.workload, batch=args.batch, ctx=args.ctx)
     gw = GpuWorkload(w, dev)
-    step = Step(gw, D)
+    step = MtpStep(gw, D, reuse=not args.no_mtp_reuse) if w.draft_steps else Step(gw, D)
     torch.cuda.synchronize()
     stream = torch.cuda.Stream()                      # graphs are captured on a non-default stream
     torch.cuda.set_stream(stream)
-    total_bytes = sum(workload_bytes(w)[:2])
+    total_bytes = sum(workload_bytes(w, not args.no_mtp_reuse)[:2])
     flush = total_bytes < 4 * L2_BYTES
     flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
 
@@ -354,21 +468,12 @@ def run_ours(args, rank, world):
     timers = {k: [None] * len(v) for k, v in call_graphs.items()}
 
     # ---- end to end: host buffers in, host buffers out, through the same calls
-    pinned_in = {
-        "q_idx": gw.q_idx.cpu().pin_memory(), "w_idx": gw.w_idx.cpu().pin_memory(),
-        "new_k": gw.new_k.cpu().pin_memory(), "new_pos": gw.new_pos.cpu().pin_memory(),
-        "new_slot": gw.new_slot.cpu().pin_memory()}
-    for l in gw.layers:
-        pinned_in[f"c{l}"] = gw.new_c[l].cpu().pin_memory()
-        pinned_in[f"r{l}"] = gw.new_r[l].cpu().pin_memory()
-        pinned_in[f"q{l}"] = gw.q_mla[l].cpu().pin_memory()
-    dev_of = {"q_idx": gw.q_idx, "w_idx": gw.w_idx, "new_k": gw.new_k, "new_pos": gw.new_pos,
-              "new_slot": gw.new_slot}
-    for l in gw.layers:
-        dev_of[f"c{l}"] = gw.new_c[l]
-        dev_of[f"r{l}"] = gw.new_r[l]
-        dev_of[f"q{l}"] = gw.q_mla[l]
-    pinned_out = {l: torch.empty(step.out[l].shape, dtype=step.out[l].dtype).pin_memory() for l in gw.layers}
+    first_in, layer_in, outs = step.e2e_io()
+    dev_of = dict(first_in)
+    for l in layer_in:
+        dev_of.update(layer_in[l])
+    pinned_in = {k: v.cpu().pin_memory() for k, v in dev_of.items()}
+    pinned_out = {l: torch.empty(outs[l].shape, dtype=outs[l].dtype).pin_memory() for l in outs}
     h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
     d2h = sum(t.numel() * t.element_size() for t in pinned_out.values())
     # One e2e step = every input copied in from pinned memory, the step, every
@@ -378,8 +483,8 @@ def run_ours(args, rank, world):
     # new latent rows, a copy-out stream reads each layer's output as soon as its
     # sparse MLA is done.  Captured as one graph like the device-timed step.
     cs_in, cs_out = torch.cuda.Stream(), torch.cuda.Stream()
-    first_keys = ["q_idx", "w_idx", "new_k", "new_pos", "new_slot"]
-    layer_keys = {l: [f"c{l}", f"r{l}", f"q{l}"] for l in gw.layers}
+    first_keys = list(first_in)
+    layer_keys = {l: list(layer_in[l]) for l in layer_in}
 
     def e2e_step():
         for k in first_keys:
@@ -390,7 +495,7 @@ def run_ours(args, rank, world):
         cs_out.wait_event(fork)
         ready = {}
         with torch.cuda.stream(cs_in):
-            for l in gw.layers:
+            for l in layer_keys:
                 for k in layer_keys[l]:
                     dev_of[k].copy_(pinned_in[k], non_blocking=True)
                 ready[l] = torch.cuda.Event()
@@ -404,7 +509,7 @@ def run_ours(args, rank, world):
             done.record(stream)
             cs_out.wait_event(done)
             with torch.cuda.stream(cs_out):
-                pinned_out[l].copy_(step.out[l], non_blocking=True)
+                pinned_out[l].copy_(outs[l], non_blocking=True)
 
         step.run(stream, before_layer=before, after_layer=after)
         join = torch.cuda.Event()
@@ -433,7 +538,7 @@ def run_ours(args, rank, world):
 
 
 # ----------------------------------------------------------------------------
-def oracle_sample(w, budget_s: float, max_requests: int = 64):
+def oracle_sample(w, budget_s: float, max_requests: int = 64, mtp_reuse: bool = True):
     """Time the fp64 oracle on whole requests of the workload until ~budget_s.
 
     Per request, the inputs are drawn with the same distributions (request-
@@ -460,7 +565,13 @@ def oracle_sample(w, budget_s: float, max_requests: int = 64):
         q_rows = synth.normal_bf16(w, f"idx_q/req{r}", (qn, 32, 128), "cpu").double().numpy()
         wr = (torch.randn((qn, 32), generator=g) / math.sqrt(32.0)).double().numpy()
         t0 = time.perf_counter()
-        topk, _ = O.request_topk(q_rows, wr, idx_cache, pt, L, qn)
+        if w.draft_steps:                                   # one MTP iteration: the draft steps in turn
+            st = O.MtpShareState()
+            st.begin(mtp_reuse, 1)
+            topk, _ = O.mtp_draft_topk(q_rows, wr, idx_cache, pt, L - qn + 1, qn, st)
+            st.end()
+        else:
+            topk, _ = O.request_topk(q_rows, wr, idx_cache, pt, L, qn)
         spent += time.perf_counter() - t0
         sel = np.unique(topk[topk >= 0])
         for l in range(len(w.layers)):
@@ -492,7 +603,7 @@ def run_reference(args, rank, world):
     for _ in range(args.warmup if args.warmup < 1 else 1):
         pass
     for _ in range(max(1, args.steps if args.steps <= 3 else 3)):
-        n, sec = oracle_sample(w, args.ref_budget)
+        n, sec = oracle_sample(w, args.ref_budget, mtp_reuse=not args.no_mtp_reuse)
         total_q += sum(w.q_len[:n])
         t_all += sec
         steps_done += 1
@@ -508,11 +619,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode32k",
-                    choices=["tiny", "decode32k", "decode1m", "verify64k", "prefill128k"])
+                    choices=["tiny", "decode32k", "decode1m", "verify64k", "prefill128k", "mtp5_1m"])
     ap.add_argument("--batch", type=int, default=None, help="shrink the workload to its first N requests (profiling)")
     ap.add_argument("--ctx", type=int, default=None, help="shrink every context proportionally (profiling)")
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per reference pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mtp-reuse", action="store_true",
+                    help="MTP workloads: every draft step runs its own indexer (the comparison point)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -545,7 +658,7 @@ def main():
     w = res["w"]
     pk = peaks()
     ms = res["ms"]
-    idx_b, kv_b, _, _ = workload_bytes(w)
+    idx_b, kv_b, _, _ = workload_bytes(w, not args.no_mtp_reuse)
     step_bytes = idx_b + kv_b
     value = job_throughput(w.total_q, world, ms)
     dom = max(res["per_call"], key=lambda k: res["per_call"][k])
@@ -581,6 +694,7 @@ def main():
             "step_frac_of_measured_hbm": step_bytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
             "step_frac_of_8tbs": step_bytes / (ms * 1e-3) / 1e9 / 8000.0,
             "us_per_call": {k: round(v, 2) for k, v in res["per_call"].items()},
+            **({"draft_steps": w.draft_steps, "mtp_reuse": not args.no_mtp_reuse} if w.draft_steps else {}),
         },
         "roofline": {"kernel": dom, **roof, "traffic": traffic, "peak_source": pk["source"],
                      "algorithmic_bytes_per_launch": dom_bytes, "algorithmic_flops_per_launch": dom_flops,
@@ -591,7 +705,7 @@ def main():
         "gpu_launches": res["launches"] * args.steps,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        n, sec = oracle_sample(w, args.ref_budget)
+        n, sec = oracle_sample(w, args.ref_budget, mtp_reuse=not args.no_mtp_reuse)
         qrows = sum(w.q_len[:n])
         line["cpu_baseline"] = {"value": qrows / sec, "unit": "query_tokens/s", "cores": os.cpu_count(),
                                 "kind": "oracle",

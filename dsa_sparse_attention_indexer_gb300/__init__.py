@@ -10,6 +10,7 @@ The function names follow the C ABI in ``include/dsa.h``.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from ctypes import POINTER, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint8, c_void_p
@@ -43,7 +44,7 @@ DEVERR_FP16_RANGE = 16
 ERR = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARGUMENT", 2: "DSA_ERR_ALIGNMENT", 3: "DSA_ERR_UNSUPPORTED",
        4: "DSA_ERR_WORKSPACE_TOO_SMALL", 5: "DSA_ERR_NO_TOPK_SOURCE", 6: "DSA_ERR_CUDA", 7: "DSA_ERR_DEVICE",
        8: "DSA_ERR_SCRATCH_LIMIT"}
-NOALLOC_SCRATCH_BYTES = 8 << 20
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class DsaLibraryMissing(ImportError):
@@ -97,6 +98,12 @@ _SIGS = {
     "dsa_topk_share_reset": (c_int32, [c_void_p]),
     "dsa_topk_share_publish": (c_int32, [c_void_p, c_int32, c_void_p, c_int64]),
     "dsa_topk_share_get": (c_int32, [c_void_p, POINTER(c_void_p), POINTER(c_int64), POINTER(c_int32)]),
+    "dsa_mtp_topk_width": (c_int32, [c_int32, c_int32, POINTER(c_int32)]),
+    "dsa_mtp_seed_write": (c_int32, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int32, c_void_p, c_void_p]),
+    "dsa_topk_share_mtp_begin": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int64, c_int32,
+                                           POINTER(c_int32)]),
+    "dsa_topk_share_needs_scoring": (c_int32, [c_void_p, POINTER(c_int32)]),
+    "dsa_topk_share_mtp_end": (c_int32, [c_void_p]),
 }
 
 
@@ -370,6 +377,63 @@ class TopkShare:
         _check("dsa_topk_share_get", lib().dsa_topk_share_get(self.handle, ctypes.byref(p),
                                                                ctypes.byref(rows), ctypes.byref(lid)))
         return p.value, rows.value, lid.value
+
+    # ---- top-k reuse across the draft steps of one MTP iteration
+    def mtp_begin(self, enabled: bool = True, eagle_topk: int = 1, keep_carry_seed: bool = False,
+                  seed: torch.Tensor = None) -> bool:
+        """Start an MTP iteration; returns whether the draft steps reuse top-k.
+        seed: optional carried device int32 [rows, 2048] (kept alive by the caller)."""
+        if seed is not None:
+            _need(seed, torch.int32, "seed")
+        on = c_int32()
+        rows = 0 if seed is None else seed.shape[0]
+        width = 0 if seed is None else seed.shape[1]
+        _check("dsa_topk_share_mtp_begin", lib().dsa_topk_share_mtp_begin(
+            self.handle, int(bool(enabled)), eagle_topk, int(bool(keep_carry_seed)), _ptr(seed), rows, width,
+            ctypes.byref(on)))
+        return bool(on.value)
+
+    def needs_scoring(self) -> bool:
+        """False while the iteration reuses published indices (skip the indexer)."""
+        v = c_int32()
+        _check("dsa_topk_share_needs_scoring", lib().dsa_topk_share_needs_scoring(self.handle, ctypes.byref(v)))
+        return bool(v.value)
+
+    def mtp_end(self):
+        _check("dsa_topk_share_mtp_end", lib().dsa_topk_share_mtp_end(self.handle))
+
+    @contextlib.contextmanager
+    def mtp_iteration(self, enabled: bool = True, eagle_topk: int = 1, keep_carry_seed: bool = False,
+                      seed: torch.Tensor = None):
+        """`with share.mtp_iteration(...) as reuse:` - begin / end around the draft steps."""
+        reuse = self.mtp_begin(enabled, eagle_topk, keep_carry_seed, seed)
+        try:
+            yield reuse
+        finally:
+            self.mtp_end()
+
+
+def dsa_mtp_topk_width(index_topk: int = 2048, index_kpool: int = 1) -> int:
+    v = c_int32()
+    _check("dsa_mtp_topk_width", lib().dsa_mtp_topk_width(index_topk, index_kpool, ctypes.byref(v)))
+    return v.value
+
+
+def dsa_mtp_seed_write(topk, *, src_row=None, n=None, seed=None, width=None, dev_status=None, stream=None):
+    """seed[r] = topk[src_row[r]] (2048 int32) followed by -1 tail slots."""
+    _need(topk, torch.int32, "topk")
+    if src_row is not None:
+        _need(src_row, torch.int32, "src_row")
+    if n is None:
+        n = topk.shape[0] if src_row is None else src_row.shape[0]
+    if width is None:
+        width = dsa_mtp_topk_width() if seed is None else seed.shape[1]
+    if seed is None:
+        seed = torch.empty((n, width), dtype=torch.int32, device=topk.device)
+    _need(seed, torch.int32, "seed")
+    _check("dsa_mtp_seed_write", lib().dsa_mtp_seed_write(
+        _ptr(topk), topk.shape[0], _ptr(src_row), n, _ptr(seed), width, _ptr(dev_status), _stream(stream)))
+    return seed
 
 
 def index_cache_scale_view(idxk_cache: torch.Tensor) -> torch.Tensor:

@@ -12,7 +12,11 @@ struct dsa_topk_share {
     int64_t rows;
     int32_t layer_id;
     bool valid;
+    bool mtp_reuse;      // inside an MTP iteration whose draft steps reuse the published indices
 };
+
+// layer id recorded for a seed carried into an MTP iteration (no layer made it)
+constexpr int32_t kCarriedSeedLayer = -2;
 
 extern "C" int32_t dsa_abi_version(void) { return 1; }
 
@@ -72,7 +76,7 @@ extern "C" dsa_status dsa_schedule_from_freq(int32_t n_layers, int32_t freq, int
 
 extern "C" dsa_status dsa_topk_share_create(dsa_topk_share** out) {
     if (!out) return DSA_ERR_INVALID_ARGUMENT;
-    dsa_topk_share* s = new (std::nothrow) dsa_topk_share{nullptr, 0, -1, false};
+    dsa_topk_share* s = new (std::nothrow) dsa_topk_share{nullptr, 0, -1, false, false};
     if (!s) return DSA_ERR_INVALID_ARGUMENT;
     *out = s;
     return DSA_OK;
@@ -109,5 +113,57 @@ extern "C" dsa_status dsa_topk_share_get(const dsa_topk_share* s, const int32_t*
     *topk = s->topk;
     if (rows) *rows = s->rows;
     if (layer_id) *layer_id = s->layer_id;
+    return DSA_OK;
+}
+
+// Top-k reuse across the draft steps of one MTP iteration ("GLM-5.3 推理全链路
+// (十一)", 优化三: the iteration's context manager turns reuse on only for one
+// draft candidate per step, keeps a carried seed on request, and clears the
+// carried indices when the iteration ends).
+extern "C" dsa_status dsa_topk_share_mtp_begin(dsa_topk_share* s, int32_t enabled, int32_t eagle_topk,
+                                               int32_t keep_carry_seed, const int32_t* seed, int64_t rows,
+                                               int32_t seed_width, int32_t* reuse_on) {
+    if (!s || eagle_topk < 1 || rows < 0) return DSA_ERR_INVALID_ARGUMENT;
+    const bool reuse = enabled != 0 && eagle_topk == 1;
+    const bool carry = reuse && keep_carry_seed != 0 && seed != nullptr;
+    if (carry && seed_width != DSA_TOPK) return DSA_ERR_UNSUPPORTED;
+    if (reuse_on) *reuse_on = reuse ? 1 : 0;
+    if (!reuse) return DSA_OK;
+    s->mtp_reuse = true;
+    if (carry) {
+        s->topk = seed;
+        s->rows = rows;
+        s->layer_id = kCarriedSeedLayer;
+        s->valid = true;
+    } else {
+        s->topk = nullptr;
+        s->rows = 0;
+        s->layer_id = -1;
+        s->valid = false;
+    }
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_topk_share_needs_scoring(const dsa_topk_share* s, int32_t* needs) {
+    if (!s || !needs) return DSA_ERR_INVALID_ARGUMENT;
+    *needs = (s->mtp_reuse && s->valid) ? 0 : 1;
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_topk_share_mtp_end(dsa_topk_share* s) {
+    if (!s) return DSA_ERR_INVALID_ARGUMENT;
+    s->mtp_reuse = false;
+    s->topk = nullptr;
+    s->rows = 0;
+    s->layer_id = -1;
+    s->valid = false;
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_mtp_topk_width(int32_t index_topk, int32_t index_kpool, int32_t* width) {
+    if (!width || index_topk < 1 || index_kpool < 1) return DSA_ERR_INVALID_ARGUMENT;
+    const int64_t w = (int64_t)index_topk + index_kpool - 1;
+    if (w > INT32_MAX) return DSA_ERR_INVALID_ARGUMENT;
+    *width = (int32_t)w;
     return DSA_OK;
 }

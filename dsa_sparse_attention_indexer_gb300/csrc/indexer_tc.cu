@@ -44,20 +44,28 @@ namespace itc {
 using namespace sm100;
 
 constexpr int kStages = 8;
+constexpr int kAcc = 16;                        // TMEM accumulators (32 columns each) in flight
+constexpr int kSSlots = 16;                     // key-scale slots (512 B each), released by the epilogue
 constexpr int kStageBytes = 16384;              // 2 x 8192 FP8 payload (two 64-token pages)
-constexpr int kPidChunk = 128;                  // tiles whose page ids the producer fetches at once
+constexpr int kPidChunk = 64;                   // tiles whose page ids a producer fetches at once
 constexpr int kCheckEvery = 4;                  // tiles between epilogue-wide checks
 constexpr int kMinTiles = 16;                   // smallest per-CTA share of tiles
-constexpr int kCap = 6144;                      // candidate buffer entries
+constexpr int kCap = 5632;                      // candidate buffer entries
+constexpr int kSegCand = kCap;                  // candidate slots of one segment in the workspace
 constexpr int kEpiThreads = 256;                // two epilogue groups of 4 warps, alternating tiles
-constexpr int kThreads = 64 + kEpiThreads;      // + producer warp + MMA warp
+constexpr int kThreads = 96 + kEpiThreads;      // + two producer warps + MMA warp
+constexpr int kProducer2Warp = (64 + kEpiThreads) / 32;   // the second producer, after the epilogue warps
 constexpr int kEpiBar = 1;
-constexpr int kTmemCols = 64;
+constexpr int kTmemCols = 32 * kAcc;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 32);
 
 constexpr int kOffStages = 0;
-constexpr int kOffScales = kOffStages + kStages * kStageBytes;   // 2 x 256 B of key scales per stage
-constexpr int kOffB = (kOffScales + kStages * 512 + 1023) / 1024 * 1024;   // quantised query, 2 x 4 KB
+// A tile's key scales (2 x 256 B) and page mask sit in a ring of their own,
+// held until the epilogue has read them, so a 16 KB payload stage is free as
+// soon as its MMAs are done and the MMA can run kAcc tiles ahead of the
+// epilogue (a compaction of the candidate buffer then stalls no copy).
+constexpr int kOffScales = kOffStages + kStages * kStageBytes;   // kSSlots x 512 B of key scales
+constexpr int kOffB = (kOffScales + kSSlots * 512 + 1023) / 1024 * 1024;   // quantised query, 2 x 4 KB
 constexpr int kOffCbKey = kOffB + 2 * 4096;                      // candidate keys
 constexpr int kOffCbPos = kOffCbKey + kCap * 4;                  // candidate positions
 constexpr int kOffHist = kOffCbPos + kCap * 4;                   // top-12-bit histogram of the candidates
@@ -65,14 +73,15 @@ constexpr int kOffHist2 = kOffHist + 4096 * 4;                   // compaction s
 constexpr int kOffSideKey = kOffHist2;                           // survivors (reuse the scratch histogram)
 constexpr int kOffSidePos = kOffSideKey + kTopK * 4;
 constexpr int kOffBars = kOffHist2 + 4096 * 4;
-constexpr int kOffPid = kOffBars + (2 * kStages + 4) * 8;
-constexpr int kOffMisc = kOffPid + kPidChunk * 2 * 8;
-constexpr int kSmemUsed = kOffMisc + 256;
+constexpr int kOffPid = kOffBars + (2 * kStages + 2 * kAcc + 2 * kSSlots + 2) * 8;
+constexpr int kOffMisc = kOffPid + 2 * kPidChunk * 2 * 8;      // one page-id buffer per producer warp
+constexpr int kMiscBytes = 512;
+constexpr int kSmemUsed = kOffMisc + kMiscBytes;
 constexpr int kSmemAlloc = kSmemUsed + 1024;                     // slack for 1 KB alignment
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 struct Misc {
-    int32_t stage_valid[kStages];
+    int32_t slot_valid[kSSlots];                // page mask of the tile in each scale slot
     uint32_t tmem_base;
     int32_t cb_count;
     uint32_t theta;
@@ -81,7 +90,10 @@ struct Misc {
     int32_t scratch[32];
     int32_t wtot[8];
 };
-static_assert(sizeof(Misc) <= 256, "misc block");
+static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
+static_assert(kAcc % 2 == 0 && kTmemCols <= 512, "accumulators alternate between two epilogue groups");
+static_assert(kSSlots >= kStages, "scale ring at least as deep as the payload ring");
+static_assert(kStages % 2 == 0 && kSSlots % 2 == 0, "each producer warp owns the stages and slots of its parity");
 static_assert(kCap % kEpiThreads == 0 && kCap / kEpiThreads <= 32, "per-thread candidate slice");
 
 __device__ __forceinline__ int64_t cta_start(int64_t g, int64_t N, int64_t G) { return g * N / G; }
@@ -343,8 +355,11 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
     uint64_t* empty = full + kStages;
-    uint64_t* accf = empty + kStages;
-    uint64_t* acce = accf + 2;
+    uint64_t* accf = empty + kStages;                      // [kAcc] accumulator written
+    uint64_t* acce = accf + kAcc;                          // [kAcc] accumulator read by the epilogue
+    uint64_t* sfull = acce + kAcc;                         // [kSSlots] key scales landed
+    uint64_t* sempty = sfull + kSSlots;                    // [kSSlots] key scales read
+    uint64_t* bdone = sempty + kSSlots;                    // [2] MMAs reading a query buffer done
     int64_t* pid = reinterpret_cast<int64_t*>(smem + kOffPid);
     Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
     uint32_t* cb_key = reinterpret_cast<uint32_t*>(smem + kOffCbKey);
@@ -358,12 +373,18 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 4);          // MMA commit + one arrive per warp of the epilogue group
+            mbar_init(&empty[s], 1);              // the MMA commit
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAcc; ++a) {
             mbar_init(&accf[a], 1);
             mbar_init(&acce[a], 4);
         }
+        for (int j = 0; j < kSSlots; ++j) {
+            mbar_init(&sfull[j], 1);
+            mbar_init(&sempty[j], 4);             // one arrive per warp of the epilogue group
+        }
+        mbar_init(&bdone[0], 1);
+        mbar_init(&bdone[1], 1);
         misc->abort = 0;
         fence_barrier_init();
     }
@@ -383,13 +404,19 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
     }
     volatile int32_t* abort_flag = &misc->abort;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        // The warp fetches the page ids of up to kPidChunk tiles at once; lane 0
-        // then issues the copies without waiting on global loads.
-        int stage = 0;
-        uint32_t phase = 0;
-        int inflight = 0;
+    if (warp == 0 || warp == kProducer2Warp) {
+        // ------------------------------------------------------------ producers
+        // Two producer warps take alternate tiles of the CTA's running tile
+        // index (one thread issuing every copy of an SM falls well short of
+        // the HBM rate; two reach it).  Tile i uses stage i % kStages and
+        // scale slot i % kSSlots, both even counts, so each warp owns the
+        // stages and slots of its parity.  A warp fetches the page ids of up
+        // to kPidChunk tiles at once into its own buffer; its lane 0 then
+        // issues the copies of its tiles without waiting on global loads.
+        const int me = warp == 0 ? 0 : 1;
+        int64_t* mypid = pid + me * kPidChunk * 2;
+        int64_t icount = 0;                                // running tile index (lane 0)
+        int64_t last = -1;                                 // last tile this warp issued (lane 0)
         bool stop = false;
         for (int s = s_begin; s < s_end && !stop; ++s) {
             const Seg sg = p.segs[s];
@@ -399,46 +426,49 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                 const int nt = min(kPidChunk, sg.hi - c0);
                 for (int k = lane; k < 2 * nt; k += 32) {
                     const int idx = c0 * 2 + k;
-                    pid[k] = idx < b.max_pages ? (int64_t)pt[idx] : (int64_t)-2;
+                    mypid[k] = idx < b.max_pages ? (int64_t)pt[idx] : (int64_t)-2;
                 }
                 __syncwarp();
                 int ok = 1;
                 if (lane == 0) {
-                    for (int tile = c0; tile < c0 + nt; ++tile) {
-                        if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) {
+                    for (int tile = c0; tile < c0 + nt; ++tile, ++icount) {
+                        if ((int)(icount & 1) != me) continue;
+                        const int stage = (int)(icount % kStages);
+                        const uint32_t phase = (uint32_t)((icount / kStages) & 1);
+                        const int slot = (int)(icount % kSSlots);
+                        const uint32_t sphase = (uint32_t)((icount / kSSlots) & 1);
+                        if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1) ||
+                            !mbar_wait(&sempty[slot], sphase ^ 1)) {
                             ok = 0;
                             break;
                         }
                         const int t0 = tile * 128;
                         const int pages = (L - t0 > 64) ? 2 : 1;
-                        uint32_t bytes = 0;
+                        uint32_t bytes = 0;                // payload bytes
                         int vmask = 0;
                         int64_t pg[2];
                         for (int j = 0; j < pages; ++j) {
-                            pg[j] = pid[(tile - c0) * 2 + j];
+                            pg[j] = mypid[(tile - c0) * 2 + j];
                             if (pg[j] >= 0 && pg[j] < b.num_pages) {
                                 vmask |= 1 << j;
-                                bytes += 8192 + 256;
+                                bytes += 8192;
                             } else if (pg[j] == -2) {
                                 record_error(st, DSA_DEVERR_INDEX_RANGE, t0 + j * 64);   // beyond the page table row
                             } else {
                                 record_error(st, DSA_DEVERR_PAGE_RANGE, pg[j]);
                             }
                         }
-                        misc->stage_valid[stage] = vmask;
+                        misc->slot_valid[slot] = vmask;     // read after sfull[slot]
                         uint8_t* sb = smem + kOffStages + stage * kStageBytes;
                         mbar_arrive_expect_tx(&full[stage], bytes);
+                        mbar_arrive_expect_tx(&sfull[slot], bytes / 32);   // 256 B per 8192 B page
                         for (int j = 0; j < pages; ++j) {
                             if (!(vmask & (1 << j))) continue;
                             tma_load_2d(sb + j * 8192, &tmap, 0, (int32_t)(pg[j] * 66), &full[stage]);
-                            bulk_load(smem + kOffScales + stage * 512 + j * 256,
-                                      cache + pg[j] * (int64_t)kIdxPageBytes + kIdxPayloadBytes, 256, &full[stage]);
+                            bulk_load(smem + kOffScales + slot * 512 + j * 256,
+                                      cache + pg[j] * (int64_t)kIdxPageBytes + kIdxPayloadBytes, 256, &sfull[slot]);
                         }
-                        ++inflight;
-                        if (++stage == kStages) {
-                            stage = 0;
-                            phase ^= 1;
-                        }
+                        last = icount;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -449,11 +479,13 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
         if (lane == 0 && stop) {
             if (!*abort_flag) record_error(st, DSA_DEVERR_TIMEOUT, 1);
             *abort_flag = 1;
-            // let the copies already issued land before the CTA winds down
-            for (int i = 0; i < kStages && inflight > 0; ++i, --inflight) {
-                stage = (stage + kStages - 1) % kStages;
-                if (stage == kStages - 1) phase ^= 1;
-                mbar_wait(&full[stage], phase, 500000000ull);
+            // let this warp's copies land before the CTA winds down: the payloads
+            // of its tiles among the last kStages, the scales among the last
+            // kSSlots (older ones were consumed before their stage or slot was
+            // refilled)
+            for (int64_t j = last; j >= 0 && j > last - kSSlots; j -= 2) {
+                if (j > last - kStages) mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1), 500000000ull);
+                mbar_wait(&sfull[j % kSSlots], (uint32_t)((j / kSSlots) & 1), 500000000ull);
             }
         }
         __syncwarp();
@@ -466,16 +498,28 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
         bool issued_any = false, stop = false;
         int last_acc = 0;
         uint32_t last_acc_phase = 0;
+        // With kAcc tiles in flight, the MMAs of two segments back may still
+        // read a query buffer when it is due to be rewritten: each segment
+        // commits to its buffer's bdone barrier, and the rewrite waits on it.
+        uint32_t bph = 0u, bpending = 0u;                  // bit j: query buffer j
         for (int s = s_begin; s < s_end && !stop; ++s) {
             const Seg sg = p.segs[s];
             const int64_t row = b.q_start[sg.r];
             uint8_t* bq = smem + kOffB + bbuf * 4096;
+            bool seg_issued = false;
             for (int tile = sg.lo; tile < sg.hi; ++tile) {
                 int ok = 1;
                 if (lane == 0) ok = (!*abort_flag && mbar_wait(&acce[acc], acc_phase ^ 1)) ? 1 : 0;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { stop = true; break; }
                 if (tile == sg.lo) {
+                    if ((bpending >> bbuf) & 1u) {
+                        if (lane == 0) ok = mbar_wait(&bdone[bbuf], (bph >> bbuf) & 1u) ? 1 : 0;
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) { stop = true; break; }
+                        bph ^= 1u << bbuf;
+                        bpending &= ~(1u << bbuf);
+                    }
                     // B operand: head `lane` row of the quantised query, 128-byte swizzled
                     const uint4* src = reinterpret_cast<const uint4*>(q8 + row * 4096 + lane * 128);
 #pragma unroll
@@ -497,6 +541,7 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                         mma_commit(&empty[stage]);
                         mma_commit(&accf[acc]);
                         issued_any = true;
+                        seg_issued = true;
                         last_acc = acc;
                         last_acc_phase = acc_phase;
                     }
@@ -504,7 +549,12 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { stop = true; break; }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
-                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                if (++acc == kAcc) { acc = 0; acc_phase ^= 1; }
+            }
+            seg_issued = __shfl_sync(0xffffffffu, seg_issued ? 1 : 0, 0) != 0;
+            if (seg_issued) {
+                if (lane == 0) mma_commit(&bdone[bbuf]);
+                bpending |= 1u << bbuf;
             }
             bbuf ^= 1;
         }
@@ -517,7 +567,8 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
     } else {
         // ------------------------------------------------------------ epilogue
         // Two groups of 4 warps; group g takes the tiles whose running index
-        // has parity g (= its TMEM accumulator).  Warp w may read TMEM lanes
+        // has parity g (accumulator index % kAcc, so the parity of the
+        // accumulator too).  Warp w may read TMEM lanes
         // 32*(w%4) .. 32*(w%4)+31, i.e. tokens 32*(w%4) .. of the tile.
         const int et = threadIdx.x - 64;
         const int grp = (warp - 2) >> 2;
@@ -543,24 +594,24 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
             bool warp_bad = false;                     // this warp saw a timeout
             for (int tile = sg.lo; tile < sg.hi; ++tile, ++gidx) {
                 if ((int)(gidx & 1) == grp && !warp_bad) {
-                    const int stage = (int)(gidx % kStages);
-                    const uint32_t phase = (uint32_t)((gidx / kStages) & 1);
-                    const int acc = (int)(gidx & 1);
-                    const uint32_t acc_phase = (uint32_t)((gidx >> 1) & 1);
+                    const int slot = (int)(gidx % kSSlots);
+                    const uint32_t sphase = (uint32_t)((gidx / kSSlots) & 1);
+                    const int acc = (int)(gidx % kAcc);
+                    const uint32_t acc_phase = (uint32_t)((gidx / kAcc) & 1);
                     int ok = __all_sync(0xffffffffu, mbar_wait(&accf[acc], acc_phase));
-                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase));   // scales + page mask
+                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sfull[slot], sphase));   // scales + page mask
                     if (ok) {
                         uint32_t v[32];
                         tc_fence_after();
                         tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 32, v);
                         tmem_ld_wait();
-                        const int vmask = misc->stage_valid[stage];
-                        const float sk = reinterpret_cast<const float*>(smem + kOffScales + stage * 512)[tok];
+                        const int vmask = misc->slot_valid[slot];
+                        const float sk = reinterpret_cast<const float*>(smem + kOffScales + slot * 512)[tok];
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) {
                             mbar_arrive(&acce[acc]);
-                            mbar_arrive(&empty[stage]);
+                            mbar_arrive(&sempty[slot]);
                         }
                         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
@@ -603,12 +654,15 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                 }
             }
             if (aborted) break;
-            // segment end: exact local top-2048 and its histogram, written out
-            if (misc->cb_count > kTopK) compact_candidates(cb_key, cb_pos, hist, hist2, side_key, side_pos, misc, et);
+            // segment end: the whole buffer and its histogram, written out.  It
+            // holds the segment's top-2048 (the filter never rose above the
+            // segment's 2048th key) and maybe more; the merge filter cuts the
+            // row's candidates at the bin of the row's 2048th key, so no exact
+            // selection is needed here.
             const int cnt = misc->cb_count;
             for (int i = et; i < cnt; i += kEpiThreads) {
-                p.cand_key[(int64_t)s * kTopK + i] = cb_key[i];
-                p.cand_pos[(int64_t)s * kTopK + i] = cb_pos[i];
+                p.cand_key[(int64_t)s * kSegCand + i] = cb_key[i];
+                p.cand_pos[(int64_t)s * kSegCand + i] = cb_pos[i];
             }
             if (et == 0) p.cand_cnt[s] = cnt;
             uint32_t* gh = p.hist + row * 4096;
@@ -634,8 +688,11 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
 //  merge_kernel, one block per query row: gathers the row's sure entries,
 //    selects the remaining 2048 - sure among the bin-b* entries exactly (ties
 //    -> lower position), sorts the 2048 by position and writes them out.
-constexpr int kFiltThreads = 256;
-constexpr int kFiltPer = kTopK / kFiltThreads;     // candidates per thread
+constexpr int kFiltThreads = 512;
+constexpr int kFiltPer = kSegCand / kFiltThreads;  // candidates per thread
+static_assert(kSegCand % kFiltThreads == 0 && kFiltPer <= 16, "two class bits per candidate in a 32-bit word");
+static_assert(4096 % (kFiltThreads * 4) == 0, "whole 16-byte histogram loads per thread");
+constexpr int kFiltBins = 4096 / kFiltThreads;     // histogram bins per thread
 
 __global__ void __launch_bounds__(kFiltThreads)
 merge_filter_kernel(BatchDev b, Plan p) {
@@ -646,12 +703,21 @@ merge_filter_kernel(BatchDev b, Plan p) {
     const int tid = threadIdx.x;
     const Seg sg = p.segs[s];
     const int64_t row = b.q_start[sg.r];
-    // b*: thread tid owns the 16 bins 4095 - 16 tid .. 4080 - 16 tid
-    const uint4* h4 = reinterpret_cast<const uint4*>(p.hist + row * 4096);
-    uint32_t c[16];
+    const int cnt = min(p.cand_cnt[s], kSegCand);
+    uint32_t* key = p.cand_key + (int64_t)s * kSegCand;
+    int32_t* pos = p.cand_pos + (int64_t)s * kSegCand;
+    uint32_t k[kFiltPer];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint4 v = __ldcg(h4 + 1023 - (tid * 4 + q));
+    for (int u = 0; u < kFiltPer; ++u) {               // keys first: their loads overlap the scan below
+        const int i = tid + u * kFiltThreads;
+        k[u] = i < cnt ? key[i] : 0u;
+    }
+    // b*: thread tid owns the kFiltBins bins 4095 - kFiltBins tid downwards
+    const uint4* h4 = reinterpret_cast<const uint4*>(p.hist + row * 4096);
+    uint32_t c[kFiltBins];
+#pragma unroll
+    for (int q = 0; q < kFiltBins / 4; ++q) {
+        const uint4 v = __ldcg(h4 + 1023 - (tid * (kFiltBins / 4) + q));
         c[4 * q + 0] = v.w;
         c[4 * q + 1] = v.z;
         c[4 * q + 2] = v.y;
@@ -659,32 +725,26 @@ merge_filter_kernel(BatchDev b, Plan p) {
     }
     int mine = 0;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) mine += (int)c[q];
+    for (int q = 0; q < kFiltBins; ++q) mine += (int)c[q];
     if (tid == 0) s_bstar = 0u;                        // fewer than 2048 candidates: keep them all
     int tot;
     int above = sel::excl_scan<kFiltThreads, 0>(mine, tid, scratch, &tot);
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        if (above < kTopK && above + (int)c[q] >= kTopK) s_bstar = (uint32_t)(4095 - (tid * 16 + q));
+    for (int q = 0; q < kFiltBins; ++q) {
+        if (above < kTopK && above + (int)c[q] >= kTopK) s_bstar = (uint32_t)(4095 - (tid * kFiltBins + q));
         above += (int)c[q];
     }
     __syncthreads();
     const uint32_t bstar = s_bstar;
-    const int cnt = min(p.cand_cnt[s], kTopK);
-    uint32_t* key = p.cand_key + (int64_t)s * kTopK;
-    int32_t* pos = p.cand_pos + (int64_t)s * kTopK;
-    uint32_t k[kFiltPer];
     int32_t ps[kFiltPer];
     uint32_t cls = 0;                                  // 2 bits per entry: 1 sure, 2 boundary
     int n_s = 0, n_b = 0;
 #pragma unroll
     for (int u = 0; u < kFiltPer; ++u) {
         const int i = tid + u * kFiltThreads;
-        const bool have = i < cnt;
-        k[u] = have ? key[i] : 0u;
-        ps[u] = have ? pos[i] : 0;
         const uint32_t bin = k[u] >> 20;
-        const uint32_t cu = !have ? 0u : bin > bstar ? 1u : bin == bstar ? 2u : 0u;
+        const uint32_t cu = i >= cnt ? 0u : bin > bstar ? 1u : bin == bstar ? 2u : 0u;
+        ps[u] = cu ? pos[i] : 0;                       // positions of the kept entries only
         cls |= cu << (2 * u);
         n_s += cu == 1u;
         n_b += cu == 2u;
@@ -728,7 +788,7 @@ struct BndSrc {
     int nseg, n;
     __device__ __forceinline__ int64_t at(int i) const {
         const int j = seg_lookup(nb_pre, nseg, i);
-        return (int64_t)j * kTopK + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
+        return (int64_t)j * kSegCand + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
     }
     template <class F>
     __device__ __forceinline__ void visit(int gt, F&& f) const {
@@ -845,12 +905,12 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     }
     if (gt == 0) mm->n_sel = 0;
     __syncthreads();
-    const uint32_t* ckey = p.cand_key + (int64_t)s0 * kTopK;
-    const int32_t* cpos = p.cand_pos + (int64_t)s0 * kTopK;
+    const uint32_t* ckey = p.cand_key + (int64_t)s0 * kSegCand;
+    const int32_t* cpos = p.cand_pos + (int64_t)s0 * kSegCand;
     n_sure = min(n_sure, kTopK);
     for (int i = gt; i < n_sure; i += kMergeThreads) {           // entries above the boundary bin: all in
         const int j = seg_lookup(ns_pre, nseg, i);
-        const int64_t x = (int64_t)j * kTopK + (i - ns_pre[j]);
+        const int64_t x = (int64_t)j * kSegCand + (i - ns_pre[j]);
         sel_pos[i] = cpos[x];
         sel_key[i] = ckey[x];
     }
@@ -859,7 +919,7 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     if (need > 0 && n_bnd <= need) {                             // the whole boundary bin fits
         for (int i = gt; i < n_bnd; i += kMergeThreads) {
             const int j = seg_lookup(nb_pre, nseg, i);
-            const int64_t x = (int64_t)j * kTopK + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
+            const int64_t x = (int64_t)j * kSegCand + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
             sel_pos[n_sure + i] = cpos[x];
             sel_key[n_sure + i] = ckey[x];
         }
@@ -867,7 +927,7 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     } else if (need > 0 && n_bnd <= kBndCap) {                   // exact selection in shared memory
         for (int i = gt; i < n_bnd; i += kMergeThreads) {
             const int j = seg_lookup(nb_pre, nseg, i);
-            const int64_t x = (int64_t)j * kTopK + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
+            const int64_t x = (int64_t)j * kSegCand + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
             bnd_pos[i] = cpos[x];
             bnd_key[i] = ckey[x];
         }
@@ -975,7 +1035,7 @@ size_t tc_plan_bytes(int64_t batch, int G) {
     b = (b + 15) / 16 * 16;
     b += nseg * sizeof(Seg);                        // segs
     b = (b + 255) / 256 * 256;
-    b += nseg * kTopK * 4 * 2;                      // cand_key, cand_pos
+    b += nseg * itc::kSegCand * 4 * 2;              // cand_key, cand_pos
     b += nseg * 4;                                  // cand_cnt
     b = (b + 255) / 256 * 256;
     return b;
@@ -996,9 +1056,9 @@ Plan carve_plan(void* base, int64_t batch, int G) {
     q += nseg * sizeof(Seg);
     q = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q) + 255) & ~uintptr_t(255));
     p.cand_key = reinterpret_cast<uint32_t*>(q);
-    q += nseg * kTopK * 4;
+    q += nseg * itc::kSegCand * 4;
     p.cand_pos = reinterpret_cast<int32_t*>(q);
-    q += nseg * kTopK * 4;
+    q += nseg * itc::kSegCand * 4;
     p.cand_cnt = reinterpret_cast<int32_t*>(q);
     p.hist = nullptr;
     return p;

@@ -17,8 +17,8 @@ struct Plan {
     int32_t* seg_first;    // [B+1] first segment of each request
     int32_t* cta_range;    // [2G] segment range of each CTA
     Seg* segs;             // [G+B]
-    uint32_t* cand_key;    // [G+B, 2048]
-    int32_t* cand_pos;     // [G+B, 2048]
+    uint32_t* cand_key;    // [G+B, segment candidate slots]
+    int32_t* cand_pos;     // [G+B, segment candidate slots]
     int32_t* cand_cnt;     // [G+B]
     uint32_t* hist;        // [T, 4096] top-12-bit key histogram of every visible score, per query row
 };

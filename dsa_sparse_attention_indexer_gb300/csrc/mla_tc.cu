@@ -196,7 +196,7 @@ __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, const vo
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if ((it & 63u) == 0u && (*abort_flag || globaltimer_ns() - t0 > 2000000000ull)) return false;
     }
 }

@@ -41,14 +41,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
                  : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
+// The same with a suspend-time hint: a thread whose phase is not complete is
+// suspended by the hardware until it completes or about `hint_ns` pass,
+// instead of coming straight back to poll.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity; gives up after `limit_ns` and
-// returns false (the caller records a timeout and winds down).
+// returns false (the caller records a timeout and winds down).  Polls after
+// the first suspend the thread in hardware (try_wait with a time hint) rather
+// than spin, and the timer is read once every 64 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if ((it & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

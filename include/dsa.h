@@ -181,8 +181,8 @@ dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_c
  * DSA_ERR_UNSUPPORTED).  The scratch is a fixed array of
  * DSA_NOALLOC_SCRATCH_BYTES inside this library, so no call allocates.  A batch
  * of T = B rows needs, on a GPU with S SMs,
- *   round_up(4224 T, 256) + 16384 T + (S + B) * 16404 + 12 (B + 1) + 8 S
- * bytes, plus up to 768 bytes of alignment (150 rows fit at S = 152, 160 do
+ *   round_up(4224 T, 256) + 16384 T + (S + B) * 45076 + 12 (B + 1) + 8 S
+ * bytes, plus up to 768 bytes of alignment (151 rows fit at S = 152, 152 do
  * not); a larger batch returns
  * DSA_ERR_SCRATCH_LIMIT and launches nothing.  Nothing in the scratch needs
  * to start at zero: the kernels clear the histogram bins and plan entries
@@ -191,7 +191,7 @@ dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_c
  * begins.  There is one scratch per device: calls that overlap in time (on
  * other streams or from other host threads) race on it, and the caller must
  * serialise them. */
-#define DSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define DSA_NOALLOC_SCRATCH_BYTES (16u << 20)
 dsa_status dsa_indexer_topk_noalloc(const void* q, const float* w, const uint8_t* idxk_cache,
                                     const dsa_batch* b, int32_t* topk, float* topk_scores,
                                     dsa_topk_share* share, int32_t layer_id,
@@ -259,6 +259,46 @@ dsa_status dsa_topk_share_reset(dsa_topk_share* s);
 dsa_status dsa_topk_share_publish(dsa_topk_share* s, int32_t layer_id, const int32_t* topk, int64_t rows);
 dsa_status dsa_topk_share_get(const dsa_topk_share* s, const int32_t** topk, int64_t* rows,
                               int32_t* layer_id);
+
+/* ---- Top-k reuse across the draft steps of one MTP iteration
+ *      ("GLM-5.3 推理全链路(十一)", sections 优化三: MTP 迭代内复用 topk and
+ *      优化四: PD 分离下的 seed 传输) -----------------------------------------------
+ * The MTP layer's draft steps can attend with the top-k of the iteration's
+ * first step instead of running their own indexer.  A seed row is a plain copy
+ * of one selected top-k row, index_topk + index_kpool - 1 int32 wide.
+ *
+ * dsa_mtp_topk_width: *width = index_topk + index_kpool - 1 (2048 for
+ *   index_topk 2048, index_kpool 1).  Both must be >= 1.
+ * dsa_mtp_seed_write: for r < n, seed[r, 0..2047] = topk[src_row[r], 0..2047]
+ *   and seed[r, 2048..width-1] = -1 (the kpool tail slots).  src_row NULL means
+ *   src_row[r] = r.  A src_row outside [0, topk_rows) yields a row of -1 and
+ *   is recorded (DSA_DEVERR_INDEX_RANGE).
+ *     topk    device int32 [topk_rows, 2048], 16-byte aligned
+ *     src_row device int32 [n] or NULL
+ *     seed    device int32 [n, width], width >= 2048, 16-byte aligned
+ * dsa_topk_share_mtp_begin: start one MTP iteration on a share handle.  Reuse
+ *   is on only when enabled != 0 and eagle_topk == 1; with several draft
+ *   candidates per step the draft rows are reordered and a carried row no
+ *   longer belongs to its request.  *reuse_on (optional) receives the decision.
+ *   With reuse on, the handle's published indices are replaced by the carried
+ *   seed when keep_carry_seed != 0 and seed != NULL (device int32 [rows, 2048];
+ *   any other seed_width returns DSA_ERR_UNSUPPORTED), and forgotten
+ *   otherwise.  With reuse off the published indices are left as they are.
+ * dsa_topk_share_needs_scoring: *needs = 0 while an iteration with reuse on
+ *   holds published indices: the draft step skips the indexer and passes
+ *   topk = NULL plus the handle to sparse MLA.  *needs = 1 otherwise: the step
+ *   runs dsa_indexer_topk with the handle, which publishes for the next steps.
+ * dsa_topk_share_mtp_end: end the iteration: reuse off, published indices
+ *   forgotten.
+ * The three share calls are host-only and do not touch the device. */
+dsa_status dsa_mtp_topk_width(int32_t index_topk, int32_t index_kpool, int32_t* width);
+dsa_status dsa_mtp_seed_write(const int32_t* topk, int64_t topk_rows, const int32_t* src_row, int64_t n,
+                              int32_t* seed, int32_t width, int32_t* dev_status, void* stream);
+dsa_status dsa_topk_share_mtp_begin(dsa_topk_share* s, int32_t enabled, int32_t eagle_topk,
+                                    int32_t keep_carry_seed, const int32_t* seed, int64_t rows,
+                                    int32_t seed_width, int32_t* reuse_on);
+dsa_status dsa_topk_share_needs_scoring(const dsa_topk_share* s, int32_t* needs);
+dsa_status dsa_topk_share_mtp_end(dsa_topk_share* s);
 
 #ifdef __cplusplus
 }

@@ -16,6 +16,9 @@ Workloads (sizes and distributions of the DSA decode / verify / prefill shapes):
 * ``decode1m``  - 4 requests, 1 decode token each, context 1,048,576, one full layer.
 * ``verify64k`` - 128 requests x 6 query tokens (1 + 5 draft), context 65536.
 * ``prefill128k`` - 1 request, 8192 new tokens on a 122,880-token prefix.
+* ``mtp5_1m``   - one MTP draft iteration: 4 requests, one MTP layer, 5 draft
+                  steps; step k holds 1,048,576 + k tokens and queries the last.
+                  The 5 draft tokens of a request are its 5 "new" tokens.
 
 Distributions: indexer q ~ N(0,1) bf16 [T,32,128]; head weights ~ N(0,1)/sqrt(32)
 fp32 [T,32]; raw index keys ~ N(0,1) bf16 [n,128]; absorbed MLA q ~ N(0,1) bf16
@@ -45,6 +48,7 @@ class Workload:
     layers: list             # "full" / "shared" per layer of the group
     boost_frac: float = 0.0  # fraction of each request's tokens with a x4 index key
     description: str = ""
+    draft_steps: int = 0     # > 0: the new tokens are the draft steps of one MTP iteration
 
     @property
     def batch(self) -> int:
@@ -104,6 +108,11 @@ def workload(name: str, *, batch: int | None = None, ctx: int | None = None) -> 
     elif name == "verify64k":
         w = Workload(name, SEED_BASE + 3, [65536] * 128, [6] * 128, ["full"],
                      description="128 requests x 6 verify tokens, context 65536, one full layer")
+    elif name == "mtp5_1m":
+        n = 5
+        w = Workload(name, SEED_BASE + 5, [1048576 + n - 1] * 4, [n] * 4, ["full"], draft_steps=n,
+                     description="one MTP iteration: 4 requests x 5 draft steps from a 1,048,576-token context, "
+                                 "one MTP layer")
     elif name == "prefill128k":
         w = Workload(name, SEED_BASE + 4, [131072], [8192], ["full"],
                      description="1 request, 8192 new tokens on a 122,880-token prefix")

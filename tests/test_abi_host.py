@@ -155,6 +155,56 @@ def test_share_handle_lifecycle(L):
         s.get()
 
 
+def test_mtp_share_state_follows_the_iteration_rules(L):
+    """The host-only MTP calls take the same decisions as the oracle's share
+    state, step by step (no device memory is touched)."""
+    from oracle import dsa_oracle as O
+    h = ctypes.c_void_p()
+    assert L.dsa_topk_share_create(ctypes.byref(h)) == 0
+    fake_topk, fake_seed = ctypes.c_void_p(0x50000000), ctypes.c_void_p(0x60000000)
+    on, needs = ctypes.c_int32(), ctypes.c_int32()
+    p, rows, lid = ctypes.c_void_p(), ctypes.c_int64(), ctypes.c_int32()
+
+    def needs_scoring():
+        assert L.dsa_topk_share_needs_scoring(h, ctypes.byref(needs)) == 0
+        return bool(needs.value)
+
+    cases = [(1, 1, 0, None), (1, 3, 0, None), (0, 1, 0, None), (1, 1, 1, fake_seed), (1, 1, 0, fake_seed),
+             (1, 2, 1, fake_seed)]
+    for enabled, etk, keep, seed in cases:
+        ora = O.MtpShareState()
+        ora_on = ora.begin(bool(enabled), etk, bool(keep), None if seed is None else [7])
+        assert L.dsa_topk_share_mtp_begin(h, enabled, etk, keep, seed, 3, 2048, ctypes.byref(on)) == 0
+        assert bool(on.value) == ora_on
+        for step in range(3):
+            assert needs_scoring() == ora.needs_scoring()
+            if ora.needs_scoring():                # the step runs the indexer, which publishes
+                if ora.reuse:
+                    ora.publish([step])
+                assert L.dsa_topk_share_publish(h, 78, fake_topk, 3) == 0
+            else:
+                assert L.dsa_topk_share_get(h, ctypes.byref(p), ctypes.byref(rows), ctypes.byref(lid)) == 0
+                assert p.value == (fake_seed.value if keep and seed is not None else fake_topk.value)
+        assert L.dsa_topk_share_mtp_end(h) == 0
+        ora.end()
+        assert needs_scoring() and L.dsa_topk_share_get(h, ctypes.byref(p), None, None) == 5
+    # argument errors
+    assert L.dsa_topk_share_mtp_begin(h, 1, 0, 0, None, 0, 0, None) == 1           # eagle topk < 1
+    assert L.dsa_topk_share_mtp_begin(h, 1, 1, 1, fake_seed, 3, 2051, None) == 3   # kpool tail not consumable
+    assert L.dsa_topk_share_mtp_begin(h, 1, 5, 1, fake_seed, 3, 2051, ctypes.byref(on)) == 0 and on.value == 0
+    assert L.dsa_topk_share_needs_scoring(h, None) == 1
+    assert L.dsa_topk_share_destroy(h) == 0
+    w = ctypes.c_int32()
+    assert L.dsa_mtp_topk_width(2048, 1, ctypes.byref(w)) == 0 and w.value == GOLDEN["mtp_seed_width"]["value"]
+    assert L.dsa_mtp_topk_width(2048, 4, ctypes.byref(w)) == 0 and w.value == 2051
+    assert L.dsa_mtp_topk_width(0, 1, ctypes.byref(w)) == 1
+    fk = ctypes.c_void_p(0x70000000)
+    assert L.dsa_mtp_seed_write(fk, 4, None, 4, fk, 2047, None, None) == 1          # width below 2048
+    assert L.dsa_mtp_seed_write(fk, 4, None, -1, fk, 2048, None, None) == 1
+    assert L.dsa_mtp_seed_write(fk, 4, None, 0, fk, 2048, None, None) == 0          # nothing to do
+    assert L.dsa_mtp_seed_write(ctypes.c_void_p(0x70000004), 4, None, 4, fk, 2048, None, None) == 2
+
+
 def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(D, "_lib", None)
     monkeypatch.setattr(D, "LIB_PATH", "/nonexistent/libdsa.so")

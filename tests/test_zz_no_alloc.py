@@ -40,7 +40,7 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 
 def test_noalloc_rejects_batches_beyond_the_scratch():
-    # 400 decode rows need more than the 8 MiB scratch on any GPU
+    # 400 decode rows need more than the 16 MiB scratch on any GPU
     w = synth.workload("decode32k", ctx=3000)
     w.seq_len = (list(w.seq_len) * 7)[:400]
     w.q_len = [1] * 400
