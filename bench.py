@@ -43,10 +43,10 @@ L2_BYTES = 129 * 1024 * 1024
 # on 16K contexts (the same 2048 selected rows each, so the same launch);
 # decode1m indexer_topk: a 256K-context capture scaled by the context (x4).
 NCU_TRAFFIC = {
-    ("decode32k", "sparse_mla_decode"): (106.1e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
-                                         "31320c22fdd05908"),
-    ("decode1m", "indexer_topk"): (567.2e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
-                                   "99ab73b01a773f59"),
+    ("decode32k", "sparse_mla_decode"): (106.3e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
+                                         "23817a9df5e77b45"),
+    ("decode1m", "indexer_topk"): (566.5e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
+                                   "8cafee69bc4c92aa"),
 }
 FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s)
 
