@@ -24,6 +24,8 @@ Sources (the four web pages collected for dsa_sparse_attention_indexer):
   the draft steps of one MTP iteration reuse the first step's top-k (only with
   one draft candidate per step), a carried seed row of index_topk +
   index_kpool - 1 int32 is a plain copy of a selected top-k row.
+* "GLM-5.3 推理全链路(十一)", section "两个框架的对照": the indexer cache may be
+  stored as MXFP4, 128/2 packed bytes + 128/32 ue8m0 scales = 68 B per token.
 
 Readings where the pages are silent (each also listed in the design notes):
 LayerNorm eps 1e-6 with optional affine; interleaved RoPE pairs (2i, 2i+1),
@@ -38,7 +40,9 @@ Parity pins: every function here is pinned by tests under ``-m "not gpu"``
 (codec vs the format definition and torch's float8 casts, layout constants the
 pages print, the 21/57 schedule, brute-force top-k, sparse == dense attention
 when the context fits in the top-k, closed forms, the MTP seed width and
-draft-step read counts the pages print, brute-force top-k per draft position).
+draft-step read counts the pages print, brute-force top-k per draft position,
+the 68-byte MXFP4 token, the E2M1 codec against its value table and rounding
+rule, the MX scale property amax / 2**e in [4, 8)).
 The MTP reading where the pages are silent: a draft step with a context of at
 most 2048 publishes its all-positions row like any other step.  The LayerNorm
 eps, RoPE base and RoPE pairing are NOT fixed by the pages: "parity unpinned" for those three
@@ -484,3 +488,154 @@ def mtp_draft_topk(q_idx, w, idx_cache, page_table_row, seq_len0, n_steps, state
         else:
             out[k] = state.indices
     return out, read
+
+
+# ----------------------------------------------------------------------------
+# MXFP4 index-K cache ("GLM-5.3 推理全链路(十一)", section 两个框架的对照: the same
+# indexer cache stored as MXFP4, head_dim/2 bytes of packed values plus
+# head_dim/block ue8m0 scales, 128/2 + 128/32 = 68 B per token).
+#
+# Readings where the pages are silent: MXFP4 as the OCP Microscaling format
+# defines it - blocks of 32 values share one E8M0 scale 2**e with
+# e = floor(log2(amax)) - 2 (2 is the exponent of E2M1's largest value, 6), the
+# elements are E2M1 rounded to nearest with ties to even and saturated at +-6;
+# amax == 0 gives e = 0.  Two values per byte, the even element in the low
+# nibble.  A page holds the 64 packed rows of 64 B, then the 64 tokens' 4 scale
+# bytes (e + 127), 4352 B in all.  The query side is unchanged (FP8, one scale
+# per head) and scores are formed on the dequantised values.
+# ----------------------------------------------------------------------------
+MXFP4_BLOCK = 32
+MXFP4_TOKEN_BYTES = INDEX_HEAD_DIM // 2 + INDEX_HEAD_DIM // MXFP4_BLOCK     # 68
+MXFP4_PAGE_BYTES = PAGE_TOKENS * MXFP4_TOKEN_BYTES                          # 4352
+E2M1_EMAX = 2                      # 6 = 1.5 * 2**2
+
+
+def e2m1_decode_table() -> np.ndarray:
+    """Value of each of the 16 E2M1 codes: sign bit 3, exponent bits 2..1 with
+    bias 1, mantissa bit 0; exponent 0 is subnormal (m * 0.5)."""
+    out = np.empty(16, dtype=np.float64)
+    for code in range(16):
+        sign = -1.0 if code & 8 else 1.0
+        exp = (code >> 1) & 3
+        man = code & 1
+        out[code] = sign * (man * 0.5 if exp == 0 else (1.0 + man / 2.0) * 2.0 ** (exp - 1))
+    return out
+
+
+_E2M1_TABLE = e2m1_decode_table()
+_E2M1_POS_VALS = _E2M1_TABLE[:8]
+
+
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    return _E2M1_TABLE[np.asarray(codes, dtype=np.int64) & 15]
+
+
+def e2m1_encode(x: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 value of each x (|x| > 6 saturates to 6), ties to the even
+    code; the sign bit follows x (a value that rounds to zero keeps it)."""
+    x = np.asarray(x, dtype=np.float64)
+    if np.any(~np.isfinite(x)):
+        raise ValueError("e2m1_encode: non-finite input")
+    ax = np.minimum(np.abs(x), _E2M1_POS_VALS[7])
+    hi = np.minimum(np.searchsorted(_E2M1_POS_VALS, ax, side="left"), 7)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E2M1_POS_VALS[hi] - ax
+    d_lo = ax - _E2M1_POS_VALS[lo]
+    code = np.where((d_lo < d_hi) | ((d_lo == d_hi) & ((lo & 1) == 0)), lo, hi)
+    code = np.where(ax == _E2M1_POS_VALS[hi], hi, code)
+    return (code | (np.signbit(x).astype(np.int64) << 3)).astype(np.uint8)
+
+
+def mxfp4_exponent(amax):
+    """Shared block exponent floor(log2(amax)) - 2, clamped to [-127, 127];
+    amax == 0 gives 0.  frexp gives floor(log2) exactly."""
+    a = np.asarray(amax, dtype=np.float64)
+    _, k = np.frexp(a)                                  # a = m * 2**k, m in [0.5, 1)
+    e = np.where(a > 0, k.astype(np.int64) - 1 - E2M1_EMAX, 0)
+    e = np.clip(e, -127, 127)
+    return e if e.ndim else int(e)
+
+
+def quantize_mxfp4(x: np.ndarray):
+    """[..., 128] -> (E2M1 codes [..., 128] in 0..15, block exponents [..., 4])."""
+    x = np.asarray(x, dtype=np.float64)
+    assert x.shape[-1] == INDEX_HEAD_DIM
+    xb = x.reshape(x.shape[:-1] + (INDEX_HEAD_DIM // MXFP4_BLOCK, MXFP4_BLOCK))
+    e = np.asarray(mxfp4_exponent(np.max(np.abs(xb), axis=-1)))
+    codes = e2m1_encode(xb / np.ldexp(1.0, e)[..., None])
+    return codes.reshape(x.shape), e
+
+
+def mxfp4_dequant(codes: np.ndarray, exps: np.ndarray) -> np.ndarray:
+    c = e2m1_decode(codes)
+    cb = c.reshape(c.shape[:-1] + (INDEX_HEAD_DIM // MXFP4_BLOCK, MXFP4_BLOCK))
+    return (cb * np.ldexp(1.0, np.asarray(exps))[..., None]).reshape(c.shape)
+
+
+def index_k_prepare_mxfp4(k: np.ndarray, pos: np.ndarray, gamma=None, beta=None,
+                          eps: float = 1e-6, rope_base: float = 10000.0):
+    """The index key of each token as MXFP4: (codes [n,128], exponents [n,4])."""
+    y = layer_norm(k, gamma, beta, eps)
+    y = rope_interleaved(y, pos, rope_base, 64)
+    return quantize_mxfp4(y)
+
+
+def mxfp4_cache_write(cache: np.ndarray, slot: np.ndarray, codes: np.ndarray, exps: np.ndarray) -> None:
+    """Write tokens into an MXFP4 index-K cache [num_pages, 4352] (uint8).
+
+    Within a page: bytes [0, 4096) hold the 64 rows of 64 packed bytes (byte j
+    = code 2j | code 2j+1 << 4), bytes [4096, 4352) the 64 tokens' 4 scale
+    bytes e + 127.  slot < 0 is skipped."""
+    assert cache.dtype == np.uint8 and cache.shape[1] == MXFP4_PAGE_BYTES
+    slot = np.asarray(slot, dtype=np.int64)
+    keep = slot >= 0
+    page, row = np.divmod(slot[keep], PAGE_TOKENS)
+    c = np.asarray(codes, dtype=np.uint8)[keep]
+    packed = (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    cache[page[:, None], row[:, None] * 64 + np.arange(64)] = packed
+    eb = (np.asarray(exps, dtype=np.int64)[keep] + 127).astype(np.uint8)
+    cache[page[:, None], PAGE_TOKENS * 64 + 4 * row[:, None] + np.arange(4)] = eb
+
+
+def mxfp4_cache_read(cache: np.ndarray, page_table_row: np.ndarray, n_tokens: int):
+    """Logical tokens 0..n-1 of one request: (codes [n,128], exponents [n,4])."""
+    j = np.arange(n_tokens, dtype=np.int64)
+    page = np.asarray(page_table_row, dtype=np.int64)[j // PAGE_TOKENS]
+    row = j % PAGE_TOKENS
+    packed = cache[page[:, None], row[:, None] * 64 + np.arange(64)]
+    codes = np.empty((n_tokens, INDEX_HEAD_DIM), dtype=np.uint8)
+    codes[:, 0::2] = packed & 15
+    codes[:, 1::2] = packed >> 4
+    exps = cache[page[:, None], PAGE_TOKENS * 64 + 4 * row[:, None] + np.arange(4)].astype(np.int64) - 127
+    return codes, exps
+
+
+def indexer_scores_mxfp4(q_codes, q_scales, w, k_codes, k_exps) -> np.ndarray:
+    """s_j = sum_m w_m * ReLU(<q_m, k_j>) with FP8 queries and MXFP4 keys."""
+    q = e4m3_decode(q_codes) * np.asarray(q_scales, np.float64)[:, None]
+    k = mxfp4_dequant(k_codes, k_exps)
+    return np.maximum(k @ q.T, 0.0) @ np.asarray(w, dtype=np.float64)
+
+
+def score_magnitude_mxfp4(q_codes, q_scales, w, k_codes, k_exps) -> np.ndarray:
+    q = e4m3_decode(q_codes) * np.asarray(q_scales, np.float64)[:, None]
+    k = mxfp4_dequant(k_codes, k_exps)
+    return np.abs(k @ q.T) @ np.abs(np.asarray(w, dtype=np.float64))
+
+
+def request_topk_mxfp4(q_idx, w, cache, page_table_row, seq_len, q_len):
+    """request_topk over an MXFP4 index-K cache."""
+    k_codes, k_exps = mxfp4_cache_read(cache, page_table_row, seq_len)
+    out = np.empty((q_len, TOPK), dtype=np.int32)
+    all_scores = []
+    for t in range(q_len):
+        n_valid = seq_len - q_len + t + 1
+        if n_valid <= TOPK:
+            out[t] = topk_positions(None, n_valid)
+            all_scores.append(None)
+            continue
+        qc, qs = index_q_quantize(q_idx[t])
+        s = indexer_scores_mxfp4(qc, qs, w[t], k_codes[:n_valid], k_exps[:n_valid])
+        out[t] = topk_positions(s, n_valid)
+        all_scores.append(s)
+    return out, all_scores

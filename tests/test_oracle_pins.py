@@ -409,3 +409,91 @@ def test_mtp_seed_write_copies_rows_and_pads_the_tail():
     assert (seed[:, 2048:] == -1).all() and (seed[2] == -1).all() and (seed[3] == -1).all()
     with pytest.raises(ValueError):
         O.mtp_seed_write(topk, np.array([0]), 2047)
+
+
+# ------------------------------------------------------------------ MXFP4 index-K cache
+def test_mxfp4_layout_constants_printed_on_the_pages():
+    assert O.MXFP4_TOKEN_BYTES == g("mxfp4_token_bytes") == 128 // 2 + 128 // g("mxfp4_block")
+    assert O.MXFP4_PAGE_BYTES == 64 * 68
+    assert O.MXFP4_TOKEN_BYTES / O.INDEX_TOKEN_BYTES < 0.52          # "the read volume halves"
+
+
+def test_e2m1_table_is_the_format_value_set():
+    t = O.e2m1_decode_table()
+    # sign-magnitude with magnitudes 2**(e-1) * (1 + m/2) for e > 0 and m/2 for e = 0
+    assert t[:8].tolist() == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(t[8:], -t[:8]) and np.signbit(t[8])
+    for c in range(16):                                           # every code round-trips
+        assert O.e2m1_encode(np.array([t[c]]))[0] == c
+
+
+def test_e2m1_encode_nearest_ties_to_even_and_saturates():
+    rng = np.random.default_rng(31)
+    x = np.concatenate([rng.uniform(-8, 8, 4000), np.arange(-7.0, 7.01, 0.25)])
+    codes = O.e2m1_encode(x)
+    v = O.e2m1_decode(codes)
+    vals = O.e2m1_decode_table()[:8]
+    for xi, vi, ci in zip(x, v, codes):                            # brute-force nearest
+        ax = min(abs(xi), 6.0)
+        d = np.abs(vals - ax)
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        assert (ci & 7) == want and (xi < 0) == bool(ci & 8)
+    # the ties, by hand
+    ties = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0, 100.0: 6.0}
+    for a, b in ties.items():
+        assert O.e2m1_decode(O.e2m1_encode(np.array([a])))[0] == b
+
+
+@pytest.mark.parametrize("amax,e", [(6.0, 0), (7.99, 0), (8.0, 1), (4.0, 0), (3.99, -1), (1.0, -2), (0.0, 0),
+                                    (2.0 ** -140, -127), (2.0 ** 140, 127)])
+def test_mx_shared_exponent_hand_values(amax, e):
+    assert O.mxfp4_exponent(amax) == e
+
+
+def test_mxfp4_block_scale_property_and_error_bound():
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((300, 128)) * np.exp2(rng.integers(-12, 12, (300, 1)))
+    codes, exps = O.quantize_mxfp4(x)
+    assert exps.shape == (300, 4)
+    xb = x.reshape(300, 4, 32)
+    amax = np.abs(xb).max(axis=-1)
+    r = amax / np.exp2(exps)
+    assert np.all((r >= 4.0) & (r < 8.0))                          # OCP: floor(log2 amax) - emax
+    deq = O.mxfp4_dequant(codes, exps).reshape(300, 4, 32)
+    step = np.exp2(exps)[..., None]
+    sat = np.abs(xb) > 6.0 * step
+    err = np.abs(deq - xb)
+    assert np.all(err[~sat] <= 1.0 * np.broadcast_to(step, xb.shape)[~sat] + 1e-300)   # half the widest gap (4 -> 6)
+    assert np.all(err[sat] <= 2.0 * np.broadcast_to(step, xb.shape)[sat])              # saturation: |x| < 8 * 2**e
+
+
+def test_mxfp4_cache_roundtrip_and_nibble_order():
+    rng = np.random.default_rng(33)
+    cache = np.zeros((4, O.MXFP4_PAGE_BYTES), dtype=np.uint8)
+    pt = np.array([2, 0, 3], dtype=np.int32)
+    n = 140
+    codes = rng.integers(0, 16, (n, 128)).astype(np.uint8)
+    exps = rng.integers(-20, 20, (n, 4))
+    slots = pt[np.arange(n) // 64] * 64 + np.arange(n) % 64
+    O.mxfp4_cache_write(cache, slots, codes, exps)
+    c2, e2 = O.mxfp4_cache_read(cache, pt, n)
+    assert np.array_equal(c2, codes) and np.array_equal(e2, exps)
+    # token 65: logical page 1 -> physical page 0, row 1; element 0 in the low nibble
+    assert cache[0, 64] == (codes[65, 0] | (codes[65, 1] << 4))
+    assert cache[0, 4096 + 4 + 2] == exps[65, 2] + 127
+
+
+def test_mxfp4_scores_brute_force():
+    rng = np.random.default_rng(34)
+    L = 7
+    q = rng.standard_normal((32, 128))
+    k = rng.standard_normal((L, 128))
+    w = rng.standard_normal(32) / math.sqrt(32)
+    qc, qs = O.index_q_quantize(q)
+    kc, ke = O.quantize_mxfp4(k)
+    s = O.indexer_scores_mxfp4(qc, qs, w, kc, ke)
+    kd = O.mxfp4_dequant(kc, ke)
+    ref = _brute_scores(O.e4m3_decode(qc) * qs[:, None], w, kd)
+    assert np.allclose(s, ref, rtol=1e-12, atol=1e-12)
+    assert np.all(O.score_magnitude_mxfp4(qc, qs, w, kc, ke) >= np.abs(s) - 1e-12)
