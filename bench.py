@@ -128,15 +128,17 @@ def workload_bytes(w, mtp_reuse=True):
     """Algorithmic bytes of one step: index-K read once per request per full
     layer, plus 656 B per selected token per query row per layer.  An MTP
     draft iteration reads index-K in its first step only when the steps reuse
-    the top-k, in every step otherwise."""
+    the top-k, in every step otherwise.  An MXFP4 index cache holds 68 B per
+    token instead of 132."""
+    tb = 68 if w.index_format == "mxfp4" else 132
     n_full = sum(1 for t in w.layers if t == "full")
     idx = 0
     kv = 0
     for L, q in zip(w.seq_len, w.q_len):
         if w.draft_steps and not mtp_reuse:
-            idx += sum(132 * (L - q + t + 1) for t in range(q))
+            idx += sum(tb * (L - q + t + 1) for t in range(q))
         else:
-            idx += 132 * (L - q + 1 if w.draft_steps else L)
+            idx += tb * (L - q + 1 if w.draft_steps else L)
         for t in range(q):
             kv += 656 * min(2048, L - q + t + 1)
     return n_full * idx, kv * len(w.layers), idx, kv
@@ -180,12 +182,12 @@ class Step:
             if before_layer is not None:
                 before_layer(l)
             if self.full[li]:
-                t("index_k_store", lambda: D.dsa_index_k_store(gw.new_k, gw.new_pos, gw.new_slot, gw.idx_cache,
+                t("index_k_store", lambda: gw.index_k_store(gw.new_k, gw.new_pos, gw.new_slot, gw.idx_cache,
                                                                  dev_status=gw.dev_status, stream=stream))
             t("latent_kv_store", lambda: D.dsa_latent_kv_store(gw.new_c[l], gw.new_r[l], gw.new_slot, gw.kv_cache[l],
                                                                  dev_status=gw.dev_status, stream=stream))
             if self.full[li]:
-                t("indexer_topk", lambda: D.dsa_indexer_topk(gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch,
+                t("indexer_topk", lambda: gw.indexer_topk(gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch,
                                                              topk=self.topk, share=self.share, layer_id=l,
                                                              ws=self.idx_ws, dev_status=gw.dev_status,
                                                              stream=stream))
@@ -213,12 +215,12 @@ class Step:
         stream = torch.cuda.current_stream()
         for li, l in enumerate(gw.layers):
             if self.full[li]:
-                out.append(("index_k_store", lambda: D.dsa_index_k_store(
+                out.append(("index_k_store", lambda: gw.index_k_store(
                     gw.new_k, gw.new_pos, gw.new_slot, gw.idx_cache, dev_status=gw.dev_status, stream=stream)))
             out.append(("latent_kv_store", (lambda l=l: D.dsa_latent_kv_store(
                 gw.new_c[l], gw.new_r[l], gw.new_slot, gw.kv_cache[l], dev_status=gw.dev_status, stream=stream))))
             if self.full[li]:
-                out.append(("indexer_topk", (lambda l=l: D.dsa_indexer_topk(
+                out.append(("indexer_topk", (lambda l=l: gw.indexer_topk(
                     gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch, topk=self.topk, share=self.share, layer_id=l,
                     ws=self.idx_ws, dev_status=gw.dev_status, stream=stream))))
             out.append(("sparse_mla_decode", (lambda l=l: D.dsa_sparse_mla_decode(
@@ -266,7 +268,7 @@ class MtpStep:
 
     def _store_k(self, k, stream):
         x = self.inp[k]
-        self.D.dsa_index_k_store(x["new_k"], x["new_pos"], x["new_slot"], self.gw.idx_cache,
+        self.gw.index_k_store(x["new_k"], x["new_pos"], x["new_slot"], self.gw.idx_cache,
                                  dev_status=self.gw.dev_status, stream=stream)
 
     def _store_c(self, k, stream):
@@ -276,7 +278,7 @@ class MtpStep:
 
     def _indexer(self, k, stream):
         x = self.inp[k]
-        self.D.dsa_indexer_topk(x["q_idx"], x["w_idx"], self.gw.idx_cache, self.batches[k], topk=self.topk,
+        self.gw.indexer_topk(x["q_idx"], x["w_idx"], self.gw.idx_cache, self.batches[k], topk=self.topk,
                                 share=self.share, layer_id=0, ws=self.idx_ws, dev_status=self.gw.dev_status,
                                 stream=stream)
 
@@ -355,7 +357,7 @@ def call_bytes(name, w):
     if name == "sparse_mla_decode":
         return kv / per
     if name == "index_k_store":
-        return w.total_q * (256 + 132) / per
+        return w.total_q * (256 + (68 if w.index_format == "mxfp4" else 132)) / per
     if name == "latent_kv_store":
         return w.total_q * (1152 + 656) / per
     return 0
@@ -382,6 +384,7 @@ def run_ours(args, rank, world):
 
     dev = f"cuda:{torch.cuda.current_device()}"
     w = synth.workload(args.workload, batch=args.batch, ctx=args.ctx)
+    w.index_format = args.index_cache
     gw = GpuWorkload(w, dev)
     step = MtpStep(gw, D, reuse=not args.no_mtp_reuse) if w.draft_steps else Step(gw, D)
     torch.cuda.synchronize()
@@ -558,10 +561,16 @@ def oracle_sample(w, budget_s: float, max_requests: int = 64, mtp_reuse: bool = 
         pt = torch.randperm(npg, generator=g).numpy().astype(np.int32)
         pos = np.arange(L)
         slots = pt[pos // 64].astype(np.int64) * 64 + pos % 64
-        idx_cache = np.zeros((npg, O.INDEX_PAGE_BYTES), np.uint8)
         k = synth.normal_bf16(w, f"idx_k/req{r}", (L, 128), "cpu")
-        codes, scales = O.index_k_prepare(k.double().numpy(), pos)
-        O.index_cache_write(idx_cache, slots, codes, scales)
+        mx = w.index_format == "mxfp4"
+        if mx:
+            idx_cache = np.zeros((npg, O.MXFP4_PAGE_BYTES), np.uint8)
+            codes, exps = O.index_k_prepare_mxfp4(k.double().numpy(), pos)
+            O.mxfp4_cache_write(idx_cache, slots, codes, exps)
+        else:
+            idx_cache = np.zeros((npg, O.INDEX_PAGE_BYTES), np.uint8)
+            codes, scales = O.index_k_prepare(k.double().numpy(), pos)
+            O.index_cache_write(idx_cache, slots, codes, scales)
         q_rows = synth.normal_bf16(w, f"idx_q/req{r}", (qn, 32, 128), "cpu").double().numpy()
         wr = (torch.randn((qn, 32), generator=g) / math.sqrt(32.0)).double().numpy()
         t0 = time.perf_counter()
@@ -570,6 +579,8 @@ def oracle_sample(w, budget_s: float, max_requests: int = 64, mtp_reuse: bool = 
             st.begin(mtp_reuse, 1)
             topk, _ = O.mtp_draft_topk(q_rows, wr, idx_cache, pt, L - qn + 1, qn, st)
             st.end()
+        elif mx:
+            topk, _ = O.request_topk_mxfp4(q_rows, wr, idx_cache, pt, L, qn)
         else:
             topk, _ = O.request_topk(q_rows, wr, idx_cache, pt, L, qn)
         spent += time.perf_counter() - t0
@@ -597,6 +608,7 @@ def run_reference(args, rank, world):
     sample of the same workload."""
     import synth
     w = synth.workload(args.workload, batch=args.batch, ctx=args.ctx)
+    w.index_format = args.index_cache
     total_q = 0
     t_all = 0.0
     steps_done = 0
@@ -624,9 +636,13 @@ def main():
     ap.add_argument("--ctx", type=int, default=None, help="shrink every context proportionally (profiling)")
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per reference pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--index-cache", default="fp8", choices=["fp8", "mxfp4"],
+                    help="index-K cache format (mxfp4: decode workloads)")
     ap.add_argument("--no-mtp-reuse", action="store_true",
                     help="MTP workloads: every draft step runs its own indexer (the comparison point)")
     args = ap.parse_args()
+    if args.index_cache == "mxfp4" and args.workload not in ("tiny", "decode32k", "decode1m"):
+        ap.error("--index-cache mxfp4 covers the decode workloads (tiny, decode32k, decode1m)")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -676,7 +692,7 @@ def main():
         roof = {"bound": "hbm", "achieved": dom_bytes / (dom_us * 1e-6) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     traffic = None
-    rec = NCU_TRAFFIC.get((w.name, dom))
+    rec = NCU_TRAFFIC.get((w.name + ("+mxfp4" if w.index_format == "mxfp4" else ""), dom))
     if rec and file_sha(rec[1]) == rec[2]:
         traffic = rec[0]
     line = {
@@ -695,6 +711,7 @@ def main():
             "step_frac_of_8tbs": step_bytes / (ms * 1e-3) / 1e9 / 8000.0,
             "us_per_call": {k: round(v, 2) for k, v in res["per_call"].items()},
             **({"draft_steps": w.draft_steps, "mtp_reuse": not args.no_mtp_reuse} if w.draft_steps else {}),
+            "index_cache": w.index_format,
         },
         "roofline": {"kernel": dom, **roof, "traffic": traffic, "peak_source": pk["source"],
                      "algorithmic_bytes_per_launch": dom_bytes, "algorithmic_flops_per_launch": dom_flops,

@@ -25,6 +25,8 @@ INDEX_HEADS = 32
 INDEX_HEAD_DIM = 128
 IDXK_TOKEN_BYTES = 132
 IDXK_PAGE_BYTES = 8448
+IDXK_MXFP4_TOKEN_BYTES = 68
+IDXK_MXFP4_PAGE_BYTES = 4352
 MLA_HEADS = 64
 LATENT_DIM = 512
 ROPE_DIM = 64
@@ -73,6 +75,10 @@ _SIGS = {
     "dsa_device_status_read": (c_int32, [c_void_p, c_void_p, POINTER(c_int32)]),
     "dsa_index_k_store": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_float,
                                     c_float, c_void_p, c_int64, c_void_p, c_void_p]),
+    "dsa_index_k_store_mxfp4": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_float,
+                                          c_float, c_void_p, c_int64, c_void_p, c_void_p]),
+    "dsa_indexer_topk_mxfp4": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_void_p, c_void_p,
+                                         c_void_p, c_int32, c_void_p, c_size_t, c_void_p, c_void_p]),
     "dsa_latent_kv_store": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64, c_void_p,
                                       c_void_p]),
     "dsa_indexer_topk_workspace_size": (c_int32, [POINTER(DsaBatch), POINTER(c_size_t)]),
@@ -225,6 +231,20 @@ def dsa_index_k_store(k, pos, slot, idxk_cache, *, gamma=None, beta=None, ln_eps
         _ptr(idxk_cache), num_pages, _ptr(dev_status), _stream(stream)))
 
 
+def dsa_index_k_store_mxfp4(k, pos, slot, idxk_cache, *, gamma=None, beta=None, ln_eps=1e-6,
+                            rope_base=10000.0, num_pages=None, dev_status=None, stream=None):
+    """dsa_index_k_store into an MXFP4 index-K cache (4352-byte pages, 32-byte aligned)."""
+    _need(k, torch.bfloat16, "k")
+    _need(pos, torch.int32, "pos")
+    _need(slot, torch.int64, "slot")
+    _need(idxk_cache, torch.uint8, "idxk_cache")
+    if num_pages is None:
+        num_pages = idxk_cache.numel() // IDXK_MXFP4_PAGE_BYTES
+    _check("dsa_index_k_store_mxfp4", lib().dsa_index_k_store_mxfp4(
+        _ptr(k), _ptr(pos), _ptr(slot), k.shape[0], _ptr(gamma), _ptr(beta), ln_eps, rope_base,
+        _ptr(idxk_cache), num_pages, _ptr(dev_status), _stream(stream)))
+
+
 def dsa_latent_kv_store(c, rope, slot, kv_cache, *, num_pages=None, dev_status=None, stream=None):
     _need(c, torch.bfloat16, "c")
     _need(rope, torch.bfloat16, "rope")
@@ -253,6 +273,24 @@ def dsa_indexer_topk(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=N
     if ws is None:
         ws = workspace(dsa_indexer_topk_workspace_size(batch), q.device)
     _check("dsa_indexer_topk", lib().dsa_indexer_topk(
+        _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
+        None if share is None else share.handle, layer_id, _ptr(ws), ws.numel(), _ptr(dev_status),
+        _stream(stream)))
+    return topk
+
+
+def dsa_indexer_topk_mxfp4(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=None, share=None,
+                           layer_id: int = 0, ws=None, dev_status=None, stream=None):
+    """dsa_indexer_topk over an MXFP4 index-K cache (decode batches)."""
+    _need(q, torch.bfloat16, "q")
+    _need(w, torch.float32, "w")
+    _need(idxk_cache, torch.uint8, "idxk_cache")
+    T = batch.total_q
+    if topk is None:
+        topk = torch.empty((T, TOPK), dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = workspace(dsa_indexer_topk_workspace_size(batch), q.device)
+    _check("dsa_indexer_topk_mxfp4", lib().dsa_indexer_topk_mxfp4(
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
         None if share is None else share.handle, layer_id, _ptr(ws), ws.numel(), _ptr(dev_status),
         _stream(stream)))

@@ -57,6 +57,37 @@ extern "C" dsa_status dsa_indexer_topk_workspace_size(const dsa_batch* b, size_t
     return DSA_OK;
 }
 
+// MXFP4 index-K cache, decode batches: the same quantised queries, plan,
+// fused score kernel (E2M1 keys, block scales in the epilogue) and merge.
+extern "C" dsa_status dsa_indexer_topk_mxfp4(const void* q, const float* w, const uint8_t* idxk_cache,
+                                             const dsa_batch* b, int32_t* topk, float* topk_scores,
+                                             dsa_topk_share* share, int32_t layer_id, void* ws,
+                                             size_t ws_bytes, int32_t* dev_status, void* stream) {
+    dsa_status vs = validate_batch(b);
+    if (vs != DSA_OK) return vs;
+    if (!q || !w || !idxk_cache || !topk) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(topk) || (reinterpret_cast<uintptr_t>(idxk_cache) & 31)) return DSA_ERR_ALIGNMENT;
+    if (b->total_q > 0) {
+        if (!use_tc_path(b)) return DSA_ERR_UNSUPPORTED;            // decode batches only
+        if (b->num_pages * 68 > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+        if (!ws) return DSA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(ws)) return DSA_ERR_ALIGNMENT;
+        if (ws_bytes < indexer_ws_bytes(b)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+        cudaStream_t s = as_stream(stream);
+        uint8_t* q8 = static_cast<uint8_t*>(ws);
+        float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
+        uint32_t* hist = reinterpret_cast<uint32_t*>(q8 + (q8_workspace_bytes(b->total_q) + 255) / 256 * 256);
+        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, hist, s);
+        if (rs != DSA_OK) return rs;
+        void* plan = reinterpret_cast<uint8_t*>(hist) + (size_t)b->total_q * 4096 * 4;
+        rs = launch_indexer_tc(q8, wq, hist, idxk_cache, b, topk, topk_scores, plan, device_sm_count(), dev_status, s,
+                               true);
+        if (rs != DSA_OK) return rs;
+    }
+    if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);
+    return DSA_OK;
+}
+
 extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_cache,
                                        const dsa_batch* b, int32_t* topk, float* topk_scores,
                                        dsa_topk_share* share, int32_t layer_id, void* ws,

@@ -480,7 +480,7 @@ struct QMapCache {
 };
 }  // namespace
 
-bool make_index_tmap(const uint8_t* cache, int64_t num_pages, CUtensorMap* out);
+bool make_index_tmap(const uint8_t* cache, int64_t num_pages, bool mx, CUtensorMap* out);
 
 static bool make_q8_tmap(const uint8_t* q8, int64_t total_q, CUtensorMap* out) {
     static QMapCache mc;
@@ -552,7 +552,7 @@ dsa_status launch_indexer_rows(const uint8_t* q8, const float* wq, const uint8_t
                                float* scores, int64_t ld, bool skip_short, bool full_rows, void* plan_ws, int G,
                                int32_t* st, cudaStream_t s) {
     CUtensorMap kmap, qmap;
-    if (!make_index_tmap(cache, b->num_pages, &kmap)) return DSA_ERR_CUDA;
+    if (!make_index_tmap(cache, b->num_pages, false, &kmap)) return DSA_ERR_CUDA;
     if (!make_q8_tmap(q8, b->total_q, &qmap)) return DSA_ERR_CUDA;
     static bool attr = false;
     if (!attr) {

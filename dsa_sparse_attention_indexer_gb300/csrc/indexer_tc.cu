@@ -58,6 +58,7 @@ constexpr int kProducer2Warp = (64 + kEpiThreads) / 32;   // the second producer
 constexpr int kEpiBar = 1;
 constexpr int kTmemCols = 32 * kAcc;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 32);
+constexpr uint32_t kIdescMx = kIdesc | (5u << 7);       // A operand E2M1 (the MXFP4 keys), B E4M3
 
 constexpr int kOffStages = 0;
 // A tile's key scales (2 x 256 B) and page mask sit in a ring of their own,
@@ -345,6 +346,13 @@ __device__ void compact_candidates(uint32_t* cb_key, int32_t* cb_pos, uint32_t* 
     epi_sync();
 }
 
+// kMx: the MXFP4 index-K cache ("GLM-5.3 推理全链路(十一)", 两个框架的对照).  The
+// TMA unpacks each page's 64 packed 64-byte rows into the same 128-byte rows as
+// FP8 (16U4_ALIGN16B: eight bytes of values, eight bytes of gap, the E2M1
+// operand layout of kind::f8f6f4), so the stage ring is unchanged; the MMA
+// takes A as E2M1 and writes one 32-column accumulator per 32-dim block (four
+// per tile), and the epilogue applies the blocks' ue8m0 scales before the ReLU.
+template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
 score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ cache,
                   const uint8_t* __restrict__ q8, const float* __restrict__ wq, BatchDev b, Plan p,
@@ -369,9 +377,16 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
     uint32_t* side_key = reinterpret_cast<uint32_t*>(smem + kOffSideKey);
     int32_t* side_pos = reinterpret_cast<int32_t*>(smem + kOffSidePos);
 
+    constexpr int kAccCols = kMx ? 128 : 32;               // TMEM columns of one tile's accumulator
+    constexpr int kAccN = kTmemCols / kAccCols;            // accumulators in flight
+    constexpr int kMapRows = kMx ? 68 : 66;                // 64 payload rows + the scales, per page
+    constexpr int kPageBytes = kMx ? DSA_IDXK_MXFP4_PAGE_BYTES : kIdxPageBytes;
+    constexpr int kPayBytes = kMx ? 64 * 64 : kIdxPayloadBytes;
+    constexpr int kSt = kStages;                           // payload stages
+    static_assert(kAccN % 2 == 0 && kAccN <= kAcc, "accumulator barriers");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kSt; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);              // the MMA commit
         }
@@ -433,8 +448,8 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                 if (lane == 0) {
                     for (int tile = c0; tile < c0 + nt; ++tile, ++icount) {
                         if ((int)(icount & 1) != me) continue;
-                        const int stage = (int)(icount % kStages);
-                        const uint32_t phase = (uint32_t)((icount / kStages) & 1);
+                        const int stage = (int)(icount % kSt);
+                        const uint32_t phase = (uint32_t)((icount / kSt) & 1);
                         const int slot = (int)(icount % kSSlots);
                         const uint32_t sphase = (uint32_t)((icount / kSSlots) & 1);
                         if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1) ||
@@ -444,14 +459,14 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                         }
                         const int t0 = tile * 128;
                         const int pages = (L - t0 > 64) ? 2 : 1;
-                        uint32_t bytes = 0;                // payload bytes
+                        int nvalid = 0;                    // pages copied
                         int vmask = 0;
                         int64_t pg[2];
                         for (int j = 0; j < pages; ++j) {
                             pg[j] = mypid[(tile - c0) * 2 + j];
                             if (pg[j] >= 0 && pg[j] < b.num_pages) {
                                 vmask |= 1 << j;
-                                bytes += 8192;
+                                ++nvalid;
                             } else if (pg[j] == -2) {
                                 record_error(st, DSA_DEVERR_INDEX_RANGE, t0 + j * 64);   // beyond the page table row
                             } else {
@@ -460,13 +475,14 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                         }
                         misc->slot_valid[slot] = vmask;     // read after sfull[slot]
                         uint8_t* sb = smem + kOffStages + stage * kStageBytes;
-                        mbar_arrive_expect_tx(&full[stage], bytes);
-                        mbar_arrive_expect_tx(&sfull[slot], bytes / 32);   // 256 B per 8192 B page
+                        // the copy counts the bytes read: 8192 FP8 or 4096 packed E2M1 per page
+                        mbar_arrive_expect_tx(&full[stage], (uint32_t)(nvalid * kPayBytes));
+                        mbar_arrive_expect_tx(&sfull[slot], (uint32_t)(nvalid * 256));
                         for (int j = 0; j < pages; ++j) {
                             if (!(vmask & (1 << j))) continue;
-                            tma_load_2d(sb + j * 8192, &tmap, 0, (int32_t)(pg[j] * 66), &full[stage]);
+                            tma_load_2d(sb + j * 8192, &tmap, 0, (int32_t)(pg[j] * kMapRows), &full[stage]);
                             bulk_load(smem + kOffScales + slot * 512 + j * 256,
-                                      cache + pg[j] * (int64_t)kIdxPageBytes + kIdxPayloadBytes, 256, &sfull[slot]);
+                                      cache + pg[j] * (int64_t)kPageBytes + kPayBytes, 256, &sfull[slot]);
                         }
                         last = icount;
                     }
@@ -484,7 +500,7 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
             // kSSlots (older ones were consumed before their stage or slot was
             // refilled)
             for (int64_t j = last; j >= 0 && j > last - kSSlots; j -= 2) {
-                if (j > last - kStages) mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1), 500000000ull);
+                if (j > last - kSt) mbar_wait(&full[j % kSt], (uint32_t)((j / kSt) & 1), 500000000ull);
                 mbar_wait(&sfull[j % kSSlots], (uint32_t)((j / kSSlots) & 1), 500000000ull);
             }
         }
@@ -535,9 +551,14 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                         const uint32_t a0 = smem_addr(smem + kOffStages + stage * kStageBytes);
                         const uint32_t b0 = smem_addr(bq);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_f8f6f4(tmem + acc * 32, desc_kmajor_sw128(a0 + 32 * k), desc_kmajor_sw128(b0 + 32 * k),
-                                       kIdesc, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k) {
+                            if constexpr (kMx)            // one accumulator per 32-dim scale block
+                                mma_f8f6f4(tmem + acc * kAccCols + 32 * k, desc_kmajor_sw128(a0 + 32 * k),
+                                           desc_kmajor_sw128(b0 + 32 * k), kIdescMx, 0u);
+                            else
+                                mma_f8f6f4(tmem + acc * 32, desc_kmajor_sw128(a0 + 32 * k),
+                                           desc_kmajor_sw128(b0 + 32 * k), kIdesc, k > 0 ? 1u : 0u);
+                        }
                         mma_commit(&empty[stage]);
                         mma_commit(&accf[acc]);
                         issued_any = true;
@@ -548,8 +569,8 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { stop = true; break; }
-                if (++stage == kStages) { stage = 0; phase ^= 1; }
-                if (++acc == kAcc) { acc = 0; acc_phase ^= 1; }
+                if (++stage == kSt) { stage = 0; phase ^= 1; }
+                if (++acc == kAccN) { acc = 0; acc_phase ^= 1; }
             }
             seg_issued = __shfl_sync(0xffffffffu, seg_issued ? 1 : 0, 0) != 0;
             if (seg_issued) {
@@ -558,6 +579,7 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
             }
             bbuf ^= 1;
         }
+        issued_any = __shfl_sync(0xffffffffu, issued_any ? 1 : 0, 0) != 0;
         if (lane == 0 && stop) {
             record_error(st, DSA_DEVERR_TIMEOUT, 2);
             *abort_flag = 1;
@@ -596,32 +618,77 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                 if ((int)(gidx & 1) == grp && !warp_bad) {
                     const int slot = (int)(gidx % kSSlots);
                     const uint32_t sphase = (uint32_t)((gidx / kSSlots) & 1);
-                    const int acc = (int)(gidx % kAcc);
-                    const uint32_t acc_phase = (uint32_t)((gidx / kAcc) & 1);
+                    const int acc = (int)(gidx % kAccN);
+                    const uint32_t acc_phase = (uint32_t)((gidx / kAccN) & 1);
                     int ok = __all_sync(0xffffffffu, mbar_wait(&accf[acc], acc_phase));
                     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sfull[slot], sphase));   // scales + page mask
                     if (ok) {
-                        uint32_t v[32];
-                        tc_fence_after();
-                        tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 32, v);
-                        tmem_ld_wait();
-                        const int vmask = misc->slot_valid[slot];
-                        const float sk = reinterpret_cast<const float*>(smem + kOffScales + slot * 512)[tok];
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) {
-                            mbar_arrive(&acce[acc]);
-                            mbar_arrive(&sempty[slot]);
-                        }
-                        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                        float score;
+                        int vmask;
+                        if constexpr (kMx) {
+                            // x_h = sum over the 4 blocks of 2^(e_b) acc_b[h], 16 heads at a time
+                            const uint32_t ew = reinterpret_cast<const uint32_t*>(smem + kOffScales + slot * 512)[tok];
+                            vmask = misc->slot_valid[slot];
+                            float sc[4];
 #pragma unroll
-                        for (int m = 0; m < 32; m += 4) {
-                            a0 = fmaf(w[m], fmaxf(__uint_as_float(v[m]), 0.f), a0);
-                            a1 = fmaf(w[m + 1], fmaxf(__uint_as_float(v[m + 1]), 0.f), a1);
-                            a2 = fmaf(w[m + 2], fmaxf(__uint_as_float(v[m + 2]), 0.f), a2);
-                            a3 = fmaf(w[m + 3], fmaxf(__uint_as_float(v[m + 3]), 0.f), a3);
+                            for (int q = 0; q < 4; ++q) {
+                                const uint32_t eb = (ew >> (8 * q)) & 255u;
+                                sc[q] = eb ? __uint_as_float(eb << 23) : __uint_as_float(0x00400000u);   // 2^(eb - 127)
+                            }
+                            float a0 = 0.f, a1 = 0.f;
+                            tc_fence_after();
+#pragma unroll
+                            for (int half = 0; half < 2; ++half) {
+                                uint32_t v[4][16];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    tmem_ld_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + acc * kAccCols + q * 32 +
+                                                           half * 16, v[q]);
+                                tmem_ld_wait();
+                                if (half == 1) {
+                                    tc_fence_before();
+                                    __syncwarp();
+                                    if (lane == 0) {
+                                        mbar_arrive(&acce[acc]);
+                                        mbar_arrive(&sempty[slot]);
+                                    }
+                                }
+#pragma unroll
+                                for (int m = 0; m < 16; m += 2) {
+                                    float x0 = sc[0] * __uint_as_float(v[0][m]), x1 = sc[0] * __uint_as_float(v[0][m + 1]);
+#pragma unroll
+                                    for (int q = 1; q < 4; ++q) {
+                                        x0 = fmaf(sc[q], __uint_as_float(v[q][m]), x0);
+                                        x1 = fmaf(sc[q], __uint_as_float(v[q][m + 1]), x1);
+                                    }
+                                    a0 = fmaf(w[half * 16 + m], fmaxf(x0, 0.f), a0);
+                                    a1 = fmaf(w[half * 16 + m + 1], fmaxf(x1, 0.f), a1);
+                                }
+                            }
+                            score = a0 + a1;
+                        } else {
+                            uint32_t v[32];
+                            tc_fence_after();
+                            tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 32, v);
+                            tmem_ld_wait();
+                            vmask = misc->slot_valid[slot];
+                            const float sk = reinterpret_cast<const float*>(smem + kOffScales + slot * 512)[tok];
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) {
+                                mbar_arrive(&acce[acc]);
+                                mbar_arrive(&sempty[slot]);
+                            }
+                            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+                            for (int m = 0; m < 32; m += 4) {
+                                a0 = fmaf(w[m], fmaxf(__uint_as_float(v[m]), 0.f), a0);
+                                a1 = fmaf(w[m + 1], fmaxf(__uint_as_float(v[m + 1]), 0.f), a1);
+                                a2 = fmaf(w[m + 2], fmaxf(__uint_as_float(v[m + 2]), 0.f), a2);
+                                a3 = fmaf(w[m + 3], fmaxf(__uint_as_float(v[m + 3]), 0.f), a3);
+                            }
+                            score = ((a0 + a1) + (a2 + a3)) * sk;
                         }
-                        const float score = ((a0 + a1) + (a2 + a3)) * sk;
                         const int pos = tile * 128 + tok;
                         const bool valid = ((vmask >> (tok >> 6)) & 1) && pos < n_valid;
                         const uint32_t key = score_key(score);
@@ -994,8 +1061,9 @@ struct MapCache {
 };
 }  // namespace
 
-bool make_index_tmap(const uint8_t* cache, int64_t num_pages, CUtensorMap* out) {
-    static MapCache mc;
+bool make_index_tmap(const uint8_t* cache, int64_t num_pages, bool mx, CUtensorMap* out) {
+    static MapCache mcs[2];
+    MapCache& mc = mcs[mx ? 1 : 0];
     if (mc.ptr == cache && mc.pages == num_pages) {
         *out = mc.map;
         return true;
@@ -1012,13 +1080,19 @@ bool make_index_tmap(const uint8_t* cache, int64_t num_pages, CUtensorMap* out) 
     }
     // The cache viewed as a [num_pages * 66, 128] byte matrix: page p's 64
     // payload rows are rows 66p .. 66p+63 (its scales fill rows 66p+64, +65).
-    cuuint64_t dims[2] = {128, (cuuint64_t)num_pages * 66};
-    cuuint64_t strides[1] = {128};
+    // FP8: the cache viewed as a [num_pages * 66, 128] byte matrix: page p's 64
+    // payload rows are rows 66p .. 66p+63 (its scales fill rows 66p+64, +65).
+    // MXFP4: a [num_pages * 68, 128] matrix of 4-bit values (64-byte rows), page
+    // p's payload rows 68p .. 68p+63; 16U4_ALIGN16B lands each row as 128 bytes,
+    // eight bytes of values then eight bytes of gap per 16 values.
+    cuuint64_t dims[2] = {128, (cuuint64_t)num_pages * (mx ? 68 : 66)};
+    cuuint64_t strides[1] = {mx ? 64u : 128u};
     cuuint32_t box[2] = {128, 64};
     cuuint32_t estr[2] = {1, 1};
-    CUresult res = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult res = encode(out, mx ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                          const_cast<uint8_t*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (res != CUDA_SUCCESS) return false;
     mc.ptr = cache;
     mc.pages = num_pages;
@@ -1066,12 +1140,14 @@ Plan carve_plan(void* base, int64_t batch, int G) {
 
 dsa_status launch_indexer_tc(const uint8_t* q8, const float* wq, uint32_t* hist, const uint8_t* cache,
                              const dsa_batch* b, int32_t* topk, float* topk_scores, void* plan_ws, int G, int32_t* st,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool mx) {
     CUtensorMap map;
-    if (!make_index_tmap(cache, b->num_pages, &map)) return DSA_ERR_CUDA;
+    if (!make_index_tmap(cache, b->num_pages, mx, &map)) return DSA_ERR_CUDA;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(itc::score_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(itc::score_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 itc::kSmemAlloc) != cudaSuccess ||
+            cudaFuncSetAttribute(itc::score_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  itc::kSmemAlloc) != cudaSuccess ||
             cudaFuncSetAttribute(itc::merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  itc::kMergeSmem) != cudaSuccess)
@@ -1083,7 +1159,8 @@ dsa_status launch_indexer_tc(const uint8_t* q8, const float* wq, uint32_t* hist,
     p.hist = hist;
     itc::plan_kernel<<<1, 1024, 0, s>>>(bd, G, p);
     DSA_CHECK_LAUNCH();
-    itc::score_topk_kernel<<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
+    if (mx) itc::score_topk_kernel<true><<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
+    else itc::score_topk_kernel<false><<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
     DSA_CHECK_LAUNCH();
     itc::merge_filter_kernel<<<(unsigned)(G + b->batch), itc::kFiltThreads, 0, s>>>(bd, p);
     DSA_CHECK_LAUNCH();

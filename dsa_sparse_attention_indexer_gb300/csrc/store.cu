@@ -17,8 +17,31 @@ struct RopeFreqs {
     double theta[32];
 };
 
+// E2M1 code of y (OCP Microscaling FP4: values 0, 0.5, 1, 1.5, 2, 3, 4, 6 with
+// a sign bit): nearest value, ties to the even code, |y| > 6 saturates to 6;
+// the sign bit follows y.  The thresholds are the midpoints between
+// neighbouring values; a midpoint goes to the neighbour whose code is even.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+    const uint32_t sign = (__float_as_uint(y) >> 31) << 3;
+    const float a = fabsf(y);
+    uint32_t m;
+    if (a <= 0.25f) m = 0;
+    else if (a < 0.75f) m = 1;
+    else if (a <= 1.25f) m = 2;
+    else if (a < 1.75f) m = 3;
+    else if (a <= 2.5f) m = 4;
+    else if (a < 3.5f) m = 5;
+    else if (a <= 5.0f) m = 6;
+    else m = 7;
+    return sign | m;
+}
+
 // One warp per token; lane l owns dims [4l, 4l+4).  RoPE pairs (2i, 2i+1)
-// never straddle lanes.
+// never straddle lanes.  kMx: the MXFP4 page layout ("GLM-5.3 推理全链路(十一)",
+// 两个框架的对照): lanes 8b .. 8b+7 hold block b of 32 dims, whose shared
+// exponent is floor(log2(amax)) - 2 (OCP MX, E2M1's largest value is 1.5 * 2^2),
+// clamped to [-127, 127]; each lane writes its 4 codes as 2 packed bytes.
+template <bool kMx>
 __global__ void __launch_bounds__(256)
 index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__ pos,
                      const int64_t* __restrict__ slot, int64_t n,
@@ -70,6 +93,21 @@ index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__
         }
     }
     float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    if constexpr (kMx) {
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        int k2 = 0;
+        frexpf(amax, &k2);                               // amax = m * 2^k2, m in [0.5, 1)
+        const int e = amax > 0.f ? max(-127, min(127, k2 - 1 - 2)) : 0;
+        const uint32_t c0 = e2m1_code(ldexpf(x[0], -e)), c1 = e2m1_code(ldexpf(x[1], -e));
+        const uint32_t c2 = e2m1_code(ldexpf(x[2], -e)), c3 = e2m1_code(ldexpf(x[3], -e));
+        const int64_t page = s / kPage;
+        const int row = (int)(s % kPage);
+        uint8_t* pg = cache + page * (int64_t)DSA_IDXK_MXFP4_PAGE_BYTES;
+        *reinterpret_cast<uint16_t*>(pg + row * 64 + lane * 2) = (uint16_t)(c0 | (c1 << 4) | (c2 << 8) | (c3 << 12));
+        if ((lane & 7) == 0) pg[kPage * 64 + row * 4 + (lane >> 3)] = (uint8_t)(e + 127);
+        return;
+    }
     amax = warp_max(amax);
     const int e = ue8m0_exponent(amax);
     const uint32_t lo = f32x2_to_e4m3x2(ldexpf(x[0], -e), ldexpf(x[1], -e));
@@ -143,7 +181,28 @@ extern "C" dsa_status dsa_index_k_store(const void* k, const int32_t* pos, const
     if (blocks > 0x7fffffff) return DSA_ERR_UNSUPPORTED;
     RopeFreqs fr;
     for (int i = 0; i < 32; ++i) fr.theta[i] = std::pow((double)rope_base, -2.0 * (double)i / 64.0);
-    index_k_store_kernel<<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
+    index_k_store_kernel<false><<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
+        static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, fr,
+        idxk_cache, num_pages, dev_status);
+    DSA_CHECK_LAUNCH();
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_index_k_store_mxfp4(const void* k, const int32_t* pos, const int64_t* slot,
+                                              int64_t n, const float* gamma, const float* beta,
+                                              float ln_eps, float rope_base, uint8_t* idxk_cache,
+                                              int64_t num_pages, int32_t* dev_status, void* stream) {
+    if (n < 0 || num_pages < 0) return DSA_ERR_INVALID_ARGUMENT;
+    if (n == 0) return DSA_OK;
+    if (!k || !pos || !slot || !idxk_cache) return DSA_ERR_INVALID_ARGUMENT;
+    if (!(ln_eps >= 0.f) || !(rope_base > 0.f)) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(k) || (reinterpret_cast<uintptr_t>(idxk_cache) & 31)) return DSA_ERR_ALIGNMENT;
+    const int warps = 8;
+    const int64_t blocks = (n + warps - 1) / warps;
+    if (blocks > 0x7fffffff) return DSA_ERR_UNSUPPORTED;
+    RopeFreqs fr;
+    for (int i = 0; i < 32; ++i) fr.theta[i] = std::pow((double)rope_base, -2.0 * (double)i / 64.0);
+    index_k_store_kernel<true><<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
         static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, fr,
         idxk_cache, num_pages, dev_status);
     DSA_CHECK_LAUNCH();

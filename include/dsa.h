@@ -56,6 +56,11 @@ extern "C" {
 #define DSA_INDEX_HEAD_DIM   128
 #define DSA_IDXK_TOKEN_BYTES 132    /* 128 B FP8 E4M3 key + 4 B scale             */
 #define DSA_IDXK_PAGE_BYTES  8448   /* [64 x 128 B payload | 64 x fp32 scale]     */
+/* MXFP4 index-K variant ("GLM-5.3 推理全链路(十一)", 两个框架的对照): per token 64 B of
+ * packed E2M1 values (element 2i in the low nibble of byte i) and four ue8m0
+ * block scales (one per 32 dims, byte e + 127).                               */
+#define DSA_IDXK_MXFP4_TOKEN_BYTES 68
+#define DSA_IDXK_MXFP4_PAGE_BYTES  4352 /* [64 x 64 B packed | 64 x 4 B scales]   */
 #define DSA_MLA_HEADS        64
 #define DSA_LATENT_DIM       512
 #define DSA_ROPE_DIM         64
@@ -138,6 +143,17 @@ dsa_status dsa_index_k_store(const void* k, const int32_t* pos, const int64_t* s
                              uint8_t* idxk_cache, int64_t num_pages,
                              int32_t* dev_status, void* stream);
 
+/* ---- Index-K store, MXFP4 variant --------------------------------------------
+ * The same LayerNorm and RoPE as dsa_index_k_store, then per block of 32 dims
+ * the OCP MX scale 2^e with e = floor(log2(amax)) - 2 (amax == 0 -> e = 0; e
+ * clamped to [-127, 127]) and E2M1 elements rounded to nearest, ties to even,
+ * saturated at +-6.  Arguments as dsa_index_k_store, except
+ *   idxk_cache device uint8 [num_pages * 4352], 32-byte aligned.              */
+dsa_status dsa_index_k_store_mxfp4(const void* k, const int32_t* pos, const int64_t* slot, int64_t n,
+                                   const float* gamma, const float* beta, float ln_eps, float rope_base,
+                                   uint8_t* idxk_cache, int64_t num_pages,
+                                   int32_t* dev_status, void* stream);
+
 /* ---- Latent KV store (writes the 656-B rows that sparse MLA gathers;
  *      "GLM-5.3 推理全链路(十一)", 主 KV 缓存里存的是什么) --------------------------
  * For each token: c (512 dims) -> four blocks of 128, each FP8 E4M3 with its own
@@ -170,6 +186,18 @@ dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_c
                             const dsa_batch* b, int32_t* topk, float* topk_scores,
                             dsa_topk_share* share, int32_t layer_id,
                             void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ---- Indexer + top-2048 over an MXFP4 index-K cache --------------------------
+ * dsa_indexer_topk for a cache written by dsa_index_k_store_mxfp4: the same
+ * queries, selection rule, outputs, share handle and workspace (sized by
+ * dsa_indexer_topk_workspace_size); scores are formed on the dequantised
+ * values (E2M1 x 2^e per 32-dim block).  Decode batches only (q_len == 1 for
+ * every request; others return DSA_ERR_UNSUPPORTED).
+ *   idxk_cache device uint8 [num_pages * 4352], 32-byte aligned               */
+dsa_status dsa_indexer_topk_mxfp4(const void* q, const float* w, const uint8_t* idxk_cache,
+                                  const dsa_batch* b, int32_t* topk, float* topk_scores,
+                                  dsa_topk_share* share, int32_t layer_id,
+                                  void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* ---- Indexer + top-2048 without a workspace argument --------------------
  * The pages have no counterpart of this call.  It serves callers that cannot

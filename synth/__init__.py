@@ -49,6 +49,7 @@ class Workload:
     boost_frac: float = 0.0  # fraction of each request's tokens with a x4 index key
     description: str = ""
     draft_steps: int = 0     # > 0: the new tokens are the draft steps of one MTP iteration
+    index_format: str = "fp8"  # index-K cache: "fp8" (132 B/token) or "mxfp4" (68 B/token)
 
     @property
     def batch(self) -> int:

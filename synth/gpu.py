@@ -34,7 +34,11 @@ class GpuWorkload:
         self.batch = D.Batch(self.seq_len, self.q_start, self.pt, w.num_pages, max_seq_len=w.max_seq_len,
                              max_q_len=w.max_q_len, total_q=w.total_q)
         self.dev_status = D.new_device_status(device)
-        self.idx_cache = torch.zeros(w.num_pages * D.IDXK_PAGE_BYTES, dtype=torch.uint8, device=device)
+        self.mx = w.index_format == "mxfp4"
+        self.idx_page_bytes = D.IDXK_MXFP4_PAGE_BYTES if self.mx else D.IDXK_PAGE_BYTES
+        self.idx_cache = torch.zeros(w.num_pages * self.idx_page_bytes, dtype=torch.uint8, device=device)
+        self.index_k_store = D.dsa_index_k_store_mxfp4 if self.mx else D.dsa_index_k_store
+        self.indexer_topk = D.dsa_indexer_topk_mxfp4 if self.mx else D.dsa_indexer_topk
         self.kv_cache = {l: torch.zeros(w.num_pages * D.KV_PAGE_BYTES, dtype=torch.uint8, device=device)
                          for l in self.layers}
         which = "all" if store_new else "prefix"
@@ -48,14 +52,18 @@ class GpuWorkload:
         for a in range(0, n, chunk_tokens):
             b_ = min(n, a + chunk_tokens)
             sl = torch.where(keep[a:b_], slot[a:b_], torch.full_like(slot[a:b_], -1))
-            D.dsa_index_k_store(k_all[a:b_], pos[a:b_].contiguous(), sl.contiguous(), self.idx_cache,
+            self.index_k_store(k_all[a:b_], pos[a:b_].contiguous(), sl.contiguous(), self.idx_cache,
                                 dev_status=self.dev_status)
         del k_all
         if w.boost_frac > 0:
             bm = boost_mask(w, device)
-            sv = D.index_cache_scale_view(self.idx_cache)
             bs = slot[bm]
-            sv[bs // PAGE, bs % PAGE] *= 4.0
+            if self.mx:                                    # x4: every block exponent + 2
+                sv = self.idx_cache.view(-1, self.idx_page_bytes)[:, 64 * 64:].view(-1, PAGE, 4)
+                sv[bs // PAGE, bs % PAGE] += 2
+            else:
+                sv = D.index_cache_scale_view(self.idx_cache)
+                sv[bs // PAGE, bs % PAGE] *= 4.0
         for l in self.layers:
             c_all, r_all = latent(w, l, n, device)
             for a in range(0, n, chunk_tokens):
