@@ -376,6 +376,25 @@ def layer_skips_topk(layer_id: int, freq: int, offset: int) -> bool:
     return max(layer_id - offset + 1, 0) % freq != 0
 
 
+def layer_skips_topk_config(layer_id: int, indexer_types=None, cli_factor: int = 1, index_topk_pattern=None,
+                            index_topk_freq: int = 1, index_skip_topk_offset=None) -> bool:
+    """Whether a layer reuses the previous top-k, from whichever schedule fields
+    a config carries, in the order the pages give ("配置里的 78 个字符"): the
+    explicit indexer_types list; else cli_factor > 1 (a fresh top-k every
+    cli_factor layers); else index_topk_pattern ('S' marks a shared layer);
+    else the index_topk_freq rule with index_skip_topk_offset, whose default 2
+    gives max(layer_id - 1, 0) % freq != 0 (layers 0 and 1 full, 2 shared).
+    Layers past the end of a list or pattern are full."""
+    if indexer_types is not None:
+        return 0 <= layer_id < len(indexer_types) and indexer_types[layer_id] == "shared"
+    if cli_factor > 1:
+        return layer_id % cli_factor != 0
+    if index_topk_pattern is not None:
+        return layer_id < len(index_topk_pattern) and index_topk_pattern[layer_id] == "S"
+    off = 2 if index_skip_topk_offset is None else index_skip_topk_offset
+    return layer_skips_topk(layer_id, index_topk_freq, off)
+
+
 # ----------------------------------------------------------------------------
 # One request through the whole step, for the tests and the CPU baseline.
 # ----------------------------------------------------------------------------

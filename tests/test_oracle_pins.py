@@ -497,3 +497,28 @@ def test_mxfp4_scores_brute_force():
     ref = _brute_scores(O.e4m3_decode(qc) * qs[:, None], w, kd)
     assert np.allclose(s, ref, rtol=1e-12, atol=1e-12)
     assert np.all(O.score_magnitude_mxfp4(qc, qs, w, kc, ke) >= np.abs(s) - 1e-12)
+
+
+# ------------------------------------------------------------------ schedule fallbacks
+def test_schedule_fallback_chain_follows_the_pages():
+    n = g("num_layers")
+    full = set(g("full_layers"))
+    types = ["full" if l in full else "shared" for l in range(n)]
+    # the explicit list wins over every other field
+    assert [not O.layer_skips_topk_config(l, indexer_types=types, cli_factor=3, index_topk_freq=2)
+            for l in range(n)] == [l in full for l in range(n)]
+    # GLM-5.3's parameterised fields give the same 21 / 57 split as its list
+    fr = [not O.layer_skips_topk_config(l, index_topk_freq=g("index_topk_freq"),
+                                        index_skip_topk_offset=g("index_skip_topk_offset")) for l in range(n)]
+    assert fr == [l in full for l in range(n)] and sum(fr) == g("n_full")
+    # the default offset: layers 0 and 1 full, layer 2 shared, then one full layer in every 4
+    d = [not O.layer_skips_topk_config(l, index_topk_freq=4) for l in range(12)]
+    assert d == [True, True, False, False, False, True, False, False, False, True, False, False]
+    # cli_factor: a fresh top-k every cli_factor layers, ahead of the pattern and the freq rule
+    assert [not O.layer_skips_topk_config(l, cli_factor=3, index_topk_pattern="SSSS", index_topk_freq=5)
+            for l in range(7)] == [True, False, False, True, False, False, True]
+    # pattern: 'S' is shared, anything else and anything past its end is full
+    assert [O.layer_skips_topk_config(l, index_topk_pattern="FSSFS") for l in range(7)] == \
+        [False, True, True, False, True, False, False]
+    # a list shorter than the model: layers past its end are full
+    assert not O.layer_skips_topk_config(5, indexer_types=["full", "shared"])
