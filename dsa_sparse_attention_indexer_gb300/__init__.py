@@ -60,6 +60,11 @@ class DsaError(RuntimeError):
         super().__init__(f"{fn} -> {self.name} ({status_string(code)})")
 
 
+class DsaScheduleConfig(ctypes.Structure):
+    _fields_ = [("indexer_types", POINTER(c_char_p)), ("n_types", c_int32), ("cli_factor", c_int32),
+                ("index_topk_pattern", c_char_p), ("index_topk_freq", c_int32), ("index_skip_topk_offset", c_int32)]
+
+
 class DsaBatch(ctypes.Structure):
     _fields_ = [("batch", c_int32), ("max_pages", c_int32), ("max_seq_len", c_int32),
                 ("max_q_len", c_int32), ("total_q", c_int64), ("num_pages", c_int64),
@@ -99,6 +104,7 @@ _SIGS = {
                                          c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
     "dsa_parse_indexer_types": (c_int32, [POINTER(c_char_p), c_int32, POINTER(c_uint8)]),
     "dsa_schedule_from_freq": (c_int32, [c_int32, c_int32, c_int32, POINTER(c_uint8)]),
+    "dsa_schedule_resolve": (c_int32, [POINTER(DsaScheduleConfig), c_int32, POINTER(c_uint8)]),
     "dsa_topk_share_create": (c_int32, [POINTER(c_void_p)]),
     "dsa_topk_share_destroy": (c_int32, [c_void_p]),
     "dsa_topk_share_reset": (c_int32, [c_void_p]),
@@ -386,6 +392,25 @@ def dsa_parse_indexer_types(types) -> list:
 def dsa_schedule_from_freq(n_layers: int, freq: int, offset: int) -> list:
     out = (c_uint8 * n_layers)()
     _check("dsa_schedule_from_freq", lib().dsa_schedule_from_freq(n_layers, freq, offset, out))
+    return [bool(v) for v in out]
+
+
+def dsa_schedule_resolve(n_layers: int, *, indexer_types=None, cli_factor: int = 1, index_topk_pattern=None,
+                         index_topk_freq: int = 1, index_skip_topk_offset=None) -> list:
+    """Full (True) / shared (False) per layer from whichever schedule fields a config carries."""
+    cfg = DsaScheduleConfig()
+    keep = None
+    if indexer_types is not None:
+        keep = (c_char_p * len(indexer_types))(*[t.encode() for t in indexer_types])
+        cfg.indexer_types = ctypes.cast(keep, POINTER(c_char_p))
+        cfg.n_types = len(indexer_types)
+    cfg.cli_factor = cli_factor
+    cfg.index_topk_pattern = None if index_topk_pattern is None else index_topk_pattern.encode()
+    cfg.index_topk_freq = index_topk_freq
+    cfg.index_skip_topk_offset = -1 if index_skip_topk_offset is None else index_skip_topk_offset
+    out = (c_uint8 * n_layers)()
+    _check("dsa_schedule_resolve", lib().dsa_schedule_resolve(ctypes.byref(cfg), n_layers, out))
+    del keep
     return [bool(v) for v in out]
 
 

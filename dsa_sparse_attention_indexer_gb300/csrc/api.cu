@@ -74,6 +74,33 @@ extern "C" dsa_status dsa_schedule_from_freq(int32_t n_layers, int32_t freq, int
     return DSA_OK;
 }
 
+extern "C" dsa_status dsa_schedule_resolve(const dsa_schedule_config* cfg, int32_t n_layers, uint8_t* is_full) {
+    if (!cfg || !is_full || n_layers < 0) return DSA_ERR_INVALID_ARGUMENT;
+    if (cfg->indexer_types) {
+        if (cfg->n_types < 0) return DSA_ERR_INVALID_ARGUMENT;
+        for (int32_t l = 0; l < cfg->n_types; ++l) {
+            const char* t = cfg->indexer_types[l];
+            if (!t || (std::strcmp(t, "full") != 0 && std::strcmp(t, "shared") != 0)) return DSA_ERR_INVALID_ARGUMENT;
+        }
+        for (int32_t l = 0; l < n_layers; ++l)
+            is_full[l] = (l < cfg->n_types && std::strcmp(cfg->indexer_types[l], "shared") == 0) ? 0 : 1;
+        return DSA_OK;
+    }
+    if (cfg->cli_factor > 1) {
+        for (int32_t l = 0; l < n_layers; ++l) is_full[l] = (l % cfg->cli_factor != 0) ? 0 : 1;
+        return DSA_OK;
+    }
+    if (cfg->index_topk_pattern) {
+        const size_t len = std::strlen(cfg->index_topk_pattern);
+        for (int32_t l = 0; l < n_layers; ++l)
+            is_full[l] = ((size_t)l < len && cfg->index_topk_pattern[l] == 'S') ? 0 : 1;
+        return DSA_OK;
+    }
+    if (cfg->index_topk_freq < 1) return DSA_ERR_INVALID_ARGUMENT;
+    const int32_t off = cfg->index_skip_topk_offset < 0 ? 2 : cfg->index_skip_topk_offset;
+    return dsa_schedule_from_freq(n_layers, cfg->index_topk_freq, off, is_full);
+}
+
 extern "C" dsa_status dsa_topk_share_create(dsa_topk_share** out) {
     if (!out) return DSA_ERR_INVALID_ARGUMENT;
     dsa_topk_share* s = new (std::nothrow) dsa_topk_share{nullptr, 0, -1, false, false};

@@ -276,6 +276,27 @@ dsa_status dsa_sparse_mla_prefill(const void* q, const int32_t* topk, const dsa_
 dsa_status dsa_parse_indexer_types(const char* const* types, int32_t n_layers, uint8_t* is_full);
 dsa_status dsa_schedule_from_freq(int32_t n_layers, int32_t freq, int32_t offset, uint8_t* is_full);
 
+/* ---- Schedule from whichever fields a model config carries ("GLM-5.3 推理全链路
+ *      (十一)", 配置里的 78 个字符: the order SGLang's dsa_layer_skips_topk checks) ---
+ * Layer l is shared (reuses the previous top-k) by the first rule that applies:
+ *   1. indexer_types != NULL: types[l] == "shared" (layers past n_types: full;
+ *      any entry other than "full" / "shared" -> DSA_ERR_INVALID_ARGUMENT);
+ *   2. cli_factor > 1: l % cli_factor != 0;
+ *   3. index_topk_pattern != NULL: pattern[l] == 'S' (past its end: full);
+ *   4. max(l - offset + 1, 0) % index_topk_freq != 0 with offset =
+ *      index_skip_topk_offset, or 2 when it is negative (absent): layers 0 and 1
+ *      full, layer 2 shared, then one full layer in every index_topk_freq.
+ * is_full[l] receives 0 / 1 for l < n_layers.                                  */
+typedef struct dsa_schedule_config {
+    const char* const* indexer_types;   /* n_types strings, or NULL            */
+    int32_t n_types;
+    int32_t cli_factor;                 /* <= 1: not set                       */
+    const char* index_topk_pattern;     /* NUL-terminated, or NULL             */
+    int32_t index_topk_freq;            /* >= 1                                */
+    int32_t index_skip_topk_offset;     /* < 0: not set (2)                    */
+} dsa_schedule_config;
+dsa_status dsa_schedule_resolve(const dsa_schedule_config* cfg, int32_t n_layers, uint8_t* is_full);
+
 /* ---- Share handle ("GLM-5.3 推理全链路(十一)", 一次前向里 topk 只算一遍) ------------
  * publish: record that `topk` (device int32 [rows,2048]) holds layer
  *   `layer_id`'s indices; the pointer is borrowed, not copied.

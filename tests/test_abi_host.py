@@ -139,6 +139,31 @@ def test_schedule_parser_and_freq_rule(L):
         D.dsa_parse_indexer_types(["full", "sparse"])
 
 
+def test_schedule_resolve_matches_the_oracle_chain(L):
+    from oracle import dsa_oracle as O
+    import random
+    rng = random.Random(5)
+    for trial in range(300):
+        n = rng.randint(0, 90)
+        kw = {}
+        if rng.random() < 0.3:
+            kw["indexer_types"] = [rng.choice(["full", "shared"]) for _ in range(rng.randint(0, 90))]
+        if rng.random() < 0.4:
+            kw["cli_factor"] = rng.randint(0, 5)
+        if rng.random() < 0.4:
+            kw["index_topk_pattern"] = "".join(rng.choice("FS") for _ in range(rng.randint(0, 90)))
+        kw["index_topk_freq"] = rng.randint(1, 6)
+        if rng.random() < 0.6:
+            kw["index_skip_topk_offset"] = rng.randint(0, 5)
+        got = D.dsa_schedule_resolve(n, **kw)
+        want = [not O.layer_skips_topk_config(l, **kw) for l in range(n)]
+        assert got == want, (trial, kw)
+    with pytest.raises(D.DsaError):
+        D.dsa_schedule_resolve(4, indexer_types=["full", "fuII"])
+    with pytest.raises(D.DsaError):
+        D.dsa_schedule_resolve(4, index_topk_freq=0)
+
+
 def test_share_handle_lifecycle(L):
     s = D.TopkShare()
     with pytest.raises(D.DsaError) as e:
