@@ -658,3 +658,38 @@ def request_topk_mxfp4(q_idx, w, cache, page_table_row, seq_len, q_len):
         out[t] = topk_positions(s, n_valid)
         all_scores.append(s)
     return out, all_scores
+
+
+# ----------------------------------------------------------------------------
+# The latent row written upstream of sparse MLA, from the A-projection outputs
+# ("GLM-5.3 推理全链路(一)", section 4.3 两个 RMSNorm 与 RoPE: kv_a_layernorm over
+# the 512-d kv_c, RoPE on the 64-d k_pe only, and the fused kernel writes the
+# result into the KV pool - and, on a layer with an indexer, the index key too).
+# Readings where the pages are silent: RMSNorm y = x / sqrt(mean(x^2) + eps)
+# times an optional gamma, eps 1e-6; the k_pe rotation uses the index key's
+# convention (interleaved pairs, base 10000, all 64 dims); the rotated values
+# are stored as bf16 rounded to nearest even (through torch's fp64 -> bf16
+# cast, a library step).
+# ----------------------------------------------------------------------------
+def rms_norm(x: np.ndarray, gamma=None, eps: float = 1e-6) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float64)
+    y = x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
+    if gamma is not None:
+        y = y * np.asarray(gamma, dtype=np.float64)
+    return y
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(np.asarray(x, dtype=np.float64))).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def latent_prepare(kv_c: np.ndarray, k_pe: np.ndarray, pos: np.ndarray, gamma=None, eps: float = 1e-6,
+                   rope_base: float = 10000.0):
+    """One latent row per token from the raw kv_c [n,512] and k_pe [n,64]:
+    (FP8 codes [n,512], scales [n,4], RoPE bf16 bits [n,64])."""
+    c = rms_norm(kv_c, gamma, eps)
+    r = rope_interleaved(np.asarray(k_pe, dtype=np.float64), pos, rope_base, ROPE_DIM)
+    codes, scales = latent_quantize(c)
+    return codes, scales, f64_to_bf16_bits(r)

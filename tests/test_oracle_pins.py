@@ -522,3 +522,35 @@ def test_schedule_fallback_chain_follows_the_pages():
         [False, True, True, False, True, False, False]
     # a list shorter than the model: layers past its end are full
     assert not O.layer_skips_topk_config(5, indexer_types=["full", "shared"])
+
+
+# ------------------------------------------------------------------ fused latent store
+def test_rms_norm_against_torch_and_its_defining_property():
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((50, 512)) * np.exp2(rng.integers(-5, 5, (50, 1)))
+    gam = rng.uniform(0.5, 1.5, 512)
+    y = O.rms_norm(x, None, 1e-6)
+    assert np.allclose((y * y).mean(axis=-1), 1.0 / (1.0 + 1e-6 / (x * x).mean(axis=-1)), rtol=1e-12)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (512,), torch.from_numpy(gam), eps=1e-6).numpy()
+    assert np.allclose(O.rms_norm(x, gam, 1e-6), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_latent_prepare_rotates_only_the_rope_dims_and_rounds_to_bf16():
+    rng = np.random.default_rng(42)
+    n = 40
+    kv = rng.standard_normal((n, 512))
+    pe = rng.standard_normal((n, 64))
+    pos = rng.integers(0, 1 << 20, n)
+    codes, scales, rbits = O.latent_prepare(kv, pe, pos)
+    # the latent part is the plain quantisation of the RMS-normalised kv_c
+    c2, s2 = O.latent_quantize(O.rms_norm(kv))
+    assert np.array_equal(codes, c2) and np.array_equal(scales, s2)
+    # the RoPE part keeps each pair's norm up to bf16 rounding, and position 0 is the identity
+    r = O.bf16_bits_to_f64(rbits)
+    assert np.allclose(np.hypot(r[:, 0::2], r[:, 1::2]), np.hypot(pe[:, 0::2], pe[:, 1::2]), rtol=2 ** -7)
+    _, _, r0 = O.latent_prepare(kv[:1], pe[:1], np.array([0]))
+    assert np.array_equal(O.bf16_bits_to_f64(r0), O.bf16_bits_to_f64(O.f64_to_bf16_bits(pe[:1])))
+    # nearest bf16: within half a bf16 ulp of the exact rotation
+    exact = O.rope_interleaved(pe, pos, 10000.0, 64)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 1e-30))) - 7)
+    assert np.all(np.abs(r - exact) <= 0.5 * ulp * (1 + 1e-9))
