@@ -147,9 +147,10 @@ def workload_bytes(w, mtp_reuse=True):
 class Step:
     """All device buffers of one step and the calls that make it up."""
 
-    def __init__(self, gw, D):
+    def __init__(self, gw, D, fused_store=False):
         self.gw = gw
         self.D = D
+        self.fused_store = fused_store    # one fused latent (+ index-K) store per layer from raw kv_c / k_pe
         w = gw.w
         dev = gw.device
         self.share = D.TopkShare()
@@ -181,11 +182,15 @@ class Step:
         for li, l in enumerate(gw.layers):
             if before_layer is not None:
                 before_layer(l)
-            if self.full[li]:
-                t("index_k_store", lambda: gw.index_k_store(gw.new_k, gw.new_pos, gw.new_slot, gw.idx_cache,
-                                                                 dev_status=gw.dev_status, stream=stream))
-            t("latent_kv_store", lambda: D.dsa_latent_kv_store(gw.new_c[l], gw.new_r[l], gw.new_slot, gw.kv_cache[l],
-                                                                 dev_status=gw.dev_status, stream=stream))
+            if self.fused_store:
+                t("latent_kv_store", lambda: self._fused(l, self.full[li], stream))
+            else:
+                if self.full[li]:
+                    t("index_k_store", lambda: gw.index_k_store(gw.new_k, gw.new_pos, gw.new_slot, gw.idx_cache,
+                                                                     dev_status=gw.dev_status, stream=stream))
+                t("latent_kv_store", lambda: D.dsa_latent_kv_store(gw.new_c[l], gw.new_r[l], gw.new_slot,
+                                                                     gw.kv_cache[l], dev_status=gw.dev_status,
+                                                                     stream=stream))
             if self.full[li]:
                 t("indexer_topk", lambda: gw.indexer_topk(gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch,
                                                              topk=self.topk, share=self.share, layer_id=l,
@@ -198,6 +203,12 @@ class Step:
             if after_layer is not None:
                 after_layer(l)
         return first_full
+
+    def _fused(self, l, full, stream):
+        gw = self.gw
+        self.D.dsa_latent_kv_store_fused(gw.new_c[l], gw.new_r[l], gw.new_pos, gw.new_slot, gw.kv_cache[l],
+                                         idx_k=gw.new_k if full else None, idxk_cache=gw.idx_cache if full else None,
+                                         dev_status=gw.dev_status, stream=stream)
 
     def e2e_io(self):
         """(inputs copied first, inputs per layer, output per layer) of the e2e step."""
@@ -214,11 +225,15 @@ class Step:
         D, gw = self.D, self.gw
         stream = torch.cuda.current_stream()
         for li, l in enumerate(gw.layers):
-            if self.full[li]:
+            if self.fused_store:
+                out.append(("latent_kv_store", (lambda l=l, f=self.full[li]: self._fused(l, f, stream))))
+            if self.full[li] and not self.fused_store:
                 out.append(("index_k_store", lambda: gw.index_k_store(
                     gw.new_k, gw.new_pos, gw.new_slot, gw.idx_cache, dev_status=gw.dev_status, stream=stream)))
-            out.append(("latent_kv_store", (lambda l=l: D.dsa_latent_kv_store(
-                gw.new_c[l], gw.new_r[l], gw.new_slot, gw.kv_cache[l], dev_status=gw.dev_status, stream=stream))))
+            if not self.fused_store:
+                out.append(("latent_kv_store", (lambda l=l: D.dsa_latent_kv_store(
+                    gw.new_c[l], gw.new_r[l], gw.new_slot, gw.kv_cache[l], dev_status=gw.dev_status,
+                    stream=stream))))
             if self.full[li]:
                 out.append(("indexer_topk", (lambda l=l: gw.indexer_topk(
                     gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch, topk=self.topk, share=self.share, layer_id=l,
@@ -386,7 +401,7 @@ def run_ours(args, rank, world):
     w = synth.workload(args.workload, batch=args.batch, ctx=args.ctx)
     w.index_format = args.index_cache
     gw = GpuWorkload(w, dev)
-    step = MtpStep(gw, D, reuse=not args.no_mtp_reuse) if w.draft_steps else Step(gw, D)
+    step = MtpStep(gw, D, reuse=not args.no_mtp_reuse) if w.draft_steps else Step(gw, D, args.fused_store)
     torch.cuda.synchronize()
     stream = torch.cuda.Stream()                      # graphs are captured on a non-default stream
     torch.cuda.set_stream(stream)
@@ -638,11 +653,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--index-cache", default="fp8", choices=["fp8", "mxfp4"],
                     help="index-K cache format (mxfp4: decode workloads)")
+    ap.add_argument("--fused-store", action="store_true",
+                    help="store each layer's latent row (and, on full layers, the index key) with the fused "
+                         "RMSNorm / RoPE call from raw kv_c and k_pe")
     ap.add_argument("--no-mtp-reuse", action="store_true",
                     help="MTP workloads: every draft step runs its own indexer (the comparison point)")
     args = ap.parse_args()
     if args.index_cache == "mxfp4" and args.workload not in ("tiny", "decode32k", "decode1m"):
         ap.error("--index-cache mxfp4 covers the decode workloads (tiny, decode32k, decode1m)")
+    if args.fused_store and (args.index_cache == "mxfp4" or args.workload == "mtp5_1m"):
+        ap.error("--fused-store writes FP8 index keys in the layer-group step")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -712,6 +732,7 @@ def main():
             "us_per_call": {k: round(v, 2) for k, v in res["per_call"].items()},
             **({"draft_steps": w.draft_steps, "mtp_reuse": not args.no_mtp_reuse} if w.draft_steps else {}),
             "index_cache": w.index_format,
+            "store": "fused" if args.fused_store else "separate",
         },
         "roofline": {"kernel": dom, **roof, "traffic": traffic, "peak_source": pk["source"],
                      "algorithmic_bytes_per_launch": dom_bytes, "algorithmic_flops_per_launch": dom_flops,

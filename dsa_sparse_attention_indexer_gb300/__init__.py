@@ -84,6 +84,9 @@ _SIGS = {
                                           c_float, c_void_p, c_int64, c_void_p, c_void_p]),
     "dsa_indexer_topk_mxfp4": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_void_p, c_void_p,
                                          c_void_p, c_int32, c_void_p, c_size_t, c_void_p, c_void_p]),
+    "dsa_latent_kv_store_fused": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_float,
+                                            c_float, c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_float,
+                                            c_void_p, c_int64, c_void_p, c_void_p]),
     "dsa_latent_kv_store": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64, c_void_p,
                                       c_void_p]),
     "dsa_indexer_topk_workspace_size": (c_int32, [POINTER(DsaBatch), POINTER(c_size_t)]),
@@ -249,6 +252,28 @@ def dsa_index_k_store_mxfp4(k, pos, slot, idxk_cache, *, gamma=None, beta=None, 
     _check("dsa_index_k_store_mxfp4", lib().dsa_index_k_store_mxfp4(
         _ptr(k), _ptr(pos), _ptr(slot), k.shape[0], _ptr(gamma), _ptr(beta), ln_eps, rope_base,
         _ptr(idxk_cache), num_pages, _ptr(dev_status), _stream(stream)))
+
+
+def dsa_latent_kv_store_fused(kv_c, k_pe, pos, slot, kv_cache, *, kv_gamma=None, rms_eps=1e-6, rope_base=10000.0,
+                              idx_k=None, idxk_cache=None, idx_gamma=None, idx_beta=None, ln_eps=1e-6,
+                              num_pages=None, idx_num_pages=None, dev_status=None, stream=None):
+    """Latent rows from raw kv_c / k_pe (RMSNorm, RoPE) and, with idx_k, the index keys too."""
+    _need(kv_c, torch.bfloat16, "kv_c")
+    _need(k_pe, torch.bfloat16, "k_pe")
+    _need(pos, torch.int32, "pos")
+    _need(slot, torch.int64, "slot")
+    _need(kv_cache, torch.uint8, "kv_cache")
+    if idx_k is not None:
+        _need(idx_k, torch.bfloat16, "idx_k")
+        _need(idxk_cache, torch.uint8, "idxk_cache")
+    if num_pages is None:
+        num_pages = kv_cache.numel() // KV_PAGE_BYTES
+    if idx_num_pages is None:
+        idx_num_pages = 0 if idxk_cache is None else idxk_cache.numel() // IDXK_PAGE_BYTES
+    _check("dsa_latent_kv_store_fused", lib().dsa_latent_kv_store_fused(
+        _ptr(kv_c), _ptr(k_pe), _ptr(pos), _ptr(slot), kv_c.shape[0], _ptr(kv_gamma), rms_eps, rope_base,
+        _ptr(kv_cache), num_pages, _ptr(idx_k), _ptr(idx_gamma), _ptr(idx_beta), ln_eps, _ptr(idxk_cache),
+        idx_num_pages, _ptr(dev_status), _stream(stream)))
 
 
 def dsa_latent_kv_store(c, rope, slot, kv_cache, *, num_pages=None, dev_status=None, stream=None):

@@ -42,22 +42,11 @@ __device__ __forceinline__ uint32_t e2m1_code(float y) {
 // exponent is floor(log2(amax)) - 2 (OCP MX, E2M1's largest value is 1.5 * 2^2),
 // clamped to [-127, 127]; each lane writes its 4 codes as 2 packed bytes.
 template <bool kMx>
-__global__ void __launch_bounds__(256)
-index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__ pos,
-                     const int64_t* __restrict__ slot, int64_t n,
-                     const float* __restrict__ gamma, const float* __restrict__ beta,
-                     float eps, RopeFreqs fr, uint8_t* __restrict__ cache,
-                     int64_t num_pages, int32_t* __restrict__ st) {
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= n) return;
-    const int64_t s = slot[t];
-    if (s < 0) return;                                   // padded row: K write skipped
-    if (s >= num_pages * kPage) {
-        if (lane == 0) record_error(st, DSA_DEVERR_SLOT_RANGE, s);
-        return;
-    }
-    const uint2 raw = *reinterpret_cast<const uint2*>(k + t * 128 + lane * 4);
+__device__ __forceinline__ void store_index_key(const uint16_t* __restrict__ krow, int32_t tpos, int64_t s,
+                                                const float* __restrict__ gamma, const float* __restrict__ beta,
+                                                float eps, const RopeFreqs& fr, uint8_t* __restrict__ cache,
+                                                int lane) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(krow + lane * 4);
     float x[4] = {bf16_bits_to_f32(raw.x & 0xffffu), bf16_bits_to_f32(raw.x >> 16),
                   bf16_bits_to_f32(raw.y & 0xffffu), bf16_bits_to_f32(raw.y >> 16)};
     // LayerNorm over 128 dims, biased variance, fp32.
@@ -79,7 +68,7 @@ index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__
     // fp64 (at positions near 2^20 an fp32 angle would be off by ~0.1 rad);
     // the reduced angle, |r| <= pi, goes through fp32 sincos.
     if (lane < 16) {
-        const double p = (double)pos[t];
+        const double p = (double)tpos;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int i = 2 * lane + h;
@@ -117,6 +106,98 @@ index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__
     uint8_t* pg = cache + page * (int64_t)kIdxPageBytes;
     *reinterpret_cast<uint32_t*>(pg + row * 128 + lane * 4) = lo | (hi << 16);
     if (lane == 0) *reinterpret_cast<float*>(pg + kIdxPayloadBytes + row * 4) = ldexpf(1.0f, e);
+}
+
+template <bool kMx>
+__global__ void __launch_bounds__(256)
+index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__ pos,
+                     const int64_t* __restrict__ slot, int64_t n,
+                     const float* __restrict__ gamma, const float* __restrict__ beta,
+                     float eps, RopeFreqs fr, uint8_t* __restrict__ cache,
+                     int64_t num_pages, int32_t* __restrict__ st) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= n) return;
+    const int64_t s = slot[t];
+    if (s < 0) return;                                   // padded row: K write skipped
+    if (s >= num_pages * kPage) {
+        if (lane == 0) record_error(st, DSA_DEVERR_SLOT_RANGE, s);
+        return;
+    }
+    store_index_key<kMx>(k + t * 128, pos[t], s, gamma, beta, eps, fr, cache, lane);
+}
+
+// The latent row from the A-projection outputs, in one pass ("GLM-5.3 推理全链路
+// (一)", 4.3 两个 RMSNorm 与 RoPE: kv_a_layernorm over kv_c, RoPE on k_pe, the
+// result written into the KV pool, and on a layer with an indexer the index key
+// into the index cache as well).  One warp per token: lane l owns latent dims
+// [16l, 16l+16) (block l/8) and the RoPE pair (2l, 2l+1).
+__global__ void __launch_bounds__(256)
+latent_store_fused_kernel(const uint16_t* __restrict__ kv_c, const uint16_t* __restrict__ k_pe,
+                          const int32_t* __restrict__ pos, const int64_t* __restrict__ slot, int64_t n,
+                          const float* __restrict__ kv_gamma, float rms_eps, RopeFreqs fr,
+                          uint8_t* __restrict__ kv_cache, int64_t num_pages,
+                          const uint16_t* __restrict__ idx_k, const float* __restrict__ idx_gamma,
+                          const float* __restrict__ idx_beta, float ln_eps, uint8_t* __restrict__ idxk_cache,
+                          int64_t idx_num_pages, int32_t* __restrict__ st) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= n) return;
+    const int64_t s = slot[t];
+    if (s < 0) return;
+    if (s < num_pages * kPage) {
+        const uint4* src = reinterpret_cast<const uint4*>(kv_c + t * 512 + lane * 16);
+        const uint4 r0 = src[0], r1 = src[1];
+        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        float x[16];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            x[2 * i] = bf16_bits_to_f32(w[i] & 0xffffu);
+            x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+            ss = fmaf(x[2 * i], x[2 * i], ss);
+            ss = fmaf(x[2 * i + 1], x[2 * i + 1], ss);
+        }
+        const float inv = 1.0f / sqrtf(warp_sum(ss) * (1.0f / 512.0f) + rms_eps);   // RMSNorm, fp32
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            x[i] *= inv;
+            if (kv_gamma) x[i] *= kv_gamma[lane * 16 + i];
+            amax = fmaxf(amax, fabsf(x[i]));
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const int e = ue8m0_exponent(amax);
+        uint32_t q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t a = f32x2_to_e4m3x2(ldexpf(x[4 * i], -e), ldexpf(x[4 * i + 1], -e));
+            const uint32_t b = f32x2_to_e4m3x2(ldexpf(x[4 * i + 2], -e), ldexpf(x[4 * i + 3], -e));
+            q[i] = a | (b << 16);
+        }
+        // RoPE pair (2l, 2l+1) of k_pe: angle reduced in fp64 as for the index key
+        const uint32_t pr = reinterpret_cast<const uint32_t*>(k_pe + t * 64)[lane];
+        const float a = bf16_bits_to_f32(pr & 0xffffu), b = bf16_bits_to_f32(pr >> 16);
+        const double ang = (double)pos[t] * fr.theta[lane];
+        const double red = fma(-6.283185307179586, rint(ang * 0.15915494309189535), ang);
+        float si, co;
+        sincosf((float)red, &si, &co);
+        const __nv_bfloat16 ra = __float2bfloat16_rn(a * co - b * si), rb = __float2bfloat16_rn(a * si + b * co);
+        const uint32_t rp = (uint32_t)__bfloat16_as_ushort(ra) | ((uint32_t)__bfloat16_as_ushort(rb) << 16);
+        uint8_t* row = kv_cache + (s / kPage) * (int64_t)kKvPageBytes + (s % kPage) * kKvTokenBytes;
+        *reinterpret_cast<uint4*>(row + lane * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+        if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 512 + (lane >> 3) * 4) = ldexpf(1.0f, e);
+        *reinterpret_cast<uint32_t*>(row + 528 + lane * 4) = rp;
+    } else if (lane == 0) {
+        record_error(st, DSA_DEVERR_SLOT_RANGE, s);
+    }
+    if (idx_k) {
+        if (s < idx_num_pages * kPage)
+            store_index_key<false>(idx_k + t * 128, pos[t], s, idx_gamma, idx_beta, ln_eps, fr, idxk_cache, lane);
+        else if (lane == 0)
+            record_error(st, DSA_DEVERR_SLOT_RANGE, s);
+    }
 }
 
 // One warp per token; lane l owns latent dims [16l, 16l+16) (block l/8) and,
@@ -205,6 +286,32 @@ extern "C" dsa_status dsa_index_k_store_mxfp4(const void* k, const int32_t* pos,
     index_k_store_kernel<true><<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
         static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, fr,
         idxk_cache, num_pages, dev_status);
+    DSA_CHECK_LAUNCH();
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_latent_kv_store_fused(const void* kv_c, const void* k_pe, const int32_t* pos,
+                                                const int64_t* slot, int64_t n, const float* kv_gamma,
+                                                float rms_eps, float rope_base, uint8_t* kv_cache, int64_t num_pages,
+                                                const void* idx_k, const float* idx_gamma, const float* idx_beta,
+                                                float ln_eps, uint8_t* idxk_cache, int64_t idx_num_pages,
+                                                int32_t* dev_status, void* stream) {
+    if (n < 0 || num_pages < 0 || idx_num_pages < 0) return DSA_ERR_INVALID_ARGUMENT;
+    if (n == 0) return DSA_OK;
+    if (!kv_c || !k_pe || !pos || !slot || !kv_cache) return DSA_ERR_INVALID_ARGUMENT;
+    if (idx_k && !idxk_cache) return DSA_ERR_INVALID_ARGUMENT;
+    if (!(rms_eps >= 0.f) || !(ln_eps >= 0.f) || !(rope_base > 0.f)) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(kv_c) || (reinterpret_cast<uintptr_t>(k_pe) & 3) || !aligned16(kv_cache)) return DSA_ERR_ALIGNMENT;
+    if (idx_k && (!aligned16(idx_k) || !aligned16(idxk_cache))) return DSA_ERR_ALIGNMENT;
+    const int warps = 8;
+    const int64_t blocks = (n + warps - 1) / warps;
+    if (blocks > 0x7fffffff) return DSA_ERR_UNSUPPORTED;
+    RopeFreqs fr;
+    for (int i = 0; i < 32; ++i) fr.theta[i] = std::pow((double)rope_base, -2.0 * (double)i / 64.0);
+    latent_store_fused_kernel<<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
+        static_cast<const uint16_t*>(kv_c), static_cast<const uint16_t*>(k_pe), pos, slot, n, kv_gamma, rms_eps,
+        fr, kv_cache, num_pages, static_cast<const uint16_t*>(idx_k), idx_gamma, idx_beta, ln_eps, idxk_cache,
+        idx_num_pages, dev_status);
     DSA_CHECK_LAUNCH();
     return DSA_OK;
 }

@@ -165,6 +165,28 @@ dsa_status dsa_latent_kv_store(const void* c, const void* rope, const int64_t* s
                                uint8_t* kv_cache, int64_t num_pages,
                                int32_t* dev_status, void* stream);
 
+/* ---- Latent store from the A-projection outputs ("GLM-5.3 推理全链路(一)", 4.3
+ *      两个 RMSNorm 与 RoPE: the fused norm/RoPE kernel writes the KV pool and, on a
+ *      layer with an indexer, the index cache) ----------------------------------
+ * For each token: kv_c (512) -> RMSNorm x / sqrt(mean(x^2) + rms_eps), times
+ * kv_gamma if given, fp32 -> the latent row of dsa_latent_kv_store (four FP8
+ * blocks with their scales); k_pe (64) -> interleaved RoPE (pairs (2i, 2i+1)
+ * rotated by pos * rope_base^(-2i/64)) -> bf16 (round to nearest even).
+ * idx_k != NULL also stores the index key of each token exactly as
+ * dsa_index_k_store does (LayerNorm idx_gamma/idx_beta/ln_eps, same RoPE) into
+ * idxk_cache at the same slot; idx_k == NULL (a shared layer) writes no key.
+ *   kv_c device bf16 [n,512], 16-byte aligned; k_pe device bf16 [n,64], 4-byte aligned
+ *   pos  device int32 [n]; slot device int64 [n] (< 0 skips the token)
+ *   kv_cache device uint8 [num_pages * 41984]; idx_k bf16 [n,128] or NULL;
+ *   idxk_cache device uint8 [idx_num_pages * 8448] (when idx_k != NULL)
+ * A slot beyond either cache is skipped and recorded (DSA_DEVERR_SLOT_RANGE). */
+dsa_status dsa_latent_kv_store_fused(const void* kv_c, const void* k_pe, const int32_t* pos, const int64_t* slot,
+                                     int64_t n, const float* kv_gamma, float rms_eps, float rope_base,
+                                     uint8_t* kv_cache, int64_t num_pages,
+                                     const void* idx_k, const float* idx_gamma, const float* idx_beta, float ln_eps,
+                                     uint8_t* idxk_cache, int64_t idx_num_pages,
+                                     int32_t* dev_status, void* stream);
+
 /* ---- Indexer + top-2048 ("vLLM 推理链路概览", DSA Indexer; "GLM-5.3 推理全链路(十一)",
  *      优化二: 短上下文直接跳过打分) ------------------------------------------------
  * For every query row i (request r, position p): the query is quantised to

@@ -478,3 +478,50 @@ def test_sparse_mla_records_bad_page_without_fault(mla_case):
     res = D.dsa_device_status_read(st)
     assert res[0] & D.DEVERR_PAGE_RANGE and res[2] == -7
     assert torch.isfinite(out).all()
+
+
+# ------------------------------------------------------------------ fused latent store
+@pytest.mark.parametrize("with_index", [False, True])
+def test_latent_store_fused_matches_oracle(with_index):
+    g = _gen(61)
+    n, num_pages = 1500, 30
+    kv = (torch.randn(n, 512, generator=g) * torch.exp2(torch.randint(-4, 5, (n, 1), generator=g).float())
+          ).to(torch.bfloat16)
+    pe = torch.randn(n, 64, generator=g).to(torch.bfloat16)
+    pos = torch.randint(0, 1 << 20, (n,), generator=g, dtype=torch.int32)
+    slots = torch.randperm(num_pages * 64, generator=g)[:n].to(torch.int64)
+    slots[::37] = -1
+    gam = torch.rand(512, generator=g) + 0.5
+    idx_k = torch.randn(n, 128, generator=g).to(torch.bfloat16) if with_index else None
+    kvc = torch.zeros(num_pages * O.LATENT_PAGE_BYTES, dtype=torch.uint8, device=DEV)
+    ikc = torch.zeros(num_pages * O.INDEX_PAGE_BYTES, dtype=torch.uint8, device=DEV) if with_index else None
+    st = D.new_device_status(DEV)
+    D.dsa_latent_kv_store_fused(kv.to(DEV), pe.to(DEV), pos.to(DEV), slots.to(DEV), kvc, kv_gamma=gam.to(DEV),
+                                idx_k=None if idx_k is None else idx_k.to(DEV), idxk_cache=ikc, dev_status=st)
+    assert D.dsa_device_status_read(st)[0] == 0
+    codes, scales, rbits = O.latent_prepare(f64(kv), f64(pe), pos.numpy(), f64(gam))
+    s = slots.numpy()
+    keep = s >= 0
+    cache = kvc.cpu().numpy().reshape(num_pages, O.LATENT_PAGE_BYTES)
+    page, row = np.divmod(s[keep], 64)
+    rows = cache[page[:, None], row[:, None] * 656 + np.arange(656)]
+    gcodes = rows[:, :512]
+    gsc = np.ascontiguousarray(rows[:, 512:528]).view("<f4").astype(np.float64)
+    grope = O.bf16_bits_to_f64(np.ascontiguousarray(rows[:, 528:656]).view("<u2"))
+    # latent: scales equal except at power-of-two amax, values within one FP8 ulp
+    smis = gsc != scales[keep]
+    assert smis.mean() < 2e-3
+    gd = O.e4m3_decode(gcodes).reshape(-1, 4, 128) * gsc[..., None]
+    od = O.e4m3_decode(codes[keep]).reshape(-1, 4, 128) * scales[keep][..., None]
+    ulp = np.maximum(O.e4m3_ulp(od / scales[keep][..., None]) * scales[keep][..., None],
+                     O.e4m3_ulp(gd / gsc[..., None]) * gsc[..., None])
+    assert np.all(np.abs(gd - od) <= ulp * (1 + 1e-12))
+    # RoPE dims: within one bf16 ulp of the oracle's nearest bf16
+    orope = O.bf16_bits_to_f64(rbits[keep])
+    bulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(orope), 1e-30))) - 7)
+    assert np.all(np.abs(grope - orope) <= bulp * (1 + 1e-9))
+    assert (grope != orope).mean() < 2e-2
+    if with_index:                                      # the same bytes as the plain index-K store
+        ref = torch.zeros_like(ikc)
+        D.dsa_index_k_store(idx_k.to(DEV), pos.to(DEV), slots.to(DEV), ref)
+        assert torch.equal(ikc, ref)
