@@ -96,3 +96,84 @@ def test_full_size_sampled_rows(name):
             rows = O.latent_cache_read_rows(kv_pages, kident, valid)
             ref, _ = O.sparse_mla(f64(gw.q_mla[l][i]), valid, rows, p)
             check_attention(outs[l][i].float().cpu().numpy(), round_bf16(ref), what=f"{name} layer {l} row {i}")
+
+
+def test_full_size_mxfp4_decode1m_sampled_row():
+    """decode1m over an MXFP4 index-K cache: one sampled row rescored by the oracle
+    at all 1,048,576 positions, from the MXFP4 pages the GPU wrote."""
+    from synth.gpu import GpuWorkload
+    w = synth.workload("decode1m")
+    w.index_format = "mxfp4"
+    gw = GpuWorkload(w, "cuda", layers=[])
+    st = D.new_device_status("cuda")
+    T = w.total_q
+    sel = torch.empty((T, D.TOPK), dtype=torch.float32, device="cuda")
+    topk = D.dsa_indexer_topk_mxfp4(gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch, topk_scores=sel, dev_status=st)
+    torch.cuda.synchronize()
+    assert D.dsa_device_status_read(st)[0] == 0
+    i = 1
+    n = int(gw.seq_len[i])
+    pages, ident = _pages(gw.idx_cache, gw.pt[i], n, D.IDXK_MXFP4_PAGE_BYTES)
+    qc, qs = O.index_q_quantize(f64(gw.q_idx[i]))
+    kc, ke = O.mxfp4_cache_read(pages, ident, n)
+    wt = f64(gw.w_idx[i])
+    s = np.empty(n)
+    m = np.empty(n)
+    for a in range(0, n, CHUNK):
+        b = min(n, a + CHUNK)
+        s[a:b] = O.indexer_scores_mxfp4(qc, qs, wt, kc[a:b], ke[a:b])
+        m[a:b] = O.score_magnitude_mxfp4(qc, qs, wt, kc[a:b], ke[a:b])
+    row = topk[i].cpu().numpy()
+    check_topk_row(row, O.topk_positions(s, n), s, m, n, what="mxfp4 decode1m")
+    check_scores(sel[i].cpu().numpy(), s[row], m[row], what="mxfp4 decode1m selected")
+
+
+def test_full_size_mtp_iteration_sampled_request():
+    """One MTP iteration at full size (4 requests, 5 draft steps from a
+    1,048,576-token context): the first step's top-2048 against the oracle, the
+    later steps carrying that row bit for bit, every step's attention against the
+    oracle from the GPU-written latent rows."""
+    from synth.gpu import GpuWorkload
+    w = synth.workload("mtp5_1m")
+    gw = GpuWorkload(w, "cuda", layers=[0])
+    nd, B = w.draft_steps, w.batch
+    st = D.new_device_status("cuda")
+
+    def rows(t, k):
+        return t.view(B, nd, *t.shape[1:])[:, k].contiguous()
+
+    q0 = torch.arange(B + 1, dtype=torch.int32, device="cuda")
+    share = D.TopkShare()
+    topk = torch.empty((B, D.TOPK), dtype=torch.int32, device="cuda")
+    sel = torch.empty((B, D.TOPK), dtype=torch.float32, device="cuda")
+    outs, carried, scored = [], [], []
+    with share.mtp_iteration(True, 1) as reuse:
+        assert reuse
+        for k in range(nd):
+            seq = (gw.seq_len - (nd - 1 - k)).contiguous()
+            bk = D.Batch(seq, q0, gw.pt, w.num_pages, max_seq_len=w.max_seq_len - (nd - 1 - k), max_q_len=1, total_q=B)
+            scored.append(share.needs_scoring())
+            if scored[-1]:
+                D.dsa_indexer_topk(rows(gw.q_idx, k), rows(gw.w_idx, k), gw.idx_cache, bk, topk=topk, topk_scores=sel,
+                                   share=share, layer_id=0, dev_status=st)
+            carried.append(topk.clone())
+            outs.append(D.dsa_sparse_mla_decode(rows(gw.q_mla[0], k), None, gw.kv_cache[0], bk, share=share,
+                                                dev_status=st))
+    torch.cuda.synchronize()
+    assert D.dsa_device_status_read(st)[0] == 0
+    assert scored == [True] + [False] * (nd - 1)
+    assert all(torch.equal(c, carried[0]) for c in carried)
+    r = 2
+    L0 = int(gw.seq_len[r]) - (nd - 1)                   # the first draft step's context
+    i0 = r * nd                                          # request r's first draft row in the workload's rows
+    idx_pages, ident = _pages(gw.idx_cache, gw.pt[r], L0, D.IDXK_PAGE_BYTES)
+    s, mag = _oracle_row_scores(idx_pages, ident, f64(gw.q_idx[i0]), f64(gw.w_idx[i0]), L0)
+    row = carried[0][r].cpu().numpy()
+    check_topk_row(row, O.topk_positions(s, L0), s, mag, L0, what="mtp step 0")
+    check_scores(sel[r].cpu().numpy(), s[row], mag[row], what="mtp step 0 selected")
+    valid = row[row >= 0]
+    kv_pages, kident = _pages(gw.kv_cache[0], gw.pt[r], L0 + nd - 1, D.KV_PAGE_BYTES)
+    lat = O.latent_cache_read_rows(kv_pages, kident, valid)
+    for k in range(nd):
+        ref, _ = O.sparse_mla(f64(gw.q_mla[0][i0 + k]), valid, lat, L0 - 1 + k)
+        check_attention(outs[k][r].float().cpu().numpy(), round_bf16(ref), what=f"mtp step {k}")
