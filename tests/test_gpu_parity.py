@@ -223,7 +223,8 @@ def indexer_case():
 
 
 # Decode batches (one query row per request) take the fused tensor-core path.
-DECODE_SEQ = [2049, 1, 100, 2048, 4097, 6000, 2100, 33000, 10000, 70000, 128 * 40, 128 * 40 + 1, 8191]
+DECODE_SEQ = [2049, 1, 100, 2048, 4097, 6000, 2100, 33000, 10000, 70000, 128 * 40, 128 * 40 + 1, 8191,
+              300000]                                   # past 2^18 positions: ranked by a sort, not a bitmap
 
 
 @pytest.fixture(scope="module")
@@ -525,3 +526,40 @@ def test_latent_store_fused_matches_oracle(with_index):
         ref = torch.zeros_like(ikc)
         D.dsa_index_k_store(idx_k.to(DEV), pos.to(DEV), slots.to(DEV), ref)
         assert torch.equal(ikc, ref)
+
+
+
+def test_indexer_topk_decode_all_keys_equal():
+    """Rows whose every cached key is the same stored bytes: every score ties, so
+    the top-2048 is positions 0..2047 exactly.  The boundary bin then holds far
+    more than 2048 candidates (the radix selection, in shared memory and in
+    place)."""
+    seq = [3000, 20000, 2049]
+    w = _small_workload(seq, [1] * len(seq), 4444)
+    g = _gen(4444)
+    pt = page_table(w, "cpu")
+    meta = batch_meta(w, "cpu")
+    one_codes, one_scales = O.index_k_prepare(f64(torch.randn(1, 128, generator=g).to(torch.bfloat16)), np.array([5]))
+    cache = np.zeros((w.num_pages, O.INDEX_PAGE_BYTES), np.uint8)
+    for r, L in enumerate(seq):
+        p = np.arange(L)
+        O.index_cache_write(cache, pt[r, p // 64].numpy().astype(np.int64) * 64 + p % 64,
+                            np.repeat(one_codes, L, axis=0), np.repeat(one_scales, L))
+    q = torch.randn(len(seq), 32, 128, generator=g).to(torch.bfloat16)
+    wt = torch.randn(len(seq), 32, generator=g).abs() / math.sqrt(32)
+    batch = D.Batch(meta["seq_len"].to(DEV), meta["q_start"].to(DEV), pt.to(DEV), w.num_pages,
+                    max_seq_len=w.max_seq_len, max_q_len=1, total_q=len(seq))
+    sc = torch.empty(len(seq), 2048, device=DEV)
+    st = D.new_device_status(DEV)
+    topk = D.dsa_indexer_topk(q.to(DEV), wt.to(DEV), torch.from_numpy(cache.reshape(-1)).to(DEV), batch,
+                              topk_scores=sc, dev_status=st)
+    assert D.dsa_device_status_read(st)[0] == 0
+    topk, sc = topk.cpu().numpy(), sc.cpu().numpy()
+    for r, L in enumerate(seq):
+        assert topk[r].tolist() == list(range(2048)), f"row {r}"
+        kc, ks = O.index_cache_read(cache, pt[r].numpy(), 1)
+        qc, qs = O.index_q_quantize(f64(q[r]))
+        s1 = O.indexer_scores(qc, qs, f64(wt[r]), kc, ks)[0]
+        m1 = O.score_magnitude(qc, qs, f64(wt[r]), kc, ks)[0]
+        check_scores(sc[r], np.full(2048, s1), np.full(2048, m1), what=f"row {r} scores")
+        assert np.all(sc[r] == sc[r][0])
