@@ -75,7 +75,7 @@ typedef int32_t dsa_status;
 #define DSA_OK                       0
 #define DSA_ERR_INVALID_ARGUMENT     1  /* null pointer, negative size, bad enum    */
 #define DSA_ERR_ALIGNMENT            2  /* a buffer is not 16-byte aligned          */
-#define DSA_ERR_UNSUPPORTED          3  /* a shape this build does not support      */
+#define DSA_ERR_UNSUPPORTED          3  /* a shape the library does not support     */
 #define DSA_ERR_WORKSPACE_TOO_SMALL  4
 #define DSA_ERR_NO_TOPK_SOURCE       5  /* shared layer with no full layer published*/
 #define DSA_ERR_CUDA                 6  /* a CUDA runtime call failed               */
