@@ -52,6 +52,7 @@ def _oracle_row_scores(idx_pages, ident, q, wt, n):
 
 CASES = {
     # workload: sampled rows (indices into the batch's query rows)
+    "tiny": [0],
     "decode32k": [0, 17, 63],
     "decode1m": [2],
     "verify64k": [0, 5, 6 * 77 + 3, 767],
