@@ -45,8 +45,8 @@ L2_BYTES = 129 * 1024 * 1024
 NCU_TRAFFIC = {
     ("decode32k", "sparse_mla_decode"): (106.3e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
                                          "23817a9df5e77b45"),
-    ("decode1m", "indexer_topk"): (568.7e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
-                                   "07e315fe036f3c3e"),
+    ("decode1m", "indexer_topk"): (568.8e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
+                                   "b13161fe2df31798"),
 }
 FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s)
 

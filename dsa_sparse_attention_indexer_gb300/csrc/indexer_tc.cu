@@ -43,14 +43,14 @@ namespace itc {
 
 using namespace sm100;
 
-constexpr int kStages = 8;
+constexpr int kStages = 9;
 constexpr int kAcc = 16;                        // TMEM accumulators (32 columns each) in flight
 constexpr int kSSlots = 16;                     // key-scale slots (512 B each), released by the epilogue
 constexpr int kStageBytes = 16384;              // 2 x 8192 FP8 payload (two 64-token pages)
 constexpr int kPidChunk = 64;                   // tiles whose page ids a producer fetches at once
 constexpr int kCheckEvery = 4;                  // tiles between epilogue-wide checks
 constexpr int kMinTiles = 16;                   // smallest per-CTA share of tiles
-constexpr int kCap = 5632;                      // candidate buffer entries
+constexpr int kCap = 4608;                      // candidate buffer entries
 constexpr int kSegCand = kCap;                  // candidate slots of one segment in the workspace
 constexpr int kEpiThreads = 256;                // two epilogue groups of 4 warps, alternating tiles
 constexpr int kThreads = 96 + kEpiThreads;      // + two producer warps + MMA warp
@@ -69,8 +69,9 @@ constexpr int kOffScales = kOffStages + kStages * kStageBytes;   // kSSlots x 51
 constexpr int kOffB = (kOffScales + kSSlots * 512 + 1023) / 1024 * 1024;   // quantised query, 2 x 4 KB
 constexpr int kOffCbKey = kOffB + 2 * 4096;                      // candidate keys
 constexpr int kOffCbPos = kOffCbKey + kCap * 4;                  // candidate positions
-constexpr int kOffHist = kOffCbPos + kCap * 4;                   // top-12-bit histogram of the candidates
-constexpr int kOffHist2 = kOffHist + 4096 * 4;                   // compaction scratch histogram
+constexpr int kOffHist = kOffCbPos + kCap * 4;                   // top-12-bit histogram of the candidates,
+                                                                 // 16-bit counts, two bins per word
+constexpr int kOffHist2 = kOffHist + 4096 * 2;                   // compaction scratch histogram
 constexpr int kOffSideKey = kOffHist2;                           // survivors (reuse the scratch histogram)
 constexpr int kOffSidePos = kOffSideKey + kTopK * 4;
 constexpr int kOffBars = kOffHist2 + 4096 * 4;
@@ -90,11 +91,12 @@ struct Misc {
     sel::Found found;
     int32_t scratch[32];
     int32_t wtot[8];
+    int64_t plast[2];                           // last tile each producer warp issued (-1: none)
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
 static_assert(kAcc % 2 == 0 && kTmemCols <= 512, "accumulators alternate between two epilogue groups");
 static_assert(kSSlots >= kStages, "scale ring at least as deep as the payload ring");
-static_assert(kStages % 2 == 0 && kSSlots % 2 == 0, "each producer warp owns the stages and slots of its parity");
+static_assert(kCap < 65536, "16-bit histogram counts");
 static_assert(kCap % kEpiThreads == 0 && kCap / kEpiThreads <= 32, "per-thread candidate slice");
 
 __device__ __forceinline__ int64_t cta_start(int64_t g, int64_t N, int64_t G) { return g * N / G; }
@@ -187,19 +189,34 @@ __device__ __forceinline__ bool epi_any(bool pred) {
 
 // Crossing bin of a 4096-bin histogram read from the top: count(bins > b) <
 // k <= count(bins >= b).  Thread et owns the 16 bins 4095-16et .. 4080-16et
-// (four 16-byte loads); the prefix over threads is a warp scan plus one
-// exchange of warp totals.
+// (four 16-byte loads of 32-bit counts, or two of 16-bit counts packed two to
+// a word, bin b in half b & 1 of word b >> 1); the prefix over threads is a
+// warp scan plus one exchange of warp totals.
+template <bool kU16>
 __device__ __forceinline__ void crossing_bin_4096(const uint32_t* h, int k, int et, Misc* misc) {
     const int lane = et & 31, wid = et >> 5;
     const uint4* h4 = reinterpret_cast<const uint4*>(h);
     uint32_t c[16];
+    if constexpr (kU16) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint4 v = h4[1023 - (et * 4 + q)];          // bins 4095-16et-4q-3 .. 4095-16et-4q
-        c[4 * q + 0] = v.w;
-        c[4 * q + 1] = v.z;
-        c[4 * q + 2] = v.y;
-        c[4 * q + 3] = v.x;
+        for (int q = 0; q < 2; ++q) {
+            const uint4 v = h4[511 - (et * 2 + q)];       // bins 4095-16et-8q-7 .. 4095-16et-8q
+            const uint32_t wv[4] = {v.w, v.z, v.y, v.x};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                c[8 * q + 2 * e] = wv[e] >> 16;
+                c[8 * q + 2 * e + 1] = wv[e] & 0xffffu;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = h4[1023 - (et * 4 + q)];      // bins 4095-16et-4q-3 .. 4095-16et-4q
+            c[4 * q + 0] = v.w;
+            c[4 * q + 1] = v.z;
+            c[4 * q + 2] = v.y;
+            c[4 * q + 3] = v.x;
+        }
     }
     int mine = 0;
 #pragma unroll
@@ -248,7 +265,7 @@ __device__ __forceinline__ void crossing_bin_256(const uint32_t* h, int k, int e
 
 // Keep the exact top-2048 (key desc, position asc) of the candidate buffer.
 // hist holds the top-12-bit histogram of the buffer on entry and of the
-// survivors on exit.  Called by all epilogue threads with cb_count > 2048.
+// survivors on exit (16-bit counts, two bins per word).  Called by all epilogue threads with cb_count > 2048.
 // The survivors' order in the buffer is not preserved (it does not matter:
 // ties are resolved by position values and the merge sorts by position).
 __device__ void compact_candidates(uint32_t* cb_key, int32_t* cb_pos, uint32_t* hist, uint32_t* hist2,
@@ -256,7 +273,7 @@ __device__ void compact_candidates(uint32_t* cb_key, int32_t* cb_pos, uint32_t* 
     constexpr int NT = kEpiThreads;
     const int n = misc->cb_count;
     constexpr int kPer = kCap / NT;                // entries per thread (strided by NT)
-    crossing_bin_4096(hist, kTopK, et, misc);
+    crossing_bin_4096<true>(hist, kTopK, et, misc);
     const uint32_t b1 = misc->found.bin;
     const int above1 = misc->found.above;            // candidates in bins above b1: all survive
     int krem = kTopK - above1;
@@ -269,7 +286,7 @@ __device__ void compact_candidates(uint32_t* cb_key, int32_t* cb_pos, uint32_t* 
     for (int u = 0; u < kPer; ++u)                   // second digit among bin b1
         if (et + u * NT < n && (k[u] >> 20) == b1) atomicAdd(&hist2[(k[u] >> 8) & 0xfffu], 1u);
     epi_sync();
-    crossing_bin_4096(hist2, krem, et, misc);
+    crossing_bin_4096<false>(hist2, krem, et, misc);
     const uint32_t b2 = misc->found.bin;
     krem -= misc->found.above;
     epi_sync();
@@ -329,9 +346,10 @@ __device__ void compact_candidates(uint32_t* cb_key, int32_t* cb_pos, uint32_t* 
         }
     }
     // survivors' histogram: bins above b1 keep their counts, b1 keeps the rest
+    uint16_t* h16 = reinterpret_cast<uint16_t*>(hist);
     for (int i = et; i < 4096; i += NT) {
-        if ((uint32_t)i < b1) hist[i] = 0u;
-        else if ((uint32_t)i == b1) hist[i] = (uint32_t)(kTopK - above1);
+        if ((uint32_t)i < b1) h16[i] = 0u;
+        else if ((uint32_t)i == b1) h16[i] = (uint16_t)(kTopK - above1);
     }
     epi_sync();
     total = min(total, kTopK);
@@ -424,10 +442,13 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
         // Two producer warps take alternate tiles of the CTA's running tile
         // index (one thread issuing every copy of an SM falls well short of
         // the HBM rate; two reach it).  Tile i uses stage i % kStages and
-        // scale slot i % kSSlots, both even counts, so each warp owns the
-        // stages and slots of its parity.  A warp fetches the page ids of up
-        // to kPidChunk tiles at once into its own buffer; its lane 0 then
-        // issues the copies of its tiles without waiting on global loads.
+        // scale slot i % kSSlots; with an odd stage count the warps share the
+        // stage ring, which is safe because tile i waits for the consumption
+        // of tile i - kStages (and the warp's own previous tile already
+        // waited for that of tile i - kStages - 2, so the parity cannot alias).
+        // A warp fetches the page ids of up to kPidChunk tiles at once into
+        // its own buffer; its lane 0 then issues the copies of its tiles
+        // without waiting on global loads.
         const int me = warp == 0 ? 0 : 1;
         int64_t* mypid = pid + me * kPidChunk * 2;
         int64_t icount = 0;                                // running tile index (lane 0)
@@ -495,15 +516,8 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
         if (lane == 0 && stop) {
             if (!*abort_flag) record_error(st, DSA_DEVERR_TIMEOUT, 1);
             *abort_flag = 1;
-            // let this warp's copies land before the CTA winds down: the payloads
-            // of its tiles among the last kStages, the scales among the last
-            // kSSlots (older ones were consumed before their stage or slot was
-            // refilled)
-            for (int64_t j = last; j >= 0 && j > last - kSSlots; j -= 2) {
-                if (j > last - kSt) mbar_wait(&full[j % kSt], (uint32_t)((j / kSt) & 1), 500000000ull);
-                mbar_wait(&sfull[j % kSSlots], (uint32_t)((j / kSSlots) & 1), 500000000ull);
-            }
         }
+        if (lane == 0) misc->plast[me] = last;          // for the drain after an abort, below
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -610,7 +624,7 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                 misc->cb_count = 0;
                 misc->theta = 0u;
             }
-            for (int i = et; i < 4096; i += kEpiThreads) hist[i] = 0u;
+            for (int i = et; i < 2048; i += kEpiThreads) hist[i] = 0u;
             epi_sync();
             bool aborted = false;
             bool warp_bad = false;                     // this warp saw a timeout
@@ -702,7 +716,7 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                                 const int idx = base + __popc(m & ((1u << lane) - 1u));
                                 cb_key[idx] = key;
                                 cb_pos[idx] = pos;
-                                atomicAdd(&hist[key >> 20], 1u);
+                                atomicAdd(&hist[key >> 21], 1u << ((key >> 16) & 16u));   // bin key >> 20, 16-bit half
                             }
                         }
                     } else {
@@ -733,8 +747,9 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
             }
             if (et == 0) p.cand_cnt[s] = cnt;
             uint32_t* gh = p.hist + row * 4096;
+            const uint16_t* h16 = reinterpret_cast<const uint16_t*>(hist);
             for (int i = et; i < 4096; i += kEpiThreads)
-                if (hist[i]) atomicAdd(&gh[i], hist[i]);
+                if (h16[i]) atomicAdd(&gh[i], (uint32_t)h16[i]);
             epi_sync();
         }
     }
@@ -742,6 +757,29 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 0 && *abort_flag) {
+        // After an abort, let every copy in flight land before the CTA ends.  A
+        // stage or scale slot is refilled only after its previous tile was
+        // consumed, so the one copy into it that may still be in flight is that
+        // of the latest tile issued to it by either warp: wait for exactly that
+        // tile's phase (an older tile's parity can alias a newer one's when the
+        // two warps share the ring).  Warp w issued every tile of parity w up
+        // to plast[w].
+        for (int ring = 0; ring < 2; ++ring) {
+            const int n = ring == 0 ? kSt : kSSlots;
+            uint64_t* bar = ring == 0 ? full : sfull;
+            for (int x = 0; x < n; ++x) {
+                int64_t jl = -1;
+                for (int w = 0; w < 2; ++w)
+                    for (int64_t j = misc->plast[w]; j >= 0 && j > misc->plast[w] - 2 * n; j -= 2)
+                        if (j % n == x) {
+                            jl = j > jl ? j : jl;
+                            break;
+                        }
+                if (jl >= 0) mbar_wait(&bar[x], (uint32_t)((jl / n) & 1), 500000000ull);
+            }
+        }
     }
 }
 

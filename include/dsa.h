@@ -231,8 +231,8 @@ dsa_status dsa_indexer_topk_mxfp4(const void* q, const float* w, const uint8_t* 
  * DSA_ERR_UNSUPPORTED).  The scratch is a fixed array of
  * DSA_NOALLOC_SCRATCH_BYTES inside this library, so no call allocates.  A batch
  * of T = B rows needs, on a GPU with S SMs,
- *   round_up(4224 T, 256) + 16384 T + (S + B) * 45076 + 12 (B + 1) + 8 S
- * bytes, plus up to 768 bytes of alignment (151 rows fit at S = 152, 152 do
+ *   round_up(4224 T, 256) + 16384 T + (S + B) * 36884 + 12 (B + 1) + 8 S
+ * bytes, plus up to 768 bytes of alignment (194 rows fit at S = 152, 195 do
  * not); a larger batch returns
  * DSA_ERR_SCRATCH_LIMIT and launches nothing.  Nothing in the scratch needs
  * to start at zero: the kernels clear the histogram bins and plan entries
