@@ -42,7 +42,9 @@ pages print, the 21/57 schedule, brute-force top-k, sparse == dense attention
 when the context fits in the top-k, closed forms, the MTP seed width and
 draft-step read counts the pages print, brute-force top-k per draft position,
 the 68-byte MXFP4 token, the E2M1 codec against its value table and rounding
-rule, the MX scale property amax / 2**e in [4, 8)).
+rule, the MX scale property amax / 2**e in [4, 8), the MXFP4 key of a token
+within the format's bound of torch's LayerNorm and a complex rotation, and a
+whole request's MXFP4 top-k against brute force).
 The MTP reading where the pages are silent: a draft step with a context of at
 most 2048 publishes its all-positions row like any other step.  The LayerNorm
 eps, RoPE base and RoPE pairing are NOT fixed by the pages: "parity unpinned" for those three

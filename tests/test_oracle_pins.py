@@ -499,6 +499,78 @@ def test_mxfp4_scores_brute_force():
     assert np.all(O.score_magnitude_mxfp4(qc, qs, w, kc, ke) >= np.abs(s) - 1e-12)
 
 
+def _e2m1_value(code):
+    # OCP MX E2M1: bit 3 sign, then magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6
+    mag = {0: 0.0, 1: 0.5, 2: 1.0, 3: 1.5, 4: 2.0, 5: 3.0, 6: 4.0, 7: 6.0}[int(code) & 7]
+    return -mag if int(code) & 8 else mag
+
+
+def _mx_values(codes, exps):
+    v = np.vectorize(_e2m1_value)(codes).reshape(codes.shape[:-1] + (4, 32))
+    return (v * np.exp2(exps)[..., None]).reshape(codes.shape)
+
+
+def test_index_k_prepare_mxfp4_within_the_format_bound_of_norm_then_rotation():
+    # independent of the oracle's own LayerNorm and RoPE: torch's LayerNorm and
+    # a complex rotation of the interleaved pairs, then the MX rounding bound
+    rng = np.random.default_rng(35)
+    n = 64
+    k = rng.standard_normal((n, 128)) * np.exp2(rng.integers(-8, 8, (n, 1))) + rng.standard_normal((n, 1))
+    pos = rng.integers(0, 1 << 20, n)
+    pos[0] = 0
+    k[5] = 3.25                                           # a constant row: LayerNorm gives 0
+    codes, exps = O.index_k_prepare_mxfp4(k, pos)
+    y = torch.nn.functional.layer_norm(torch.from_numpy(k), (128,), eps=1e-6)
+    i = torch.arange(32, dtype=torch.float64)
+    ang = torch.from_numpy(pos.astype(np.float64))[:, None] * 10000.0 ** (-2.0 * i / 64)
+    z = torch.complex(y[:, 0:64:2], y[:, 1:64:2]) * torch.polar(torch.ones_like(ang), ang)
+    ref = y.clone()
+    ref[:, 0:64:2], ref[:, 1:64:2] = z.real, z.imag
+    ref = ref.numpy()
+    got = _mx_values(codes, exps)
+    step = np.repeat(np.exp2(exps), 32, axis=1)
+    sat = np.abs(ref) > 6.0 * step
+    err = np.abs(got - ref)
+    assert np.all(err[~sat] <= step[~sat] * (1 + 1e-9))   # at most half of the widest code gap (4 -> 6)
+    assert np.all(err[sat] <= 2.0 * step[sat] * (1 + 1e-9))
+    blk = np.abs(ref).reshape(n, 4, 32).max(axis=-1)
+    live = blk > 1e-9
+    r = blk[live] / np.exp2(exps[live])
+    assert np.all((r >= 4.0 * (1 - 1e-9)) & (r < 8.0 * (1 + 1e-9)))   # shared exponent floor(log2 amax) - 2
+    assert not np.any(got[5]) and np.all(exps[5] == 0)    # constant row
+    assert np.allclose(got[0], _mx_values(*O.quantize_mxfp4(y.numpy()[:1]))[0])   # position 0: no rotation
+
+
+def test_request_topk_mxfp4_brute_force_and_short_context_rule():
+    rng = np.random.default_rng(36)
+    L, q_len = 2053, 6                                    # query tokens at positions 2047..2052
+    npg = 33
+    cache = np.zeros((npg, O.MXFP4_PAGE_BYTES), np.uint8)
+    pt = rng.permutation(npg).astype(np.int32)
+    codes, exps = O.index_k_prepare_mxfp4(rng.standard_normal((L, 128)), np.arange(L))
+    O.mxfp4_cache_write(cache, pt[np.arange(L) // 64] * 64 + np.arange(L) % 64, codes, exps)
+    qi = rng.standard_normal((q_len, 32, 128))
+    w = rng.standard_normal((q_len, 32))
+    topk, scores = O.request_topk_mxfp4(qi, w, cache, pt, L, q_len)
+    kd = _mx_values(codes, exps)                          # from the codes as written, not read back
+    for t in range(q_len):
+        n = L - q_len + t + 1
+        if n <= 2048:
+            assert topk[t].tolist() == list(range(n)) + [-1] * (2048 - n)
+            assert scores[t] is None
+            continue
+        qc, qs = O.index_q_quantize(qi[t])
+        qd = O.e4m3_decode(qc) * qs[:, None]
+        # scores by a matrix route (not the pins' loop helper): sum_m w_m relu(q_m . k_j)
+        ref = np.maximum(kd[:n] @ qd.T, 0.0) @ w[t]
+        assert np.allclose(scores[t], ref, rtol=1e-10, atol=1e-10)
+        order = sorted(range(n), key=lambda j: (-ref[j], j))   # key desc, ties to the lower position
+        kth = ref[order[2047]]
+        want, got = set(order[:2048]), set(topk[t].tolist())
+        assert len(got) == 2048 and max(got) <= n - 1
+        assert all(abs(ref[j] - kth) <= 1e-9 * max(1.0, abs(kth)) for j in want ^ got)
+
+
 # ------------------------------------------------------------------ schedule fallbacks
 def test_schedule_fallback_chain_follows_the_pages():
     n = g("num_layers")
