@@ -88,6 +88,12 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // Request index of query row `row`: the r with q_start[r] <= row < q_start[r+1].
 __device__ __forceinline__ int row_request(const int32_t* q_start, int B, int64_t row) {
+    // In a decode batch (one query row per request) row r is request r: two
+    // independent loads confirm that in one round trip.  The test accepts only
+    // the one request whose rows contain `row` (an empty request never passes
+    // it), so the search below gives the same answer whenever it is skipped.
+    const int g = (int)(row < (int64_t)(B - 1) ? row : (int64_t)(B - 1));
+    if (g >= 0 && (int64_t)__ldg(q_start + g) <= row && row < (int64_t)__ldg(q_start + g + 1)) return g;
     int lo = 0, hi = B - 1;
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;

@@ -77,11 +77,9 @@ extern "C" dsa_status dsa_indexer_topk_mxfp4(const void* q, const float* w, cons
         uint8_t* q8 = static_cast<uint8_t*>(ws);
         float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
         uint32_t* hist = reinterpret_cast<uint32_t*>(q8 + (q8_workspace_bytes(b->total_q) + 255) / 256 * 256);
-        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, hist, s);
-        if (rs != DSA_OK) return rs;
         void* plan = reinterpret_cast<uint8_t*>(hist) + (size_t)b->total_q * 4096 * 4;
-        rs = launch_indexer_tc(q8, wq, hist, idxk_cache, b, topk, topk_scores, plan, device_sm_count(), dev_status, s,
-                               true);
+        dsa_status rs = launch_indexer_tc(q, w, q8, wq, hist, idxk_cache, b, topk, topk_scores, plan,
+                                          device_sm_count(), dev_status, s, true);
         if (rs != DSA_OK) return rs;
     }
     if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);
@@ -107,17 +105,18 @@ extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint
         const int64_t ld = score_ld(b);
         if (b->num_pages * 66 > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
         const bool tc = use_tc_path(b);
-        uint32_t* hist = tc ? reinterpret_cast<uint32_t*>(sc) : nullptr;
-        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, hist, s);
-        if (rs != DSA_OK) return rs;
         if (tc) {
+            uint32_t* hist = reinterpret_cast<uint32_t*>(sc);
             const int G = device_sm_count();
             void* plan = reinterpret_cast<uint8_t*>(sc) + (size_t)b->total_q * 4096 * 4;
-            rs = launch_indexer_tc(q8, wq, hist, idxk_cache, b, topk, topk_scores, plan, G, dev_status, s);
+            dsa_status rs = launch_indexer_tc(q, w, q8, wq, hist, idxk_cache, b, topk, topk_scores, plan, G,
+                                              dev_status, s);
             if (rs != DSA_OK) return rs;
             if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);
             return DSA_OK;
         }
+        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, nullptr, s);
+        if (rs != DSA_OK) return rs;
         void* plan = reinterpret_cast<uint8_t*>(sc) + ((size_t)b->total_q * (size_t)ld * 4 + 255) / 256 * 256;
         rs = launch_indexer_rows(q8, wq, idxk_cache, b, sc, ld, true, false, plan, device_sm_count(), dev_status, s);
         if (rs != DSA_OK) return rs;

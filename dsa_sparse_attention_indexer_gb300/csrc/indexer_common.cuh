@@ -50,4 +50,24 @@ inline size_t q8_workspace_bytes(int64_t total_q) { return (size_t)total_q * (40
 dsa_status launch_index_q_quant(const void* q, const float* w, int64_t rows, uint8_t* q8, float* wq,
                                 uint32_t* hist, cudaStream_t s);
 
+// Index-Q quantisation of one (row, head) g = row * 32 + head by one warp:
+// 128 bf16 -> 128 E4M3 codes with one ue8m0 scale 2^e, folded into the head
+// weight (w' = w * 2^e, exact); also clears the row's 128-word slice of the
+// top-12-bit histogram when hist is given.
+__device__ __forceinline__ void index_q_quant_warp(const uint16_t* __restrict__ q, const float* __restrict__ w,
+                                                   int64_t g, int lane, uint8_t* __restrict__ q8,
+                                                   float* __restrict__ wq, uint32_t* __restrict__ hist) {
+    if (hist) reinterpret_cast<uint4*>(hist + g * 128)[lane] = make_uint4(0, 0, 0, 0);
+    const uint2 raw = *reinterpret_cast<const uint2*>(q + g * 128 + lane * 4);
+    const float x0 = bf16_bits_to_f32(raw.x & 0xffffu), x1 = bf16_bits_to_f32(raw.x >> 16);
+    const float x2 = bf16_bits_to_f32(raw.y & 0xffffu), x3 = bf16_bits_to_f32(raw.y >> 16);
+    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+    amax = warp_max(amax);
+    const int e = ue8m0_exponent(amax);
+    const uint32_t lo = f32x2_to_e4m3x2(ldexpf(x0, -e), ldexpf(x1, -e));
+    const uint32_t hi = f32x2_to_e4m3x2(ldexpf(x2, -e), ldexpf(x3, -e));
+    *reinterpret_cast<uint32_t*>(q8 + g * 128 + lane * 4) = lo | (hi << 16);
+    if (lane == 0) wq[g] = w[g] * ldexpf(1.0f, e);
+}
+
 }  // namespace dsa

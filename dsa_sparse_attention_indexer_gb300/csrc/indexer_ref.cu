@@ -13,24 +13,14 @@
 
 namespace dsa {
 
-// One warp per (row, head): 128 bf16 -> 128 E4M3 codes + w * 2^e.
+// One warp per (row, head): 128 bf16 -> 128 E4M3 codes + w * 2^e (row histogram reset).
 __global__ void __launch_bounds__(256)
 index_q_quant_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w, int64_t rows,
                      uint8_t* __restrict__ q8, float* __restrict__ wq, uint32_t* __restrict__ hist) {
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // row*32 + head
     if (g >= rows * 32) return;
-    if (hist) reinterpret_cast<uint4*>(hist + g * 128)[lane] = make_uint4(0, 0, 0, 0);   // row histogram reset
-    const uint2 raw = *reinterpret_cast<const uint2*>(q + g * 128 + lane * 4);
-    const float x0 = bf16_bits_to_f32(raw.x & 0xffffu), x1 = bf16_bits_to_f32(raw.x >> 16);
-    const float x2 = bf16_bits_to_f32(raw.y & 0xffffu), x3 = bf16_bits_to_f32(raw.y >> 16);
-    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-    amax = warp_max(amax);
-    const int e = ue8m0_exponent(amax);
-    const uint32_t lo = f32x2_to_e4m3x2(ldexpf(x0, -e), ldexpf(x1, -e));
-    const uint32_t hi = f32x2_to_e4m3x2(ldexpf(x2, -e), ldexpf(x3, -e));
-    *reinterpret_cast<uint32_t*>(q8 + g * 128 + lane * 4) = lo | (hi << 16);
-    if (lane == 0) wq[g] = w[g] * ldexpf(1.0f, e);
+    index_q_quant_warp(q, w, g, lane, q8, wq, hist);
 }
 
 }  // namespace dsa

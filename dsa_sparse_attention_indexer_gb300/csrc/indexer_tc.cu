@@ -102,15 +102,16 @@ static_assert(kCap % kEpiThreads == 0 && kCap / kEpiThreads <= 32, "per-thread c
 __device__ __forceinline__ int64_t cta_start(int64_t g, int64_t N, int64_t G) { return g * N / G; }
 __device__ __forceinline__ int64_t cta_of_tile(int64_t x, int64_t N, int64_t G) { return ((x + 1) * G + N - 1) / N - 1; }
 
-// Single CTA of 1024 threads.
-__global__ void __launch_bounds__(1024)
-plan_kernel(BatchDev b, int G_launch, Plan p) {
-    __shared__ int32_t scratch[32];
+// The work plan, by one block of NT threads: tile prefix over the requests
+// that need scoring, an equal share of tiles per CTA (at least kMinTiles), and
+// the segments (request x CTA pieces) each CTA streams.
+template <int NT>
+__device__ void plan_block(BatchDev b, int G_launch, Plan p, int32_t* scratch) {
     int G = G_launch;                                  // CTAs that get a share (<= G_launch)
     const int gt = threadIdx.x;
     // pass 1: tile prefix over requests that need scoring
     int64_t run = 0;
-    for (int base = 0; base < b.batch; base += 1024) {
+    for (int base = 0; base < b.batch; base += NT) {
         const int r = base + gt;
         int tiles = 0;
         if (r < b.batch) {
@@ -119,7 +120,7 @@ plan_kernel(BatchDev b, int G_launch, Plan p) {
             tiles = (qn > 0 && L > kTopK) ? (L + 127) / 128 : 0;
         }
         int total;
-        const int ex = sel::excl_scan<1024, 0>(tiles, gt, scratch, &total);
+        const int ex = sel::excl_scan<NT, 0>(tiles, gt, scratch, &total);
         if (r < b.batch) p.tile_start[r] = run + ex;
         run += total;
     }
@@ -130,7 +131,7 @@ plan_kernel(BatchDev b, int G_launch, Plan p) {
     __syncthreads();
     // pass 2: pieces per request (CTA boundaries inside it) and their prefix
     int32_t srun = 0;
-    for (int base = 0; base < b.batch; base += 1024) {
+    for (int base = 0; base < b.batch; base += NT) {
         const int r = base + gt;
         int np = 0;
         if (r < b.batch) {
@@ -138,19 +139,19 @@ plan_kernel(BatchDev b, int G_launch, Plan p) {
             if (s1 > s0) np = (int)(cta_of_tile(s1 - 1, N, G) - cta_of_tile(s0, N, G) + 1);
         }
         int total;
-        const int ex = sel::excl_scan<1024, 0>(np, gt, scratch, &total);
+        const int ex = sel::excl_scan<NT, 0>(np, gt, scratch, &total);
         if (r < b.batch) p.seg_first[r] = srun + ex;
         srun += total;
     }
     if (gt == 0) p.seg_first[b.batch] = srun;
-    for (int g = gt; g < G_launch; g += 1024) {          // every launched CTA, also the idle ones
+    for (int g = gt; g < G_launch; g += NT) {          // every launched CTA, also the idle ones
         p.cta_range[2 * g] = 0;
         p.cta_range[2 * g + 1] = 0;
     }
     __syncthreads();
     // pass 3: segment records, one thread per segment
     const int32_t ns_total = srun;
-    for (int s = gt; s < ns_total; s += 1024) {
+    for (int s = gt; s < ns_total; s += NT) {
         int lo = 0, hi = b.batch - 1;                  // request r: seg_first[r] <= s < seg_first[r+1]
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -167,11 +168,27 @@ plan_kernel(BatchDev b, int G_launch, Plan p) {
     __syncthreads();
     // pass 4: each CTA's contiguous run of segments
     const int32_t ns = srun;
-    for (int s = gt; s < ns; s += 1024) {
+    for (int s = gt; s < ns; s += NT) {
         const int32_t g = p.segs[s].cta;
         if (s == 0 || p.segs[s - 1].cta != g) p.cta_range[2 * g] = s;
         if (s == ns - 1 || p.segs[s + 1].cta != g) p.cta_range[2 * g + 1] = s + 1;
     }
+}
+
+// One launch before the score kernel: block 0 builds the plan, blocks 1.. quantise
+// the index queries (one warp per (row, head)) and clear the row histograms.  The
+// two jobs are independent, so they share the launch instead of running back to back.
+constexpr int kPrepThreads = 256;
+__global__ void __launch_bounds__(kPrepThreads)
+prep_kernel(BatchDev b, int G_launch, Plan p, const uint16_t* __restrict__ q, const float* __restrict__ w,
+            int64_t rows, uint8_t* __restrict__ q8, float* __restrict__ wq) {
+    __shared__ int32_t scratch[32];
+    if (blockIdx.x == 0) {
+        plan_block<kPrepThreads>(b, G_launch, p, scratch);
+        return;
+    }
+    const int64_t g = (int64_t)(blockIdx.x - 1) * (kPrepThreads / 32) + (threadIdx.x >> 5);   // row*32 + head
+    if (g < rows * 32) index_q_quant_warp(q, w, g, threadIdx.x & 31, q8, wq, p.hist);
 }
 
 __device__ __forceinline__ void epi_sync() { sel::gsync<kEpiThreads, kEpiBar>(); }
@@ -1176,9 +1193,9 @@ Plan carve_plan(void* base, int64_t batch, int G) {
     return p;
 }
 
-dsa_status launch_indexer_tc(const uint8_t* q8, const float* wq, uint32_t* hist, const uint8_t* cache,
-                             const dsa_batch* b, int32_t* topk, float* topk_scores, void* plan_ws, int G, int32_t* st,
-                             cudaStream_t s, bool mx) {
+dsa_status launch_indexer_tc(const void* q, const float* w, uint8_t* q8, float* wq, uint32_t* hist,
+                             const uint8_t* cache, const dsa_batch* b, int32_t* topk, float* topk_scores, void* plan_ws,
+                             int G, int32_t* st, cudaStream_t s, bool mx) {
     CUtensorMap map;
     if (!make_index_tmap(cache, b->num_pages, mx, &map)) return DSA_ERR_CUDA;
     static bool attr = false;
@@ -1195,7 +1212,9 @@ dsa_status launch_indexer_tc(const uint8_t* q8, const float* wq, uint32_t* hist,
     BatchDev bd = to_dev(b);
     Plan p = carve_plan(plan_ws, b->batch, G);
     p.hist = hist;
-    itc::plan_kernel<<<1, 1024, 0, s>>>(bd, G, p);
+    const int64_t qblocks = (b->total_q * 32 + itc::kPrepThreads / 32 - 1) / (itc::kPrepThreads / 32);
+    itc::prep_kernel<<<(unsigned)(1 + qblocks), itc::kPrepThreads, 0, s>>>(bd, G, p, static_cast<const uint16_t*>(q),
+                                                                        w, b->total_q, q8, wq);
     DSA_CHECK_LAUNCH();
     if (mx) itc::score_topk_kernel<true><<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
     else itc::score_topk_kernel<false><<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);

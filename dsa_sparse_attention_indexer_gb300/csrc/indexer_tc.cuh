@@ -24,10 +24,14 @@ struct Plan {
 };
 
 size_t tc_plan_bytes(int64_t batch, int G);
-// mx: the cache is the MXFP4 index-K layout (DSA_IDXK_MXFP4_PAGE_BYTES pages).
-dsa_status launch_indexer_tc(const uint8_t* q8, const float* wq, uint32_t* hist, const uint8_t* cache,
-                             const dsa_batch* b, int32_t* topk, float* topk_scores, void* plan_ws, int G, int32_t* st,
-                             cudaStream_t s, bool mx = false);
+// The decode indexer + top-2048 from the bf16 index queries q [T,32,128] and
+// head weights w [T,32]: quantises q into q8 / wq (T x 4096 B, T x 32 fp32)
+// and clears hist (T x 4096 words) in the launch that builds the plan, then
+// scores and selects.  mx: the cache is the MXFP4 index-K layout
+// (DSA_IDXK_MXFP4_PAGE_BYTES pages).
+dsa_status launch_indexer_tc(const void* q, const float* w, uint8_t* q8, float* wq, uint32_t* hist,
+                             const uint8_t* cache, const dsa_batch* b, int32_t* topk, float* topk_scores, void* plan_ws,
+                             int G, int32_t* st, cudaStream_t s, bool mx = false);
 int device_sm_count();
 
 size_t mt_plan_bytes(int64_t batch, int64_t total_q);

@@ -70,9 +70,7 @@ extern "C" dsa_status dsa_indexer_topk_noalloc(const void* q, const float* w, co
         float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
         uint32_t* hist = reinterpret_cast<uint32_t*>(q8 + qbytes);
         void* plan = reinterpret_cast<uint8_t*>(hist) + (size_t)b->total_q * 4096 * 4;
-        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, hist, s);
-        if (rs != DSA_OK) return rs;
-        rs = launch_indexer_tc(q8, wq, hist, idxk_cache, b, topk, topk_scores, plan, G, dev_status, s);
+        dsa_status rs = launch_indexer_tc(q, w, q8, wq, hist, idxk_cache, b, topk, topk_scores, plan, G, dev_status, s);
         if (rs != DSA_OK) return rs;
     }
     if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);
