@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -39,21 +40,46 @@ L2_BYTES = 129 * 1024 * 1024
 
 # DRAM traffic per launch from an ncu capture, keyed by (workload, call), with the
 # kernel source it was taken on; valid only while that source is unchanged
-# (sha256 prefix).  decode32k sparse_mla_decode: a capture of its 64 decode rows
-# on 16K contexts (the same 2048 selected rows each, so the same launch);
-# decode1m indexer_topk: a 256K-context capture scaled by the context (x4).
+# (sha256 prefix over the .cu file and every local header it includes).
+# decode32k sparse_mla_decode: a capture of its 64 decode rows on 16K contexts
+# (the same 2048 selected rows each, so the same launch); decode1m
+# indexer_topk: a 256K-context capture scaled by the context (x4).
 NCU_TRAFFIC = {
-    ("decode32k", "sparse_mla_decode"): (106.3e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
-                                         "23817a9df5e77b45"),
-    ("decode1m", "indexer_topk"): (568.8e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
-                                   "b13161fe2df31798"),
+    ("decode32k", "sparse_mla_decode"): (106.4e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
+                                         "cbab89bbdfd0c0d0"),
+    ("decode1m", "indexer_topk"): (567.4e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
+                                   "e534425f845f9b67"),
 }
 FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s)
 
 
 def file_sha(path):
-    with open(os.path.join(ROOT, path), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 prefix of a CUDA source and the local headers it includes
+    (csrc/ and include/), each once, in first-include order."""
+    dirs = [os.path.dirname(os.path.join(ROOT, path)), os.path.join(ROOT, "include")]
+    seen, order = set(), []
+
+    def visit(full):
+        if full in seen:
+            return
+        seen.add(full)
+        order.append(full)
+        with open(full, "rb") as f:
+            for line in f.read().decode("utf-8", "replace").splitlines():
+                m = re.match(r'\s*#\s*include\s+"([^"]+)"', line)
+                if m:
+                    for d in dirs:
+                        cand = os.path.join(d, m.group(1))
+                        if os.path.exists(cand):
+                            visit(cand)
+                            break
+
+    visit(os.path.join(ROOT, path))
+    h = hashlib.sha256()
+    for full in order:
+        with open(full, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def peaks():
