@@ -373,6 +373,26 @@ class MtpStep:
 KERNELS_PER_CALL = {"index_k_store": 1, "latent_kv_store": 1, "indexer_topk": 4, "sparse_mla_decode": 1}
 
 
+def kernels_per_call(name, rows, sms):
+    """Kernels one call launches.  The indexer launches four either way (decode:
+    prep, score, merge filter, merge; multi-token: quantisation, plan, score
+    rows, select).  Sparse MLA launches one kernel when its rows are cut into
+    clusters of 2 or 4 CTAs or taken whole, and a second, the log-sum-exp
+    combine, when CTAs leave partials: the library's split rule, restated."""
+    if name != "sparse_mla_decode":
+        return KERNELS_PER_CALL[name]
+    if rows < sms:
+        per = sms // rows
+        c = min(per, 22) if per >= 8 else 4 if per >= 4 else 2 if per >= 2 else 1
+        ctas = rows * c
+    else:
+        ctas = sms
+    if rows <= ctas:
+        c, extra = divmod(ctas, rows)
+        return 1 if extra == 0 and c in (2, 4) else 2
+    return 2 if rows < 8 * ctas else 1
+
+
 def call_flops(name, w):
     """Tensor-core FLOPs of one launch of a call: the indexer's FP8 scoring
     (32 heads x 128 dims x 2 per visible token and query row) and sparse MLA's
@@ -577,8 +597,10 @@ def run_ours(args, rank, world):
 
     if world > 1:
         ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mla_rows = len(w.seq_len) if w.draft_steps else w.total_q     # a draft step's launch: one row per request
     return dict(w=w, ms=ms, e2e_ms=e2e_ms, per_call=per_call, per_launch=per_launch, clocks=clocks,
-                h2d=h2d, d2h=d2h, launches=sum(KERNELS_PER_CALL[k] * len(v) for k, v in timers.items()))
+                h2d=h2d, d2h=d2h, launches=sum(kernels_per_call(k, mla_rows, sms) * len(v) for k, v in timers.items()))
 
 
 # ----------------------------------------------------------------------------
