@@ -46,9 +46,9 @@ L2_BYTES = 129 * 1024 * 1024
 # indexer_topk: a 256K-context capture scaled by the context (x4).
 NCU_TRAFFIC = {
     ("decode32k", "sparse_mla_decode"): (106.4e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
-                                         "cbab89bbdfd0c0d0"),
+                                         "c5458f620d669e68"),
     ("decode1m", "indexer_topk"): (567.4e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
-                                   "e534425f845f9b67"),
+                                   "aca40d28e5cd4b96"),
 }
 FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s)
 

@@ -448,7 +448,7 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
     const uint32_t tmem = misc->tmem_base;
     int s_begin = p.cta_range[2 * blockIdx.x], s_end = p.cta_range[2 * blockIdx.x + 1];
     const int nseg_max = (int)gridDim.x + b.batch;    // segment slots in the workspace
-    if (s_begin < 0 || s_end > nseg_max || s_begin > s_end) {   // never for a plan from plan_kernel
+    if (s_begin < 0 || s_end > nseg_max || s_begin > s_end) {   // never for a plan from prep_kernel
         if (threadIdx.x == 0) record_error(st, DSA_DEVERR_INDEX_RANGE, s_begin);
         s_begin = s_end = 0;
     }

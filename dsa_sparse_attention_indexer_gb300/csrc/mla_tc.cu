@@ -919,7 +919,6 @@ combine_kernel(Args a) {
 
 }  // namespace mtc
 
-// CTAs per row when rows are fewer than SMs: a cluster of at most 8.
 // CTAs per row when rows are fewer than SMs: a cluster of 2 or 4 when that
 // fills the GPU best, else (tiny batches) up to one CTA per tile of the row,
 // merged through global partials.
