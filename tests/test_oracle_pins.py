@@ -273,6 +273,36 @@ def test_request_topk_short_context_rule_and_causality():
             assert len(scores[t]) == n
 
 
+def test_request_topk_invariant_under_page_permutation_and_linear_in_the_key_scale():
+    rng = np.random.default_rng(12)
+    L, q_len = 4200, 2
+    kc, ks = O.index_k_prepare(rng.standard_normal((L, 128)), np.arange(L))
+    qi = rng.standard_normal((q_len, 32, 128))
+    w = rng.standard_normal((q_len, 32)) / math.sqrt(32)
+    pages = (L + 63) // 64
+    outs = []
+    for seed, pool in ((1, pages), (2, pages + 9)):     # two physical layouts of the same request
+        pt = np.random.default_rng(seed).permutation(pool)[:pages].astype(np.int32)
+        cache = np.zeros((pool, O.INDEX_PAGE_BYTES), np.uint8)
+        O.index_cache_write(cache, pt[np.arange(L) // 64] * 64 + np.arange(L) % 64, kc, ks)
+        outs.append(O.request_topk(qi, w, cache, pt, L, q_len))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    for a, b in zip(outs[0][1], outs[1][1]):
+        assert np.array_equal(a, b)
+    # a power-of-two boost of some keys' scales (the x4 tokens of the 32K workload)
+    # multiplies exactly their scores by 4 and leaves every other score unchanged
+    qc, qs = O.index_q_quantize(qi[1])
+    boost = np.zeros(L, bool)
+    boost[::97] = True
+    s0 = O.indexer_scores(qc, qs, w[1], kc, ks)
+    s1 = O.indexer_scores(qc, qs, w[1], kc, np.where(boost, 4.0 * ks, ks))
+    assert np.array_equal(s1[boost], 4.0 * s0[boost]) and np.array_equal(s1[~boost], s0[~boost])
+    top0 = set(O.topk_positions(s0, L).tolist())
+    top1 = set(O.topk_positions(s1, L).tolist())
+    # a boosted key already selected with a positive score stays selected
+    assert all(j in top1 for j in np.flatnonzero(boost) if j in top0 and s0[j] > 0)
+
+
 # ------------------------------------------------------------------ sparse MLA
 def test_sparse_mla_equals_dense_sdpa_when_context_fits():
     rng = np.random.default_rng(10)
