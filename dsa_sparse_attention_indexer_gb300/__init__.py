@@ -157,14 +157,28 @@ def _stream(stream):
     return c_void_p(stream.cuda_stream)
 
 
-def _need(t: torch.Tensor, dtype, name: str, device=None):
+def _need(t: torch.Tensor, dtype, name: str, device=None, numel=None):
+    """A device argument of the C ABI: a contiguous CUDA tensor of `dtype`, on
+    `device` when given, with at least `numel` elements when given.  The
+    library reads and writes through raw pointers, so a host tensor, a tensor on
+    another GPU or a short buffer is rejected here, before any launch."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor, got one on {t.device}")
+    if device is not None and t.device != torch.device(device):
+        raise ValueError(f"{name} is on {t.device}, the call's other tensors on {device}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call needs {numel}")
     return t
+
+
+def _opt(t, dtype, name: str, device=None, numel=None):
+    return None if t is None else _need(t, dtype, name, device, numel)
 
 
 # ---------------------------------------------------------------------------
@@ -214,6 +228,7 @@ def new_device_status(device) -> torch.Tensor:
 
 
 def dsa_device_status_read(dev_status: torch.Tensor, stream=None):
+    _need(dev_status, torch.int32, "dev_status", numel=4)
     out = (c_int32 * 4)()
     code = lib().dsa_device_status_read(_ptr(dev_status), _stream(stream), out)
     if code not in (0, 7):
@@ -222,17 +237,27 @@ def dsa_device_status_read(dev_status: torch.Tensor, stream=None):
 
 
 def dsa_device_status_reset(dev_status: torch.Tensor, stream=None):
+    _need(dev_status, torch.int32, "dev_status", numel=4)
     _check("dsa_device_status_reset", lib().dsa_device_status_reset(_ptr(dev_status), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------
+def _store_args(k, pos, slot, idxk_cache, gamma, beta, dev_status):
+    _need(k, torch.bfloat16, "k")
+    dev, n = k.device, k.shape[0]
+    _need(k, torch.bfloat16, "k", dev, n * INDEX_HEAD_DIM)
+    _need(pos, torch.int32, "pos", dev, n)
+    _need(slot, torch.int64, "slot", dev, n)
+    _need(idxk_cache, torch.uint8, "idxk_cache", dev)
+    _opt(gamma, torch.float32, "gamma", dev, INDEX_HEAD_DIM)
+    _opt(beta, torch.float32, "beta", dev, INDEX_HEAD_DIM)
+    _opt(dev_status, torch.int32, "dev_status", dev, 4)
+    return n
+
+
 def dsa_index_k_store(k, pos, slot, idxk_cache, *, gamma=None, beta=None, ln_eps=1e-6,
                       rope_base=10000.0, num_pages=None, dev_status=None, stream=None):
-    _need(k, torch.bfloat16, "k")
-    _need(pos, torch.int32, "pos")
-    _need(slot, torch.int64, "slot")
-    _need(idxk_cache, torch.uint8, "idxk_cache")
-    n = k.shape[0]
+    n = _store_args(k, pos, slot, idxk_cache, gamma, beta, dev_status)
     if num_pages is None:
         num_pages = idxk_cache.numel() // IDXK_PAGE_BYTES
     _check("dsa_index_k_store", lib().dsa_index_k_store(
@@ -243,10 +268,7 @@ def dsa_index_k_store(k, pos, slot, idxk_cache, *, gamma=None, beta=None, ln_eps
 def dsa_index_k_store_mxfp4(k, pos, slot, idxk_cache, *, gamma=None, beta=None, ln_eps=1e-6,
                             rope_base=10000.0, num_pages=None, dev_status=None, stream=None):
     """dsa_index_k_store into an MXFP4 index-K cache (4352-byte pages, 32-byte aligned)."""
-    _need(k, torch.bfloat16, "k")
-    _need(pos, torch.int32, "pos")
-    _need(slot, torch.int64, "slot")
-    _need(idxk_cache, torch.uint8, "idxk_cache")
+    _store_args(k, pos, slot, idxk_cache, gamma, beta, dev_status)
     if num_pages is None:
         num_pages = idxk_cache.numel() // IDXK_MXFP4_PAGE_BYTES
     _check("dsa_index_k_store_mxfp4", lib().dsa_index_k_store_mxfp4(
@@ -259,13 +281,19 @@ def dsa_latent_kv_store_fused(kv_c, k_pe, pos, slot, kv_cache, *, kv_gamma=None,
                               num_pages=None, idx_num_pages=None, dev_status=None, stream=None):
     """Latent rows from raw kv_c / k_pe (RMSNorm, RoPE) and, with idx_k, the index keys too."""
     _need(kv_c, torch.bfloat16, "kv_c")
-    _need(k_pe, torch.bfloat16, "k_pe")
-    _need(pos, torch.int32, "pos")
-    _need(slot, torch.int64, "slot")
-    _need(kv_cache, torch.uint8, "kv_cache")
+    dev, n = kv_c.device, kv_c.shape[0]
+    _need(kv_c, torch.bfloat16, "kv_c", dev, n * LATENT_DIM)
+    _need(k_pe, torch.bfloat16, "k_pe", dev, n * ROPE_DIM)
+    _need(pos, torch.int32, "pos", dev, n)
+    _need(slot, torch.int64, "slot", dev, n)
+    _need(kv_cache, torch.uint8, "kv_cache", dev)
+    _opt(kv_gamma, torch.float32, "kv_gamma", dev, LATENT_DIM)
+    _opt(dev_status, torch.int32, "dev_status", dev, 4)
     if idx_k is not None:
-        _need(idx_k, torch.bfloat16, "idx_k")
-        _need(idxk_cache, torch.uint8, "idxk_cache")
+        _need(idx_k, torch.bfloat16, "idx_k", dev, n * INDEX_HEAD_DIM)
+        _need(idxk_cache, torch.uint8, "idxk_cache", dev)
+        _opt(idx_gamma, torch.float32, "idx_gamma", dev, INDEX_HEAD_DIM)
+        _opt(idx_beta, torch.float32, "idx_beta", dev, INDEX_HEAD_DIM)
     if num_pages is None:
         num_pages = kv_cache.numel() // KV_PAGE_BYTES
     if idx_num_pages is None:
@@ -278,14 +306,35 @@ def dsa_latent_kv_store_fused(kv_c, k_pe, pos, slot, kv_cache, *, kv_gamma=None,
 
 def dsa_latent_kv_store(c, rope, slot, kv_cache, *, num_pages=None, dev_status=None, stream=None):
     _need(c, torch.bfloat16, "c")
-    _need(rope, torch.bfloat16, "rope")
-    _need(slot, torch.int64, "slot")
-    _need(kv_cache, torch.uint8, "kv_cache")
+    dev, n = c.device, c.shape[0]
+    _need(c, torch.bfloat16, "c", dev, n * LATENT_DIM)
+    _need(rope, torch.bfloat16, "rope", dev, n * ROPE_DIM)
+    _need(slot, torch.int64, "slot", dev, n)
+    _need(kv_cache, torch.uint8, "kv_cache", dev)
+    _opt(dev_status, torch.int32, "dev_status", dev, 4)
     if num_pages is None:
         num_pages = kv_cache.numel() // KV_PAGE_BYTES
     _check("dsa_latent_kv_store", lib().dsa_latent_kv_store(
         _ptr(c), _ptr(rope), _ptr(slot), c.shape[0], _ptr(kv_cache), num_pages, _ptr(dev_status),
         _stream(stream)))
+
+
+def _indexer_args(q, w, idxk_cache, batch: Batch) -> int:
+    """Checks the indexer's inputs against the batch; returns its query rows T."""
+    _need(q, torch.bfloat16, "q")
+    T = batch.total_q
+    _need(q, torch.bfloat16, "q", q.device, T * INDEX_HEADS * INDEX_HEAD_DIM)
+    _need(w, torch.float32, "w", q.device, T * INDEX_HEADS)
+    _need(idxk_cache, torch.uint8, "idxk_cache", q.device)
+    _need(batch.seq_len, torch.int32, "batch.seq_len", q.device)
+    return T
+
+
+def _ws(ws, nbytes, device):
+    """The call's workspace: allocated when not given, else a uint8 CUDA buffer."""
+    if ws is None:
+        return workspace(nbytes, device)
+    return _need(ws, torch.uint8, "ws", device)
 
 
 def dsa_indexer_topk_workspace_size(batch: Batch) -> int:
@@ -295,14 +344,13 @@ def dsa_indexer_topk_workspace_size(batch: Batch) -> int:
 def dsa_indexer_topk(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=None, share=None,
                      layer_id: int = 0, ws=None, dev_status=None, stream=None):
     """Indexer + top-2048.  Returns topk int32 [T, 2048] (allocated if not given)."""
-    _need(q, torch.bfloat16, "q")
-    _need(w, torch.float32, "w")
-    _need(idxk_cache, torch.uint8, "idxk_cache")
-    T = batch.total_q
+    T = _indexer_args(q, w, idxk_cache, batch)
     if topk is None:
         topk = torch.empty((T, TOPK), dtype=torch.int32, device=q.device)
-    if ws is None:
-        ws = workspace(dsa_indexer_topk_workspace_size(batch), q.device)
+    _need(topk, torch.int32, "topk", q.device, T * TOPK)
+    _opt(topk_scores, torch.float32, "topk_scores", q.device, T * TOPK)
+    _opt(dev_status, torch.int32, "dev_status", q.device, 4)
+    ws = _ws(ws, dsa_indexer_topk_workspace_size(batch) if ws is None else 0, q.device)
     _check("dsa_indexer_topk", lib().dsa_indexer_topk(
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
         None if share is None else share.handle, layer_id, _ptr(ws), ws.numel(), _ptr(dev_status),
@@ -313,14 +361,13 @@ def dsa_indexer_topk(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=N
 def dsa_indexer_topk_mxfp4(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=None, share=None,
                            layer_id: int = 0, ws=None, dev_status=None, stream=None):
     """dsa_indexer_topk over an MXFP4 index-K cache (decode batches)."""
-    _need(q, torch.bfloat16, "q")
-    _need(w, torch.float32, "w")
-    _need(idxk_cache, torch.uint8, "idxk_cache")
-    T = batch.total_q
+    T = _indexer_args(q, w, idxk_cache, batch)
     if topk is None:
         topk = torch.empty((T, TOPK), dtype=torch.int32, device=q.device)
-    if ws is None:
-        ws = workspace(dsa_indexer_topk_workspace_size(batch), q.device)
+    _need(topk, torch.int32, "topk", q.device, T * TOPK)
+    _opt(topk_scores, torch.float32, "topk_scores", q.device, T * TOPK)
+    _opt(dev_status, torch.int32, "dev_status", q.device, 4)
+    ws = _ws(ws, dsa_indexer_topk_workspace_size(batch) if ws is None else 0, q.device)
     _check("dsa_indexer_topk_mxfp4", lib().dsa_indexer_topk_mxfp4(
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
         None if share is None else share.handle, layer_id, _ptr(ws), ws.numel(), _ptr(dev_status),
@@ -331,12 +378,12 @@ def dsa_indexer_topk_mxfp4(q, w, idxk_cache, batch: Batch, *, topk=None, topk_sc
 def dsa_indexer_topk_noalloc(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=None, share=None,
                              layer_id: int = 0, dev_status=None, stream=None):
     """dsa_indexer_topk for decode batches on the library's fixed scratch (no workspace)."""
-    _need(q, torch.bfloat16, "q")
-    _need(w, torch.float32, "w")
-    _need(idxk_cache, torch.uint8, "idxk_cache")
-    T = batch.total_q
+    T = _indexer_args(q, w, idxk_cache, batch)
     if topk is None:
         topk = torch.empty((T, TOPK), dtype=torch.int32, device=q.device)
+    _need(topk, torch.int32, "topk", q.device, T * TOPK)
+    _opt(topk_scores, torch.float32, "topk_scores", q.device, T * TOPK)
+    _opt(dev_status, torch.int32, "dev_status", q.device, 4)
     _check("dsa_indexer_topk_noalloc", lib().dsa_indexer_topk_noalloc(
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
         None if share is None else share.handle, layer_id, _ptr(dev_status), _stream(stream)))
@@ -346,12 +393,13 @@ def dsa_indexer_topk_noalloc(q, w, idxk_cache, batch: Batch, *, topk=None, topk_
 def dsa_indexer_scores(q, w, idxk_cache, batch: Batch, *, ld=None, scores=None, ws=None,
                        dev_status=None, stream=None):
     """Full fp32 score rows [T, ld] (debug / parity hook)."""
-    T = batch.total_q
+    T = _indexer_args(q, w, idxk_cache, batch)
     ld = batch.c.max_seq_len if ld is None else ld
     if scores is None:
         scores = torch.empty((T, ld), dtype=torch.float32, device=q.device)
-    if ws is None:
-        ws = workspace(_ws_size("dsa_indexer_scores_workspace_size", batch), q.device)
+    _need(scores, torch.float32, "scores", q.device, T * ld)
+    _opt(dev_status, torch.int32, "dev_status", q.device, 4)
+    ws = _ws(ws, _ws_size("dsa_indexer_scores_workspace_size", batch) if ws is None else 0, q.device)
     _check("dsa_indexer_scores", lib().dsa_indexer_scores(
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(scores), ld, _ptr(ws), ws.numel(),
         _ptr(dev_status), _stream(stream)))
@@ -360,11 +408,14 @@ def dsa_indexer_scores(q, w, idxk_cache, batch: Batch, *, ld=None, scores=None, 
 
 def dsa_topk_from_scores(scores, valid_len, *, max_len=None, topk=None, stream=None):
     _need(scores, torch.float32, "scores")
-    _need(valid_len, torch.int32, "valid_len")
+    if scores.dim() != 2:
+        raise ValueError(f"scores must be [rows, ld], got shape {tuple(scores.shape)}")
     rows, ld = scores.shape
+    _need(valid_len, torch.int32, "valid_len", scores.device, rows)
     max_len = ld if max_len is None else max_len
     if topk is None:
         topk = torch.empty((rows, TOPK), dtype=torch.int32, device=scores.device)
+    _need(topk, torch.int32, "topk", scores.device, rows * TOPK)
     n = c_size_t(0)
     _check("dsa_topk_from_scores_workspace_size",
            lib().dsa_topk_from_scores_workspace_size(rows, max_len, ctypes.byref(n)))
@@ -380,13 +431,19 @@ def dsa_sparse_mla_workspace_size(batch: Batch) -> int:
 
 def _mla(fn, q, topk, kv_cache, batch, softmax_scale, out, out_dtype, lse, share, ws, dev_status, stream):
     _need(q, torch.bfloat16, "q")
-    _need(kv_cache, torch.uint8, "kv_cache")
     T = batch.total_q
+    dev = q.device
+    _need(q, torch.bfloat16, "q", dev, T * MLA_HEADS * QK_DIM)
+    _need(kv_cache, torch.uint8, "kv_cache", dev)
+    _need(batch.seq_len, torch.int32, "batch.seq_len", dev)
+    _opt(topk, torch.int32, "topk", dev, T * TOPK)
+    out_t = torch.float32 if out_dtype == DTYPE_F32 else torch.bfloat16
     if out is None:
-        out = torch.empty((T, MLA_HEADS, LATENT_DIM),
-                          dtype=torch.float32 if out_dtype == DTYPE_F32 else torch.bfloat16, device=q.device)
-    if ws is None:
-        ws = workspace(dsa_sparse_mla_workspace_size(batch), q.device)
+        out = torch.empty((T, MLA_HEADS, LATENT_DIM), dtype=out_t, device=dev)
+    _need(out, out_t, "out", dev, T * MLA_HEADS * LATENT_DIM)
+    _opt(lse, torch.float32, "lse", dev, T * MLA_HEADS)
+    _opt(dev_status, torch.int32, "dev_status", dev, 4)
+    ws = _ws(ws, dsa_sparse_mla_workspace_size(batch) if ws is None else 0, dev)
     _check(fn, getattr(lib(), fn)(
         _ptr(q), _ptr(topk), None if share is None else share.handle, _ptr(kv_cache), batch.ref(),
         softmax_scale, _ptr(out), out_dtype, _ptr(lse), _ptr(ws), ws.numel(), _ptr(dev_status),
@@ -456,6 +513,7 @@ class TopkShare:
         _check("dsa_topk_share_reset", lib().dsa_topk_share_reset(self.handle))
 
     def publish(self, layer_id: int, topk: torch.Tensor):
+        _need(topk, torch.int32, "topk", numel=topk.shape[0] * TOPK)
         _check("dsa_topk_share_publish",
                lib().dsa_topk_share_publish(self.handle, layer_id, _ptr(topk), topk.shape[0]))
 
@@ -509,16 +567,17 @@ def dsa_mtp_topk_width(index_topk: int = 2048, index_kpool: int = 1) -> int:
 
 def dsa_mtp_seed_write(topk, *, src_row=None, n=None, seed=None, width=None, dev_status=None, stream=None):
     """seed[r] = topk[src_row[r]] (2048 int32) followed by -1 tail slots."""
-    _need(topk, torch.int32, "topk")
+    _need(topk, torch.int32, "topk", numel=topk.shape[0] * TOPK)
     if src_row is not None:
-        _need(src_row, torch.int32, "src_row")
+        _need(src_row, torch.int32, "src_row", topk.device)
     if n is None:
         n = topk.shape[0] if src_row is None else src_row.shape[0]
     if width is None:
         width = dsa_mtp_topk_width() if seed is None else seed.shape[1]
     if seed is None:
         seed = torch.empty((n, width), dtype=torch.int32, device=topk.device)
-    _need(seed, torch.int32, "seed")
+    _need(seed, torch.int32, "seed", topk.device, n * width)
+    _opt(dev_status, torch.int32, "dev_status", topk.device, 4)
     _check("dsa_mtp_seed_write", lib().dsa_mtp_seed_write(
         _ptr(topk), topk.shape[0], _ptr(src_row), n, _ptr(seed), width, _ptr(dev_status), _stream(stream)))
     return seed

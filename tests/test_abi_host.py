@@ -12,6 +12,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 import dsa_sparse_attention_indexer_gb300 as D
 
@@ -169,11 +170,8 @@ def test_share_handle_lifecycle(L):
     with pytest.raises(D.DsaError) as e:
         s.get()
     assert e.value.code == 5
-    class FakeT:
-        shape = (7, 2048)
-        def data_ptr(self):
-            return 0x50000000
-    s.publish(6, FakeT())
+    # the handle only records the pointer: publish a fake one through the C call
+    assert L.dsa_topk_share_publish(s.handle, 6, ctypes.c_void_p(0x50000000), 7) == 0
     assert s.get() == (0x50000000, 7, 6)
     s.reset()
     with pytest.raises(D.DsaError):
@@ -235,3 +233,25 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(D, "LIB_PATH", "/nonexistent/libdsa.so")
     with pytest.raises(D.DsaLibraryMissing):
         D.lib()
+
+
+def test_binding_rejects_host_tensors_and_wrong_dtypes():
+    # the library reads and writes through raw device pointers: a host tensor or
+    # a wrong element type is refused in the binding, before any call into it
+    bf = torch.zeros(4, 128, dtype=torch.bfloat16)
+    i32 = torch.zeros(4, dtype=torch.int32)
+    i64 = torch.zeros(4, dtype=torch.int64)
+    u8 = torch.zeros(8448, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        D.dsa_index_k_store(bf, i32, i64, u8)
+    with pytest.raises(TypeError, match="torch.bfloat16"):
+        D.dsa_index_k_store(bf.float(), i32, i64, u8)
+    with pytest.raises(ValueError, match="contiguous"):
+        D.dsa_index_k_store(bf.t(), i32, i64, u8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        D.Batch(i32, torch.zeros(5, dtype=torch.int32), torch.zeros(4, 2, dtype=torch.int32), 8,
+                max_seq_len=128, max_q_len=1, total_q=4)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        D.dsa_topk_from_scores(torch.zeros(2, 4096), torch.zeros(2, dtype=torch.int32))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        D.dsa_device_status_read(torch.zeros(4, dtype=torch.int32))
