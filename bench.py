@@ -46,7 +46,7 @@ L2_BYTES = 129 * 1024 * 1024
 # indexer_topk: a 256K-context capture scaled by the context (x4).
 NCU_TRAFFIC = {
     ("decode32k", "sparse_mla_decode"): (106.4e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
-                                         "c5458f620d669e68"),
+                                         "52f4ec9dacd7f088"),
     ("decode1m", "indexer_topk"): (567.4e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
                                    "aca40d28e5cd4b96"),
 }
@@ -389,7 +389,7 @@ def kernels_per_call(name, rows, sms):
         ctas = sms
     if rows <= ctas:
         c, extra = divmod(ctas, rows)
-        return 1 if extra == 0 and c in (2, 4) else 2
+        return 1 if extra == 0 and c in (1, 2, 4) else 2
     return 2 if rows < 8 * ctas else 1
 
 

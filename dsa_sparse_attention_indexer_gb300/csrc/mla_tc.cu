@@ -1002,7 +1002,8 @@ dsa_status launch_sparse_mla_tc(const void* q, const int32_t* topk, const uint8_
     mtc::sparse_mla_tc_kernel<<<(unsigned)G, mtc::kThreads, mtc::kSmemAlloc, s>>>(a);
     DSA_CHECK_LAUNCH();
     unsigned nx = 0;                                        // combine blocks: candidate rows
-    if (a.sp.mode == mtc::SPLIT_ROW_CTAS) nx = (unsigned)b->total_q;
+    if (a.sp.mode == mtc::SPLIT_ROW_CTAS)                   // one CTA per row (c = 1, no extra): each row
+        nx = (a.sp.c > 1 || a.sp.extra > 0) ? (unsigned)b->total_q : 0u;   // written whole, nothing to merge
     else if (a.sp.mode == mtc::SPLIT_EQUAL) nx = (unsigned)(G - 1);
     if (nx > 0) {
         mtc::combine_kernel<<<dim3(nx, 64), mtc::kCombThreads, 0, s>>>(a);
