@@ -48,3 +48,27 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2"],
                        env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_algorithmic_bytes_follow_the_pages_accounting():
+    # 132 B of index-K per context token, read once per request and full layer,
+    # plus 656 B per selected latent row (at most 2048 per query row) per layer;
+    # the 1M-token decode batch and the tiny case by hand, the 32K batch by sum
+    import bench
+    import synth
+    w = synth.workload("decode1m")
+    idx, kv = bench.workload_bytes(w)[:2]
+    assert idx == 4 * 1_048_576 * 132 and kv == 4 * 2048 * 656
+    assert idx + kv == 559_022_080
+    w = synth.workload("decode32k")
+    idx, kv = bench.workload_bytes(w)[:2]
+    assert w.layers == ["full", "shared", "shared", "shared"]
+    assert idx == 132 * sum(w.seq_len)
+    assert kv == 4 * 656 * sum(min(2048, L) for L in w.seq_len)
+    t = synth.workload("tiny")
+    idx, kv = bench.workload_bytes(t)[:2]
+    assert idx == 132 * t.seq_len[0] and kv == 656 * min(2048, t.seq_len[0]) * len(t.layers)
+    # an MXFP4 index cache: 68 B per token instead of 132
+    m = synth.workload("decode1m")
+    m.index_format = "mxfp4"
+    assert bench.workload_bytes(m)[0] == 4 * 1_048_576 * 68
