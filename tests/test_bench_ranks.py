@@ -72,3 +72,16 @@ def test_algorithmic_bytes_follow_the_pages_accounting():
     m = synth.workload("decode1m")
     m.index_format = "mxfp4"
     assert bench.workload_bytes(m)[0] == 4 * 1_048_576 * 68
+
+
+def test_launch_count_follows_the_sparse_mla_split():
+    # 152 SMs: 1..19 decode rows take one CTA per tile (partials, combine kernel);
+    # 20..38 rows run as clusters of 4 and 39..76 as clusters of 2 (merged in
+    # the cluster); 77..152 rows one CTA each (written whole); 153..1215 rows
+    # equal shares (combine kernel); 1216 and more whole rows per CTA
+    import bench
+    k = bench.kernels_per_call
+    for rows, n in [(1, 2), (4, 2), (19, 2), (20, 1), (38, 1), (39, 1), (64, 1), (76, 1), (77, 1), (100, 1),
+                    (152, 1), (153, 2), (1215, 2), (1216, 1), (8192, 1)]:
+        assert k("sparse_mla_decode", rows, 152) == n, rows
+    assert k("indexer_topk", 64, 152) == 4 and k("index_k_store", 64, 152) == 1
