@@ -675,8 +675,8 @@ def run_reference(args, rank, world):
     total_q = 0
     t_all = 0.0
     steps_done = 0
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        pass
+    # The NumPy oracle has nothing to warm (no compilation, no device caches), so
+    # --warmup adds no passes; at most 3 timed passes keep any --steps within minutes.
     for _ in range(max(1, args.steps if args.steps <= 3 else 3)):
         n, sec = oracle_sample(w, args.ref_budget, mtp_reuse=not args.no_mtp_reuse)
         total_q += sum(w.q_len[:n])
