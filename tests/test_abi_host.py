@@ -255,3 +255,24 @@ def test_binding_rejects_host_tensors_and_wrong_dtypes():
         D.dsa_topk_from_scores(torch.zeros(2, 4096), torch.zeros(2, dtype=torch.int32))
     with pytest.raises(ValueError, match="CUDA tensor"):
         D.dsa_device_status_read(torch.zeros(4, dtype=torch.int32))
+
+
+def test_decode_workspace_follows_the_header_formula(L):
+    # dsa.h gives the decode indexer's scratch for T = B rows on S SMs as
+    #   round_up(4224 T, 256) + 16384 T + (S + B) * 36884 + 12 (B + 1) + 8 S
+    # plus at most 768 bytes of alignment; the workspace call sizes it for
+    # S = 1024, so its answer must fall in that window
+    text = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "dsa.h")).read()
+    per_seg = int(re.search(r"\(S \+ B\) \* (\d+)", text).group(1))
+    n = ctypes.c_size_t(0)
+    for B in (1, 4, 64, 151, 300, 1000):
+        b = _fake_batch(B=B, T=B, max_q=1)
+        assert L.dsa_indexer_topk_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0
+        S = 1024
+        base = (4224 * B + 255) // 256 * 256 + 16384 * B + (S + B) * per_seg + 12 * (B + 1) + 8 * S
+        assert base <= n.value <= base + 768, (B, n.value - base)
+    # and the row limit the header states for 152 SMs follows from it, alignment included
+    fit, nofit = (int(x) for x in re.search(r"\((\d+) rows fit at S = 152, (\d+) do", text).groups())
+    need = lambda B: (4224 * B + 255) // 256 * 256 + 16384 * B + (152 + B) * per_seg + 12 * (B + 1) + 8 * 152
+    assert nofit == fit + 1
+    assert need(fit) + 768 <= 16 << 20 < need(nofit)
