@@ -37,8 +37,10 @@ ties in the top-k go to the lower position, -0.0 equals +0.0, and the selected
 positions are listed in ascending order followed by -1 padding.
 
 Parity pins: every function here is pinned by tests under ``-m "not gpu"``
-(codec vs the format definition and torch's float8 casts, layout constants the
-pages print, the 21/57 schedule, brute-force top-k, sparse == dense attention
+(codec vs the format definition and torch's float8 casts, the E4M3 spacing used
+by the one-ulp bar against the value set torch decodes, the score magnitude D_j
+against the score without cancellation and a term-by-term sum with it, layout
+constants the pages print, the 21/57 schedule, brute-force top-k, sparse == dense attention
 when the context fits in the top-k, closed forms, the MTP seed width and
 draft-step read counts the pages print, brute-force top-k per draft position,
 the 68-byte MXFP4 token, the E2M1 codec against its value table and rounding

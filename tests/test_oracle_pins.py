@@ -83,6 +83,33 @@ def test_quantised_block_within_half_ulp_and_no_saturation():
     assert np.all(err <= O.e4m3_ulp(x / scales[:, None]) / 2 + 1e-300)
 
 
+def _torch_e4m3_values():
+    """Finite non-negative E4M3 values in code order, decoded by torch's cast."""
+    v = torch.arange(0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.all(np.diff(v) > 0)
+    return v
+
+
+def test_e4m3_ulp_is_the_gap_to_the_next_value_of_the_format():
+    # The one-ulp store bar rests on this spacing, so it is pinned to the value
+    # set torch decodes, not to the oracle's own table: at every finite
+    # non-negative code the spacing is the distance to the next code's value
+    # (the largest code, 448, keeps the spacing of its binade), and strictly
+    # between two neighbouring codes it is the gap between them.
+    v = _torch_e4m3_values()
+    gaps = np.append(np.diff(v), v[-1] - v[-2])
+    assert np.array_equal(O.e4m3_ulp(v), gaps)
+    assert np.array_equal(O.e4m3_ulp(-v), gaps)                    # sign-blind
+    rng = np.random.default_rng(31)
+    t = rng.uniform(0.0, 1.0, v.size - 1)
+    inner = v[:-1] + t * (v[1:] - v[:-1])
+    inner = inner[(inner > v[:-1]) & (inner < v[1:])]
+    lo = np.searchsorted(v, inner, side="right") - 1
+    assert np.array_equal(O.e4m3_ulp(inner), v[lo + 1] - v[lo])
+    # a doubled or halved spacing would move these hand values
+    assert O.e4m3_ulp(1.0) == 0.125 and O.e4m3_ulp(448.0) == 32.0 and O.e4m3_ulp(2.0 ** -9) == 2.0 ** -9
+
+
 # ------------------------------------------------------------------ LayerNorm / RoPE
 def test_layer_norm_matches_torch_and_moments():
     rng = np.random.default_rng(4)
@@ -213,6 +240,43 @@ def test_indexer_scores_brute_force():
     assert np.array_equal(O.indexer_scores(qc, qs, 4.0 * w, kc, ks), 4.0 * s)
     D = O.score_magnitude(qc, qs, w, kc, ks)
     assert np.all(D >= np.abs(s) - 1e-12)
+
+
+def test_score_magnitude_equals_the_score_without_cancellation_and_brute_force_with_it():
+    # D_j scales the 1e-3 score bar, so an over-estimate would loosen every
+    # score check.  Without cancellation (every w_m > 0 and every dot >= 0)
+    # D_j is |s_j| exactly; with cancellation it is the plain sum of
+    # |w_m| |<q_m, k_j>| written out term by term.
+    rng = np.random.default_rng(32)
+    L = 11
+    q = np.abs(rng.standard_normal((32, 128)))
+    k = np.abs(rng.standard_normal((L, 128)))
+    w = np.abs(rng.standard_normal(32)) + 0.01
+    qc, qs = O.index_q_quantize(q)
+    kc, ks = O.quantize_blocks_128(k)
+    s = O.indexer_scores(qc, qs, w, kc, ks)
+    assert np.all(s > 0)
+    assert np.array_equal(O.score_magnitude(qc, qs, w, kc, ks), s)
+
+    q = rng.standard_normal((32, 128))
+    k = rng.standard_normal((L, 128))
+    w = rng.standard_normal(32) / math.sqrt(32)
+    qc, qs = O.index_q_quantize(q)
+    kc, ks = O.quantize_blocks_128(k)
+    dec = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    qd = dec(qc) * qs[:, None]
+    kd = dec(kc) * ks[:, None]
+    ref = np.zeros(L)
+    for j in range(L):
+        for m in range(32):
+            dot = 0.0
+            for d in range(128):
+                dot += qd[m, d] * kd[j, d]
+            ref[j] += abs(w[m]) * abs(dot)
+    D = O.score_magnitude(qc, qs, w, kc, ks)
+    assert np.allclose(D, ref, rtol=1e-12, atol=0.0)
+    s = O.indexer_scores(qc, qs, w, kc, ks)
+    assert np.any(D > np.abs(s) * 1.5)                  # this case does cancel
 
 
 # ------------------------------------------------------------------ top-k
