@@ -151,10 +151,23 @@ def _ptr(t):
     return None if t is None else c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _stream(stream, device=None):
+    """The raw cudaStream_t of `stream` (default: the current stream of
+    `device`).  A stream on another device than the call's tensors is refused:
+    the kernels would run there with this device's pointers."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and stream.device != torch.device(device):
+        raise ValueError(f"stream is on {stream.device}, the call's tensors on {device}")
     return c_void_p(stream.cuda_stream)
+
+
+def _call(fn: str, device, *args):
+    """Run C entry point `fn` with `device` current, so that the library's
+    per-device set-up, its device queries and a default stream all refer to the
+    device that holds the call's tensors."""
+    with torch.cuda.device(device):
+        _check(fn, getattr(lib(), fn)(*args))
 
 
 def _need(t: torch.Tensor, dtype, name: str, device=None, numel=None):
@@ -230,7 +243,8 @@ def new_device_status(device) -> torch.Tensor:
 def dsa_device_status_read(dev_status: torch.Tensor, stream=None):
     _need(dev_status, torch.int32, "dev_status", numel=4)
     out = (c_int32 * 4)()
-    code = lib().dsa_device_status_read(_ptr(dev_status), _stream(stream), out)
+    with torch.cuda.device(dev_status.device):
+        code = lib().dsa_device_status_read(_ptr(dev_status), _stream(stream, dev_status.device), out)
     if code not in (0, 7):
         _check("dsa_device_status_read", code)
     return list(out)
@@ -238,7 +252,7 @@ def dsa_device_status_read(dev_status: torch.Tensor, stream=None):
 
 def dsa_device_status_reset(dev_status: torch.Tensor, stream=None):
     _need(dev_status, torch.int32, "dev_status", numel=4)
-    _check("dsa_device_status_reset", lib().dsa_device_status_reset(_ptr(dev_status), _stream(stream)))
+    _call("dsa_device_status_reset", dev_status.device, _ptr(dev_status), _stream(stream, dev_status.device))
 
 
 # ---------------------------------------------------------------------------
@@ -260,9 +274,9 @@ def dsa_index_k_store(k, pos, slot, idxk_cache, *, gamma=None, beta=None, ln_eps
     n = _store_args(k, pos, slot, idxk_cache, gamma, beta, dev_status)
     if num_pages is None:
         num_pages = idxk_cache.numel() // IDXK_PAGE_BYTES
-    _check("dsa_index_k_store", lib().dsa_index_k_store(
+    _call("dsa_index_k_store", k.device,
         _ptr(k), _ptr(pos), _ptr(slot), n, _ptr(gamma), _ptr(beta), ln_eps, rope_base,
-        _ptr(idxk_cache), num_pages, _ptr(dev_status), _stream(stream)))
+        _ptr(idxk_cache), num_pages, _ptr(dev_status), _stream(stream, k.device))
 
 
 def dsa_index_k_store_mxfp4(k, pos, slot, idxk_cache, *, gamma=None, beta=None, ln_eps=1e-6,
@@ -271,9 +285,9 @@ def dsa_index_k_store_mxfp4(k, pos, slot, idxk_cache, *, gamma=None, beta=None, 
     _store_args(k, pos, slot, idxk_cache, gamma, beta, dev_status)
     if num_pages is None:
         num_pages = idxk_cache.numel() // IDXK_MXFP4_PAGE_BYTES
-    _check("dsa_index_k_store_mxfp4", lib().dsa_index_k_store_mxfp4(
+    _call("dsa_index_k_store_mxfp4", k.device,
         _ptr(k), _ptr(pos), _ptr(slot), k.shape[0], _ptr(gamma), _ptr(beta), ln_eps, rope_base,
-        _ptr(idxk_cache), num_pages, _ptr(dev_status), _stream(stream)))
+        _ptr(idxk_cache), num_pages, _ptr(dev_status), _stream(stream, k.device))
 
 
 def dsa_latent_kv_store_fused(kv_c, k_pe, pos, slot, kv_cache, *, kv_gamma=None, rms_eps=1e-6, rope_base=10000.0,
@@ -298,10 +312,10 @@ def dsa_latent_kv_store_fused(kv_c, k_pe, pos, slot, kv_cache, *, kv_gamma=None,
         num_pages = kv_cache.numel() // KV_PAGE_BYTES
     if idx_num_pages is None:
         idx_num_pages = 0 if idxk_cache is None else idxk_cache.numel() // IDXK_PAGE_BYTES
-    _check("dsa_latent_kv_store_fused", lib().dsa_latent_kv_store_fused(
+    _call("dsa_latent_kv_store_fused", kv_c.device,
         _ptr(kv_c), _ptr(k_pe), _ptr(pos), _ptr(slot), kv_c.shape[0], _ptr(kv_gamma), rms_eps, rope_base,
         _ptr(kv_cache), num_pages, _ptr(idx_k), _ptr(idx_gamma), _ptr(idx_beta), ln_eps, _ptr(idxk_cache),
-        idx_num_pages, _ptr(dev_status), _stream(stream)))
+        idx_num_pages, _ptr(dev_status), _stream(stream, kv_c.device))
 
 
 def dsa_latent_kv_store(c, rope, slot, kv_cache, *, num_pages=None, dev_status=None, stream=None):
@@ -314,9 +328,9 @@ def dsa_latent_kv_store(c, rope, slot, kv_cache, *, num_pages=None, dev_status=N
     _opt(dev_status, torch.int32, "dev_status", dev, 4)
     if num_pages is None:
         num_pages = kv_cache.numel() // KV_PAGE_BYTES
-    _check("dsa_latent_kv_store", lib().dsa_latent_kv_store(
+    _call("dsa_latent_kv_store", c.device,
         _ptr(c), _ptr(rope), _ptr(slot), c.shape[0], _ptr(kv_cache), num_pages, _ptr(dev_status),
-        _stream(stream)))
+        _stream(stream, c.device))
 
 
 def _indexer_args(q, w, idxk_cache, batch: Batch) -> int:
@@ -351,10 +365,10 @@ def dsa_indexer_topk(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=N
     _opt(topk_scores, torch.float32, "topk_scores", q.device, T * TOPK)
     _opt(dev_status, torch.int32, "dev_status", q.device, 4)
     ws = _ws(ws, dsa_indexer_topk_workspace_size(batch) if ws is None else 0, q.device)
-    _check("dsa_indexer_topk", lib().dsa_indexer_topk(
+    _call("dsa_indexer_topk", q.device,
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
         None if share is None else share.handle, layer_id, _ptr(ws), ws.numel(), _ptr(dev_status),
-        _stream(stream)))
+        _stream(stream, q.device))
     return topk
 
 
@@ -368,10 +382,10 @@ def dsa_indexer_topk_mxfp4(q, w, idxk_cache, batch: Batch, *, topk=None, topk_sc
     _opt(topk_scores, torch.float32, "topk_scores", q.device, T * TOPK)
     _opt(dev_status, torch.int32, "dev_status", q.device, 4)
     ws = _ws(ws, dsa_indexer_topk_workspace_size(batch) if ws is None else 0, q.device)
-    _check("dsa_indexer_topk_mxfp4", lib().dsa_indexer_topk_mxfp4(
+    _call("dsa_indexer_topk_mxfp4", q.device,
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
         None if share is None else share.handle, layer_id, _ptr(ws), ws.numel(), _ptr(dev_status),
-        _stream(stream)))
+        _stream(stream, q.device))
     return topk
 
 
@@ -384,9 +398,9 @@ def dsa_indexer_topk_noalloc(q, w, idxk_cache, batch: Batch, *, topk=None, topk_
     _need(topk, torch.int32, "topk", q.device, T * TOPK)
     _opt(topk_scores, torch.float32, "topk_scores", q.device, T * TOPK)
     _opt(dev_status, torch.int32, "dev_status", q.device, 4)
-    _check("dsa_indexer_topk_noalloc", lib().dsa_indexer_topk_noalloc(
+    _call("dsa_indexer_topk_noalloc", q.device,
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(topk), _ptr(topk_scores),
-        None if share is None else share.handle, layer_id, _ptr(dev_status), _stream(stream)))
+        None if share is None else share.handle, layer_id, _ptr(dev_status), _stream(stream, q.device))
     return topk
 
 
@@ -400,9 +414,9 @@ def dsa_indexer_scores(q, w, idxk_cache, batch: Batch, *, ld=None, scores=None, 
     _need(scores, torch.float32, "scores", q.device, T * ld)
     _opt(dev_status, torch.int32, "dev_status", q.device, 4)
     ws = _ws(ws, _ws_size("dsa_indexer_scores_workspace_size", batch) if ws is None else 0, q.device)
-    _check("dsa_indexer_scores", lib().dsa_indexer_scores(
+    _call("dsa_indexer_scores", q.device,
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(scores), ld, _ptr(ws), ws.numel(),
-        _ptr(dev_status), _stream(stream)))
+        _ptr(dev_status), _stream(stream, q.device))
     return scores
 
 
@@ -420,8 +434,8 @@ def dsa_topk_from_scores(scores, valid_len, *, max_len=None, topk=None, stream=N
     _check("dsa_topk_from_scores_workspace_size",
            lib().dsa_topk_from_scores_workspace_size(rows, max_len, ctypes.byref(n)))
     ws = workspace(n.value, scores.device)
-    _check("dsa_topk_from_scores", lib().dsa_topk_from_scores(
-        _ptr(scores), ld, _ptr(valid_len), rows, max_len, _ptr(topk), _ptr(ws), ws.numel(), _stream(stream)))
+    _call("dsa_topk_from_scores", scores.device,
+        _ptr(scores), ld, _ptr(valid_len), rows, max_len, _ptr(topk), _ptr(ws), ws.numel(), _stream(stream, scores.device))
     return topk
 
 
@@ -444,10 +458,10 @@ def _mla(fn, q, topk, kv_cache, batch, softmax_scale, out, out_dtype, lse, share
     _opt(lse, torch.float32, "lse", dev, T * MLA_HEADS)
     _opt(dev_status, torch.int32, "dev_status", dev, 4)
     ws = _ws(ws, dsa_sparse_mla_workspace_size(batch) if ws is None else 0, dev)
-    _check(fn, getattr(lib(), fn)(
-        _ptr(q), _ptr(topk), None if share is None else share.handle, _ptr(kv_cache), batch.ref(),
-        softmax_scale, _ptr(out), out_dtype, _ptr(lse), _ptr(ws), ws.numel(), _ptr(dev_status),
-        _stream(stream)))
+    _call(fn, dev,
+          _ptr(q), _ptr(topk), None if share is None else share.handle, _ptr(kv_cache), batch.ref(),
+          softmax_scale, _ptr(out), out_dtype, _ptr(lse), _ptr(ws), ws.numel(), _ptr(dev_status),
+          _stream(stream, dev))
     return out
 
 
@@ -578,8 +592,8 @@ def dsa_mtp_seed_write(topk, *, src_row=None, n=None, seed=None, width=None, dev
         seed = torch.empty((n, width), dtype=torch.int32, device=topk.device)
     _need(seed, torch.int32, "seed", topk.device, n * width)
     _opt(dev_status, torch.int32, "dev_status", topk.device, 4)
-    _check("dsa_mtp_seed_write", lib().dsa_mtp_seed_write(
-        _ptr(topk), topk.shape[0], _ptr(src_row), n, _ptr(seed), width, _ptr(dev_status), _stream(stream)))
+    _call("dsa_mtp_seed_write", topk.device,
+        _ptr(topk), topk.shape[0], _ptr(src_row), n, _ptr(seed), width, _ptr(dev_status), _stream(stream, topk.device))
     return seed
 
 

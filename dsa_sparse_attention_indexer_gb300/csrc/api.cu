@@ -3,9 +3,47 @@
 // and the share handle that carries a full layer's indices to the shared
 // layers after it ("GLM-5.3 推理全链路(十一)", 一次前向里 topk 只算一遍).
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <vector>
 
 #include "dsa_internal.cuh"
+
+namespace dsa {
+
+dsa_status ensure_smem_limit(const void* func, int bytes) {
+    struct Applied {
+        const void* func;
+        int device;
+        int bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Applied> applied;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Applied& a : applied)
+        if (a.func == func && a.device == dev && a.bytes >= bytes) return DSA_OK;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    applied.push_back(Applied{func, dev, bytes});
+    return DSA_OK;
+}
+
+void* tensor_map_encode_fn() {
+    static void* const fn = [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<void*>(nullptr);
+        return f;
+    }();
+    return fn;
+}
+
+}  // namespace dsa
 
 struct dsa_topk_share {
     const int32_t* topk;

@@ -116,4 +116,14 @@ __device__ __forceinline__ int row_request(const int32_t* q_start, int B, int64_
 namespace dsa {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Raises kernel `func`'s dynamic shared-memory limit to `bytes` on the current
+// device.  The limit is a per-device setting, so it is applied once per
+// (kernel, device); the record of what was applied is guarded by a lock, so
+// host threads may call concurrently.
+dsa_status ensure_smem_limit(const void* func, int bytes);
+
+// The driver's cuTensorMapEncodeTiled (CUDA 12.0 ABI), looked up once per
+// process (thread-safe); NULL if the driver does not provide it.
+void* tensor_map_encode_fn();
 }  // namespace dsa

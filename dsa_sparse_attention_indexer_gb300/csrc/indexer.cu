@@ -121,13 +121,8 @@ extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint
         rs = launch_indexer_rows(q8, wq, idxk_cache, b, sc, ld, true, false, plan, device_sm_count(), dev_status, s);
         if (rs != DSA_OK) return rs;
         BatchDev bd = to_dev(b);
-        static bool attr = false;
-        if (!attr) {
-            if (cudaFuncSetAttribute(indexer_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem) !=
-                cudaSuccess)
-                return DSA_ERR_CUDA;
-            attr = true;
-        }
+        if (ensure_smem_limit(reinterpret_cast<const void*>(&indexer_select_kernel), kSelSmem) != DSA_OK)
+            return DSA_ERR_CUDA;
         indexer_select_kernel<<<(unsigned)b->total_q, kSelThreads, kSelSmem, s>>>(sc, ld, bd, topk, topk_scores);
         DSA_CHECK_LAUNCH();
     }

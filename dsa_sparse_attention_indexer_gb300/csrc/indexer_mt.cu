@@ -483,21 +483,13 @@ struct QMapCache {
 bool make_index_tmap(const uint8_t* cache, int64_t num_pages, bool mx, CUtensorMap* out);
 
 static bool make_q8_tmap(const uint8_t* q8, int64_t total_q, CUtensorMap* out) {
-    static QMapCache mc;
+    static thread_local QMapCache mc;                  // per host thread: no lock needed
     if (mc.ptr == q8 && mc.rows == total_q) {
         *out = mc.map;
         return true;
     }
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    if (!encode) {
-        cudaDriverEntryPointQueryResult q;
-        void* fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !fn)
-            return false;
-        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
+    const auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+    if (!encode) return false;
     // q8 viewed as a [T * 32, 128] byte matrix (row = one head of one query row);
     // a box is one row block: 256 rows, rows past T * 32 read as zeros.
     cuuint64_t dims[2] = {128, (cuuint64_t)total_q * 32};
@@ -554,13 +546,8 @@ dsa_status launch_indexer_rows(const uint8_t* q8, const float* wq, const uint8_t
     CUtensorMap kmap, qmap;
     if (!make_index_tmap(cache, b->num_pages, false, &kmap)) return DSA_ERR_CUDA;
     if (!make_q8_tmap(q8, b->total_q, &qmap)) return DSA_ERR_CUDA;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(imt::score_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 imt::kSmemAlloc) != cudaSuccess)
-            return DSA_ERR_CUDA;
-        attr = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(&imt::score_rows_kernel), imt::kSmemAlloc) != DSA_OK)
+        return DSA_ERR_CUDA;
     BatchDev bd = to_dev(b);
     imt::MtPlan p = carve_mt_plan(plan_ws, b->batch, b->total_q);
     imt::plan_kernel<<<1, 1024, 0, s>>>(bd, skip_short ? 1 : 0, full_rows ? 1 : 0, p);

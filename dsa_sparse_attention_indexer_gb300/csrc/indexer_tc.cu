@@ -1116,25 +1116,18 @@ struct MapCache {
 };
 }  // namespace
 
+// The last map encoded by this host thread for each cache format: a map holds
+// only the address and the extents, so it is valid on whichever device owns
+// the address, and a per-thread cache needs no lock.
 bool make_index_tmap(const uint8_t* cache, int64_t num_pages, bool mx, CUtensorMap* out) {
-    static MapCache mcs[2];
+    static thread_local MapCache mcs[2];
     MapCache& mc = mcs[mx ? 1 : 0];
     if (mc.ptr == cache && mc.pages == num_pages) {
         *out = mc.map;
         return true;
     }
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    if (!encode) {
-        cudaDriverEntryPointQueryResult q;
-        void* fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !fn)
-            return false;
-        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    // The cache viewed as a [num_pages * 66, 128] byte matrix: page p's 64
-    // payload rows are rows 66p .. 66p+63 (its scales fill rows 66p+64, +65).
+    const auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+    if (!encode) return false;
     // FP8: the cache viewed as a [num_pages * 66, 128] byte matrix: page p's 64
     // payload rows are rows 66p .. 66p+63 (its scales fill rows 66p+64, +65).
     // MXFP4: a [num_pages * 68, 128] matrix of 4-bit values (64-byte rows), page
@@ -1198,17 +1191,10 @@ dsa_status launch_indexer_tc(const void* q, const float* w, uint8_t* q8, float* 
                              int G, int32_t* st, cudaStream_t s, bool mx) {
     CUtensorMap map;
     if (!make_index_tmap(cache, b->num_pages, mx, &map)) return DSA_ERR_CUDA;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(itc::score_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 itc::kSmemAlloc) != cudaSuccess ||
-            cudaFuncSetAttribute(itc::score_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 itc::kSmemAlloc) != cudaSuccess ||
-            cudaFuncSetAttribute(itc::merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 itc::kMergeSmem) != cudaSuccess)
-            return DSA_ERR_CUDA;
-        attr = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(&itc::score_topk_kernel<false>), itc::kSmemAlloc) != DSA_OK ||
+        ensure_smem_limit(reinterpret_cast<const void*>(&itc::score_topk_kernel<true>), itc::kSmemAlloc) != DSA_OK ||
+        ensure_smem_limit(reinterpret_cast<const void*>(&itc::merge_kernel), itc::kMergeSmem) != DSA_OK)
+        return DSA_ERR_CUDA;
     BatchDev bd = to_dev(b);
     Plan p = carve_plan(plan_ws, b->batch, G);
     p.hist = hist;

@@ -963,13 +963,8 @@ size_t mla_tc_ws_bytes(int64_t total_q, int G) {
 dsa_status launch_sparse_mla_tc(const void* q, const int32_t* topk, const uint8_t* kv, const dsa_batch* b,
                                 float softmax_scale, void* out, int32_t out_dtype, float* lse, void* ws,
                                 int G, int32_t* st, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(mtc::sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 mtc::kSmemAlloc) != cudaSuccess)
-            return DSA_ERR_CUDA;
-        attr = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(&mtc::sparse_mla_tc_kernel), mtc::kSmemAlloc) != DSA_OK)
+        return DSA_ERR_CUDA;
     mtc::Args a;
     a.q = static_cast<const uint16_t*>(q);
     a.topk = topk;

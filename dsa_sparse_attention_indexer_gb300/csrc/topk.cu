@@ -40,13 +40,8 @@ extern "C" dsa_status dsa_topk_from_scores(const float* scores, int64_t ld, cons
     if (rows == 0) return DSA_OK;
     if (!scores || !valid_len || !topk) return DSA_ERR_INVALID_ARGUMENT;
     if (max_len > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(topk_from_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem) !=
-            cudaSuccess)
-            return DSA_ERR_CUDA;
-        attr = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(&topk_from_scores_kernel), kSelSmem) != DSA_OK)
+        return DSA_ERR_CUDA;
     topk_from_scores_kernel<<<rows, kSelThreads, kSelSmem, as_stream(stream)>>>(scores, ld, valid_len, max_len, topk);
     DSA_CHECK_LAUNCH();
     return DSA_OK;

@@ -29,6 +29,12 @@
  *     optional device status block `dev_status` (DSA_DEVICE_STATUS_WORDS int32,
  *     device; NULL = do not record).  Read it with dsa_device_status_read().
  *   - No call throws, exits or traps.
+ *   - A call runs on the CUDA device that is current on the calling host
+ *     thread; every buffer it gets must live on that device.  The library's
+ *     one-time set-up (kernel shared-memory limits, TMA descriptor encoding)
+ *     is kept per device and per host thread, so several host threads and
+ *     several devices may use the library at once.  Calls that share a
+ *     workspace or an output buffer must still be ordered by the caller.
  *   - "bf16" buffers hold IEEE bfloat16 bit patterns (uint16).
  *
  * Token positions: request r holds seq_len[r] cached tokens, INCLUDING its
