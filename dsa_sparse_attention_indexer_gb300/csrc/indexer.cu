@@ -8,11 +8,6 @@
 
 namespace dsa {
 
-__global__ void __launch_bounds__(256)
-index_scores_ref_kernel(const uint8_t* __restrict__ q8, const float* __restrict__ wq,
-                        const uint8_t* __restrict__ cache, BatchDev b, float* __restrict__ scores,
-                        int64_t ld, int32_t* __restrict__ st);
-
 // One CTA per query row: select over the row's p + 1 visible scores.
 __global__ void __launch_bounds__(kSelThreads)
 indexer_select_kernel(const float* __restrict__ scores, int64_t ld, BatchDev b,

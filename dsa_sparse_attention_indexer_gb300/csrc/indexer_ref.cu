@@ -1,12 +1,9 @@
-// Lightning-indexer building blocks that materialise full score rows:
-//   * index-Q quantisation (FP8 E4M3 + one ue8m0 scale per head, folded into
-//     the head weight: w'_m = w_m * 2^e_m, exact) - "GLM-5.3 推理全链路(十一)",
-//     读取路径里的两条"非缓存"字节: Q is [tokens, 32, 128] FP8 plus a scale
-//     per 128 dims;
-//   * a CUDA-core scorer s_j = sk_j * sum_m w'_m ReLU(<q8_m, k8_j>) that writes
-//     every score ("vLLM 推理链路概览", DSA Indexer), used by the
-//     dsa_indexer_scores parity hook.  ReLU commutes with the positive scales,
-//     so this equals sum_m w_m ReLU(<q_m, k_j>) on the dequantised values.
+// Index-Q quantisation for the multi-token indexer and the dsa_indexer_scores
+// hook: FP8 E4M3 with one ue8m0 scale per head, folded into the head weight
+// (w'_m = w_m * 2^e_m, exact) - "GLM-5.3 推理全链路(十一)", 读取路径里的两条
+// "非缓存"字节: Q is [tokens, 32, 128] FP8 plus a scale per 128 dims.  The
+// scores themselves come from the tensor-core kernels (indexer_tc.cu for
+// decode batches, indexer_mt.cu for the others and for dsa_indexer_scores).
 #include "dsa_internal.cuh"
 #include "indexer_common.cuh"
 #include "indexer_tc.cuh"

@@ -7,21 +7,28 @@
 // heads] in FP8: the index-K tile (128 tokens = two 64-token pages) is the A
 // operand (M = 128), the request's quantised query the B operand (N = 32).
 //
-//  1. plan kernel: cuts the concatenated tiles of all requests that need
-//     scoring (context > 2048) into one contiguous, equal share per CTA; a
-//     share is split at request boundaries into segments.
-//  2. score kernel (persistent, one CTA per SM, warp-specialised):
-//       warp 0     TMA producer: per tile, two 8 KB payload boxes through a
-//                  128-byte-swizzled tensor map + the two 256-B scale rows,
-//                  into a 4-stage ring;
-//       warp 1     tcgen05.mma issuer (kind::f8f6f4, M=128, N=32, K=4x32) into
-//                  a double-buffered TMEM accumulator;
-//       warps 2-5  epilogue: tcgen05.ld of a token's 32 head dots, ReLU, head-
-//                  weighted sum, times the token's key scale; keys above the
-//                  running threshold are appended to a shared-memory candidate
-//                  buffer, which is compacted to its exact top-2048 (radix
-//                  select) whenever it fills; the threshold rises to the
-//                  2048th key.  A segment ends with its exact local top-2048.
+//  1. prep kernel: block 0 cuts the concatenated tiles of all requests that
+//     need scoring (context > 2048) into one contiguous, equal share per CTA
+//     (a share is split at request boundaries into segments); the other
+//     blocks quantise the index queries, a warp per head, and clear the row
+//     histograms.
+//  2. score kernel (persistent, one CTA per SM, warp-specialised, 11 warps):
+//       warps 0, 10  TMA producers, taking alternate tiles: per tile, two 8 KB
+//                    payload boxes through a 128-byte-swizzled tensor map into
+//                    a 9-stage ring the two warps share, and the two 256-B
+//                    key-scale rows by bulk copy into a ring of their own;
+//       warp 1       tcgen05.mma issuer (kind::f8f6f4, M=128, N=32, K=4x32)
+//                    into one of 16 TMEM accumulators, so the tensor pipe runs
+//                    up to 16 tiles ahead of the epilogue;
+//       warps 2-9    epilogue, two groups of four warps taking alternate
+//                    tiles: tcgen05.ld of a token's 32 head dots, ReLU, head-
+//                    weighted sum, times the token's key scale; keys above the
+//                    running threshold are appended to a shared-memory
+//                    candidate buffer (4608 entries with a 4096-bin histogram
+//                    of 16-bit counts), compacted by radix select whenever it
+//                    fills; the threshold rises to the 2048th key.  At a
+//                    segment end the buffer and its histogram go to the
+//                    workspace.
 //     No full score row is ever written to memory.
 //  3. merge: one block per segment keeps the candidates at or above the bin
 //     of its row's 2048th key (the row histogram of all segment candidates
