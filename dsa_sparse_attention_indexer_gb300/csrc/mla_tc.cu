@@ -44,14 +44,20 @@
 //               rescaled only when a head's max grows by more than 2^8), P
 //               written as fp16 P^T rows.  At a piece start they convert the
 //               row's Q to fp16 while the loaders build the slot list and
-//               gather the first tile.  Thread 0 also issues the MMAs and
+//               gather the first tile; the row is first multiplied by the
+//               power of two that puts its largest |q| in [2^14, 2^15)
+//               (exact), and the inverse is folded into the softmax scale, so
+//               every finite q is inside fp16's range.  Thread 0 also issues the MMAs and
 //               warp 0 owns the TMEM allocation.
 //   warps 8-15  loaders: build the row piece's list of cache slots and gather
 //               each tile's 656-B latent rows into
 //               registers one tile ahead (all 18 16-byte pieces of a lane in
 //               flight at once), then dequantise group by group into the
 //               128-byte-swizzled fp16 tile (c * scale is exact in fp16 for
-//               scales in [2^-15, 2^7]; the RoPE dims convert from bf16).
+//               scales in [2^-15, 2^7]; the RoPE dims convert from bf16, exact
+//               for |r| in [2^-17, 2^16)).  A scale outside that range, or a
+//               RoPE value of 2^16 or more (clamped, so the scores stay
+//               finite), is recorded as DSA_DEVERR_FP16_RANGE.
 // Every wait is time-bounded; a timeout is recorded and the CTA winds down.
 #include <type_traits>
 
@@ -115,6 +121,7 @@ struct Misc {
     uint32_t tmem_base;
     int32_t abort;
     int32_t scratch[8];
+    uint32_t qmax[kSoftWarps];  // per softmax warp: largest bf16 magnitude of the row's q
     int32_t ntok[kMaxPieces];
 };
 static_assert(sizeof(Misc) <= 512, "misc block");
@@ -229,6 +236,23 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_h2(uint32_t two, __half2 sc2) 
 }
 __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t w) {
     return pack_h2(bf16_bits_to_f32(w & 0xffffu), bf16_bits_to_f32(w >> 16));
+}
+// Two bf16 key RoPE values -> two fp16.  A magnitude of 2^16 or more (inf and
+// NaN included) does not fit fp16: it is clamped to +-65280 (the largest bf16
+// below fp16's maximum), so the scores stay finite, and bad is set.  Every
+// other bf16 value converts exactly, except those below 2^-17, whose error
+// (under 2^-25 absolute) is far below the attention tolerance.
+__device__ __forceinline__ uint32_t rope_bf16x2_to_h2(uint32_t w, uint32_t& bad) {
+    const uint32_t over = __vcmpgeu2(w & 0x7fff7fffu, 0x47804780u);   // per half: |x| >= 2^16
+    bad |= over;
+    return bf16x2_to_h2((w & ~over) | (over & ((w & 0x80008000u) | 0x477f477fu)));
+}
+// A query pair multiplied by the row's power of two `sc` (exact in fp32) ->
+// two fp16.  After that scaling no |value| reaches 2^15, so nothing
+// overflows; values more than 2^39 below the row's largest are rounded to
+// fp16's subnormal grid (absolute error under 2^-25 after the scaling).
+__device__ __forceinline__ uint32_t bf16x2_scaled_to_h2(uint32_t w, float sc) {
+    return pack_h2(bf16_bits_to_f32(w & 0xffffu) * sc, bf16_bits_to_f32(w >> 16) * sc);
 }
 
 // Reduce 32 values across the 32 lanes of a warp: afterwards lane l holds the
@@ -428,14 +452,14 @@ sparse_mla_tc_kernel(Args a) {
             //      latent groups 0..3 (free once that tile's P.V of block g is done)
             for (int t = 0; t < ntiles && ok; ++t, ++gt) {
                 const uint32_t ph = (uint32_t)((gt - 1) & 1);
-                uint32_t bad_scale = 0;
+                uint32_t bad_scale = 0;                    // a latent scale or a RoPE value fp16 cannot hold
                 if (gt > 0 && !(ok = wait_ab(&bars[B_SFULL], ph, abort_flag))) break;
 #pragma unroll
                 for (int i = 0; i < 3; ++i) {
                     const int tk = lw * kTokPerLoadWarp + 4 * i + (lane >> 3);
                     *reinterpret_cast<uint4*>(smem + kOffKV + 8 * kBlk + tk * 128 + ((c8 ^ (tk & 7)) * 16)) =
-                        make_uint4(bf16x2_to_h2(rope[i].x), bf16x2_to_h2(rope[i].y), bf16x2_to_h2(rope[i].z),
-                                   bf16x2_to_h2(rope[i].w));
+                        make_uint4(rope_bf16x2_to_h2(rope[i].x, bad_scale), rope_bf16x2_to_h2(rope[i].y, bad_scale),
+                                   rope_bf16x2_to_h2(rope[i].z, bad_scale), rope_bf16x2_to_h2(rope[i].w, bad_scale));
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -527,27 +551,51 @@ sparse_mla_tc_kernel(Args a) {
             // ---- Q of the row -> fp16, K-major, 128-byte swizzle.  Every S^T MMA of the
             //      previous piece has completed (each was waited for), so Q is free; the
             //      loaders meanwhile build the slot list and gather the first tile.
+            //      The row is first scaled by the power of two 2^kq that puts its largest |q|
+            //      in [2^14, 2^15): exact, and it keeps every q value inside fp16's range
+            //      whatever the row's magnitude; 2^-kq is folded into the softmax scale.
+            float row_sl2 = a.scale_log2;
             {
-                const uint16_t* qrow = a.q + row * (64 * 576);
+                static_assert(64 * 72 == 18 * kSoftThreads, "18 16-byte pieces of q per thread");
+                const uint4* qrow = reinterpret_cast<const uint4*>(a.q + row * (64 * 576));
+                uint32_t mx = 0;                           // two bf16 magnitudes, compared as integers
 #pragma unroll 1
-                for (int c0 = tid; c0 < 64 * 72; c0 += 6 * kSoftThreads) {   // 18 pieces per thread, 6 in flight
+                for (int u0 = 0; u0 < 18; u0 += 6) {       // pass 1: the row's largest |q|, 6 loads in flight
                     uint4 qv[6];
 #pragma unroll
-                    for (int u = 0; u < 6; ++u) {
-                        const int c = c0 + u * kSoftThreads;
-                        qv[u] = c < 64 * 72 ? __ldg(reinterpret_cast<const uint4*>(qrow) + c) : make_uint4(0, 0, 0, 0);
-                    }
+                    for (int u = 0; u < 6; ++u) qv[u] = __ldg(qrow + tid + (u0 + u) * kSoftThreads);
+#pragma unroll
+                    for (int u = 0; u < 6; ++u)
+                        mx = __vmaxu2(mx, __vmaxu2(__vmaxu2(qv[u].x & 0x7fff7fffu, qv[u].y & 0x7fff7fffu),
+                                                   __vmaxu2(qv[u].z & 0x7fff7fffu, qv[u].w & 0x7fff7fffu)));
+                }
+                mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
+                if (lane == 0) misc->qmax[warp] = mx;
+                soft_sync();
+                uint32_t amax = 0;
+#pragma unroll
+                for (int v = 0; v < kSoftWarps; ++v) amax = max(amax, misc->qmax[v]);
+                // exponent of the largest |q| (bf16 bits: 8 exponent bits above 7 mantissa bits)
+                const int eq = amax == 0 ? 14 : (int)(amax >> 7) - 127;
+                const int kq = min(126, max(-126, 14 - eq));
+                const float sc = __int_as_float((127 + kq) << 23);
+                row_sl2 = a.scale_log2 * __int_as_float((127 - kq) << 23);
+#pragma unroll 1
+                for (int u0 = 0; u0 < 18; u0 += 6) {       // pass 2 (from L2): scale, convert, store
+                    uint4 qv[6];
+#pragma unroll
+                    for (int u = 0; u < 6; ++u) qv[u] = __ldg(qrow + tid + (u0 + u) * kSoftThreads);
 #pragma unroll
                     for (int u = 0; u < 6; ++u) {
-                        const int c = c0 + u * kSoftThreads;
-                        if (c >= 64 * 72) continue;
+                        const int c = tid + (u0 + u) * kSoftThreads;
                         const int h = c / 72, cq = c % 72;
                         const int blk = cq >> 3, ch = cq & 7;
                         *reinterpret_cast<uint4*>(smem + kOffQ + blk * 8192 + h * 128 + ((ch ^ (h & 7)) * 16)) =
-                            make_uint4(bf16x2_to_h2(qv[u].x), bf16x2_to_h2(qv[u].y), bf16x2_to_h2(qv[u].z),
-                                       bf16x2_to_h2(qv[u].w));
+                            make_uint4(bf16x2_scaled_to_h2(qv[u].x, sc), bf16x2_scaled_to_h2(qv[u].y, sc),
+                                       bf16x2_scaled_to_h2(qv[u].z, sc), bf16x2_scaled_to_h2(qv[u].w, sc));
                     }
                 }
+                if (tid == 0 && amax >= 0x7f80u) record_error(a.st, DSA_DEVERR_FP16_RANGE, (int64_t)row);   // inf / NaN in q
                 fence_proxy_async_smem();
             }
             int ok = mbar_wait(&bars[B_QFULL], (uint32_t)(k & 1)) ? 1 : 0;
@@ -580,7 +628,7 @@ sparse_mla_tc_kernel(Args a) {
                     tmem_ld_32x32b_x32(lane_addr + kColS + hh * 32, u);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) v[h] = valid ? __uint_as_float(u[h]) * a.scale_log2 : -INFINITY;
+                    for (int h = 0; h < 32; ++h) v[h] = valid ? __uint_as_float(u[h]) * row_sl2 : -INFINITY;
                 };
                 float v[32];
                 tc_fence_after();

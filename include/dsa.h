@@ -95,8 +95,12 @@ typedef int32_t dsa_status;
 #define DSA_DEVERR_PAGE_RANGE    2   /* page_table entry outside [0, num_pages)    */
 #define DSA_DEVERR_INDEX_RANGE   4   /* top-k index >= seq_len of its request      */
 #define DSA_DEVERR_TIMEOUT       8   /* a bounded wait inside a kernel gave up     */
-#define DSA_DEVERR_FP16_RANGE   16   /* latent scale outside [2^-15, 2^7]: the
-                                        sparse-MLA fp16 operands are inexact       */
+#define DSA_DEVERR_FP16_RANGE   16   /* sparse MLA computes in fp16: a latent
+                                        scale outside [2^-15, 2^7], a key RoPE
+                                        value with |r| >= 2^16 (clamped) or an
+                                        inf / NaN in q makes an operand inexact.
+                                        q itself is scaled per row by a power of
+                                        two, so any finite q is in range        */
 
 /* Output dtypes of the sparse MLA calls. */
 #define DSA_DTYPE_BF16 0

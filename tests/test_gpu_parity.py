@@ -481,6 +481,54 @@ def test_sparse_mla_records_bad_page_without_fault(mla_case):
     assert torch.isfinite(out).all()
 
 
+def test_sparse_mla_query_rows_of_any_magnitude_and_rope_overflow(mla_case):
+    # The kernel computes in fp16; every query row is first scaled by a power of
+    # two, so rows far outside fp16's range (x 2^20) or deep in its subnormals
+    # (x 2^-20) still match the oracle.  A key RoPE value of 2^16 or more does
+    # not fit fp16: it is recorded, and the output stays finite.
+    c = mla_case
+    w = c["w"]
+    ocache = c["cache"].cpu().numpy().reshape(w.num_pages, -1)
+    pt = c["batch"].page_table.cpu().numpy()
+    qs = c["batch"].q_start.cpu().numpy()
+    q = c["q"].clone()
+    rows = {3: 2.0 ** 20, 5: 2.0 ** -20, 11: 2.0 ** 16}
+    for i, f in rows.items():
+        q[i] = (q[i].double() * f).to(torch.bfloat16)      # exact: a power of two
+    assert q[3].float().abs().max() > 65504.0
+    st = D.new_device_status(DEV)
+    lse = torch.empty(w.total_q, 64, device=DEV)
+    out = D.dsa_sparse_mla_decode(q, c["topk"], c["cache"], c["batch"], out_dtype=D.DTYPE_F32, lse=lse,
+                                  dev_status=st)
+    assert D.dsa_device_status_read(st)[0] == 0
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    topk = c["topk"].cpu().numpy()
+    for i in range(w.total_q):
+        r = int(np.searchsorted(qs, i, side="right") - 1)
+        p = w.seq_len[r] - w.q_len[r] + (i - qs[r])
+        if i in rows:
+            krows = O.latent_cache_read_rows(ocache, pt[r], np.maximum(topk[i], 0))
+            ref, ref_lse = O.sparse_mla(f64(q[i]), topk[i], krows, p)
+        else:
+            ref, ref_lse = c["out"][i], c["lse"][i]
+        check_attention(out[i], ref, what=f"scaled q row {i}")
+        assert np.allclose(lse[i], ref_lse, rtol=1e-5, atol=1e-4)
+    # one selected token of row 3 gets a RoPE value beyond fp16's range
+    j = int(topk[3][topk[3] >= 0][7])
+    bad_cache = ocache.copy()
+    r3 = int(np.searchsorted(qs, 3, side="right") - 1)
+    page, slot = pt[r3][j // 64], j % 64
+    off = slot * O.LATENT_TOKEN_BYTES + 512 + 16 + 2 * 5
+    big = torch.tensor([70000.0]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint8)
+    bad_cache[page, off:off + 2] = big
+    st = D.new_device_status(DEV)
+    out = D.dsa_sparse_mla_decode(c["q"], c["topk"], torch.from_numpy(bad_cache.reshape(-1)).to(DEV), c["batch"],
+                                  out_dtype=D.DTYPE_F32, dev_status=st)
+    res = D.dsa_device_status_read(st)
+    assert res[0] & D.DEVERR_FP16_RANGE
+    assert torch.isfinite(out).all()
+
+
 # ------------------------------------------------------------------ fused latent store
 @pytest.mark.parametrize("with_index", [False, True])
 def test_latent_store_fused_matches_oracle(with_index):
