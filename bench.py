@@ -50,7 +50,33 @@ NCU_TRAFFIC = {
     ("decode1m", "indexer_topk"): (567.4e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
                                    "aca40d28e5cd4b96"),
 }
-FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s), used only if the
+                             # FP8 GEMM measurement below cannot run
+
+
+def measure_fp8_tflops(device, n=8192, reps=10):
+    """Dense FP8 (E4M3 x E4M3 -> bf16) tensor throughput of this GPU: the
+    library GEMM (torch._scaled_mm) on n^3, best of `reps`, CUDA events.  The
+    denominator for the indexer's FP8 contraction; None if unavailable."""
+    try:
+        a = torch.randn(n, n, device=device).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=device).to(torch.float8_e4m3fn).t()     # column-major second operand
+        one = torch.ones((), device=device)
+        for _ in range(3):
+            torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        torch.cuda.synchronize()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:
+        return None
 
 
 def file_sha(path):
@@ -170,6 +196,27 @@ def workload_bytes(w, mtp_reuse=True):
     return n_full * idx, kv * len(w.layers), idx, kv
 
 
+def _timer(timers, stream, external=False):
+    """t(name, fn): runs fn on `stream`, bracketed by timing events kept in
+    timers[name] when timers is given.  external=True makes the events
+    recordable inside a CUDA graph capture, so a captured step carries its own
+    per-call timestamps."""
+
+    def t(name, fn):
+        if timers is None:
+            fn()
+            return
+        kw = {"enable_timing": True}
+        if external:
+            kw["external"] = True
+        e0, e1 = torch.cuda.Event(**kw), torch.cuda.Event(**kw)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        timers.setdefault(name, []).append((e0, e1))
+    return t
+
+
 class Step:
     """All device buffers of one step and the calls that make it up."""
 
@@ -187,22 +234,12 @@ class Step:
         self.full = [t == "full" for t in w.layers]
         self.launches_per_step = 0
 
-    def run(self, stream, timers=None, before_layer=None, after_layer=None):
+    def run(self, stream, timers=None, before_layer=None, after_layer=None, external=False):
         """One step on `stream`.  before_layer(l) / after_layer(l), when given, run
         just before layer l's first call and just after its sparse MLA (the e2e
         graph hangs its per-layer copies there)."""
         D, gw = self.D, self.gw
-
-        def t(name, fn):
-            if timers is None:
-                fn()
-                return
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            timers.setdefault(name, []).append((e0, e1))
+        t = _timer(timers, stream, external)
 
         first_full = True
         for li, l in enumerate(gw.layers):
@@ -329,17 +366,8 @@ class MtpStep:
                                      share=None if topk is not None else self.share, out=self.out[k],
                                      ws=self.mla_ws, dev_status=self.gw.dev_status, stream=stream)
 
-    def run(self, stream, timers=None, before_layer=None, after_layer=None):
-        def t(name, fn):
-            if timers is None:
-                fn()
-                return
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            timers.setdefault(name, []).append((e0, e1))
+    def run(self, stream, timers=None, before_layer=None, after_layer=None, external=False):
+        t = _timer(timers, stream, external)
 
         with self.share.mtp_iteration(enabled=self.reuse, eagle_topk=1):
             for k in range(self.n):
@@ -438,13 +466,13 @@ def job_throughput(rows_per_rank, world, ms):
 
 
 # ----------------------------------------------------------------------------
-def run_ours(args, rank, world):
+def run_ours(args, rank, world, workload=None, with_e2e=True):
     import dsa_sparse_attention_indexer_gb300 as D
     import synth
     from synth.gpu import GpuWorkload
 
     dev = f"cuda:{torch.cuda.current_device()}"
-    w = synth.workload(args.workload, batch=args.batch, ctx=args.ctx)
+    w = synth.workload(workload or args.workload, batch=args.batch, ctx=args.ctx)
     w.index_format = args.index_cache
     gw = GpuWorkload(w, dev)
     step = MtpStep(gw, D, reuse=not args.no_mtp_reuse) if w.draft_steps else Step(gw, D, args.fused_store)
@@ -512,24 +540,68 @@ def run_ours(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    # per-call device time: each call's own graph, replayed back to back
-    per_call, per_launch = {}, {}
+    # Per-call device time, two ways.
+    # (a) inside the step: a second capture of the whole step carries timing
+    #     events between its calls, so every call is timed where it runs, with
+    #     the caches as the step leaves them; averaged over replays.
+    # (b) alone and cold: each call's own graph, one replay after a 256 MB
+    #     write that evicts L2, averaged over replays.
     reps = max(3, min(args.steps, 20))
+    per_call, per_launch, counts = {}, {}, {}
+    in_step_ok = True
+    try:
+        inst_timers = {}
+        inst = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(inst, stream=stream):
+            step.run(stream, timers=inst_timers, external=True)
+        torch.cuda.synchronize()
+        acc = {k: 0.0 for k in inst_timers}
+        for _ in range(reps):
+            inst.replay()
+            torch.cuda.synchronize()
+            for k, evs in inst_timers.items():
+                acc[k] += sum(e0.elapsed_time(e1) for e0, e1 in evs)
+        for k, evs in inst_timers.items():
+            per_call[k] = acc[k] * 1000.0 / reps
+            per_launch[k] = per_call[k] / len(evs)
+            counts[k] = len(evs)
+        del inst
+    except Exception:                                  # events not capturable here: time an eager step
+        in_step_ok = False
+        acc, counts = {}, {}
+        for _ in range(reps):
+            tm = {}
+            step.run(stream, timers=tm)
+            torch.cuda.synchronize()
+            for k, evs in tm.items():
+                acc[k] = acc.get(k, 0.0) + sum(e0.elapsed_time(e1) for e0, e1 in evs)
+                counts[k] = len(evs)
+        for k in acc:
+            per_call[k] = acc[k] * 1000.0 / reps
+            per_launch[k] = per_call[k] / counts[k]
+    cold_call, cold_launch = {}, {}
+    cold_flush = flush_buf if flush_buf is not None else torch.empty(256 * 1024 * 1024, dtype=torch.uint8,
+                                                                       device=dev)
     for name, graphs in call_graphs.items():
         tot = 0.0
         for g_ in graphs:
-            if flush:
-                flush_buf.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
             for _ in range(reps):
+                cold_flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
                 g_.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            tot += e0.elapsed_time(e1) / reps
-        per_call[name] = tot * 1000.0
-        per_launch[name] = tot * 1000.0 / len(graphs)
+                e1.record(stream)
+                e1.synchronize()
+                tot += e0.elapsed_time(e1) / reps
+        cold_call[name] = tot * 1000.0
+        cold_launch[name] = tot * 1000.0 / len(graphs)
+    if flush_buf is None:
+        del cold_flush
     timers = {k: [None] * len(v) for k, v in call_graphs.items()}
+    if not with_e2e:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        return dict(w=w, ms=ms, per_call=per_call, per_launch=per_launch, cold_call=cold_call,
+                    cold_launch=cold_launch, in_step=in_step_ok, clocks=clocks, flush=flush)
 
     # ---- end to end: host buffers in, host buffers out, through the same calls
     first_in, layer_in, outs = step.e2e_io()
@@ -599,8 +671,9 @@ def run_ours(args, rank, world):
         ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mla_rows = len(w.seq_len) if w.draft_steps else w.total_q     # a draft step's launch: one row per request
-    return dict(w=w, ms=ms, e2e_ms=e2e_ms, per_call=per_call, per_launch=per_launch, clocks=clocks,
-                h2d=h2d, d2h=d2h, launches=sum(kernels_per_call(k, mla_rows, sms) * len(v) for k, v in timers.items()))
+    return dict(w=w, ms=ms, e2e_ms=e2e_ms, per_call=per_call, per_launch=per_launch, cold_call=cold_call,
+                cold_launch=cold_launch, in_step=in_step_ok, clocks=clocks, flush=flush, h2d=h2d, d2h=d2h,
+                launches=sum(kernels_per_call(k, mla_rows, sms) * len(v) for k, v in timers.items()))
 
 
 # ----------------------------------------------------------------------------
@@ -687,6 +760,36 @@ def run_reference(args, rank, world):
 
 
 # ----------------------------------------------------------------------------
+def roofline(res, pk):
+    """The roofline record of a run's dominant call: its algorithmic bytes (or
+    tensor FLOPs, when those take longer at the measured peak) per launch over
+    the launch's in-step event time, against the measured HBM copy bandwidth
+    (or the measured tensor peak of the call's operand type)."""
+    w = res["w"]
+    dom = max(res["per_call"], key=lambda k: res["per_call"][k])
+    dom_us = res["per_launch"][dom]
+    dom_bytes = call_bytes(dom, w)
+    dom_flops = call_flops(dom, w)
+    fp8 = dom == "indexer_topk"
+    tensor_peak = pk["fp8_tflops"] if fp8 else pk["bf16_tflops"]
+    tensor_bound = dom_flops / (tensor_peak * 1e12) > dom_bytes / (pk["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": dom_flops / (dom_us * 1e-6) / 1e12, "peak": tensor_peak,
+                "unit": "TFLOP/s", "peak_note": ("FP8: " + pk["fp8_source"]) if fp8 else "fp16: measured bf16 burst"}
+    else:
+        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_us * 1e-6) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    traffic = None
+    rec = NCU_TRAFFIC.get((w.name + ("+mxfp4" if w.index_format == "mxfp4" else ""), dom))
+    if rec and file_sha(rec[1]) == rec[2]:
+        traffic = rec[0]
+    cold = res["cold_launch"].get(dom)
+    return {"kernel": dom, **roof, "traffic": traffic, "peak_source": pk["source"],
+            "algorithmic_bytes_per_launch": dom_bytes, "algorithmic_flops_per_launch": dom_flops,
+            "us_per_launch": dom_us, "us_per_launch_alone_l2_flushed": cold,
+            "frac_alone_l2_flushed": (roof["frac"] * dom_us / cold) if cold else None}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -706,6 +809,10 @@ def main():
                          "RMSNorm / RoPE call from raw kv_c and k_pe")
     ap.add_argument("--no-mtp-reuse", action="store_true",
                     help="MTP workloads: every draft step runs its own indexer (the comparison point)")
+    ap.add_argument("--secondary", default="decode1m",
+                    choices=["none", "tiny", "decode32k", "decode1m", "verify64k", "prefill128k", "mtp5_1m"],
+                    help="a second workload measured after the headline one and reported in its line's "
+                         "'secondary' block (device time and roofline only)")
     args = ap.parse_args()
     if args.index_cache == "mxfp4" and args.workload not in ("tiny", "decode32k", "decode1m"):
         ap.error("--index-cache mxfp4 covers the decode workloads (tiny, decode32k, decode1m)")
@@ -738,31 +845,20 @@ def main():
     if world > 1:
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
+    dev = f"cuda:{torch.cuda.current_device()}"
+    pk = peaks()
+    fp8_meas = measure_fp8_tflops(dev)
+    if fp8_meas is not None:
+        pk["fp8_tflops"], pk["fp8_source"] = fp8_meas, "measured (torch._scaled_mm E4M3 8192^3, best of 10)"
+    else:
+        pk["fp8_tflops"], pk["fp8_source"] = pk["bf16_tflops"] * FP8_OVER_BF16, "measured bf16 x nominal 2"
     res = run_ours(args, rank, world)
     w = res["w"]
-    pk = peaks()
     ms = res["ms"]
     idx_b, kv_b, _, _ = workload_bytes(w, not args.no_mtp_reuse)
     step_bytes = idx_b + kv_b
     value = job_throughput(w.total_q, world, ms)
-    dom = max(res["per_call"], key=lambda k: res["per_call"][k])
-    dom_us = res["per_launch"][dom]
-    dom_bytes = call_bytes(dom, w)
-    dom_flops = call_flops(dom, w)
-    tensor_peak = pk["bf16_tflops"] * (FP8_OVER_BF16 if dom == "indexer_topk" else 1.0)
-    tensor_bound = dom_flops / (tensor_peak * 1e12) > dom_bytes / (pk["hbm_gbs"] * 1e9)
-    if tensor_bound:
-        roof = {"bound": "tensor", "achieved": dom_flops / (dom_us * 1e-6) / 1e12, "peak": tensor_peak,
-                "unit": "TFLOP/s",
-                "peak_note": ("FP8: measured bf16 burst x the nominal FP8/BF16 ratio" if dom == "indexer_topk"
-                              else "fp16: measured bf16 burst")}
-    else:
-        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_us * 1e-6) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    traffic = None
-    rec = NCU_TRAFFIC.get((w.name + ("+mxfp4" if w.index_format == "mxfp4" else ""), dom))
-    if rec and file_sha(rec[1]) == rec[2]:
-        traffic = rec[0]
+    roof = roofline(res, pk)
     line = {
         "metric": METRIC, "value": value, "unit": "query_tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -771,25 +867,44 @@ def main():
             "workload": w.name, "description": w.description, "batch": w.batch, "q_len": w.q_len[0],
             "mean_ctx": float(np.mean(w.seq_len)), "layers": w.layers,
             "us_per_layer": ms * 1000.0 / len(w.layers),
-            "l2": ("flushed (256 MB write) between timed steps" if step_bytes < 4 * L2_BYTES else
+            "l2": ("flushed (256 MB write) between timed steps" if res["flush"] else
                    f"inputs larger than L2 ({step_bytes / 1e6:.0f} MB algorithmic bytes per step), no flush"),
             "algorithmic_bytes_per_step": step_bytes,
             "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
             "step_frac_of_measured_hbm": step_bytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
             "step_frac_of_8tbs": step_bytes / (ms * 1e-3) / 1e9 / 8000.0,
             "us_per_call": {k: round(v, 2) for k, v in res["per_call"].items()},
+            "us_per_call_timing": ("events between the calls inside the captured step" if res["in_step"]
+                                   else "events between the calls of an eager step"),
+            "us_per_launch_alone_l2_flushed": {k: round(v, 2) for k, v in res["cold_launch"].items()},
             **({"draft_steps": w.draft_steps, "mtp_reuse": not args.no_mtp_reuse} if w.draft_steps else {}),
             "index_cache": w.index_format,
             "store": "fused" if args.fused_store else "separate",
         },
-        "roofline": {"kernel": dom, **roof, "traffic": traffic, "peak_source": pk["source"],
-                     "algorithmic_bytes_per_launch": dom_bytes, "algorithmic_flops_per_launch": dom_flops,
-                     "us_per_launch": dom_us},
+        "roofline": roof,
+        "peaks": {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"], "source": pk["source"],
+                  "fp8_tflops": pk["fp8_tflops"], "fp8_source": pk["fp8_source"]},
         "clocks": res["clocks"],
         "e2e": {"value": job_throughput(w.total_q, world, res["e2e_ms"]), "unit": "query_tokens/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"], "ms_per_step": res["e2e_ms"]},
         "gpu_launches": res["launches"] * args.steps,
     }
+    if args.secondary != "none" and args.secondary != w.name:
+        del res
+        torch.cuda.empty_cache()
+        r2 = run_ours(args, rank, world, workload=args.secondary, with_e2e=False)
+        w2 = r2["w"]
+        b2 = sum(workload_bytes(w2)[:2])
+        line["secondary"] = {
+            "workload": w2.name, "description": w2.description,
+            "value": job_throughput(w2.total_q, world, r2["ms"]), "unit": "query_tokens/s",
+            "ms_per_step": r2["ms"], "algorithmic_bytes_per_step": b2,
+            "step_hbm_gbs": b2 / (r2["ms"] * 1e-3) / 1e9,
+            "step_frac_of_measured_hbm": b2 / (r2["ms"] * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "us_per_call": {k: round(v, 2) for k, v in r2["per_call"].items()},
+            "us_per_launch_alone_l2_flushed": {k: round(v, 2) for k, v in r2["cold_launch"].items()},
+            "roofline": roofline(r2, pk), "clocks": r2["clocks"],
+        }
     if rank == 0 and not args.no_cpu_baseline:
         n, sec = oracle_sample(w, args.ref_budget, mtp_reuse=not args.no_mtp_reuse)
         qrows = sum(w.q_len[:n])
