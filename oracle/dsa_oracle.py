@@ -46,7 +46,8 @@ draft-step read counts the pages print, brute-force top-k per draft position,
 the 68-byte MXFP4 token, the E2M1 codec against its value table and rounding
 rule, the MX scale property amax / 2**e in [4, 8), the MXFP4 key of a token
 within the format's bound of torch's LayerNorm and a complex rotation, and a
-whole request's MXFP4 top-k against brute force).
+whole request's MXFP4 top-k against brute force, the context-parallel merges of
+top-k candidates and of attention parts against brute force and dense attention).
 The MTP reading where the pages are silent: a draft step with a context of at
 most 2048 publishes its all-positions row like any other step.  The LayerNorm
 eps, RoPE base and RoPE pairing are NOT fixed by the pages: "parity unpinned" for those three
@@ -356,6 +357,57 @@ def sparse_mla(q: np.ndarray, positions: np.ndarray, kv_rows: np.ndarray,
     l = p.sum(axis=1, keepdims=True)
     out = (p @ kv[:, :LATENT_DIM]) / l
     lse = (m + np.log(l))[:, 0]
+    return out, lse
+
+
+# ----------------------------------------------------------------------------
+# Context-parallel split of one long request over G ranks ("GLM-5.3 推理全链路
+# (十一)", 两个框架的对照: with prefill context parallelism the indexer's reads
+# are spread over the ranks; "Accelerating GLM-5.3-Flash on H200", prefill 的
+# 重点是少搬一次、少等一次: CP4 on the prefill side).  Each rank holds a disjoint
+# slice of the request's positions, scores it, and keeps its own top-k; the
+# top-k of the whole context is the top-k of the union of those lists, because
+# every globally selected position is also selected within its own slice.
+# Attention over the selected positions splits the same way: a rank attends
+# over the selected positions it holds, and the parts are combined by their
+# log-sum-exp.
+# ----------------------------------------------------------------------------
+def cp_merge_topk(cand_pos_list, cand_score_list, k: int = TOPK) -> np.ndarray:
+    """Top-k of the union of per-rank candidate lists.
+
+    cand_pos_list[g]: global positions (-1 = no candidate); cand_score_list[g]:
+    their scores.  Order: descending score, ties to the lower position, -0.0
+    equal to +0.0.  Returns int32 [k]: the selected positions ascending, -1
+    padded.
+    """
+    pos = np.concatenate([np.asarray(p, dtype=np.int64).ravel() for p in cand_pos_list])
+    sc = np.concatenate([np.asarray(s, dtype=np.float64).ravel() for s in cand_score_list])
+    keep = pos >= 0
+    pos, sc = pos[keep], sc[keep] + 0.0
+    order = np.lexsort((pos, -sc))[:k]
+    out = np.full(k, -1, dtype=np.int32)
+    sel = np.sort(pos[order])
+    out[:sel.size] = sel
+    return out
+
+
+def lse_merge(outs, lses):
+    """Softmax attention over a disjoint union of key sets, from the parts.
+
+    outs[g] [H, D]: attention normalised within part g; lses[g] [H]: the
+    natural-log sum of exp(score) over part g (-inf for an empty part).  With
+    M = max_g lse_g and w_g = exp(lse_g - M):
+        out = sum_g w_g out_g / sum_g w_g,   lse = M + log(sum_g w_g).
+    Returns (out [H, D], lse [H]); a head empty in every part gives 0 and -inf.
+    """
+    lses = np.stack([np.asarray(x, dtype=np.float64) for x in lses])    # [G, H]
+    outs = np.stack([np.asarray(x, dtype=np.float64) for x in outs])    # [G, H, D]
+    M = np.max(lses, axis=0)                                            # [H]
+    finite = np.isfinite(M)
+    w = np.where(np.isfinite(lses), np.exp(lses - np.where(finite, M, 0.0)), 0.0)
+    den = w.sum(axis=0)
+    out = np.where(finite[:, None], (w[:, :, None] * outs).sum(axis=0) / np.where(finite, den, 1.0)[:, None], 0.0)
+    lse = np.where(finite, M + np.log(np.where(finite, den, 1.0)), -np.inf)
     return out, lse
 
 

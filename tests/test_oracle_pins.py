@@ -720,3 +720,65 @@ def test_latent_prepare_rotates_only_the_rope_dims_and_rounds_to_bf16():
     exact = O.rope_interleaved(pe, pos, 10000.0, 64)
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 1e-30))) - 7)
     assert np.all(np.abs(r - exact) <= 0.5 * ulp * (1 + 1e-9))
+
+
+# ------------------------------------------------------------------ context-parallel merges
+@pytest.mark.parametrize("cuts", [(1000,), (700, 1900), (5, 2100, 2200)])
+def test_cp_merge_topk_of_slice_topks_is_the_whole_topk(cuts):
+    # Scores with heavy ties and signed zeros over L positions, cut into
+    # disjoint slices; each slice keeps its own top-k by brute force; the merge
+    # of those lists must be the brute-force top-k of the whole row.
+    rng = np.random.default_rng(41 + len(cuts))
+    L, k = 2400, 64
+    s = rng.integers(-40, 40, L).astype(np.float64) / 8.0
+    s[rng.integers(0, L, 50)] = -0.0
+    edges = [0, *cuts, L]
+    cand_pos, cand_sc = [], []
+    for a, b in zip(edges[:-1], edges[1:]):
+        loc = _brute_topk(s[a:b], min(k, b - a))
+        cand_pos.append(np.array(loc) + a)
+        cand_sc.append(s[a:b][loc])
+    got = O.cp_merge_topk(cand_pos, cand_sc, k=k)
+    assert got.tolist() == _brute_topk(s, k)
+    # at the full width, against an independent argsort of (score desc, position asc)
+    L2 = 9000
+    s2 = np.round(rng.standard_normal(L2) * 4) / 4
+    order = sorted(range(L2), key=lambda j: (-(s2[j] + 0.0), j))[:2048]
+    pos, sc = [], []
+    for a, b in ((0, 3000), (3000, 3001), (3001, L2)):
+        loc = sorted(range(a, b), key=lambda j: (-(s2[j] + 0.0), j))[:2048]
+        pos.append(np.array(loc + [-1] * (2048 - len(loc))))
+        sc.append(np.array([s2[j] for j in loc] + [0.0] * (2048 - len(loc))))
+    assert O.cp_merge_topk(pos, sc).tolist() == sorted(order)
+
+
+def test_lse_merge_of_attention_parts_equals_dense_attention():
+    # Attention over a key set split into parts, each normalised on its own with
+    # its log-sum-exp, merges to dense softmax attention over all keys (torch SDPA
+    # in fp64), including an empty part.
+    rng = np.random.default_rng(43)
+    H, D, n = 4, 16, 37
+    q = rng.standard_normal((H, D))
+    k = rng.standard_normal((n, D)) * 2.0
+    v = rng.standard_normal((n, D))
+    parts = [np.arange(0, 11), np.arange(11, 11), np.arange(11, 30), np.arange(30, n)]
+    outs, lses = [], []
+    for idx in parts:
+        if idx.size == 0:
+            outs.append(np.zeros((H, D)))
+            lses.append(np.full(H, -np.inf))
+            continue
+        sc = q @ k[idx].T
+        m = sc.max(axis=1, keepdims=True)
+        p = np.exp(sc - m)
+        outs.append(p @ v[idx] / p.sum(axis=1, keepdims=True))
+        lses.append(m[:, 0] + np.log(p.sum(axis=1)))
+    out, lse = O.lse_merge(outs, lses)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None, :, None, :], torch.from_numpy(k)[None, None].expand(1, H, n, D),
+        torch.from_numpy(v)[None, None].expand(1, H, n, D), scale=1.0)[0, :, 0, :].numpy()
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+    ref_lse = np.log(np.exp(q @ k.T).sum(axis=1))
+    assert np.allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+    out0, lse0 = O.lse_merge([np.zeros((H, D))] * 2, [np.full(H, -np.inf)] * 2)
+    assert not out0.any() and np.all(np.isneginf(lse0))
