@@ -119,6 +119,11 @@ _SIGS = {
                                            POINTER(c_int32)]),
     "dsa_topk_share_needs_scoring": (c_int32, [c_void_p, POINTER(c_int32)]),
     "dsa_topk_share_mtp_end": (c_int32, [c_void_p]),
+    "dsa_cp_topk_merge": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int64, c_void_p, c_void_p, c_void_p,
+                                    c_void_p]),
+    "dsa_cp_topk_localize": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dsa_cp_attention_merge": (c_int32, [c_void_p, c_void_p, c_int32, c_int64, c_void_p, c_int32, c_void_p,
+                                         c_void_p]),
 }
 
 
@@ -601,3 +606,151 @@ def index_cache_scale_view(idxk_cache: torch.Tensor) -> torch.Tensor:
     """fp32 [num_pages, 64] view of the per-token scales inside an index-K cache."""
     pages = idxk_cache.view(-1, IDXK_PAGE_BYTES)
     return pages[:, PAGE_TOKENS * INDEX_HEAD_DIM:].view(torch.float32)
+
+
+# ---------------------------------------------------------------------------
+# Context-parallel split of long requests over the ranks of a process group
+# ("GLM-5.3 推理全链路(十一)", 两个框架的对照; "Accelerating GLM-5.3-Flash on H200",
+# prefill 的重点是少搬一次、少等一次).  See dsa.h for the steps.
+CP_MAX_RANKS = 8
+
+
+def dsa_cp_topk_merge(cand_pos, cand_scores, pos_offset, *, topk=None, topk_scores=None, dev_status=None,
+                      stream=None):
+    """Global top-2048 from every rank's list: cand_pos / cand_scores [G, rows, 2048],
+    pos_offset int64 [G, rows].  Returns topk int32 [rows, 2048]."""
+    _need(cand_pos, torch.int32, "cand_pos")
+    if cand_pos.dim() != 3 or cand_pos.shape[2] != TOPK:
+        raise ValueError(f"cand_pos must be [G, rows, {TOPK}], got {tuple(cand_pos.shape)}")
+    G, rows = cand_pos.shape[0], cand_pos.shape[1]
+    dev = cand_pos.device
+    _need(cand_scores, torch.float32, "cand_scores", dev, G * rows * TOPK)
+    _need(pos_offset, torch.int64, "pos_offset", dev, G * rows)
+    if topk is None:
+        topk = torch.empty((rows, TOPK), dtype=torch.int32, device=dev)
+    _need(topk, torch.int32, "topk", dev, rows * TOPK)
+    _opt(topk_scores, torch.float32, "topk_scores", dev, rows * TOPK)
+    _opt(dev_status, torch.int32, "dev_status", dev, 4)
+    _call("dsa_cp_topk_merge", dev, _ptr(cand_pos), _ptr(cand_scores), _ptr(pos_offset), G, rows, _ptr(topk),
+          _ptr(topk_scores), _ptr(dev_status), _stream(stream, dev))
+    return topk
+
+
+def dsa_cp_topk_localize(topk, slice_start, slice_len, *, local_topk=None, stream=None):
+    """This rank's share of a global top-k list, in local positions, compacted."""
+    _need(topk, torch.int32, "topk")
+    rows, dev = topk.shape[0], topk.device
+    _need(topk, torch.int32, "topk", dev, rows * TOPK)
+    _need(slice_start, torch.int64, "slice_start", dev, rows)
+    _need(slice_len, torch.int64, "slice_len", dev, rows)
+    if local_topk is None:
+        local_topk = torch.empty((rows, TOPK), dtype=torch.int32, device=dev)
+    _need(local_topk, torch.int32, "local_topk", dev, rows * TOPK)
+    _call("dsa_cp_topk_localize", dev, _ptr(topk), rows, _ptr(slice_start), _ptr(slice_len), _ptr(local_topk),
+          _stream(stream, dev))
+    return local_topk
+
+
+def dsa_cp_attention_merge(o_parts, lse_parts, *, out=None, out_dtype=DTYPE_BF16, lse=None, stream=None):
+    """Attention over the union of the ranks' selected positions from their
+    parts: o_parts fp32 [G, rows, 64, 512], lse_parts fp32 [G, rows, 64]."""
+    _need(o_parts, torch.float32, "o_parts")
+    if o_parts.dim() != 4 or tuple(o_parts.shape[2:]) != (MLA_HEADS, LATENT_DIM):
+        raise ValueError(f"o_parts must be [G, rows, 64, 512], got {tuple(o_parts.shape)}")
+    G, rows, dev = o_parts.shape[0], o_parts.shape[1], o_parts.device
+    _need(lse_parts, torch.float32, "lse_parts", dev, G * rows * MLA_HEADS)
+    out_t = torch.float32 if out_dtype == DTYPE_F32 else torch.bfloat16
+    if out is None:
+        out = torch.empty((rows, MLA_HEADS, LATENT_DIM), dtype=out_t, device=dev)
+    _need(out, out_t, "out", dev, rows * MLA_HEADS * LATENT_DIM)
+    _opt(lse, torch.float32, "lse", dev, rows * MLA_HEADS)
+    _call("dsa_cp_attention_merge", dev, _ptr(o_parts), _ptr(lse_parts), G, rows, _ptr(out), out_dtype, _ptr(lse),
+          _stream(stream, dev))
+    return out
+
+
+class LibraryOps:
+    """The per-rank steps of the context-parallel split, as library calls."""
+
+    def indexer_topk(self, q, w, idxk_cache, batch, ws=None, dev_status=None, stream=None):
+        T = batch.total_q
+        topk = torch.empty((T, TOPK), dtype=torch.int32, device=q.device)
+        scores = torch.empty((T, TOPK), dtype=torch.float32, device=q.device)
+        dsa_indexer_topk(q, w, idxk_cache, batch, topk=topk, topk_scores=scores, ws=ws, dev_status=dev_status,
+                         stream=stream)
+        return topk, scores
+
+    def topk_merge(self, cand_pos, cand_scores, pos_offset, dev_status=None, stream=None):
+        return dsa_cp_topk_merge(cand_pos, cand_scores, pos_offset, dev_status=dev_status, stream=stream)
+
+    def topk_localize(self, topk, slice_start, slice_len, stream=None):
+        return dsa_cp_topk_localize(topk, slice_start, slice_len, stream=stream)
+
+    def sparse_mla(self, q, local_topk, kv_cache, batch, softmax_scale, ws=None, dev_status=None, stream=None):
+        T = batch.total_q
+        lse = torch.empty((T, MLA_HEADS), dtype=torch.float32, device=q.device)
+        out = dsa_sparse_mla_decode(q, local_topk, kv_cache, batch, softmax_scale=softmax_scale, out_dtype=DTYPE_F32,
+                                    lse=lse, ws=ws, dev_status=dev_status, stream=stream)
+        return out, lse
+
+    def attention_merge(self, o_parts, lse_parts, out_dtype, stream=None):
+        T = o_parts.shape[1]
+        lse = torch.empty((T, MLA_HEADS), dtype=torch.float32, device=o_parts.device)
+        out = dsa_cp_attention_merge(o_parts, lse_parts, out_dtype=out_dtype, lse=lse, stream=stream)
+        return out, lse
+
+
+def _gather_ranks(t, group):
+    """[G, *t.shape]: every rank's t, in rank order (the exchange step)."""
+    import torch.distributed as dist
+    G = dist.get_world_size(group)
+    if dist.get_backend(group) == "nccl":
+        out = torch.empty((G, *t.shape), dtype=t.dtype, device=t.device)
+        dist.all_gather_into_tensor(out, t.contiguous(), group=group)
+        return out
+    parts = [torch.empty_like(t) for _ in range(G)]
+    dist.all_gather(parts, t.contiguous(), group=group)
+    return torch.stack(parts)
+
+
+class ContextParallel:
+    """One layer's indexer and sparse MLA for requests whose positions are cut
+    into disjoint slices, one per rank of `group` (at most 8 ranks).  This rank
+    holds its slice of every request in its own caches, described by `batch`
+    as requests of seq_len = slice length with local positions; slice_start
+    (int64 [rows], device) gives the global position of each row's local
+    position 0, slice_len the slice's length.  Every slice must be longer than
+    2048 tokens.  Two exchanges per layer: at most 2048 (score, position) pairs
+    per row and rank after the indexer, one [64, 512] fp32 part and its
+    log-sum-exp per row and rank after sparse MLA.
+
+    `ops` performs the per-rank steps; it defaults to the library's calls."""
+
+    def __init__(self, group=None, ops=None, gather=None):
+        import torch.distributed as dist
+        self.group = group
+        self.world = dist.get_world_size(group)
+        if self.world > CP_MAX_RANKS:
+            raise ValueError(f"at most {CP_MAX_RANKS} ranks, the group has {self.world}")
+        self.ops = ops if ops is not None else LibraryOps()
+        self._gather = gather if gather is not None else (lambda t: _gather_ranks(t, group))
+
+    def indexer_topk(self, q, w, idxk_cache, batch, slice_start, *, share=None, layer_id=0, ws=None,
+                     dev_status=None, stream=None):
+        """The global top-2048 of every row (global positions, ascending)."""
+        local, scores = self.ops.indexer_topk(q, w, idxk_cache, batch, ws=ws, dev_status=dev_status, stream=stream)
+        cand_pos = self._gather(local)
+        cand_scores = self._gather(scores)
+        offsets = self._gather(slice_start)
+        topk = self.ops.topk_merge(cand_pos, cand_scores, offsets, dev_status=dev_status, stream=stream)
+        if share is not None:
+            share.publish(layer_id, topk)
+        return topk
+
+    def sparse_mla(self, q, topk, kv_cache, batch, slice_start, slice_len, *, softmax_scale=1.0 / 16,
+                   out_dtype=DTYPE_BF16, ws=None, dev_status=None, stream=None):
+        """Attention of every row over its global top-2048; returns (out, lse)."""
+        local = self.ops.topk_localize(topk, slice_start, slice_len, stream=stream)
+        o, lse = self.ops.sparse_mla(q, local, kv_cache, batch, softmax_scale, ws=ws, dev_status=dev_status,
+                                     stream=stream)
+        return self.ops.attention_merge(self._gather(o), self._gather(lse), out_dtype, stream=stream)

@@ -300,6 +300,57 @@ dsa_status dsa_sparse_mla_prefill(const void* q, const int32_t* topk, const dsa_
                                   void* out, int32_t out_dtype, float* lse,
                                   void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* ---- Context-parallel split of long requests ("GLM-5.3 推理全链路(十一)", 两个框架的
+ *      对照: with prefill context parallelism the indexer's reads are spread over
+ *      the ranks; "Accelerating GLM-5.3-Flash on H200", prefill 的重点是少搬一次、少等
+ *      一次: CP4 on the prefill side) ---------------------------------------------
+ * A request's positions are cut into G <= 8 disjoint slices, one per rank; a
+ * rank holds its slice in its own caches, as a request of seq_len = slice
+ * length with local positions 0.., and runs the single-GPU calls on it.  Each
+ * slice must be longer than 2048 tokens (a shorter one selects all its
+ * positions without scores).  Per query row:
+ *   1. dsa_indexer_topk on the slice gives the rank's top-2048 (local
+ *      positions) and their scores (topk_scores);
+ *   2. the caller gathers every rank's lists, [G, rows, 2048] int32 and fp32,
+ *      and each slice's first global position, [G, rows] int64;
+ *   3. dsa_cp_topk_merge: the global top-2048, which is the top-2048 of the
+ *      union of the lists (a position selected over the whole context is
+ *      also selected within its own slice); same order and ties as
+ *      dsa_indexer_topk, global positions ascending, -1 padded;
+ *   4. dsa_cp_topk_localize: the rank's share of the global list, as local
+ *      positions compacted to the front of each row, -1 padded;
+ *   5. sparse MLA on the slice with that list, fp32 output and lse;
+ *   6. the caller gathers every rank's (out, lse), [G, rows, 64, 512] fp32 and
+ *      [G, rows, 64] fp32;
+ *   7. dsa_cp_attention_merge: softmax attention over the union,
+ *      out = sum_g w_g out_g / sum_g w_g with w_g = exp(lse_g - max_g lse_g),
+ *      lse = max_g lse_g + log(sum_g w_g) (a head empty on every rank: 0, -inf).
+ * dsa_cp_topk_merge
+ *   cand_pos    device int32 [G, rows, 2048]: local positions, -1 = none
+ *   cand_scores device fp32 [G, rows, 2048]: their scores
+ *   pos_offset  device int64 [G, rows]: global position of local position 0
+ *   topk        device int32 [rows, 2048]; topk_scores device fp32 [rows, 2048]
+ *               or NULL (0 for -1 entries)
+ *   A global position outside [0, 2^31 - 1) is skipped and recorded
+ *   (DSA_DEVERR_INDEX_RANGE).  Slices must not overlap.
+ * dsa_cp_topk_localize
+ *   topk        device int32 [rows, 2048] global positions
+ *   slice_start device int64 [rows], slice_len device int64 [rows]: this rank's
+ *               slice [start, start + len) of each row's request
+ *   local_topk  device int32 [rows, 2048], not the same buffer as topk
+ * dsa_cp_attention_merge
+ *   o_parts     device fp32 [G, rows, 64, 512]; lse_parts device fp32 [G, rows, 64]
+ *               (natural log, -inf for a rank with no selected position)
+ *   out         device [rows, 64, 512] bf16 or fp32 per out_dtype
+ *   lse         device fp32 [rows, 64] or NULL                                   */
+dsa_status dsa_cp_topk_merge(const int32_t* cand_pos, const float* cand_scores, const int64_t* pos_offset,
+                             int32_t ranks, int64_t rows, int32_t* topk, float* topk_scores,
+                             int32_t* dev_status, void* stream);
+dsa_status dsa_cp_topk_localize(const int32_t* topk, int64_t rows, const int64_t* slice_start,
+                                const int64_t* slice_len, int32_t* local_topk, void* stream);
+dsa_status dsa_cp_attention_merge(const float* o_parts, const float* lse_parts, int32_t ranks, int64_t rows,
+                                  void* out, int32_t out_dtype, float* lse, void* stream);
+
 /* ---- Full / shared layer schedule ("GLM-5.3 推理全链路(十一)", 配置里的 78 个字符) --
  * dsa_parse_indexer_types: types[l] is "full" or "shared"; is_full[l] = 1/0.
  *   An unknown string returns DSA_ERR_INVALID_ARGUMENT.

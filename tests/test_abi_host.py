@@ -126,6 +126,26 @@ def test_indexer_and_mla_argument_errors(L):
     assert L.dsa_topk_from_scores(fk, 10, fk, 0, 10, fk, None, 0, None) == 0      # zero rows: no launch
 
 
+def test_context_parallel_argument_errors(L):
+    fk = ctypes.c_void_p(0x30000000)
+    odd = ctypes.c_void_p(0x30000004)
+    # merge: rank count outside 1..8, null inputs, unaligned lists; zero rows launch nothing
+    assert L.dsa_cp_topk_merge(fk, fk, fk, 0, 4, fk, None, None, None) == 1
+    assert L.dsa_cp_topk_merge(fk, fk, fk, 9, 4, fk, None, None, None) == 1
+    assert L.dsa_cp_topk_merge(None, fk, fk, 2, 4, fk, None, None, None) == 1
+    assert L.dsa_cp_topk_merge(odd, fk, fk, 2, 4, fk, None, None, None) == 2
+    assert L.dsa_cp_topk_merge(fk, fk, fk, 2, 0, fk, None, None, None) == 0
+    # localize: in place is refused; negative rows
+    assert L.dsa_cp_topk_localize(fk, 4, fk, fk, fk, None) == 1
+    assert L.dsa_cp_topk_localize(fk, -1, fk, fk, ctypes.c_void_p(0x31000000), None) == 1
+    assert L.dsa_cp_topk_localize(fk, 0, fk, fk, ctypes.c_void_p(0x31000000), None) == 0
+    # attention merge: bad dtype, null parts, unaligned output
+    assert L.dsa_cp_attention_merge(fk, fk, 2, 4, fk, 7, None, None) == 1
+    assert L.dsa_cp_attention_merge(None, fk, 2, 4, fk, 0, None, None) == 1
+    assert L.dsa_cp_attention_merge(fk, fk, 2, 4, odd, 0, None, None) == 2
+    assert L.dsa_cp_attention_merge(fk, fk, 2, 0, fk, 0, None, None) == 0
+
+
 def test_schedule_parser_and_freq_rule(L):
     full = GOLDEN["full_layers"]["value"]
     types = ["full" if l in full else "shared" for l in range(78)]
