@@ -379,7 +379,7 @@ def dsa_indexer_topk(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=N
 
 def dsa_indexer_topk_mxfp4(q, w, idxk_cache, batch: Batch, *, topk=None, topk_scores=None, share=None,
                            layer_id: int = 0, ws=None, dev_status=None, stream=None):
-    """dsa_indexer_topk over an MXFP4 index-K cache (decode batches)."""
+    """dsa_indexer_topk over an MXFP4 index-K cache (at most 65535 query rows)."""
     T = _indexer_args(q, w, idxk_cache, batch)
     if topk is None:
         topk = torch.empty((T, TOPK), dtype=torch.int32, device=q.device)

@@ -3,38 +3,57 @@
 // 优化二 for the short-context rule).
 #include "dsa_internal.cuh"
 #include "indexer_common.cuh"
-#include "topk_common.cuh"
 #include "indexer_tc.cuh"
 
 namespace dsa {
 
-// One CTA per query row: select over the row's p + 1 visible scores.
-__global__ void __launch_bounds__(kSelThreads)
-indexer_select_kernel(const float* __restrict__ scores, int64_t ld, BatchDev b,
-                      int32_t* __restrict__ topk, float* __restrict__ topk_scores) {
-    extern __shared__ __align__(16) uint8_t sel_smem[];
+// Decode batches (one query row per request) take the fused tensor-core path;
+// other batches the multi-row tensor-core path, which streams each row's
+// candidates into workspace slots (no score row is written).
+inline bool use_tc_path(const dsa_batch* b) { return b->max_q_len == 1 && b->total_q == b->batch; }
+
+inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// The fused decode path for T query rows: quantised queries, row histograms and
+// its plan, for any GPU of up to 1024 SMs.
+inline size_t decode_ws_bytes(int64_t T, int64_t batch) {
+    return round256(q8_workspace_bytes(T)) + (size_t)T * 4096 * 4 + tc_plan_bytes(batch, 1024);
+}
+// MXFP4 cache, several rows per request: every query row becomes a request of
+// its own (context = its position + 1, its request's page-table row), built in
+// the workspace after the decode path's part.
+inline size_t mx_rows_virtual_bytes(const dsa_batch* b) {
+    return round256((size_t)(2 * b->total_q + 1) * 4) + round256((size_t)b->total_q * b->max_pages * 4);
+}
+
+// Decode batches: the fused path.  Other batches: row histograms + the
+// multi-row plan with its candidate slots for the current device's SM count
+// (O(T x 4608) candidates, no score rows), or the MXFP4 call's virtual decode
+// batch, whichever is larger.
+inline size_t indexer_ws_bytes(const dsa_batch* b) {
+    if (use_tc_path(b)) return decode_ws_bytes(b->total_q, b->batch);
+    const size_t fp8 = round256(q8_workspace_bytes(b->total_q)) + (size_t)b->total_q * 4096 * 4 +
+                       mt_topk_bytes(b->batch, b->total_q, device_sm_count());
+    const size_t mx = decode_ws_bytes(b->total_q, b->total_q) + mx_rows_virtual_bytes(b);
+    return fp8 > mx ? fp8 : mx;
+}
+
+// Row i of a multi-row batch as request i of a decode batch.
+__global__ void __launch_bounds__(256)
+virtual_rows_kernel(BatchDev b, int32_t* __restrict__ seq_v, int32_t* __restrict__ qs_v,
+                    int32_t* __restrict__ pt_v) {
     const int64_t row = blockIdx.x;
     const int r = row_request(b.q_start, b.batch, row);
     const int qn = b.q_start[r + 1] - b.q_start[r];
-    const int64_t t = row - b.q_start[r];
-    int64_t n = (int64_t)b.seq_len[r] - qn + t + 1;            // positions 0..p
-    if (n > ld) n = ld;                                          // seq_len beyond the declared bound
-    select_topk_row(scores + row * ld, n, topk + row * kTopK, topk_scores ? topk_scores + row * kTopK : nullptr,
-                    sel_smem);
-}
-
-inline int64_t score_ld(const dsa_batch* b) { return ((int64_t)b->max_seq_len + 3) / 4 * 4; }
-
-// Decode batches (one query row per request) take the fused tensor-core path;
-// other batches score into full rows and select from them.
-inline bool use_tc_path(const dsa_batch* b) { return b->max_q_len == 1 && b->total_q == b->batch; }
-
-inline size_t indexer_ws_bytes(const dsa_batch* b) {
-    const size_t qbytes = (q8_workspace_bytes(b->total_q) + 255) / 256 * 256;
-    if (use_tc_path(b))   // row histograms + plan, for any GPU of up to 1024 SMs
-        return qbytes + (size_t)b->total_q * 4096 * 4 + tc_plan_bytes(b->batch, 1024);
-    const size_t sbytes = ((size_t)b->total_q * (size_t)score_ld(b) * 4 + 255) / 256 * 256;
-    return qbytes + sbytes + mt_plan_bytes(b->batch, b->total_q);
+    const int p = b.seq_len[r] - qn + (int)(row - b.q_start[r]);
+    if (threadIdx.x == 0) {
+        seq_v[row] = p + 1;
+        qs_v[row] = (int32_t)row;
+        if (row == b.total_q - 1) qs_v[row + 1] = (int32_t)(row + 1);
+    }
+    const int32_t* src = b.page_table + (int64_t)r * b.max_pages;
+    int32_t* dst = pt_v + row * b.max_pages;
+    for (int k = threadIdx.x; k < b.max_pages; k += 256) dst[k] = src[k];
 }
 
 }  // namespace dsa
@@ -52,8 +71,10 @@ extern "C" dsa_status dsa_indexer_topk_workspace_size(const dsa_batch* b, size_t
     return DSA_OK;
 }
 
-// MXFP4 index-K cache, decode batches: the same quantised queries, plan,
-// fused score kernel (E2M1 keys, block scales in the epilogue) and merge.
+// MXFP4 index-K cache: the same quantised queries, plan, fused score kernel
+// (E2M1 keys, block scales in the epilogue) and merge as the decode path.  A
+// batch with several rows per request runs as a virtual decode batch of one
+// request per row (each row reads its request's keys up to its position).
 extern "C" dsa_status dsa_indexer_topk_mxfp4(const void* q, const float* w, const uint8_t* idxk_cache,
                                              const dsa_batch* b, int32_t* topk, float* topk_scores,
                                              dsa_topk_share* share, int32_t layer_id, void* ws,
@@ -63,17 +84,31 @@ extern "C" dsa_status dsa_indexer_topk_mxfp4(const void* q, const float* w, cons
     if (!q || !w || !idxk_cache || !topk) return DSA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(topk) || (reinterpret_cast<uintptr_t>(idxk_cache) & 31)) return DSA_ERR_ALIGNMENT;
     if (b->total_q > 0) {
-        if (!use_tc_path(b)) return DSA_ERR_UNSUPPORTED;            // decode batches only
         if (b->num_pages * 68 > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+        if (!use_tc_path(b) && b->total_q > 65535) return DSA_ERR_UNSUPPORTED;   // rows as requests
         if (!ws) return DSA_ERR_INVALID_ARGUMENT;
         if (!aligned16(ws)) return DSA_ERR_ALIGNMENT;
         if (ws_bytes < indexer_ws_bytes(b)) return DSA_ERR_WORKSPACE_TOO_SMALL;
         cudaStream_t s = as_stream(stream);
         uint8_t* q8 = static_cast<uint8_t*>(ws);
         float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
-        uint32_t* hist = reinterpret_cast<uint32_t*>(q8 + (q8_workspace_bytes(b->total_q) + 255) / 256 * 256);
+        uint32_t* hist = reinterpret_cast<uint32_t*>(q8 + round256(q8_workspace_bytes(b->total_q)));
         void* plan = reinterpret_cast<uint8_t*>(hist) + (size_t)b->total_q * 4096 * 4;
-        dsa_status rs = launch_indexer_tc(q, w, q8, wq, hist, idxk_cache, b, topk, topk_scores, plan,
+        dsa_batch vb = *b;
+        if (!use_tc_path(b)) {
+            uint8_t* vbase = static_cast<uint8_t*>(ws) + decode_ws_bytes(b->total_q, b->total_q);
+            int32_t* seq_v = reinterpret_cast<int32_t*>(vbase);
+            int32_t* qs_v = seq_v + b->total_q;
+            int32_t* pt_v = reinterpret_cast<int32_t*>(vbase + round256((size_t)(2 * b->total_q + 1) * 4));
+            virtual_rows_kernel<<<(unsigned)b->total_q, 256, 0, s>>>(to_dev(b), seq_v, qs_v, pt_v);
+            DSA_CHECK_LAUNCH();
+            vb.batch = (int32_t)b->total_q;
+            vb.max_q_len = 1;
+            vb.seq_len = seq_v;
+            vb.q_start = qs_v;
+            vb.page_table = pt_v;
+        }
+        dsa_status rs = launch_indexer_tc(q, w, q8, wq, hist, idxk_cache, &vb, topk, topk_scores, plan,
                                           device_sm_count(), dev_status, s, true);
         if (rs != DSA_OK) return rs;
     }
@@ -97,7 +132,6 @@ extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint
         uint8_t* q8 = static_cast<uint8_t*>(ws);
         float* wq = reinterpret_cast<float*>(q8 + (size_t)b->total_q * 4096);
         float* sc = reinterpret_cast<float*>(q8 + (q8_workspace_bytes(b->total_q) + 255) / 256 * 256);
-        const int64_t ld = score_ld(b);
         if (b->num_pages * 66 > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
         const bool tc = use_tc_path(b);
         if (tc) {
@@ -110,16 +144,13 @@ extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint
             if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);
             return DSA_OK;
         }
-        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, nullptr, s);
+        uint32_t* hist = reinterpret_cast<uint32_t*>(sc);
+        dsa_status rs = launch_index_q_quant(q, w, b->total_q, q8, wq, hist, s);   // also clears hist
         if (rs != DSA_OK) return rs;
-        void* plan = reinterpret_cast<uint8_t*>(sc) + ((size_t)b->total_q * (size_t)ld * 4 + 255) / 256 * 256;
-        rs = launch_indexer_rows(q8, wq, idxk_cache, b, sc, ld, true, false, plan, device_sm_count(), dev_status, s);
+        void* plan = reinterpret_cast<uint8_t*>(sc) + (size_t)b->total_q * 4096 * 4;
+        rs = launch_indexer_rows_topk(q8, wq, hist, idxk_cache, b, topk, topk_scores, plan, device_sm_count(),
+                                      dev_status, s);
         if (rs != DSA_OK) return rs;
-        BatchDev bd = to_dev(b);
-        if (ensure_smem_limit(reinterpret_cast<const void*>(&indexer_select_kernel), kSelSmem) != DSA_OK)
-            return DSA_ERR_CUDA;
-        indexer_select_kernel<<<(unsigned)b->total_q, kSelThreads, kSelSmem, s>>>(sc, ld, bd, topk, topk_scores);
-        DSA_CHECK_LAUNCH();
     }
     if (share) return dsa_topk_share_publish(share, layer_id, topk, b->total_q);
     return DSA_OK;

@@ -20,11 +20,29 @@
 //                  swizzle) plus their 256-B scale rows, into an 8-stage ring;
 //       warp 1     tcgen05.mma issuer (kind::f8f6f4, M=128, N=32R, K=4x32)
 //                  into a double-buffered TMEM accumulator of 256 columns;
-//       warps 2-9  two epilogue groups taking alternate tiles: per token and
-//                  row, ReLU, head-weighted sum, times the key scale; the score
-//                  rows are written coalesced (32 consecutive positions per warp
-//                  store).  Positions beyond a row's own position, and pages
-//                  outside the pool, get -inf.
+//       warps 2-13 three epilogue groups of four warps, all on every tile:
+//                  group g takes its third of the block's rows (three warps
+//                  per SM sub-partition on the same tile, so TMEM loads and
+//                  arithmetic of different warps overlap while the MMA fills
+//                  the other accumulator); per token and row, ReLU,
+//                  head-weighted sum (packed f32x2 FMA), times the key scale.
+//  3. top-k (dsa_indexer_topk): no score row is written.  A CTA's share of a
+//     row block is a piece; each row of a piece streams its candidates into a
+//     slot of 4608 in the workspace: scores above the row's rising threshold
+//     are appended (a warp reserves its rows' room with one shared atomic per
+//     tile and stores the entries after its next tile's arithmetic).  Every
+//     four tiles the epilogue checks the slots; a slot that may not hold the
+//     next four tiles is compacted: loaded into registers, one histogram pass
+//     over its key range finds the bin of its 2048th key, the entries from
+//     that bin up stay (at least 2048; an exact radix selection when the bin
+//     is crowded) and the threshold rises to the bin's lower edge.  At the
+//     piece end the slot's keys join the row's 12-bit key histogram.
+//     The merge of the decode indexer (per-slot filter at the bin of the row's
+//     2048th key, then an exact per-row selection) gives the row's top-2048.
+//     The global top-2048 is inside the union of the pieces' top-2048s.
+//     Scores (dsa_indexer_scores): the rows are written coalesced (32
+//     consecutive positions per warp store); positions beyond a row's own
+//     position, and pages outside the pool, get -inf.
 // Every wait is time-bounded; a timeout is recorded and the CTA winds down.
 #include "dsa_internal.cuh"
 #include "indexer_common.cuh"
@@ -44,7 +62,10 @@ constexpr int kStages = 8;
 constexpr int kStageBytes = 16384;              // 2 x 8192 FP8 payload (two 64-token pages)
 constexpr int kQBytes = kRows * 32 * 128;       // one row block's quantised queries (256 x 128 B)
 constexpr int kPidChunk = 64;                   // tiles whose page ids the producer fetches at once
-constexpr int kEpiThreads = 256;                // two epilogue groups of 4 warps, alternating tiles
+constexpr int kGroups = 3;                      // epilogue groups of 4 warps, all on every tile
+constexpr int kEpiThreads = 128 * kGroups;
+constexpr int kEpiWarps = kEpiThreads / 32;
+constexpr int kPerGrp = (kRows + kGroups - 1) / kGroups;   // rows of a block one group scores, at most
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 512;                  // 2 accumulators x 256 columns
 
@@ -53,18 +74,29 @@ constexpr int kOffQ = kOffStages + kStages * kStageBytes;          // 2 row-bloc
 constexpr int kOffScales = kOffQ + 2 * kQBytes;                     // 2 x 256 B of key scales per stage
 constexpr int kOffBars = kOffScales + kStages * 512;
 constexpr int kOffPid = kOffBars + (2 * kStages + 9) * 8;
-constexpr int kOffMisc = kOffPid + kPidChunk * 2 * 8;
-constexpr int kSmemUsed = kOffMisc + 128;
+constexpr int kOffHist = kOffPid + kPidChunk * 2 * 8;          // 4096-bin radix histogram (compaction)
+constexpr int kOffMisc = kOffHist + 4096 * 4;
+constexpr int kMiscBytes = 512;
+constexpr int kSmemUsed = kOffMisc + kMiscBytes;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 static_assert(kOffQ % 1024 == 0 && kQBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+constexpr int kEpiBar = 1;                      // named barrier of the two epilogue groups
+constexpr int kSlotCap = kSegCandidates;        // candidate entries of one row of a piece
+constexpr int kCheckEvery = 4;                  // tiles between epilogue-wide checks of the slots
+static_assert(kSlotCap - kCheckEvery * 128 > kTopK, "room above the 2048 kept by a compaction");
 
 struct Misc {
     int32_t stage_valid[kStages];
     uint32_t tmem_base;
     int32_t abort;
+    int32_t cnt[kRows];                         // candidates in each row's slot of the current piece
+    uint32_t theta[kRows];                      // each row's threshold: only keys above it are candidates
+    int32_t bad;                                // an epilogue warp gave up
+    sel::Found found;
+    int32_t scratch[32];
 };
-static_assert(sizeof(Misc) <= 128, "misc block");
+static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
 
 // Work plan (device buffers in the caller's workspace).
 struct MtPlan {
@@ -72,9 +104,24 @@ struct MtPlan {
     int32_t* rb_req;       // [NBmax] request of each row block
     int64_t* item_start;   // [NBmax+1] (row block, tile) prefix
     int32_t* nb;           // [1] row blocks in this batch
+    // streaming top-k only (NULL otherwise): the pieces (CTA shares) of each
+    // row block, and the candidate slots of their rows.  Row rr of row block
+    // rb's j-th piece owns slot 8 piece_first[rb] + rr npieces(rb) + j, so
+    // each query row's slots are contiguous.
+    int32_t* piece_first;  // [NBmax+1]
+    int32_t* slot_row;     // [8 (NBmax + G)] query row of each slot, -1 = unused
+    int32_t* row_seg0;     // [T] first slot of each query row
+    int32_t* row_segn;     // [T] its slot count
+    int32_t* nslots;       // [1]
+    uint32_t* cand_key;    // [8 (NBmax + G), kSlotCap]
+    int32_t* cand_pos;
+    int32_t* cand_cnt;     // [8 (NBmax + G)]
+    uint32_t* hist;        // [T, 4096] top-12-bit key histogram of each row's candidates
+    int32_t G;             // CTAs the items are cut for
 };
 
 __device__ __forceinline__ int64_t cta_start(int64_t g, int64_t N, int64_t G) { return g * N / G; }
+__device__ __forceinline__ int64_t cta_of_item(int64_t x, int64_t N, int64_t G) { return ((x + 1) * G + N - 1) / N - 1; }
 
 // Rows [t0, t0 + R) of request r: R and the tiles to score -- up to its last
 // row's position, or (full_rows) the whole context.
@@ -133,6 +180,48 @@ plan_kernel(BatchDev b, int skip_short, int full_rows, MtPlan p) {
         irun += total;
     }
     if (gt == 0) p.item_start[NB] = irun;
+    if (!p.piece_first) return;
+    __syncthreads();
+    // pass 3 (streaming top-k): pieces of each row block, and the slots of their rows
+    const int64_t N = irun;
+    const int64_t G = p.G;
+    int32_t prun = 0;
+    for (int base = 0; base < NB; base += 1024) {
+        const int rb = base + gt;
+        int np = 0;
+        if (rb < NB) {
+            const int64_t s0 = p.item_start[rb], s1 = p.item_start[rb + 1];
+            if (s1 > s0) np = (int)(cta_of_item(s1 - 1, N, G) - cta_of_item(s0, N, G) + 1);
+        }
+        int total;
+        const int ex = sel::excl_scan<1024, 0>(np, gt, scratch, &total);
+        if (rb < NB) p.piece_first[rb] = prun + ex;
+        prun += total;
+    }
+    if (gt == 0) {
+        p.piece_first[NB] = prun;
+        *p.nslots = kRows * prun;
+    }
+    for (int i = gt; i < kRows * prun; i += 1024) p.slot_row[i] = -1;
+    for (int64_t i = gt; i < b.total_q; i += 1024) {          // rows without slots: not scored
+        p.row_seg0[i] = 0;
+        p.row_segn[i] = 0;
+    }
+    __syncthreads();
+    for (int rb = gt; rb < NB; rb += 1024) {
+        const int r = p.rb_req[rb];
+        const int t0 = (rb - p.rb_first[r]) * kRows;
+        const int qn = b.q_start[r + 1] - b.q_start[r];
+        const int R = min(kRows, qn - t0);
+        const int np = p.piece_first[rb + 1] - p.piece_first[rb];
+        const int base = kRows * p.piece_first[rb];
+        for (int rr = 0; rr < R; ++rr) {
+            const int64_t row = (int64_t)b.q_start[r] + t0 + rr;
+            p.row_seg0[row] = base + rr * np;
+            p.row_segn[row] = np;
+            for (int j = 0; j < np; ++j) p.slot_row[base + rr * np + j] = (int32_t)row;
+        }
+    }
 }
 
 // Row block holding item i (item_start is non-decreasing, item_start[NB] = N).
@@ -175,6 +264,192 @@ __device__ __forceinline__ bool walk_next(Walk& w, const MtPlan& p) {
     return false;
 }
 
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, %1;" ::"n"(kEpiBar), "n"(kEpiThreads) : "memory"); }
+
+constexpr int kSlotPer = kSlotCap / kEpiThreads;   // slot entries per epilogue thread
+static_assert(kSlotCap % kEpiThreads == 0, "whole slot entries per thread");
+
+// A slot's entries held in the epilogue threads' registers (entry et + u *
+// kEpiThreads in k[u], p[u]), as a selection source.
+struct RegSrc {
+    const uint32_t (&k)[kSlotPer];
+    const int32_t (&p)[kSlotPer];
+    int n, et;
+    template <class F>
+    __device__ __forceinline__ void visit(int, F&& f) const {
+#pragma unroll
+        for (int u = 0; u < kSlotPer; ++u) {
+            const bool a = et + u * kEpiThreads < n;
+            f(a, a ? k[u] : 0u, a ? p[u] : 0);
+        }
+    }
+};
+
+// Entries a compaction may keep before it falls back to the exact selection.
+constexpr int kKeepMax = kTopK + 512;
+static_assert(kKeepMax <= kSlotCap - kCheckEvery * 128, "a compaction always makes room");
+
+// Compaction of a slot of *n > 2048 entries in global memory, all epilogue
+// threads: one batch of loads into registers, then one histogram pass of
+// 4096 equal-width bins over the slot's key range [lo, hi] gives the bin b*
+// of the 2048th largest key.  T = the lower edge of b*: the slot keeps every
+// key >= T (at least 2048 entries), and a later key <= T cannot enter the
+// top-2048 (2048 kept entries are at or above it, at lower positions).  When
+// b* is crowded (ties, a narrow range) and more than kKeepMax would stay, the
+// exact radix selection keeps exactly the top-2048 (key, then lower position)
+// and T is the 2048th key.  Survivors are written back in any order; returns
+// T, the slot's new threshold.
+__device__ uint32_t compact_slot(uint32_t* key, int32_t* pos, int* n, int et, uint32_t* hist, int* scratch,
+                                 sel::Found* found) {
+    const int cnt = *n;
+    const int lane = et & 31, wid = et >> 5;
+    uint32_t k[kSlotPer];
+    int32_t ps[kSlotPer];
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int u = 0; u < kSlotPer; ++u) {
+        const int i = et + u * kEpiThreads;
+        const bool have = i < cnt;
+        k[u] = have ? __ldcg(key + i) : 0u;
+        ps[u] = have ? __ldcg(pos + i) : 0;
+        if (have) {
+            lo = min(lo, k[u]);
+            hi = max(hi, k[u]);
+        }
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (lane == 0) {
+        scratch[wid] = (int)lo;
+        scratch[kEpiWarps + wid] = (int)hi;
+    }
+    for (int i = et; i < 4096; i += kEpiThreads) hist[i] = 0u;
+    epi_sync();
+#pragma unroll
+    for (int v = 0; v < kEpiWarps; ++v) {
+        lo = min(lo, (uint32_t)scratch[v]);
+        hi = max(hi, (uint32_t)scratch[kEpiWarps + v]);
+    }
+    const uint32_t span = hi - lo;
+    const int shift = (span >> 12) ? 32 - __clz((int)(span >> 12)) : 0;   // (span >> shift) < 4096
+#pragma unroll
+    for (int u = 0; u < kSlotPer; ++u)
+        if (et + u * kEpiThreads < cnt) atomicAdd(&hist[(k[u] - lo) >> shift], 1u);
+    epi_sync();                                        // every scratch read above is done too
+    constexpr int kPer = (4096 + kEpiThreads - 1) / kEpiThreads;   // bins per thread, from the top
+    int mine = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int bin = 4095 - (et * kPer + q);
+        if (bin >= 0) mine += (int)hist[bin];
+    }
+    int total;
+    int above = sel::excl_scan<kEpiThreads, kEpiBar>(mine, et, scratch, &total);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int bin = 4095 - (et * kPer + q);
+        const int c = bin >= 0 ? (int)hist[bin] : 0;
+        if (above < kTopK && above + c >= kTopK) {
+            found->bin = (uint32_t)bin;
+            found->above = above + c;                  // entries in bins >= b*
+        }
+        above += c;
+    }
+    epi_sync();
+    sel::Threshold th{lo + (found->bin << shift), 0x7fffffff};
+    if (found->above > kKeepMax) {
+        epi_sync();                                    // found is rewritten by the selection
+        RegSrc src{k, ps, cnt, et};
+        th = sel::topk_threshold<kEpiThreads, kEpiBar>(src, kTopK, et, hist, scratch, found);
+    }
+    // survivors in warp order, then u, then lane: one scan of the warps' counts,
+    // and each store instruction of a warp writes consecutive entries
+    unsigned km[kSlotPer];
+    int wcount = 0;
+#pragma unroll
+    for (int u = 0; u < kSlotPer; ++u) {
+        km[u] = __ballot_sync(0xffffffffu, et + u * kEpiThreads < cnt && th.keep(k[u], ps[u]));
+        wcount += __popc(km[u]);
+    }
+    const int wbase = sel::excl_scan<kEpiThreads, kEpiBar>(lane == 0 ? wcount : 0, et, scratch, &total);
+    int at = __shfl_sync(0xffffffffu, wbase, 0);                 // every load is done
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int u = 0; u < kSlotPer; ++u) {
+        if ((km[u] >> lane) & 1u) {
+            const int o = at + __popc(km[u] & below);
+            key[o] = k[u];
+            pos[o] = ps[u];
+        }
+        at += __popc(km[u]);
+    }
+    if (et == 0) *n = total;
+    epi_sync();
+    return th.kth;
+}
+
+// Head-weighted ReLU sum of one token's 32 head logits (TMEM words) for one
+// query row: sum_m w_m max(l_m, 0), eight partial sums in four packed pairs.
+__device__ __forceinline__ float head_sum(const uint32_t (&v)[32], const float* __restrict__ w) {
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    float2 a[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a[j] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int m4 = 0; m4 < 8; ++m4) {
+        const float4 ww = __ldg(w4 + m4);
+        const float2 x01 = make_float2(fmaxf(__uint_as_float(v[4 * m4 + 0]), 0.f),
+                                       fmaxf(__uint_as_float(v[4 * m4 + 1]), 0.f));
+        const float2 x23 = make_float2(fmaxf(__uint_as_float(v[4 * m4 + 2]), 0.f),
+                                       fmaxf(__uint_as_float(v[4 * m4 + 3]), 0.f));
+        a[(2 * m4) & 3] = __ffma2_rn(make_float2(ww.x, ww.y), x01, a[(2 * m4) & 3]);
+        a[(2 * m4 + 1) & 3] = __ffma2_rn(make_float2(ww.z, ww.w), x23, a[(2 * m4 + 1) & 3]);
+    }
+    return ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
+}
+
+// Wait for this thread's TMEM loads, then pin the loaded registers after the
+// wait (the compiler sees them defined here, so no use moves above it).
+__device__ __forceinline__ void tmem_wait_regs(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;");
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// Scores of this thread's token (TMEM lane) for nr <= kPerGrp consecutive rows:
+// tbase + 32 j holds row j's 32 head logits, w + 32 j its head weights.  Rows
+// go in pairs: both loads, one wait, both sums.
+__device__ __forceinline__ void row_scores(uint32_t tbase, const float* __restrict__ w, int nr, float sk,
+                                           float (&s)[kPerGrp]) {
+#pragma unroll
+    for (int j = 0; j < kPerGrp; j += 2) {
+        if (j < nr) {
+            uint32_t va[32], vb[32];
+            tmem_ld_32x32b_x32(tbase + j * 32, va);
+            if (j + 1 < nr) tmem_ld_32x32b_x32(tbase + (j + 1) * 32, vb);
+            tmem_wait_regs(va);
+            reg_fence(vb);
+            s[j] = head_sum(va, w + j * 32) * sk;
+            if (j + 1 < nr) s[j + 1] = head_sum(vb, w + (j + 1) * 32) * sk;
+        }
+    }
+}
+
+// kStream: stream each row's candidates into its slots (dsa_indexer_topk);
+// otherwise write the score rows (dsa_indexer_scores).
+template <bool kStream>
 __global__ void __launch_bounds__(kThreads, 1)
 score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                   const uint8_t* __restrict__ cache, const float* __restrict__ wq, BatchDev b, MtPlan p,
@@ -195,16 +470,17 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 4);          // MMA commit + one arrive per warp of the epilogue group
+            mbar_init(&empty[s], 1 + kEpiWarps);  // MMA commit + one arrive per epilogue warp
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&accf[a], 1);
-            mbar_init(&acce[a], 4);
+            mbar_init(&acce[a], kEpiWarps);
             mbar_init(&qfull[a], 1);
             mbar_init(&qempty[a], 1);
         }
         mbar_init(drain, 1);
         misc->abort = 0;
+        misc->bad = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -389,26 +665,88 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // Group g takes the tiles whose running index has parity g (= its
-        // accumulator).  Warp w reads TMEM lanes 32 (w % 4) .., i.e. tokens
-        // 32 (w % 4) .. of the tile.
+        // Every group takes every tile (accumulator = running index parity),
+        // group g its share of the block's rows.  Warp w reads TMEM lanes
+        // 32 (w % 4) .., i.e. tokens 32 (w % 4) .. of the tile.  Streaming: the
+        // groups meet at a named barrier at each piece start, every kCheckEvery
+        // tiles of a piece and at its end, where full slots are compacted.
         const int grp = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int tok = quarter * 32 + lane;
+        const int et = threadIdx.x - 64;                 // 0 .. kEpiThreads - 1
+        uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
         Walk w;
         walk_begin(w, p, NB, i0, i1);
         int64_t gidx = 0;
         bool bad = false;
+        bool piece_start = true;
+        int ptile = 0;                                   // tiles of the current piece walked so far
+        int slot0 = 0, np = 0;                           // the piece's slot of row 0 and the row block's pieces
+        uint32_t th[kPerGrp];                              // the group's rows' thresholds (copies of misc->theta)
+#pragma unroll
+        for (int j = 0; j < kPerGrp; ++j) th[j] = 0u;
+        // Values of the current row block, read when it starts.
+        int r = 0, t0 = 0, qn = 0, R = 0, rlo = 0, nr = 0, p0 = 0;
+        int64_t row0 = 0, item0 = 0;
+        // Streaming: the previous tile's candidates, stored once its reservation
+        // (a shared atomic) has returned, i.e. after the next tile's arithmetic.
+        unsigned pend_m[kPerGrp];
+        uint32_t pend_key[kPerGrp];
+        int pend_pos = 0, pend_base = 0;
+        uint32_t* kslot = nullptr;                       // the group's first row's slot in this piece
+        int32_t* pslot = nullptr;
+        int64_t rstride = 0;                             // from one row's slot to the next row's
+#pragma unroll
+        for (int j = 0; j < kPerGrp; ++j) pend_m[j] = 0u;
+        auto flush = [&]() {
+            if constexpr (kStream) {
+                const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+                for (int j = 0; j < kPerGrp; ++j) {
+                    const int b_j = __shfl_sync(0xffffffffu, pend_base, j);
+                    if ((pend_m[j] >> lane) & 1u) {
+                        const int64_t at = j * rstride + b_j + __popc(pend_m[j] & below);
+                        kslot[at] = pend_key[j];
+                        pslot[at] = pend_pos;
+                    }
+                    pend_m[j] = 0u;
+                }
+            }
+        };
+        bool new_block = true;
         while (w.i < w.i_end) {
+            if (new_block) {
+                r = p.rb_req[w.rb];
+                t0 = (w.rb - p.rb_first[r]) * kRows;
+                qn = b.q_start[r + 1] - b.q_start[r];
+                R = min(kRows, qn - t0);
+                rlo = (grp * R + kGroups - 1) / kGroups;           // the group's rows: rlo .. rlo + nr - 1
+                nr = ((grp + 1) * R + kGroups - 1) / kGroups - rlo;
+                row0 = b.q_start[r] + t0;
+                p0 = b.seq_len[r] - qn + t0;                      // position of the block's first row
+                item0 = p.item_start[w.rb];
+            }
+            if (kStream && piece_start) {
+                const int64_t N = p.item_start[NB];
+                const int64_t g0 = cta_of_item(p.item_start[w.rb], N, G);
+                np = p.piece_first[w.rb + 1] - p.piece_first[w.rb];
+                slot0 = kRows * p.piece_first[w.rb] + (int)(blockIdx.x - g0);
+                epi_sync();                              // the previous piece is finished
+                if (et < kRows) {
+                    misc->cnt[et] = 0;
+                    misc->theta[et] = 0u;                // key 0: below every score
+                }
+                epi_sync();
+#pragma unroll
+                for (int j = 0; j < kPerGrp; ++j) th[j] = 0u;
+                rstride = (int64_t)np * kSlotCap;
+                kslot = p.cand_key + (int64_t)(slot0 + rlo * np) * kSlotCap;
+                pslot = p.cand_pos + (int64_t)(slot0 + rlo * np) * kSlotCap;
+                ptile = 0;
+            }
             if (!bad && __any_sync(0xffffffffu, *abort_flag != 0)) bad = true;   // another role gave up
-            if ((int)(gidx & 1) == grp && !bad) {
-                const int r = p.rb_req[w.rb];
-                const int t0 = (w.rb - p.rb_first[r]) * kRows;
-                const int L = b.seq_len[r];
-                const int qn = b.q_start[r + 1] - b.q_start[r];
-                const int R = min(kRows, qn - t0);
-                const int64_t row0 = b.q_start[r] + t0;
-                const int tile = (int)(w.i - p.item_start[w.rb]);
+            if (!bad) {
+                const int tile = (int)(w.i - item0);
                 const int stage = (int)(gidx % kStages);
                 const uint32_t phase = (uint32_t)((gidx / kStages) & 1);
                 const int acc = (int)(gidx & 1);
@@ -425,24 +763,32 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     const float sk = reinterpret_cast<const float*>(smem + kOffScales + stage * 512)[tok];
                     const int pos = tile * 128 + tok;
                     const bool page_ok = (vmask >> (tok >> 6)) & 1;
-                    const int p0 = L - qn + t0;               // position of the block's first row
-                    for (int rr = 0; rr < R; ++rr) {
-                        uint32_t v[32];
-                        tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + rr * 32, v);
-                        tmem_ld_wait();
-                        const float4* w4 = reinterpret_cast<const float4*>(wq + (row0 + rr) * 32);
-                        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                    float sc[kPerGrp];
+                    if (nr > 0)
+                        row_scores(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + rlo * 32,
+                                   wq + (row0 + rlo) * 32, nr, sk, sc);
+                    if constexpr (kStream) {
+                        // candidates above each row's threshold: one ballot per row, then lane j
+                        // reserves row rlo + j's room (the group's atomics go out together);
+                        // the previous tile's candidates are stored first
+                        flush();
+                        unsigned mine = 0;
 #pragma unroll
-                        for (int m4 = 0; m4 < 8; ++m4) {
-                            const float4 ww = __ldg(w4 + m4);
-                            a0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * m4 + 0]), 0.f), a0);
-                            a1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * m4 + 1]), 0.f), a1);
-                            a2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * m4 + 2]), 0.f), a2);
-                            a3 = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * m4 + 3]), 0.f), a3);
+                        for (int j = 0; j < kPerGrp; ++j) {
+                            const uint32_t key = score_key(sc[j]);
+                            const bool pass = j < nr && page_ok && pos <= p0 + rlo + j && key > th[j];
+                            pend_m[j] = __ballot_sync(0xffffffffu, pass);
+                            pend_key[j] = key;
+                            if (lane == j) mine = pend_m[j];
                         }
-                        const float score = ((a0 + a1) + (a2 + a3)) * sk;
-                        if (pos < ld)
-                            scores[(row0 + rr) * ld + pos] = (page_ok && pos <= p0 + rr) ? score : -INFINITY;
+                        pend_base = 0;
+                        if (mine) pend_base = atomicAdd(&misc->cnt[rlo + lane], __popc(mine));
+                        pend_pos = pos;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kPerGrp; ++j)
+                            if (j < nr && pos < ld)
+                                scores[(row0 + rlo + j) * ld + pos] = (page_ok && pos <= p0 + rlo + j) ? sc[j] : -INFINITY;
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -459,7 +805,41 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
             }
             ++gidx;
-            walk_next(w, p);
+            ++ptile;
+            const bool piece_end = w.i + 1 >= w.rb_end || w.i + 1 >= w.i_end;
+            if (kStream && (piece_end || ptile % kCheckEvery == 0)) {
+                // every tile of the piece so far is in the slots: compact the slots that
+                // may not hold the next kCheckEvery tiles, and at the piece end publish them
+                flush();
+                if (lane == 0 && bad) misc->bad = 1;
+                epi_sync();
+                const bool any_bad = misc->bad != 0;
+                if (!any_bad) {
+                    for (int rr = 0; rr < R; ++rr) {
+                        if (misc->cnt[rr] <= kSlotCap - kCheckEvery * 128) continue;
+                        const int64_t sl = (int64_t)(slot0 + rr * np) * kSlotCap;
+                        const uint32_t t = compact_slot(p.cand_key + sl, p.cand_pos + sl, &misc->cnt[rr], et, hist,
+                                                        misc->scratch, &misc->found);
+                        if (et == 0) misc->theta[rr] = t;
+                        epi_sync();
+                    }
+#pragma unroll
+                    for (int j = 0; j < kPerGrp; ++j) th[j] = misc->theta[rlo + j];
+                }
+                if (piece_end) {
+                    for (int rr = 0; rr < kRows; ++rr) {
+                        const int slot = slot0 + rr * np;
+                        if (rr >= R) break;
+                        const int cnt = any_bad ? 0 : misc->cnt[rr];
+                        if (et == 0) p.cand_cnt[slot] = cnt;
+                        uint32_t* gh = p.hist + (row0 + rr) * 4096;
+                        for (int i = et; i < cnt; i += kEpiThreads)
+                            atomicAdd(&gh[__ldcg(p.cand_key + (int64_t)slot * kSlotCap + i) >> 20], 1u);
+                    }
+                }
+            }
+            piece_start = walk_next(w, p);
+            new_block = piece_start;
         }
     }
     tc_fence_before();
@@ -506,32 +886,47 @@ static bool make_q8_tmap(const uint8_t* q8, int64_t total_q, CUtensorMap* out) {
     return true;
 }
 
-size_t mt_plan_bytes(int64_t batch, int64_t total_q) {
+// Workspace of the multi-row plan; with `slots` (streaming top-k) also the
+// pieces, the slot index and the candidate slots for a grid of G CTAs.
+static size_t mt_plan_layout(int64_t batch, int64_t total_q, int G, bool slots, imt::MtPlan* p, void* base) {
     const int64_t nb_max = (total_q + imt::kRows - 1) / imt::kRows + batch;
-    size_t b = 0;
-    b += (size_t)(batch + 1) * 4;                       // rb_first
-    b = (b + 15) / 16 * 16;
-    b += (size_t)nb_max * 4;                            // rb_req
-    b = (b + 15) / 16 * 16;
-    b += (size_t)(nb_max + 1) * 8;                      // item_start
-    b += 16;                                            // nb
-    return (b + 255) / 256 * 256;
+    const int64_t nslots = (int64_t)imt::kRows * (nb_max + G);
+    uint8_t* q = static_cast<uint8_t*>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) -> uint8_t* {
+        off = (off + align - 1) / align * align;
+        uint8_t* at = q ? q + off : nullptr;
+        off += bytes;
+        return at;
+    };
+    imt::MtPlan m{};
+    m.rb_first = reinterpret_cast<int32_t*>(take((size_t)(batch + 1) * 4, 16));
+    m.rb_req = reinterpret_cast<int32_t*>(take((size_t)nb_max * 4, 16));
+    m.item_start = reinterpret_cast<int64_t*>(take((size_t)(nb_max + 1) * 8, 16));
+    m.nb = reinterpret_cast<int32_t*>(take(16, 16));
+    m.G = G;
+    if (slots) {
+        m.piece_first = reinterpret_cast<int32_t*>(take((size_t)(nb_max + 1) * 4, 16));
+        m.slot_row = reinterpret_cast<int32_t*>(take((size_t)nslots * 4, 16));
+        m.row_seg0 = reinterpret_cast<int32_t*>(take((size_t)total_q * 4, 16));
+        m.row_segn = reinterpret_cast<int32_t*>(take((size_t)total_q * 4, 16));
+        m.nslots = reinterpret_cast<int32_t*>(take(16, 16));
+        m.cand_cnt = reinterpret_cast<int32_t*>(take((size_t)nslots * 4, 256));
+        m.cand_key = reinterpret_cast<uint32_t*>(take((size_t)nslots * imt::kSlotCap * 4, 256));
+        m.cand_pos = reinterpret_cast<int32_t*>(take((size_t)nslots * imt::kSlotCap * 4, 256));
+    }
+    if (p) *p = m;
+    return (off + 255) / 256 * 256;
+}
+
+size_t mt_plan_bytes(int64_t batch, int64_t total_q) { return mt_plan_layout(batch, total_q, 0, false, nullptr, nullptr); }
+size_t mt_topk_bytes(int64_t batch, int64_t total_q, int G) {
+    return mt_plan_layout(batch, total_q, G, true, nullptr, nullptr);
 }
 
 static imt::MtPlan carve_mt_plan(void* base, int64_t batch, int64_t total_q) {
-    const int64_t nb_max = (total_q + imt::kRows - 1) / imt::kRows + batch;
-    uint8_t* q = static_cast<uint8_t*>(base);
     imt::MtPlan p;
-    size_t off = 0;
-    p.rb_first = reinterpret_cast<int32_t*>(q + off);
-    off += (size_t)(batch + 1) * 4;
-    off = (off + 15) / 16 * 16;
-    p.rb_req = reinterpret_cast<int32_t*>(q + off);
-    off += (size_t)nb_max * 4;
-    off = (off + 15) / 16 * 16;
-    p.item_start = reinterpret_cast<int64_t*>(q + off);
-    off += (size_t)(nb_max + 1) * 8;
-    p.nb = reinterpret_cast<int32_t*>(q + off);
+    mt_plan_layout(batch, total_q, 0, false, &p, base);
     return p;
 }
 
@@ -546,15 +941,49 @@ dsa_status launch_indexer_rows(const uint8_t* q8, const float* wq, const uint8_t
     CUtensorMap kmap, qmap;
     if (!make_index_tmap(cache, b->num_pages, false, &kmap)) return DSA_ERR_CUDA;
     if (!make_q8_tmap(q8, b->total_q, &qmap)) return DSA_ERR_CUDA;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(&imt::score_rows_kernel), imt::kSmemAlloc) != DSA_OK)
+    if (ensure_smem_limit(reinterpret_cast<const void*>(&imt::score_rows_kernel<false>), imt::kSmemAlloc) != DSA_OK)
         return DSA_ERR_CUDA;
     BatchDev bd = to_dev(b);
     imt::MtPlan p = carve_mt_plan(plan_ws, b->batch, b->total_q);
+    p.G = G;
     imt::plan_kernel<<<1, 1024, 0, s>>>(bd, skip_short ? 1 : 0, full_rows ? 1 : 0, p);
     DSA_CHECK_LAUNCH();
-    imt::score_rows_kernel<<<G, imt::kThreads, imt::kSmemAlloc, s>>>(kmap, qmap, cache, wq, bd, p, scores, ld, st);
+    imt::score_rows_kernel<false><<<G, imt::kThreads, imt::kSmemAlloc, s>>>(kmap, qmap, cache, wq, bd, p, scores, ld, st);
     DSA_CHECK_LAUNCH();
     return DSA_OK;
+}
+
+// Indexer top-2048 of every query row of a multi-row batch without score rows:
+// plan, streaming score kernel, then the decode indexer's merge in row mode.
+// hist: [T, 4096] words, cleared by the query quantisation before this call.
+dsa_status launch_indexer_rows_topk(const uint8_t* q8, const float* wq, uint32_t* hist, const uint8_t* cache,
+                                    const dsa_batch* b, int32_t* topk, float* topk_scores, void* plan_ws, int G,
+                                    int32_t* st, cudaStream_t s) {
+    CUtensorMap kmap, qmap;
+    if (!make_index_tmap(cache, b->num_pages, false, &kmap)) return DSA_ERR_CUDA;
+    if (!make_q8_tmap(q8, b->total_q, &qmap)) return DSA_ERR_CUDA;
+    if (ensure_smem_limit(reinterpret_cast<const void*>(&imt::score_rows_kernel<true>), imt::kSmemAlloc) != DSA_OK)
+        return DSA_ERR_CUDA;
+    BatchDev bd = to_dev(b);
+    imt::MtPlan p;
+    mt_plan_layout(b->batch, b->total_q, G, true, &p, plan_ws);
+    p.hist = hist;
+    imt::plan_kernel<<<1, 1024, 0, s>>>(bd, 1, 0, p);
+    DSA_CHECK_LAUNCH();
+    imt::score_rows_kernel<true><<<G, imt::kThreads, imt::kSmemAlloc, s>>>(kmap, qmap, cache, wq, bd, p, nullptr, 0, st);
+    DSA_CHECK_LAUNCH();
+    Plan mp{};
+    mp.cand_key = p.cand_key;
+    mp.cand_pos = p.cand_pos;
+    mp.cand_cnt = p.cand_cnt;
+    mp.hist = hist;
+    mp.slot_row = p.slot_row;
+    mp.row_seg0 = p.row_seg0;
+    mp.row_segn = p.row_segn;
+    mp.nslots = p.nslots;
+    mp.seg_stride = imt::kSlotCap;
+    const int64_t nb_max = (b->total_q + imt::kRows - 1) / imt::kRows + b->batch;
+    return launch_topk_merge(b, mp, (int64_t)imt::kRows * (nb_max + G), topk, topk_scores, s);
 }
 
 }  // namespace dsa

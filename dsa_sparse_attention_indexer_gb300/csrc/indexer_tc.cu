@@ -59,6 +59,7 @@ constexpr int kCheckEvery = 4;                  // tiles between epilogue-wide c
 constexpr int kMinTiles = 16;                   // smallest per-CTA share of tiles
 constexpr int kCap = 4608;                      // candidate buffer entries
 constexpr int kSegCand = kCap;                  // candidate slots of one segment in the workspace
+static_assert(kSegCand == kSegCandidates, "segment slots shared with the multi-row indexer");
 constexpr int kEpiThreads = 256;                // two epilogue groups of 4 warps, alternating tiles
 constexpr int kThreads = 96 + kEpiThreads;      // + two producer warps + MMA warp
 constexpr int kProducer2Warp = (64 + kEpiThreads) / 32;   // the second producer, after the epilogue warps
@@ -828,13 +829,18 @@ merge_filter_kernel(BatchDev b, Plan p) {
     __shared__ int32_t scratch[32];
     __shared__ uint32_t s_bstar;
     const int s = blockIdx.x;
-    if (s >= p.seg_first[b.batch]) return;             // launched for the most segments a plan can hold
+    int64_t row;
+    if (p.slot_row) {                                  // row mode
+        if (s >= *p.nslots || p.slot_row[s] < 0) return;
+        row = p.slot_row[s];
+    } else {
+        if (s >= p.seg_first[b.batch]) return;         // launched for the most segments a plan can hold
+        row = b.q_start[p.segs[s].r];
+    }
     const int tid = threadIdx.x;
-    const Seg sg = p.segs[s];
-    const int64_t row = b.q_start[sg.r];
     const int cnt = min(p.cand_cnt[s], kSegCand);
-    uint32_t* key = p.cand_key + (int64_t)s * kSegCand;
-    int32_t* pos = p.cand_pos + (int64_t)s * kSegCand;
+    uint32_t* key = p.cand_key + (int64_t)s * p.seg_stride;
+    int32_t* pos = p.cand_pos + (int64_t)s * p.seg_stride;
     uint32_t k[kFiltPer];
 #pragma unroll
     for (int u = 0; u < kFiltPer; ++u) {               // keys first: their loads overlap the scan below
@@ -915,9 +921,10 @@ struct BndSrc {
     const int32_t* ns_pre;      // [nseg + 1] prefix of sure counts (shared memory)
     const int32_t* nb_pre;      // [nseg + 1] prefix of boundary counts (shared memory)
     int nseg, n;
+    int64_t stride;             // entries from one segment slot to the next
     __device__ __forceinline__ int64_t at(int i) const {
         const int j = seg_lookup(nb_pre, nseg, i);
-        return (int64_t)j * kSegCand + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
+        return (int64_t)j * stride + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
     }
     template <class F>
     __device__ __forceinline__ void visit(int gt, F&& f) const {
@@ -1023,7 +1030,8 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
         return;
     }
     // filtered counts of the row's segments (nseg <= number of CTAs <= 1024)
-    const int s0 = p.seg_first[r], nseg = p.seg_first[r + 1] - s0;
+    const int s0 = p.row_seg0 ? p.row_seg0[row] : p.seg_first[r];
+    const int nseg = p.row_seg0 ? p.row_segn[row] : p.seg_first[r + 1] - s0;
     const int packed = gt < nseg ? p.cand_cnt[s0 + gt] : 0;
     int n_sure, n_bnd;
     const int es = sel::excl_scan<kMergeThreads, 0>(packed & 0xffff, gt, mm->scratch, &n_sure);
@@ -1034,12 +1042,12 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     }
     if (gt == 0) mm->n_sel = 0;
     __syncthreads();
-    const uint32_t* ckey = p.cand_key + (int64_t)s0 * kSegCand;
-    const int32_t* cpos = p.cand_pos + (int64_t)s0 * kSegCand;
+    const uint32_t* ckey = p.cand_key + (int64_t)s0 * p.seg_stride;
+    const int32_t* cpos = p.cand_pos + (int64_t)s0 * p.seg_stride;
     n_sure = min(n_sure, kTopK);
     for (int i = gt; i < n_sure; i += kMergeThreads) {           // entries above the boundary bin: all in
         const int j = seg_lookup(ns_pre, nseg, i);
-        const int64_t x = (int64_t)j * kSegCand + (i - ns_pre[j]);
+        const int64_t x = (int64_t)j * p.seg_stride + (i - ns_pre[j]);
         sel_pos[i] = cpos[x];
         sel_key[i] = ckey[x];
     }
@@ -1048,7 +1056,7 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     if (need > 0 && n_bnd <= need) {                             // the whole boundary bin fits
         for (int i = gt; i < n_bnd; i += kMergeThreads) {
             const int j = seg_lookup(nb_pre, nseg, i);
-            const int64_t x = (int64_t)j * kSegCand + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
+            const int64_t x = (int64_t)j * p.seg_stride + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
             sel_pos[n_sure + i] = cpos[x];
             sel_key[n_sure + i] = ckey[x];
         }
@@ -1056,7 +1064,7 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     } else if (need > 0 && n_bnd <= kBndCap) {                   // exact selection in shared memory
         for (int i = gt; i < n_bnd; i += kMergeThreads) {
             const int j = seg_lookup(nb_pre, nseg, i);
-            const int64_t x = (int64_t)j * kSegCand + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
+            const int64_t x = (int64_t)j * p.seg_stride + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
             bnd_pos[i] = cpos[x];
             bnd_key[i] = ckey[x];
         }
@@ -1076,7 +1084,7 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     } else if (need > 0) {                                       // boundary bin too large: select in place
         if (gt == 0) mm->n_sel = n_sure;
         __syncthreads();
-        BndSrc src{ckey, cpos, ns_pre, nb_pre, nseg, n_bnd};
+        BndSrc src{ckey, cpos, ns_pre, nb_pre, nseg, n_bnd, p.seg_stride};
         const sel::Threshold th = sel::topk_threshold<kMergeThreads, 0>(src, need, gt, hist, mm->scratch, &mm->found,
                                                                         1, ckey[src.at(0)] >> 20);
         src.visit(gt, [&](bool a, uint32_t key, int32_t pos) {
@@ -1190,6 +1198,8 @@ Plan carve_plan(void* base, int64_t batch, int G) {
     q += nseg * itc::kSegCand * 4;
     p.cand_cnt = reinterpret_cast<int32_t*>(q);
     p.hist = nullptr;
+    p.slot_row = p.row_seg0 = p.row_segn = p.nslots = nullptr;
+    p.seg_stride = itc::kSegCand;
     return p;
 }
 
@@ -1212,8 +1222,18 @@ dsa_status launch_indexer_tc(const void* q, const float* w, uint8_t* q8, float* 
     if (mx) itc::score_topk_kernel<true><<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
     else itc::score_topk_kernel<false><<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
     DSA_CHECK_LAUNCH();
-    itc::merge_filter_kernel<<<(unsigned)(G + b->batch), itc::kFiltThreads, 0, s>>>(bd, p);
-    DSA_CHECK_LAUNCH();
+    return launch_topk_merge(b, p, (int64_t)G + b->batch, topk, topk_scores, s);
+}
+
+dsa_status launch_topk_merge(const dsa_batch* b, Plan p, int64_t max_segs, int32_t* topk, float* topk_scores,
+                             cudaStream_t s) {
+    if (ensure_smem_limit(reinterpret_cast<const void*>(&itc::merge_kernel), itc::kMergeSmem) != DSA_OK)
+        return DSA_ERR_CUDA;
+    BatchDev bd = to_dev(b);
+    if (max_segs > 0) {
+        itc::merge_filter_kernel<<<(unsigned)max_segs, itc::kFiltThreads, 0, s>>>(bd, p);
+        DSA_CHECK_LAUNCH();
+    }
     itc::merge_kernel<<<(unsigned)b->total_q, itc::kMergeThreads, itc::kMergeSmem, s>>>(bd, p, topk, topk_scores);
     DSA_CHECK_LAUNCH();
     return DSA_OK;

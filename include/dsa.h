@@ -212,7 +212,12 @@ dsa_status dsa_latent_kv_store_fused(const void* kv_c, const void* k_pe, const i
  *   topk_scores device fp32 [T,2048] or NULL: the score of each selected
  *               position (0 for -1 entries and for short contexts)
  *   share       NULL, or a share handle that receives (layer_id, topk, T)
- *   ws          device workspace of at least dsa_indexer_topk_workspace_size() bytes */
+ *   ws          device workspace of at least dsa_indexer_topk_workspace_size() bytes.
+ *               A decode batch (one query row per request) needs O(T) bytes for
+ *               any GPU; a batch with several rows per request needs row
+ *               histograms plus candidate slots of 4608 entries per query row
+ *               and CTA share, O(T x 4608), sized for the SM count of the device
+ *               current at the size call (call both on the same device).       */
 dsa_status dsa_indexer_topk_workspace_size(const dsa_batch* b, size_t* bytes);
 dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_cache,
                             const dsa_batch* b, int32_t* topk, float* topk_scores,
@@ -223,8 +228,10 @@ dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_c
  * dsa_indexer_topk for a cache written by dsa_index_k_store_mxfp4: the same
  * queries, selection rule, outputs, share handle and workspace (sized by
  * dsa_indexer_topk_workspace_size); scores are formed on the dequantised
- * values (E2M1 x 2^e per 32-dim block).  Decode batches only (q_len == 1 for
- * every request; others return DSA_ERR_UNSUPPORTED).
+ * values (E2M1 x 2^e per 32-dim block).  A batch with several query rows per
+ * request (verify, prefill) runs each row as a decode row over its request's
+ * keys up to its position, so each row reads the keys once; at most 65535
+ * rows (DSA_ERR_UNSUPPORTED beyond).
  *   idxk_cache device uint8 [num_pages * 4352], 32-byte aligned               */
 dsa_status dsa_indexer_topk_mxfp4(const void* q, const float* w, const uint8_t* idxk_cache,
                                   const dsa_batch* b, int32_t* topk, float* topk_scores,

@@ -162,13 +162,114 @@ def test_indexer_topk_mxfp4_records_bad_page_without_fault(mx_case):
     assert not np.any((topk[4] >= 3 * 64) & (topk[4] < 4 * 64))   # the skipped page contributes nothing
 
 
-def test_indexer_topk_mxfp4_rejects_multi_token_rows():
-    w = Workload("mx2", 1, [3000], [2], ["full"])
+# Several query rows per request (speculative verify, prefill chunks): row t of
+# a request sees positions 0 .. L - q_len + t; rows of 2047 and 2048 visible
+# positions take the short-context rule.
+MXR_SEQ = [9000, 2050, 40000, 3000]
+MXR_Q = [4, 4, 3, 5]
+
+
+def _mx_keys(seq, seed):
+    g = _gen(seed)
+    return g, [f64(torch.randn(L, 128, generator=g).to(torch.bfloat16)) for L in seq]
+
+
+@pytest.fixture(scope="module")
+def mx_rows_case():
+    w = Workload("mxr", 6161, list(MXR_SEQ), list(MXR_Q), ["full"])
+    g, raws = _mx_keys(MXR_SEQ, 6161)
+    pt = page_table(w, "cpu")
+    meta = batch_meta(w, "cpu")
+    mx = np.zeros((w.num_pages, PB), np.uint8)
+    fp8 = np.zeros((w.num_pages, O.INDEX_PAGE_BYTES), np.uint8)
+    for r, L in enumerate(MXR_SEQ):
+        p = np.arange(L)
+        slots = pt[r, p // 64].numpy().astype(np.int64) * 64 + p % 64
+        codes, exps = O.index_k_prepare_mxfp4(raws[r], p)
+        O.mxfp4_cache_write(mx, slots, codes, exps)
+        c8, s8 = O.index_k_prepare(raws[r], p)
+        O.index_cache_write(fp8, slots, c8, s8)
+    q = torch.randn(w.total_q, 32, 128, generator=g).to(torch.bfloat16)
+    wt = torch.randn(w.total_q, 32, generator=g) / math.sqrt(32)
+    qs = meta["q_start"].numpy()
+    rows = []
+    for r, L in enumerate(MXR_SEQ):
+        ql = MXR_Q[r]
+        topk, scores = O.request_topk_mxfp4(f64(q[qs[r]:qs[r] + ql]), f64(wt[qs[r]:qs[r] + ql]), mx, pt[r].numpy(),
+                                            L, ql)
+        kc, ke = O.mxfp4_cache_read(mx, pt[r].numpy(), L)
+        k8, s8 = O.index_cache_read(fp8, pt[r].numpy(), L)
+        for t in range(ql):
+            i = qs[r] + t
+            n = L - ql + t + 1
+            row = dict(i=i, n=n, topk=topk[t], s=scores[t])
+            if n > 2048:
+                qc, qsc = O.index_q_quantize(f64(q[i]))
+                row["mag"] = O.score_magnitude_mxfp4(qc, qsc, f64(wt[i]), kc[:n], ke[:n])
+                s_fp8 = O.indexer_scores(qc, qsc, f64(wt[i]), k8[:n], s8[:n])
+                row["overlap"] = len(set(O.topk_positions(s_fp8, n).tolist()) & set(topk[t].tolist())) / 2048
+            rows.append(row)
+    batch = D.Batch(meta["seq_len"].to(DEV), meta["q_start"].to(DEV), pt.to(DEV), w.num_pages,
+                    max_seq_len=w.max_seq_len, max_q_len=max(MXR_Q), total_q=w.total_q)
+    return dict(w=w, mx=torch.from_numpy(mx.reshape(-1)).to(DEV), fp8=torch.from_numpy(fp8.reshape(-1)).to(DEV),
+                q=q.to(DEV), wt=wt.to(DEV), batch=batch, rows=rows)
+
+
+def test_indexer_topk_mxfp4_multi_token_rows_match_oracle(mx_rows_case):
+    c = mx_rows_case
+    T = c["w"].total_q
+    sc = torch.empty(T, 2048, device=DEV)
+    st = D.new_device_status(DEV)
+    topk = D.dsa_indexer_topk_mxfp4(c["q"], c["wt"], c["mx"], c["batch"], topk_scores=sc, dev_status=st)
+    assert D.dsa_device_status_read(st)[0] == 0
+    topk, sc = topk.cpu().numpy(), sc.cpu().numpy()
+    ndiff = 0
+    for row in c["rows"]:
+        i = row["i"]
+        if row["n"] <= 2048:
+            assert np.array_equal(topk[i], row["topk"]), f"short row {i}"
+            continue
+        ndiff += check_topk_row(topk[i], row["topk"], row["s"], row["mag"], row["n"], what=f"row {i}")
+        check_scores(sc[i], row["s"][topk[i]], row["mag"][topk[i]], what=f"selected scores row {i}")
+    assert ndiff <= 4
+    nbytes = D.dsa_indexer_topk_workspace_size(c["batch"])
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)   # a dirty workspace changes nothing
+    again = D.dsa_indexer_topk_mxfp4(c["q"], c["wt"], c["mx"], c["batch"], ws=ws).cpu().numpy()
+    assert np.array_equal(again, topk)
+
+
+# The MXFP4 keys change the selection itself ("GLM-5.3 推理全链路(十一)", 两个框架的
+# 对照): on these Gaussian keys the oracle's MXFP4 and FP8 top-2048 share 0.88 to
+# 0.93 of their positions.  The library's two selections must share as much (up to
+# the positions the parity rule lets differ) and never fall below 0.85.
+OVERLAP_FLOOR = 0.85
+
+
+def test_indexer_topk_mxfp4_vs_fp8_selection_overlap(mx_rows_case):
+    c = mx_rows_case
+    t4 = D.dsa_indexer_topk_mxfp4(c["q"], c["wt"], c["mx"], c["batch"]).cpu().numpy()
+    t8 = D.dsa_indexer_topk(c["q"], c["wt"], c["fp8"], c["batch"]).cpu().numpy()
+    seen = []
+    for row in c["rows"]:
+        i = row["i"]
+        if row["n"] <= 2048:
+            assert np.array_equal(t4[i], t8[i])
+            continue
+        ov = len(set(t4[i].tolist()) & set(t8[i].tolist())) / 2048
+        seen.append(ov)
+        assert ov >= OVERLAP_FLOOR, f"row {i}: overlap {ov:.3f}"
+        assert abs(ov - row["overlap"]) <= 0.01, f"row {i}: overlap {ov:.3f}, oracle {row['overlap']:.3f}"
+    assert len(seen) >= 10
+
+
+def test_indexer_topk_mxfp4_refuses_too_many_rows():
+    w = Workload("mx2", 1, [70000], [65536], ["full"])
     meta = batch_meta(w, "cpu")
     batch = D.Batch(meta["seq_len"].to(DEV), meta["q_start"].to(DEV), page_table(w, DEV), w.num_pages,
-                    max_seq_len=3000, max_q_len=2, total_q=2)
+                    max_seq_len=70000, max_q_len=65536, total_q=65536)
     with pytest.raises(D.DsaError) as e:
-        D.dsa_indexer_topk_mxfp4(torch.zeros(2, 32, 128, dtype=torch.bfloat16, device=DEV),
-                                 torch.zeros(2, 32, device=DEV), torch.zeros(w.num_pages * PB, dtype=torch.uint8,
-                                                                               device=DEV), batch)
+        D.dsa_indexer_topk_mxfp4(torch.zeros(65536, 32, 128, dtype=torch.bfloat16, device=DEV),
+                                 torch.zeros(65536, 32, device=DEV), torch.zeros(w.num_pages * PB, dtype=torch.uint8,
+                                                                                 device=DEV), batch,
+                                 ws=torch.empty(4096, dtype=torch.uint8, device=DEV))
     assert e.value.name == "DSA_ERR_UNSUPPORTED"

@@ -611,3 +611,83 @@ def test_indexer_topk_decode_all_keys_equal():
         m1 = O.score_magnitude(qc, qs, f64(wt[r]), kc, ks)[0]
         check_scores(sc[r], np.full(2048, s1), np.full(2048, m1), what=f"row {r} scores")
         assert np.all(sc[r] == sc[r][0])
+
+
+# ------------------------------------------------------------------ multi-row top-k without score rows
+# Batches with several query rows per request stream each row's candidates into
+# workspace slots, compacting a slot to its exact top-2048 when it fills.  These
+# contexts are long enough that a row block is cut into several CTA pieces and
+# slots fill several times.
+LONG_SEQ = [40000, 25000, 9000, 2100]
+LONG_Q = [6, 8, 3, 5]
+
+
+@pytest.fixture(scope="module")
+def multirow_long_case():
+    return _build_indexer_case(LONG_SEQ, LONG_Q, 4321, boost_req=1)
+
+
+def test_indexer_topk_multirow_streaming_matches_oracle(multirow_long_case):
+    _check_indexer_topk(multirow_long_case, 4)
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xFF])
+def test_indexer_topk_multirow_dirty_workspace_and_repeat(multirow_long_case, fill):
+    c = multirow_long_case
+    nbytes = D.dsa_indexer_topk_workspace_size(c["batch"])
+    ws = torch.full((nbytes,), fill, dtype=torch.uint8, device=DEV)
+    st = D.new_device_status(DEV)
+    a = D.dsa_indexer_topk(c["q"], c["wt"], c["cache"], c["batch"], ws=ws, dev_status=st)
+    b = D.dsa_indexer_topk(c["q"], c["wt"], c["cache"], c["batch"], ws=ws, dev_status=st)
+    assert D.dsa_device_status_read(st)[0] == 0
+    assert torch.equal(a, b)
+    got = a.cpu().numpy()
+    for row in c["rows"]:
+        check_topk_row(got[row["i"]], row["topk"], row["s"], row["mag"], row["n"], what=f"row {row['i']}")
+
+
+def test_indexer_topk_multirow_workspace_has_no_score_rows():
+    # the workspace holds candidate slots, not T x context score rows: for 8192
+    # rows on a 131072-token context it stays far below the 4.29 GB of fp32 rows
+    seq, ql = [131072], [8192]
+    w = _small_workload(seq, ql, 1)
+    meta = batch_meta(w, "cpu")
+    pt = torch.zeros((1, 131072 // 64), dtype=torch.int32)
+    batch = D.Batch(meta["seq_len"].to(DEV), meta["q_start"].to(DEV), pt.to(DEV), 2048, max_seq_len=131072,
+                    max_q_len=8192, total_q=8192)
+    nbytes = D.dsa_indexer_topk_workspace_size(batch)
+    assert nbytes < 8192 * 131072 * 4 // 4
+
+
+def test_indexer_topk_multirow_all_keys_equal():
+    """Multi-row batches whose every cached key is the same: every score ties,
+    so each row with more than 2048 visible positions selects 0..2047 exactly,
+    through compactions of slots made entirely of ties."""
+    seq, ql = [20000, 5000], [4, 7]
+    w = _small_workload(seq, ql, 4545)
+    g = _gen(4545)
+    pt = page_table(w, "cpu")
+    meta = batch_meta(w, "cpu")
+    one_codes, one_scales = O.index_k_prepare(f64(torch.randn(1, 128, generator=g).to(torch.bfloat16)), np.array([5]))
+    cache = np.zeros((w.num_pages, O.INDEX_PAGE_BYTES), np.uint8)
+    for r, L in enumerate(seq):
+        p = np.arange(L)
+        O.index_cache_write(cache, pt[r, p // 64].numpy().astype(np.int64) * 64 + p % 64,
+                            np.repeat(one_codes, L, axis=0), np.repeat(one_scales, L))
+    T = sum(ql)
+    q = torch.randn(T, 32, 128, generator=g).to(torch.bfloat16)
+    wt = torch.randn(T, 32, generator=g).abs() / math.sqrt(32)
+    batch = D.Batch(meta["seq_len"].to(DEV), meta["q_start"].to(DEV), pt.to(DEV), w.num_pages,
+                    max_seq_len=w.max_seq_len, max_q_len=max(ql), total_q=T)
+    sc = torch.empty(T, 2048, device=DEV)
+    st = D.new_device_status(DEV)
+    topk = D.dsa_indexer_topk(q.to(DEV), wt.to(DEV), torch.from_numpy(cache.reshape(-1)).to(DEV), batch,
+                              topk_scores=sc, dev_status=st)
+    assert D.dsa_device_status_read(st)[0] == 0
+    topk, sc = topk.cpu().numpy(), sc.cpu().numpy()
+    qs = meta["q_start"].numpy()
+    for r, L in enumerate(seq):
+        for t in range(ql[r]):
+            i = qs[r] + t
+            assert topk[i].tolist() == list(range(2048)), f"row {i}"
+            assert np.all(sc[i] == sc[i][0])
