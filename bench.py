@@ -401,12 +401,15 @@ class MtpStep:
 KERNELS_PER_CALL = {"index_k_store": 1, "latent_kv_store": 1, "indexer_topk": 4, "sparse_mla_decode": 1}
 
 
-def kernels_per_call(name, rows, sms):
-    """Kernels one call launches.  The indexer launches four either way (decode:
-    prep, score, merge filter, merge; multi-token: quantisation, plan, score
-    rows, select).  Sparse MLA launches one kernel when its rows are cut into
+def kernels_per_call(name, rows, sms, multi_row=False):
+    """Kernels one call launches.  The indexer launches four for a decode batch
+    (prep, score, merge filter, merge) and five for a batch with several rows
+    per request (FP8: quantisation, plan, score rows, merge filter, merge;
+    MXFP4: the virtual decode batch, then the four).  Sparse MLA launches one kernel when its rows are cut into
     clusters of 2 or 4 CTAs or taken whole, and a second, the log-sum-exp
     combine, when CTAs leave partials: the library's split rule, restated."""
+    if name == "indexer_topk" and multi_row:
+        return 5
     if name != "sparse_mla_decode":
         return KERNELS_PER_CALL[name]
     if rows < sms:
@@ -466,6 +469,29 @@ def job_throughput(rows_per_rank, world, ms):
 
 
 # ----------------------------------------------------------------------------
+def selection_overlap(gw, D):
+    """How much the MXFP4 index-K cache changes the selection: for every query
+    row with more than 2048 visible positions, the share of its FP8 top-2048
+    that the MXFP4 top-2048 also holds (same keys, queries and weights; the
+    other format's cache is stored outside the timed region)."""
+    other = gw.other_index_cache()
+    fp8, mx = (other, gw.idx_cache) if gw.mx else (gw.idx_cache, other)
+    t8 = D.dsa_indexer_topk(gw.q_idx, gw.w_idx, fp8, gw.batch)
+    t4 = D.dsa_indexer_topk_mxfp4(gw.q_idx, gw.w_idx, mx, gw.batch)
+    w = gw.w
+    n_vis = torch.tensor([L - ql + t + 1 for L, ql in zip(w.seq_len, w.q_len) for t in range(ql)],
+                         device=t8.device)
+    both = torch.sort(torch.cat([t8, t4], 1), 1).values
+    common = ((both[:, 1:] == both[:, :-1]) & (both[:, 1:] >= 0)).sum(1).double() / 2048.0
+    common = common[n_vis > 2048]
+    del other, t8, t4, both
+    torch.cuda.empty_cache()
+    if common.numel() == 0:
+        return {"rows": 0}
+    return {"mean": round(float(common.mean()), 4), "min": round(float(common.min()), 4),
+            "rows": int(common.numel())}
+
+
 def run_ours(args, rank, world, workload=None, with_e2e=True):
     import dsa_sparse_attention_indexer_gb300 as D
     import synth
@@ -598,10 +624,11 @@ def run_ours(args, rank, world, workload=None, with_e2e=True):
     if flush_buf is None:
         del cold_flush
     timers = {k: [None] * len(v) for k, v in call_graphs.items()}
+    overlap = selection_overlap(gw, D)
     if not with_e2e:
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         return dict(w=w, ms=ms, per_call=per_call, per_launch=per_launch, cold_call=cold_call,
-                    cold_launch=cold_launch, in_step=in_step_ok, clocks=clocks, flush=flush)
+                    cold_launch=cold_launch, in_step=in_step_ok, clocks=clocks, flush=flush, overlap=overlap)
 
     # ---- end to end: host buffers in, host buffers out, through the same calls
     first_in, layer_in, outs = step.e2e_io()
@@ -673,7 +700,9 @@ def run_ours(args, rank, world, workload=None, with_e2e=True):
     mla_rows = len(w.seq_len) if w.draft_steps else w.total_q     # a draft step's launch: one row per request
     return dict(w=w, ms=ms, e2e_ms=e2e_ms, per_call=per_call, per_launch=per_launch, cold_call=cold_call,
                 cold_launch=cold_launch, in_step=in_step_ok, clocks=clocks, flush=flush, h2d=h2d, d2h=d2h,
-                launches=sum(kernels_per_call(k, mla_rows, sms) * len(v) for k, v in timers.items()))
+                overlap=overlap,
+                launches=sum(kernels_per_call(k, mla_rows, sms, multi_row=max(w.q_len) > 1 and not w.draft_steps)
+                             * len(v) for k, v in timers.items()))
 
 
 # ----------------------------------------------------------------------------
@@ -803,7 +832,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per reference pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--index-cache", default="fp8", choices=["fp8", "mxfp4"],
-                    help="index-K cache format (mxfp4: decode workloads)")
+                    help="index-K cache format")
     ap.add_argument("--fused-store", action="store_true",
                     help="store each layer's latent row (and, on full layers, the index key) with the fused "
                          "RMSNorm / RoPE call from raw kv_c and k_pe")
@@ -814,8 +843,8 @@ def main():
                     help="a second workload measured after the headline one and reported in its line's "
                          "'secondary' block (device time and roofline only)")
     args = ap.parse_args()
-    if args.index_cache == "mxfp4" and args.workload not in ("tiny", "decode32k", "decode1m"):
-        ap.error("--index-cache mxfp4 covers the decode workloads (tiny, decode32k, decode1m)")
+    if args.index_cache == "mxfp4" and args.workload == "mtp5_1m":
+        ap.error("--index-cache mxfp4 covers every workload but mtp5_1m (its draft steps share FP8 selections)")
     if args.fused_store and (args.index_cache == "mxfp4" or args.workload == "mtp5_1m"):
         ap.error("--fused-store writes FP8 index keys in the layer-group step")
 
@@ -880,6 +909,7 @@ def main():
             **({"draft_steps": w.draft_steps, "mtp_reuse": not args.no_mtp_reuse} if w.draft_steps else {}),
             "index_cache": w.index_format,
             "store": "fused" if args.fused_store else "separate",
+            "mxfp4_vs_fp8_topk_overlap": res["overlap"],
         },
         "roofline": roof,
         "peaks": {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"], "source": pk["source"],
@@ -904,6 +934,7 @@ def main():
             "us_per_call": {k: round(v, 2) for k, v in r2["per_call"].items()},
             "us_per_launch_alone_l2_flushed": {k: round(v, 2) for k, v in r2["cold_launch"].items()},
             "roofline": roofline(r2, pk), "clocks": r2["clocks"],
+            "mxfp4_vs_fp8_topk_overlap": r2["overlap"],
         }
     if rank == 0 and not args.no_cpu_baseline:
         n, sec = oracle_sample(w, args.ref_budget, mtp_reuse=not args.no_mtp_reuse)

@@ -26,6 +26,7 @@ class GpuWorkload:
                  chunk_tokens: int = 1 << 22):
         self.w = w
         self.device = device
+        self._D = D
         self.layers = list(range(len(w.layers))) if layers is None else list(layers)
         self.pt = page_table(w, device)
         meta = batch_meta(w, device)
@@ -90,6 +91,33 @@ class GpuWorkload:
         st = D.dsa_device_status_read(self.dev_status)
         if st[0] != 0:
             raise RuntimeError(f"device errors while filling caches: {st}")
+
+    def other_index_cache(self, chunk_tokens: int = 1 << 22) -> torch.Tensor:
+        """The index-K cache of the same keys (and boosts) in the other format
+        (MXFP4 for an FP8 workload, FP8 for an MXFP4 one), through the
+        library's own store."""
+        D, w = self._D, self.w
+        mx = not self.mx
+        pb = D.IDXK_MXFP4_PAGE_BYTES if mx else D.IDXK_PAGE_BYTES
+        cache = torch.zeros(w.num_pages * pb, dtype=torch.uint8, device=self.device)
+        store = D.dsa_index_k_store_mxfp4 if mx else D.dsa_index_k_store
+        n = self.all_pos.numel()
+        k_all = index_keys(w, n, self.device)
+        for a in range(0, n, chunk_tokens):
+            b_ = min(n, a + chunk_tokens)
+            store(k_all[a:b_], self.all_pos[a:b_].contiguous(), self.all_slot[a:b_].contiguous(), cache,
+                  dev_status=self.dev_status)
+        del k_all
+        if w.boost_frac > 0:
+            bs = self.all_slot[boost_mask(w, self.device)]
+            if mx:
+                sv = cache.view(-1, pb)[:, 64 * 64:].view(-1, PAGE, 4)
+                sv[bs // PAGE, bs % PAGE] += 2
+            else:
+                sv = D.index_cache_scale_view(cache)
+                sv[bs // PAGE, bs % PAGE] *= 4.0
+        torch.cuda.synchronize()
+        return cache
 
     # raw host copies for the oracle ------------------------------------------
     def request_rows(self, r: int):
