@@ -112,10 +112,49 @@ __device__ __forceinline__ int row_request(const int32_t* q_start, int B, int64_
         cudaError_t e_ = cudaGetLastError();                                 \
         if (e_ != cudaSuccess) return DSA_ERR_CUDA;                          \
     } while (0)
+#define DSA_CHECK(call)                                                      \
+    do {                                                                     \
+        if ((call) != cudaSuccess) return DSA_ERR_CUDA;                      \
+    } while (0)
 
 namespace dsa {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Programmatic dependent launch.  A kernel launched by launch_pdl may begin
+// while the stream's previous kernel is still running; before its first
+// access to global memory it calls pdl_wait(), which returns once that kernel
+// has finished and its writes are visible (at once when there is none).  A
+// kernel calls pdl_trigger() after its own pdl_wait() to let the next one
+// start early, so everything before its predecessor has finished by the time
+// the next kernel runs any code.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              unsigned cluster, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
 
 // Raises kernel `func`'s dynamic shared-memory limit to `bytes` on the current
 // device.  The limit is a per-device setting, so it is applied once per

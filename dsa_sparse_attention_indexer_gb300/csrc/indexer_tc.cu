@@ -191,6 +191,8 @@ __global__ void __launch_bounds__(kPrepThreads)
 prep_kernel(BatchDev b, int G_launch, Plan p, const uint16_t* __restrict__ q, const float* __restrict__ w,
             int64_t rows, uint8_t* __restrict__ q8, float* __restrict__ wq) {
     __shared__ int32_t scratch[32];
+    pdl_wait();
+    pdl_trigger();
     if (blockIdx.x == 0) {
         plan_block<kPrepThreads>(b, G_launch, p, scratch);
         return;
@@ -454,6 +456,7 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc->tmem_base;
+    pdl_wait();                                            // the plan and the quantised queries
     int s_begin = p.cta_range[2 * blockIdx.x], s_end = p.cta_range[2 * blockIdx.x + 1];
     const int nseg_max = (int)gridDim.x + b.batch;    // segment slots in the workspace
     if (s_begin < 0 || s_end > nseg_max || s_begin > s_end) {   // never for a plan from prep_kernel
@@ -779,6 +782,7 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
         }
     }
     __syncthreads();
+    pdl_trigger();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -828,6 +832,8 @@ __global__ void __launch_bounds__(kFiltThreads)
 merge_filter_kernel(BatchDev b, Plan p) {
     __shared__ int32_t scratch[32];
     __shared__ uint32_t s_bstar;
+    pdl_wait();
+    pdl_trigger();
     const int s = blockIdx.x;
     int64_t row;
     if (p.slot_row) {                                  // row mode
@@ -1015,6 +1021,8 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     uint32_t* bnd_key = reinterpret_cast<uint32_t*>(msm + kMOffBndKey);
     int32_t* bnd_pos = reinterpret_cast<int32_t*>(msm + kMOffBndPos);
     MergeMisc* mm = reinterpret_cast<MergeMisc*>(msm + kMOffMisc);
+    pdl_wait();
+    pdl_trigger();
     const int64_t row = blockIdx.x;
     const int gt = threadIdx.x;
     const int r = row_request(b.q_start, b.batch, row);
@@ -1216,12 +1224,14 @@ dsa_status launch_indexer_tc(const void* q, const float* w, uint8_t* q8, float* 
     Plan p = carve_plan(plan_ws, b->batch, G);
     p.hist = hist;
     const int64_t qblocks = (b->total_q * 32 + itc::kPrepThreads / 32 - 1) / (itc::kPrepThreads / 32);
-    itc::prep_kernel<<<(unsigned)(1 + qblocks), itc::kPrepThreads, 0, s>>>(bd, G, p, static_cast<const uint16_t*>(q),
-                                                                        w, b->total_q, q8, wq);
-    DSA_CHECK_LAUNCH();
-    if (mx) itc::score_topk_kernel<true><<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
-    else itc::score_topk_kernel<false><<<G, itc::kThreads, itc::kSmemAlloc, s>>>(map, cache, q8, wq, bd, p, st);
-    DSA_CHECK_LAUNCH();
+    DSA_CHECK(launch_pdl(itc::prep_kernel, dim3((unsigned)(1 + qblocks)), dim3(itc::kPrepThreads), 0, s, 1, bd, G, p,
+                         static_cast<const uint16_t*>(q), w, b->total_q, q8, wq));
+    if (mx)
+        DSA_CHECK(launch_pdl(itc::score_topk_kernel<true>, dim3(G), dim3(itc::kThreads), itc::kSmemAlloc, s, 1, map,
+                             cache, q8, wq, bd, p, st));
+    else
+        DSA_CHECK(launch_pdl(itc::score_topk_kernel<false>, dim3(G), dim3(itc::kThreads), itc::kSmemAlloc, s, 1, map,
+                             cache, q8, wq, bd, p, st));
     return launch_topk_merge(b, p, (int64_t)G + b->batch, topk, topk_scores, s);
 }
 
@@ -1231,11 +1241,10 @@ dsa_status launch_topk_merge(const dsa_batch* b, Plan p, int64_t max_segs, int32
         return DSA_ERR_CUDA;
     BatchDev bd = to_dev(b);
     if (max_segs > 0) {
-        itc::merge_filter_kernel<<<(unsigned)max_segs, itc::kFiltThreads, 0, s>>>(bd, p);
-        DSA_CHECK_LAUNCH();
+        DSA_CHECK(launch_pdl(itc::merge_filter_kernel, dim3((unsigned)max_segs), dim3(itc::kFiltThreads), 0, s, 1, bd, p));
     }
-    itc::merge_kernel<<<(unsigned)b->total_q, itc::kMergeThreads, itc::kMergeSmem, s>>>(bd, p, topk, topk_scores);
-    DSA_CHECK_LAUNCH();
+    DSA_CHECK(launch_pdl(itc::merge_kernel, dim3((unsigned)b->total_q), dim3(itc::kMergeThreads), itc::kMergeSmem, s, 1,
+                         bd, p, topk, topk_scores));
     return DSA_OK;
 }
 

@@ -334,6 +334,7 @@ sparse_mla_tc_kernel(Args a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc->tmem_base;
+    pdl_wait();                                            // the top-k and the caches
 
     auto timeout = [&](int where) {
         record_error(a.st, DSA_DEVERR_TIMEOUT, where);
@@ -777,6 +778,7 @@ sparse_mla_tc_kernel(Args a) {
     }
     tc_fence_before();
     __syncthreads();
+    pdl_trigger();
     // ---- merge of the row inside its cluster (all 16 warps).  Every CTA
     //      reaches both cluster barriers and sends its full share, whatever
     //      happened above; a CTA that gave up contributes zeros (sum 0).  The
@@ -898,6 +900,8 @@ combine_kernel(Args a) {
     __shared__ float w_s[kMaxParts];
     __shared__ float inv_s;
     __shared__ int64_t u_s[kMaxParts];
+    pdl_wait();
+    pdl_trigger();
     int64_t row;
     if (a.sp.mode == SPLIT_ROW_CTAS) {
         row = blockIdx.x;
@@ -1027,30 +1031,17 @@ dsa_status launch_sparse_mla_tc(const void* q, const int32_t* topk, const uint8_
     a.part_ml = a.part_o + (size_t)2 * G * 64 * 512;
     a.st = st;
     if (a.sp.cluster > 1) {                                 // one cluster per row
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)G);
-        cfg.blockDim = dim3(mtc::kThreads);
-        cfg.dynamicSmemBytes = mtc::kSmemAlloc;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)a.sp.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, mtc::sparse_mla_tc_kernel, a) != cudaSuccess) return DSA_ERR_CUDA;
+        DSA_CHECK(launch_pdl(mtc::sparse_mla_tc_kernel, dim3((unsigned)G), dim3(mtc::kThreads), mtc::kSmemAlloc, s,
+                             (unsigned)a.sp.cluster, a));
         return DSA_OK;                                      // merged inside the clusters
     }
-    mtc::sparse_mla_tc_kernel<<<(unsigned)G, mtc::kThreads, mtc::kSmemAlloc, s>>>(a);
-    DSA_CHECK_LAUNCH();
+    DSA_CHECK(launch_pdl(mtc::sparse_mla_tc_kernel, dim3((unsigned)G), dim3(mtc::kThreads), mtc::kSmemAlloc, s, 1, a));
     unsigned nx = 0;                                        // combine blocks: candidate rows
     if (a.sp.mode == mtc::SPLIT_ROW_CTAS)                   // one CTA per row (c = 1, no extra): each row
         nx = (a.sp.c > 1 || a.sp.extra > 0) ? (unsigned)b->total_q : 0u;   // written whole, nothing to merge
     else if (a.sp.mode == mtc::SPLIT_EQUAL) nx = (unsigned)(G - 1);
     if (nx > 0) {
-        mtc::combine_kernel<<<dim3(nx, 64), mtc::kCombThreads, 0, s>>>(a);
-        DSA_CHECK_LAUNCH();
+        DSA_CHECK(launch_pdl(mtc::combine_kernel, dim3(nx, 64), dim3(mtc::kCombThreads), 0, s, 1, a));
     }
     return DSA_OK;
 }

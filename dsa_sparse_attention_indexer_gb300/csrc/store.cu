@@ -115,6 +115,8 @@ index_k_store_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__
                      const float* __restrict__ gamma, const float* __restrict__ beta,
                      float eps, RopeFreqs fr, uint8_t* __restrict__ cache,
                      int64_t num_pages, int32_t* __restrict__ st) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= n) return;
@@ -206,6 +208,8 @@ __global__ void __launch_bounds__(256)
 latent_store_kernel(const uint16_t* __restrict__ c, const uint16_t* __restrict__ rope,
                     const int64_t* __restrict__ slot, int64_t n, uint8_t* __restrict__ cache,
                     int64_t num_pages, int32_t* __restrict__ st) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= n) return;
@@ -262,10 +266,9 @@ extern "C" dsa_status dsa_index_k_store(const void* k, const int32_t* pos, const
     if (blocks > 0x7fffffff) return DSA_ERR_UNSUPPORTED;
     RopeFreqs fr;
     for (int i = 0; i < 32; ++i) fr.theta[i] = std::pow((double)rope_base, -2.0 * (double)i / 64.0);
-    index_k_store_kernel<false><<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
-        static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, fr,
-        idxk_cache, num_pages, dev_status);
-    DSA_CHECK_LAUNCH();
+    DSA_CHECK(launch_pdl(index_k_store_kernel<false>, dim3((unsigned)blocks), dim3(warps * 32), 0, as_stream(stream), 1,
+                         static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, fr, idxk_cache, num_pages,
+                         dev_status));
     return DSA_OK;
 }
 
@@ -283,10 +286,9 @@ extern "C" dsa_status dsa_index_k_store_mxfp4(const void* k, const int32_t* pos,
     if (blocks > 0x7fffffff) return DSA_ERR_UNSUPPORTED;
     RopeFreqs fr;
     for (int i = 0; i < 32; ++i) fr.theta[i] = std::pow((double)rope_base, -2.0 * (double)i / 64.0);
-    index_k_store_kernel<true><<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
-        static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, fr,
-        idxk_cache, num_pages, dev_status);
-    DSA_CHECK_LAUNCH();
+    DSA_CHECK(launch_pdl(index_k_store_kernel<true>, dim3((unsigned)blocks), dim3(warps * 32), 0, as_stream(stream), 1,
+                         static_cast<const uint16_t*>(k), pos, slot, n, gamma, beta, ln_eps, fr, idxk_cache, num_pages,
+                         dev_status));
     return DSA_OK;
 }
 
@@ -326,9 +328,8 @@ extern "C" dsa_status dsa_latent_kv_store(const void* c, const void* rope, const
     const int warps = 8;
     const int64_t blocks = (n + warps - 1) / warps;
     if (blocks > 0x7fffffff) return DSA_ERR_UNSUPPORTED;
-    latent_store_kernel<<<(unsigned)blocks, warps * 32, 0, as_stream(stream)>>>(
-        static_cast<const uint16_t*>(c), static_cast<const uint16_t*>(rope), slot, n, kv_cache,
-        num_pages, dev_status);
-    DSA_CHECK_LAUNCH();
+    DSA_CHECK(launch_pdl(latent_store_kernel, dim3((unsigned)blocks), dim3(warps * 32), 0, as_stream(stream), 1,
+                         static_cast<const uint16_t*>(c), static_cast<const uint16_t*>(rope), slot, n, kv_cache,
+                         num_pages, dev_status));
     return DSA_OK;
 }
