@@ -13,7 +13,7 @@ from __future__ import annotations
 import contextlib
 import ctypes
 import os
-from ctypes import POINTER, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint8, c_void_p
+from ctypes import POINTER, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint8, c_uint64, c_void_p
 
 import torch
 
@@ -78,6 +78,7 @@ _SIGS = {
     "dsa_status_string": (c_char_p, [c_int32]),
     "dsa_device_status_reset": (c_int32, [c_void_p, c_void_p]),
     "dsa_device_status_read": (c_int32, [c_void_p, c_void_p, POINTER(c_int32)]),
+    "dsa_debug_set_wait_limit_ns": (c_int32, [c_uint64]),
     "dsa_index_k_store": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_float,
                                     c_float, c_void_p, c_int64, c_void_p, c_void_p]),
     "dsa_index_k_store_mxfp4": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_float,
@@ -254,6 +255,12 @@ def dsa_device_status_read(dev_status: torch.Tensor, stream=None):
         _check("dsa_device_status_read", code)
     return list(out)
 
+
+
+def dsa_debug_set_wait_limit_ns(ns: int) -> None:
+    """Testing hook: limit (ns) of the decode score kernel's pipeline waits for
+    later launches, process-wide (2e9 by default; 0 = give up at once)."""
+    _check("dsa_debug_set_wait_limit_ns", lib().dsa_debug_set_wait_limit_ns(int(ns)))
 
 def dsa_device_status_reset(dev_status: torch.Tensor, stream=None):
     _need(dev_status, torch.int32, "dev_status", numel=4)

@@ -2,6 +2,7 @@
 // full/shared layer schedule ("GLM-5.3 推理全链路(十一)", 配置里的 78 个字符)
 // and the share handle that carries a full layer's indices to the shared
 // layers after it ("GLM-5.3 推理全链路(十一)", 一次前向里 topk 只算一遍).
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -43,7 +44,15 @@ void* tensor_map_encode_fn() {
     return fn;
 }
 
+static std::atomic<uint64_t> g_wait_ns{2000000000ull};
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 }  // namespace dsa
+
+extern "C" dsa_status dsa_debug_set_wait_limit_ns(uint64_t ns) {
+    dsa::g_wait_ns.store(ns, std::memory_order_relaxed);
+    return DSA_OK;
+}
 
 struct dsa_topk_share {
     const int32_t* topk;

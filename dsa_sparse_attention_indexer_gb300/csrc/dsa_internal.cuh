@@ -121,6 +121,10 @@ namespace dsa {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Limit of the pipeline waits of later launches that take it (the decode
+// score kernel); 2 s unless dsa_debug_set_wait_limit_ns changed it.
+uint64_t wait_limit_ns();
+
 // Programmatic dependent launch.  A kernel launched by launch_pdl may begin
 // while the stream's previous kernel is still running; before its first
 // access to global memory it calls pdl_wait(), which returns once that kernel

@@ -15,6 +15,7 @@ struct BatchDev {
     const int32_t* seq_len;
     const int32_t* q_start;
     const int32_t* page_table;
+    uint64_t wait_ns;      // limit of the decode score kernel's pipeline waits (normally 2 s)
 };
 
 inline BatchDev to_dev(const dsa_batch* b) {
@@ -28,6 +29,7 @@ inline BatchDev to_dev(const dsa_batch* b) {
     d.seq_len = b->seq_len;
     d.q_start = b->q_start;
     d.page_table = b->page_table;
+    d.wait_ns = wait_limit_ns();
     return d;
 }
 

@@ -172,6 +172,7 @@ __device__ void plan_block(BatchDev b, int G_launch, Plan p, int32_t* scratch) {
         const int64_t tlo = (g == g0) ? s0 : cta_start(g, N, G);
         const int64_t thi = (g == g1) ? s1 : cta_start(g + 1, N, G);
         p.segs[s] = Seg{r, (int32_t)(tlo - s0), (int32_t)(thi - s0), (int32_t)g};
+        p.cand_cnt[s] = 0;                             // a segment the score kernel gives up on stays empty
     }
     __syncthreads();
     // pass 4: each CTA's contiguous run of segments
@@ -501,8 +502,8 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                         const uint32_t phase = (uint32_t)((icount / kSt) & 1);
                         const int slot = (int)(icount % kSSlots);
                         const uint32_t sphase = (uint32_t)((icount / kSSlots) & 1);
-                        if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1) ||
-                            !mbar_wait(&sempty[slot], sphase ^ 1)) {
+                        if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, b.wait_ns) ||
+                            !mbar_wait(&sempty[slot], sphase ^ 1, b.wait_ns)) {
                             ok = 0;
                             break;
                         }
@@ -567,12 +568,12 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
             bool seg_issued = false;
             for (int tile = sg.lo; tile < sg.hi; ++tile) {
                 int ok = 1;
-                if (lane == 0) ok = (!*abort_flag && mbar_wait(&acce[acc], acc_phase ^ 1)) ? 1 : 0;
+                if (lane == 0) ok = (!*abort_flag && mbar_wait(&acce[acc], acc_phase ^ 1, b.wait_ns)) ? 1 : 0;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { stop = true; break; }
                 if (tile == sg.lo) {
                     if ((bpending >> bbuf) & 1u) {
-                        if (lane == 0) ok = mbar_wait(&bdone[bbuf], (bph >> bbuf) & 1u) ? 1 : 0;
+                        if (lane == 0) ok = mbar_wait(&bdone[bbuf], (bph >> bbuf) & 1u, b.wait_ns) ? 1 : 0;
                         ok = __shfl_sync(0xffffffffu, ok, 0);
                         if (!ok) { stop = true; break; }
                         bph ^= 1u << bbuf;
@@ -587,7 +588,7 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                     __syncwarp();
                 }
                 if (lane == 0) {
-                    ok = mbar_wait(&full[stage], phase) ? 1 : 0;
+                    ok = mbar_wait(&full[stage], phase, b.wait_ns) ? 1 : 0;
                     if (ok) {
                         tc_fence_after();
                         const uint32_t a0 = smem_addr(smem + kOffStages + stage * kStageBytes);
@@ -625,8 +626,10 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
         if (lane == 0 && stop) {
             record_error(st, DSA_DEVERR_TIMEOUT, 2);
             *abort_flag = 1;
-            if (issued_any) mbar_wait(&accf[last_acc], last_acc_phase, 500000000ull);   // MMAs in flight
         }
+        // no MMA in flight when the TMEM is released, also when the epilogue gave up
+        // after every tile was issued (MMAs complete in issue order)
+        if (lane == 0 && issued_any) mbar_wait(&accf[last_acc], last_acc_phase, 500000000ull);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
@@ -662,8 +665,8 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                     const uint32_t sphase = (uint32_t)((gidx / kSSlots) & 1);
                     const int acc = (int)(gidx % kAccN);
                     const uint32_t acc_phase = (uint32_t)((gidx / kAccN) & 1);
-                    int ok = __all_sync(0xffffffffu, mbar_wait(&accf[acc], acc_phase));
-                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sfull[slot], sphase));   // scales + page mask
+                    int ok = __all_sync(0xffffffffu, mbar_wait(&accf[acc], acc_phase, b.wait_ns));
+                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sfull[slot], sphase, b.wait_ns));   // scales + page mask
                     if (ok) {
                         float score;
                         int vmask;

@@ -133,6 +133,16 @@ dsa_status dsa_device_status_reset(int32_t* dev_status, void* stream);
 /* Synchronise `stream`, copy the block into host_out[4]; returns DSA_ERR_DEVICE
  * when any error bit is set, DSA_OK otherwise. */
 dsa_status dsa_device_status_read(const int32_t* dev_status, void* stream, int32_t* host_out);
+/* Testing hook for failure detection, process-wide: the limit, in ns, of the
+ * pipeline waits of the decode indexer's score kernel (dsa_indexer_topk and
+ * dsa_indexer_topk_mxfp4 on a batch of one row per request) launched after
+ * the call.  2e9 (2 s) by default; 0 makes every wait that is not already
+ * satisfied give up at once.  A wait that gives up records
+ * DSA_DEVERR_TIMEOUT; the kernel then lets its copies and MMAs in flight
+ * finish, releases its tensor memory and returns, the merge sees only the
+ * segments finished before, and the call's top-k is then meaningless.
+ * Always DSA_OK. */
+dsa_status dsa_debug_set_wait_limit_ns(uint64_t ns);
 
 /* ---- Index-K store ("GLM-5.3 推理全链路(一)", 4.5 闪电索引器; "GLM-5.3 推理全链路(十一)",
  *      索引器缓存里存的是什么) -------------------------------------------------
