@@ -492,6 +492,31 @@ def selection_overlap(gw, D):
             "rows": int(common.numel())}
 
 
+def scorer_comparison(gw, D, reps=5):
+    """Decode batches: device time of the score rows from the tensor-core
+    kernel (dsa_indexer_scores) and from the CUDA-core kernel kept to measure
+    it against (dsa_indexer_scores_cuda_core), CUDA events, mean of `reps`
+    after one warm-up; outside the timed region."""
+    w = gw.w
+    if max(w.q_len) > 1 or w.draft_steps or gw.mx:
+        return None
+    out = {}
+    sc = torch.empty((w.total_q, w.max_seq_len), dtype=torch.float32, device=gw.device)
+    for name, fn in (("tensor_cores", D.dsa_indexer_scores), ("cuda_cores", D.dsa_indexer_scores_cuda_core)):
+        fn(gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch, scores=sc)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn(gw.q_idx, gw.w_idx, gw.idx_cache, gw.batch, scores=sc)
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = round(e0.elapsed_time(e1) * 1000.0 / reps, 1)
+    del sc
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, workload=None, with_e2e=True):
     import dsa_sparse_attention_indexer_gb300 as D
     import synth
@@ -625,10 +650,12 @@ def run_ours(args, rank, world, workload=None, with_e2e=True):
         del cold_flush
     timers = {k: [None] * len(v) for k, v in call_graphs.items()}
     overlap = selection_overlap(gw, D)
+    scorers = scorer_comparison(gw, D)
     if not with_e2e:
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         return dict(w=w, ms=ms, per_call=per_call, per_launch=per_launch, cold_call=cold_call,
-                    cold_launch=cold_launch, in_step=in_step_ok, clocks=clocks, flush=flush, overlap=overlap)
+                    cold_launch=cold_launch, in_step=in_step_ok, clocks=clocks, flush=flush, overlap=overlap,
+                    scorers=scorers)
 
     # ---- end to end: host buffers in, host buffers out, through the same calls
     first_in, layer_in, outs = step.e2e_io()
@@ -700,7 +727,7 @@ def run_ours(args, rank, world, workload=None, with_e2e=True):
     mla_rows = len(w.seq_len) if w.draft_steps else w.total_q     # a draft step's launch: one row per request
     return dict(w=w, ms=ms, e2e_ms=e2e_ms, per_call=per_call, per_launch=per_launch, cold_call=cold_call,
                 cold_launch=cold_launch, in_step=in_step_ok, clocks=clocks, flush=flush, h2d=h2d, d2h=d2h,
-                overlap=overlap,
+                overlap=overlap, scorers=scorers,
                 launches=sum(kernels_per_call(k, mla_rows, sms, multi_row=max(w.q_len) > 1 and not w.draft_steps)
                              * len(v) for k, v in timers.items()))
 
@@ -910,6 +937,7 @@ def main():
             "index_cache": w.index_format,
             "store": "fused" if args.fused_store else "separate",
             "mxfp4_vs_fp8_topk_overlap": res["overlap"],
+            "indexer_score_rows_us": res["scorers"],
         },
         "roofline": roof,
         "peaks": {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"], "source": pk["source"],
@@ -935,6 +963,7 @@ def main():
             "us_per_launch_alone_l2_flushed": {k: round(v, 2) for k, v in r2["cold_launch"].items()},
             "roofline": roofline(r2, pk), "clocks": r2["clocks"],
             "mxfp4_vs_fp8_topk_overlap": r2["overlap"],
+            "indexer_score_rows_us": r2["scorers"],
         }
     if rank == 0 and not args.no_cpu_baseline:
         n, sec = oracle_sample(w, args.ref_budget, mtp_reuse=not args.no_mtp_reuse)

@@ -98,6 +98,8 @@ _SIGS = {
     "dsa_indexer_scores_workspace_size": (c_int32, [POINTER(DsaBatch), POINTER(c_size_t)]),
     "dsa_indexer_scores": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_void_p, c_int64,
                                      c_void_p, c_size_t, c_void_p, c_void_p]),
+    "dsa_indexer_scores_cuda_core": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(DsaBatch), c_void_p, c_int64,
+                                     c_void_p, c_size_t, c_void_p, c_void_p]),
     "dsa_topk_from_scores_workspace_size": (c_int32, [c_int32, c_int64, POINTER(c_size_t)]),
     "dsa_topk_from_scores": (c_int32, [c_void_p, c_int64, c_void_p, c_int32, c_int64, c_void_p, c_void_p,
                                        c_size_t, c_void_p]),
@@ -427,6 +429,22 @@ def dsa_indexer_scores(q, w, idxk_cache, batch: Batch, *, ld=None, scores=None, 
     _opt(dev_status, torch.int32, "dev_status", q.device, 4)
     ws = _ws(ws, _ws_size("dsa_indexer_scores_workspace_size", batch) if ws is None else 0, q.device)
     _call("dsa_indexer_scores", q.device,
+        _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(scores), ld, _ptr(ws), ws.numel(),
+        _ptr(dev_status), _stream(stream, q.device))
+    return scores
+
+
+def dsa_indexer_scores_cuda_core(q, w, idxk_cache, batch: Batch, *, ld=None, scores=None, ws=None,
+                                 dev_status=None, stream=None):
+    """dsa_indexer_scores from the CUDA-core kernel (decode batches; comparison only)."""
+    T = _indexer_args(q, w, idxk_cache, batch)
+    ld = batch.c.max_seq_len if ld is None else ld
+    if scores is None:
+        scores = torch.empty((T, ld), dtype=torch.float32, device=q.device)
+    _need(scores, torch.float32, "scores", q.device, T * ld)
+    _opt(dev_status, torch.int32, "dev_status", q.device, 4)
+    ws = _ws(ws, T * (4096 + 128) if ws is None else 0, q.device)
+    _call("dsa_indexer_scores_cuda_core", q.device,
         _ptr(q), _ptr(w), _ptr(idxk_cache), batch.ref(), _ptr(scores), ld, _ptr(ws), ws.numel(),
         _ptr(dev_status), _stream(stream, q.device))
     return scores

@@ -282,6 +282,16 @@ dsa_status dsa_indexer_scores_workspace_size(const dsa_batch* b, size_t* bytes);
 dsa_status dsa_indexer_scores(const void* q, const float* w, const uint8_t* idxk_cache,
                               const dsa_batch* b, float* scores, int64_t ld,
                               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+/* The same score rows from a CUDA-core kernel (no tensor cores), for decode
+ * batches only (one query row per request, at most 65535 of them; else
+ * DSA_ERR_UNSUPPORTED): kept to measure the tensor-core path against.  Same
+ * quantised queries, E4M3 products and fp32 sums, in another order, so its
+ * scores meet the same tolerance.  Entries j >= seq_len of a row are not
+ * written; pages out of range give -inf and are recorded.
+ *   ws: device workspace of at least T * (4096 + 128) bytes, 16-byte aligned. */
+dsa_status dsa_indexer_scores_cuda_core(const void* q, const float* w, const uint8_t* idxk_cache,
+                                        const dsa_batch* b, float* scores, int64_t ld,
+                                        void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* Parity hook: top-2048 of given fp32 score rows, same selection rule and
  * output order as dsa_indexer_topk.  Row r uses scores[r*ld + 0 .. valid_len[r]-1].

@@ -300,6 +300,27 @@ def test_indexer_topk_matches_oracle(indexer_case):
     _check_indexer_topk(indexer_case, 2)
 
 
+def test_indexer_scores_cuda_core_match_oracle_and_the_tensor_core_rows(decode_case):
+    """The CUDA-core scorer kept for comparison: same scores within the bar,
+    on a decode batch (a 300K-token request included)."""
+    c = decode_case
+    st = D.new_device_status(DEV)
+    S = D.dsa_indexer_scores_cuda_core(c["q"], c["wt"], c["cache"], c["batch"], dev_status=st).cpu().numpy()
+    assert D.dsa_device_status_read(st)[0] == 0
+    T = D.dsa_indexer_scores(c["q"], c["wt"], c["cache"], c["batch"]).cpu().numpy()
+    for row in c["rows"]:
+        i, n = row["i"], row["n"]
+        check_scores(S[i, :n], row["s"], row["mag"], what=f"row {i}")
+        check_scores(S[i, :n], T[i, :n].astype(np.float64), 2 * row["mag"], what=f"row {i} vs tensor cores")
+
+
+def test_indexer_scores_cuda_core_refuses_multi_token_rows(indexer_case):
+    with pytest.raises(D.DsaError) as e:
+        D.dsa_indexer_scores_cuda_core(indexer_case["q"], indexer_case["wt"], indexer_case["cache"],
+                                       indexer_case["batch"])
+    assert e.value.name == "DSA_ERR_UNSUPPORTED"
+
+
 def test_indexer_topk_fed_oracle_fp32_scores_is_bit_exact(indexer_case):
     c = indexer_case
     rows = [r for r in c["rows"] if r["n"] > 0]
