@@ -334,7 +334,6 @@ sparse_mla_tc_kernel(Args a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc->tmem_base;
-    pdl_wait();                                            // the top-k and the caches
 
     auto timeout = [&](int where) {
         record_error(a.st, DSA_DEVERR_TIMEOUT, where);
@@ -343,6 +342,9 @@ sparse_mla_tc_kernel(Args a) {
 
     if (warp >= kLoadWarp0) {
         // ================================================================ loaders
+        // Only the loaders read what the previous kernel may write (the top-k):
+        // they wait for it, while the softmax warps already convert the first Q.
+        pdl_wait();
         const int lt = tid - kLoadWarp0 * 32;            // 0..255
         const int lw = lt >> 5;                            // 0..7
         const int c8 = lane & 7;                           // 16-byte piece of a 128-byte group
