@@ -45,10 +45,12 @@ L2_BYTES = 129 * 1024 * 1024
 # (the same 2048 selected rows each, so the same launch); decode1m
 # indexer_topk: a 256K-context capture scaled by the context (x4).
 NCU_TRAFFIC = {
-    ("decode32k", "sparse_mla_decode"): (106.4e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
-                                         "52f4ec9dacd7f088"),
-    ("decode1m", "indexer_topk"): (567.4e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
-                                   "aca40d28e5cd4b96"),
+    ("decode32k", "sparse_mla_decode"): (105.6e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
+                                         "97bedb434c65f695"),
+    ("decode1m", "indexer_topk"): (554.2e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
+                                   "033c0473da2f8ec6"),
+    ("verify64k", "indexer_topk"): (1383.7e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_mt.cu",
+                                    "37aa6ad3f8fff382"),
 }
 FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s), used only if the
                              # FP8 GEMM measurement below cannot run
