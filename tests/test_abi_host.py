@@ -126,6 +126,21 @@ def test_indexer_and_mla_argument_errors(L):
     assert L.dsa_topk_from_scores(fk, 10, fk, 0, 10, fk, None, 0, None) == 0      # zero rows: no launch
 
 
+def test_cuda_core_scorer_and_mxfp4_rows_argument_errors(L):
+    fk = ctypes.c_void_p(0x30000000)
+    ws = ctypes.c_void_p(0x40000000)
+    b = _fake_batch()
+    assert L.dsa_indexer_scores_cuda_core(None, fk, fk, ctypes.byref(b), fk, 4096, ws, 1 << 20, None, None) == 1
+    assert L.dsa_indexer_scores_cuda_core(fk, fk, fk, ctypes.byref(b), fk, 100, ws, 1 << 20, None, None) == 1   # ld
+    assert L.dsa_indexer_scores_cuda_core(fk, fk, fk, ctypes.byref(b), fk, 4096, ws, 16, None, None) == 4
+    multi = _fake_batch(B=2, T=4, max_q=2)
+    assert L.dsa_indexer_scores_cuda_core(fk, fk, fk, ctypes.byref(multi), fk, 4096, ws, 1 << 20, None, None) == 3
+    # MXFP4 with several rows per request: at most 65535 rows (each becomes a one-row request)
+    big = _fake_batch(B=1, T=70000, max_q=70000, max_seq=80000, pages=2000)
+    assert L.dsa_indexer_topk_mxfp4(fk, fk, fk, ctypes.byref(big), fk, None, None, 0, ws, 1 << 40, None, None) == 3
+    assert L.dsa_debug_set_wait_limit_ns(2_000_000_000) == 0
+
+
 def test_context_parallel_argument_errors(L):
     fk = ctypes.c_void_p(0x30000000)
     odd = ctypes.c_void_p(0x30000004)
