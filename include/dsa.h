@@ -240,8 +240,9 @@ dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_c
  * dsa_indexer_topk_workspace_size); scores are formed on the dequantised
  * values (E2M1 x 2^e per 32-dim block).  A batch with several query rows per
  * request (verify, prefill) runs each row as a decode row over its request's
- * keys up to its position, so each row reads the keys once; at most 65535
- * rows (DSA_ERR_UNSUPPORTED beyond).
+ * keys up to its position: a request's keys are read once per row (the FP8
+ * call reads them once per block of 8 rows); at most 65535 rows
+ * (DSA_ERR_UNSUPPORTED beyond).
  *   idxk_cache device uint8 [num_pages * 4352], 32-byte aligned               */
 dsa_status dsa_indexer_topk_mxfp4(const void* q, const float* w, const uint8_t* idxk_cache,
                                   const dsa_batch* b, int32_t* topk, float* topk_scores,
