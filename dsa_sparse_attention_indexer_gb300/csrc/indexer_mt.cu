@@ -681,6 +681,9 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         bool bad = false;
         bool piece_start = true;
         int ptile = 0;                                   // tiles of the current piece walked so far
+        // The next check of the slots: a slot takes at most 128 entries a tile, so
+        // a check after (capacity - fullest slot) / 128 tiles finds none overflowed.
+        int next_check = kSlotCap / 128;
         int slot0 = 0, np = 0;                           // the piece's slot of row 0 and the row block's pieces
         uint32_t th[kPerGrp];                              // the group's rows' thresholds (copies of misc->theta)
 #pragma unroll
@@ -743,6 +746,7 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 kslot = p.cand_key + (int64_t)(slot0 + rlo * np) * kSlotCap;
                 pslot = p.cand_pos + (int64_t)(slot0 + rlo * np) * kSlotCap;
                 ptile = 0;
+                next_check = kSlotCap / 128;
             }
             if (!bad && __any_sync(0xffffffffu, *abort_flag != 0)) bad = true;   // another role gave up
             if (!bad) {
@@ -807,24 +811,32 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             ++gidx;
             ++ptile;
             const bool piece_end = w.i + 1 >= w.rb_end || w.i + 1 >= w.i_end;
-            if (kStream && (piece_end || ptile % kCheckEvery == 0)) {
+            if (kStream && (piece_end || ptile == next_check)) {
                 // every tile of the piece so far is in the slots: compact the slots that
-                // may not hold the next kCheckEvery tiles, and at the piece end publish them
+                // may not hold the next kCheckEvery tiles, schedule the next check, and at
+                // the piece end publish the slots (up to 4608 entries each, no compaction)
                 flush();
                 if (lane == 0 && bad) misc->bad = 1;
                 epi_sync();
                 const bool any_bad = misc->bad != 0;
                 if (!any_bad) {
-                    for (int rr = 0; rr < R; ++rr) {
-                        if (misc->cnt[rr] <= kSlotCap - kCheckEvery * 128) continue;
-                        const int64_t sl = (int64_t)(slot0 + rr * np) * kSlotCap;
-                        const uint32_t t = compact_slot(p.cand_key + sl, p.cand_pos + sl, &misc->cnt[rr], et, hist,
-                                                        misc->scratch, &misc->found);
-                        if (et == 0) misc->theta[rr] = t;
-                        epi_sync();
-                    }
+                    if (!piece_end) {
+                        for (int rr = 0; rr < R; ++rr) {
+                            if (misc->cnt[rr] <= kSlotCap - kCheckEvery * 128) continue;
+                            const int64_t sl = (int64_t)(slot0 + rr * np) * kSlotCap;
+                            const uint32_t t = compact_slot(p.cand_key + sl, p.cand_pos + sl, &misc->cnt[rr], et,
+                                                            hist, misc->scratch, &misc->found);
+                            if (et == 0) misc->theta[rr] = t;
+                            epi_sync();
+                        }
 #pragma unroll
-                    for (int j = 0; j < kPerGrp; ++j) th[j] = misc->theta[rlo + j];
+                        for (int j = 0; j < kPerGrp; ++j) th[j] = misc->theta[rlo + j];
+                    }
+                    int fullest = 0;                        // the same value in every thread
+                    for (int rr = 0; rr < R; ++rr) fullest = max(fullest, misc->cnt[rr]);
+                    next_check = ptile + max(1, (kSlotCap - fullest) / 128);
+                } else {
+                    next_check = ptile + kCheckEvery;
                 }
                 if (piece_end) {
                     for (int rr = 0; rr < kRows; ++rr) {
@@ -837,6 +849,7 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                             atomicAdd(&gh[__ldcg(p.cand_key + (int64_t)slot * kSlotCap + i) >> 20], 1u);
                     }
                 }
+                epi_sync();                             // every read of the shared state above is done
             }
             piece_start = walk_next(w, p);
             new_block = piece_start;
