@@ -659,6 +659,9 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
             epi_sync();
             bool aborted = false;
             bool warp_bad = false;                     // this warp saw a timeout
+            // The next epilogue-wide check, in tiles of the segment: the buffer takes at
+            // most 128 candidates a tile, so it cannot overflow before (kCap - count) / 128.
+            int next_check = kCap / 128;
             for (int tile = sg.lo; tile < sg.hi; ++tile, ++gidx) {
                 if ((int)(gidx & 1) == grp && !warp_bad) {
                     const int slot = (int)(gidx % kSSlots);
@@ -758,11 +761,18 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
                         }
                     }
                 }
-                // epilogue-wide decisions (abort, buffer room) every few tiles and at the segment end
-                if (((tile - sg.lo + 1) % kCheckEvery) == 0 || tile + 1 == sg.hi) {
+                // epilogue-wide decisions (abort, buffer room) when the buffer might fill, and
+                // at the segment end.  The count is read between two barriers, so every
+                // thread sees the same value and none appends before all have read it.
+                if (tile - sg.lo + 1 == next_check || tile + 1 == sg.hi) {
                     if (epi_any(warp_bad)) { aborted = true; break; }
-                    if (misc->cb_count > kCap - kCheckEvery * 128)
+                    const int c = misc->cb_count;
+                    if (epi_any(c > kCap - kCheckEvery * 128)) {
                         compact_candidates(cb_key, cb_pos, hist, hist2, side_key, side_pos, misc, et);
+                        next_check = tile - sg.lo + 1 + (kCap - kTopK) / 128;   // at most 2048 kept
+                    } else {
+                        next_check = tile - sg.lo + 1 + max(1, (kCap - c) / 128);
+                    }
                 }
             }
             if (aborted) break;
