@@ -41,16 +41,16 @@ L2_BYTES = 129 * 1024 * 1024
 # DRAM traffic per launch from an ncu capture, keyed by (workload, call), with the
 # kernel source it was taken on; valid only while that source is unchanged
 # (sha256 prefix over the .cu file and every local header it includes).
-# decode32k sparse_mla_decode: a capture of its 64 decode rows on 16K contexts
-# (the same 2048 selected rows each, so the same launch); decode1m
-# indexer_topk: a 256K-context capture scaled by the context (x4).
+# All three are full-size captures of dram__bytes_read.sum + dram__bytes_write.sum
+# (one pass): the sparse-MLA kernel of decode32k, the score kernel of the decode1m
+# and of the verify64k indexer call.
 NCU_TRAFFIC = {
-    ("decode32k", "sparse_mla_decode"): (105.6e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
-                                         "97bedb434c65f695"),
+    ("decode32k", "sparse_mla_decode"): (105.3e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
+                                         "a1a0d6a0fabb68c3"),
     ("decode1m", "indexer_topk"): (554.2e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
-                                   "033c0473da2f8ec6"),
-    ("verify64k", "indexer_topk"): (1383.7e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_mt.cu",
-                                    "37aa6ad3f8fff382"),
+                                   "a15bce1542c95afa"),
+    ("verify64k", "indexer_topk"): (1383.5e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_mt.cu",
+                                    "5025f35e4c0d991d"),
 }
 FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s), used only if the
                              # FP8 GEMM measurement below cannot run
