@@ -267,10 +267,14 @@ __device__ __forceinline__ bool walk_next(Walk& w, const MtPlan& p) {
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, %1;" ::"n"(kEpiBar), "n"(kEpiThreads) : "memory"); }
 
 constexpr int kSlotPer = kSlotCap / kEpiThreads;   // slot entries per epilogue thread
-static_assert(kSlotCap % kEpiThreads == 0, "whole slot entries per thread");
+static_assert(kSlotCap % (4 * kEpiThreads) == 0, "whole groups of four slot entries per thread");
 
-// A slot's entries held in the epilogue threads' registers (entry et + u *
-// kEpiThreads in k[u], p[u]), as a selection source.
+// Slot entry held in register u of epilogue thread et: groups of four
+// consecutive entries (one 16-byte load), the thread's groups kEpiThreads apart.
+__device__ __forceinline__ int slot_entry(int u, int et) { return ((u >> 2) * kEpiThreads + et) * 4 + (u & 3); }
+
+// A slot's entries held in the epilogue threads' registers (entry
+// slot_entry(u, et) in k[u], p[u]), as a selection source.
 struct RegSrc {
     const uint32_t (&k)[kSlotPer];
     const int32_t (&p)[kSlotPer];
@@ -279,7 +283,7 @@ struct RegSrc {
     __device__ __forceinline__ void visit(int, F&& f) const {
 #pragma unroll
         for (int u = 0; u < kSlotPer; ++u) {
-            const bool a = et + u * kEpiThreads < n;
+            const bool a = slot_entry(u, et) < n;
             f(a, a ? k[u] : 0u, a ? p[u] : 0);
         }
     }
@@ -307,12 +311,20 @@ __device__ uint32_t compact_slot(uint32_t* key, int32_t* pos, int* n, int et, ui
     int32_t ps[kSlotPer];
     uint32_t lo = 0xffffffffu, hi = 0u;
 #pragma unroll
+    for (int g = 0; g < kSlotPer / 4; ++g) {          // 16-byte loads (slots are 16-byte aligned, 4608 long)
+        const int i0 = (g * kEpiThreads + et) * 4;
+        uint4 kv = make_uint4(0u, 0u, 0u, 0u), pv = make_uint4(0u, 0u, 0u, 0u);
+        if (i0 < cnt) {
+            kv = __ldcg(reinterpret_cast<const uint4*>(key + i0));
+            pv = __ldcg(reinterpret_cast<const uint4*>(pos + i0));
+        }
+        k[4 * g + 0] = kv.x; k[4 * g + 1] = kv.y; k[4 * g + 2] = kv.z; k[4 * g + 3] = kv.w;
+        ps[4 * g + 0] = (int32_t)pv.x; ps[4 * g + 1] = (int32_t)pv.y;
+        ps[4 * g + 2] = (int32_t)pv.z; ps[4 * g + 3] = (int32_t)pv.w;
+    }
+#pragma unroll
     for (int u = 0; u < kSlotPer; ++u) {
-        const int i = et + u * kEpiThreads;
-        const bool have = i < cnt;
-        k[u] = have ? __ldcg(key + i) : 0u;
-        ps[u] = have ? __ldcg(pos + i) : 0;
-        if (have) {
+        if (slot_entry(u, et) < cnt) {
             lo = min(lo, k[u]);
             hi = max(hi, k[u]);
         }
@@ -334,7 +346,7 @@ __device__ uint32_t compact_slot(uint32_t* key, int32_t* pos, int* n, int et, ui
     const int shift = (span >> 12) ? 32 - __clz((int)(span >> 12)) : 0;   // (span >> shift) < 4096
 #pragma unroll
     for (int u = 0; u < kSlotPer; ++u)
-        if (et + u * kEpiThreads < cnt) atomicAdd(&hist[(k[u] - lo) >> shift], 1u);
+        if (slot_entry(u, et) < cnt) atomicAdd(&hist[(k[u] - lo) >> shift], 1u);
     epi_sync();                                        // every scratch read above is done too
     constexpr int kPer = (4096 + kEpiThreads - 1) / kEpiThreads;   // bins per thread, from the top
     int mine = 0;
@@ -368,7 +380,7 @@ __device__ uint32_t compact_slot(uint32_t* key, int32_t* pos, int* n, int et, ui
     int wcount = 0;
 #pragma unroll
     for (int u = 0; u < kSlotPer; ++u) {
-        km[u] = __ballot_sync(0xffffffffu, et + u * kEpiThreads < cnt && th.keep(k[u], ps[u]));
+        km[u] = __ballot_sync(0xffffffffu, slot_entry(u, et) < cnt && th.keep(k[u], ps[u]));
         wcount += __popc(km[u]);
     }
     const int wbase = sel::excl_scan<kEpiThreads, kEpiBar>(lane == 0 ? wcount : 0, et, scratch, &total);
