@@ -49,8 +49,8 @@ NCU_TRAFFIC = {
                                          "a1a0d6a0fabb68c3"),
     ("decode1m", "indexer_topk"): (554.2e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
                                    "a15bce1542c95afa"),
-    ("verify64k", "indexer_topk"): (1383.5e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_mt.cu",
-                                    "5025f35e4c0d991d"),
+    ("verify64k", "indexer_topk"): (1377.5e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_mt.cu",
+                                    "a5370c32af216c65"),
 }
 FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s), used only if the
                              # FP8 GEMM measurement below cannot run

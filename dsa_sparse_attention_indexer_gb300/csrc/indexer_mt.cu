@@ -25,18 +25,21 @@
 //                  per SM sub-partition on the same tile, so TMEM loads and
 //                  arithmetic of different warps overlap while the MMA fills
 //                  the other accumulator); per token and row, ReLU,
-//                  head-weighted sum (packed f32x2 FMA), times the key scale.
+//                  head-weighted sum (packed f32x2 FMA; the block's head
+//                  weights staged in shared memory), times the key scale.
 //  3. top-k (dsa_indexer_topk): no score row is written.  A CTA's share of a
 //     row block is a piece; each row of a piece streams its candidates into a
 //     slot of 4608 in the workspace: scores above the row's rising threshold
 //     are appended (a warp reserves its rows' room with one shared atomic per
-//     tile and stores the entries after its next tile's arithmetic).  Every
-//     four tiles the epilogue checks the slots; a slot that may not hold the
-//     next four tiles is compacted: loaded into registers, one histogram pass
-//     over its key range finds the bin of its 2048th key, the entries from
-//     that bin up stay (at least 2048; an exact radix selection when the bin
-//     is crowded) and the threshold rises to the bin's lower edge.  At the
-//     piece end the slot's keys join the row's 12-bit key histogram.
+//     tile and stores the entries after its next tile's arithmetic).  A slot
+//     takes at most 128 entries a tile, so the epilogue checks the slots
+//     (4608 - fullest) / 128 tiles after the last check; a slot that may not
+//     hold the next four tiles is compacted: loaded into registers (16-byte
+//     loads), one histogram pass over its key range finds the bin of its
+//     2048th key, the entries from that bin up stay (at least 2048; an exact
+//     radix selection when the bin is crowded) and the threshold rises to the
+//     bin's lower edge.  At the piece end the slot's keys join the row's
+//     12-bit key histogram.
 //     The merge of the decode indexer (per-slot filter at the bin of the row's
 //     2048th key, then an exact per-row selection) gives the row's top-2048.
 //     The global top-2048 is inside the union of the pieces' top-2048s.
@@ -77,7 +80,9 @@ constexpr int kOffPid = kOffBars + (2 * kStages + 9) * 8;
 constexpr int kOffHist = kOffPid + kPidChunk * 2 * 8;          // 4096-bin radix histogram (compaction)
 constexpr int kOffMisc = kOffHist + 4096 * 4;
 constexpr int kMiscBytes = 512;
-constexpr int kSmemUsed = kOffMisc + kMiscBytes;
+constexpr int kOffW = (kOffMisc + kMiscBytes + 15) / 16 * 16;   // the row block's head weights (fp32)
+static_assert(kOffW % 16 == 0, "16-byte loads of the head weights");
+constexpr int kSmemUsed = kOffW + kRows * 32 * 4;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 static_assert(kOffQ % 1024 == 0 && kQBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
@@ -402,6 +407,8 @@ __device__ uint32_t compact_slot(uint32_t* key, int32_t* pos, int* n, int et, ui
 
 // Head-weighted ReLU sum of one token's 32 head logits (TMEM words) for one
 // query row: sum_m w_m max(l_m, 0), eight partial sums in four packed pairs.
+// w: the row's 32 weights in shared memory (copied once per row block; global
+// loads of them on every tile cost about 5 % of the kernel).
 __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], const float* __restrict__ w) {
     const float4* w4 = reinterpret_cast<const float4*>(w);
     float2 a[4];
@@ -409,7 +416,7 @@ __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], const float* 
     for (int j = 0; j < 4; ++j) a[j] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int m4 = 0; m4 < 8; ++m4) {
-        const float4 ww = __ldg(w4 + m4);
+        const float4 ww = w4[m4];
         const float2 x01 = make_float2(fmaxf(__uint_as_float(v[4 * m4 + 0]), 0.f),
                                        fmaxf(__uint_as_float(v[4 * m4 + 1]), 0.f));
         const float2 x23 = make_float2(fmaxf(__uint_as_float(v[4 * m4 + 2]), 0.f),
@@ -687,6 +694,7 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int tok = quarter * 32 + lane;
         const int et = threadIdx.x - 64;                 // 0 .. kEpiThreads - 1
         uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
+        float* wsm = reinterpret_cast<float*>(smem + kOffW);
         Walk w;
         walk_begin(w, p, NB, i0, i1);
         int64_t gidx = 0;
@@ -741,12 +749,18 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 p0 = b.seq_len[r] - qn + t0;                      // position of the block's first row
                 item0 = p.item_start[w.rb];
             }
+            if (!kStream && new_block) {                 // the block's head weights, once per block
+                epi_sync();
+                if (et < R * 32) wsm[et] = wq[row0 * 32 + et];
+                epi_sync();
+            }
             if (kStream && piece_start) {
                 const int64_t N = p.item_start[NB];
                 const int64_t g0 = cta_of_item(p.item_start[w.rb], N, G);
                 np = p.piece_first[w.rb + 1] - p.piece_first[w.rb];
                 slot0 = kRows * p.piece_first[w.rb] + (int)(blockIdx.x - g0);
                 epi_sync();                              // the previous piece is finished
+                if (et < R * 32) wsm[et] = wq[row0 * 32 + et];   // the block's head weights
                 if (et < kRows) {
                     misc->cnt[et] = 0;
                     misc->theta[et] = 0u;                // key 0: below every score
@@ -782,7 +796,7 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     float sc[kPerGrp];
                     if (nr > 0)
                         row_scores(tmem + ((uint32_t)(quarter * 32) << 16) + acc * 256 + rlo * 32,
-                                   wq + (row0 + rlo) * 32, nr, sk, sc);
+                                   wsm + rlo * 32, nr, sk, sc);
                     if constexpr (kStream) {
                         // candidates above each row's threshold: one ballot per row, then lane j
                         // reserves row rlo + j's room (the group's atomics go out together);
