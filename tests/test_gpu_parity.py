@@ -667,6 +667,33 @@ def test_indexer_topk_multirow_dirty_workspace_and_repeat(multirow_long_case, fi
         check_topk_row(got[row["i"]], row["topk"], row["s"], row["mag"], row["n"], what=f"row {row['i']}")
 
 
+# Requests with one or two rows in a multi-row batch leave some epilogue groups
+# without rows (a group takes a third of a block's rows); requests with more
+# than 8 rows span several row blocks, the last one ragged.
+MIXED_SEQ = [30000, 12000, 5000, 20000, 2200]
+MIXED_Q = [1, 2, 9, 17, 10]
+
+
+@pytest.fixture(scope="module")
+def multirow_mixed_case():
+    return _build_indexer_case(MIXED_SEQ, MIXED_Q, 2468, boost_req=3)
+
+
+def test_indexer_topk_multirow_groups_without_rows_and_several_row_blocks(multirow_mixed_case):
+    _check_indexer_topk(multirow_mixed_case, 4)
+
+
+def test_indexer_scores_multirow_groups_without_rows_and_several_row_blocks(multirow_mixed_case):
+    c = multirow_mixed_case
+    st = D.new_device_status(DEV)
+    sc = D.dsa_indexer_scores(c["q"], c["wt"], c["cache"], c["batch"], dev_status=st).cpu().numpy()
+    assert D.dsa_device_status_read(st)[0] == 0
+    for row in c["rows"]:
+        i, n = row["i"], row["n"]
+        check_scores(sc[i, :n], row["s"], row["mag"], what=f"row {i}")
+        assert np.all(np.isneginf(sc[i, n:c["w"].seq_len[row["r"]]]))     # causal: j > p masked
+
+
 def test_indexer_topk_multirow_workspace_has_no_score_rows():
     # the workspace holds candidate slots, not T x context score rows: for 8192
     # rows on a 131072-token context it stays far below the 4.29 GB of fp32 rows
