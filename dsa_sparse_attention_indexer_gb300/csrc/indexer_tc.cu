@@ -1003,7 +1003,14 @@ __device__ __forceinline__ void sort2048_regs(uint64_t& a, uint64_t& c, uint64_t
 }
 
 constexpr int kMergeThreads = 1024;
+// Boundary-bin capacity of the merge (entries kept in shared memory; the same
+// bytes later hold the row's position bitmap, 64 positions per entry).  The
+// large one serves contexts up to 1M positions with one block per SM; the
+// small one (about 72 KB of shared memory) lets two blocks share an SM, for
+// batches with more rows than SMs whose contexts fit its bitmap.  A larger
+// bin is selected in place from the workspace, a longer row by a sort.
 constexpr int kBndCap = 16384;
+constexpr int kBndSmall = 4096;
 constexpr int kMaxSegs = 1024;
 constexpr int kMOffHist = 0;
 constexpr int kMOffSelPos = kMOffHist + 4096 * 4;                 // selected positions, then keys: 2048 x u64 for the sort
@@ -1011,9 +1018,7 @@ constexpr int kMOffSelKey = kMOffSelPos + kTopK * 4;
 constexpr int kMOffNs = kMOffSelKey + kTopK * 4;
 constexpr int kMOffNb = kMOffNs + (kMaxSegs + 1) * 4;
 constexpr int kMOffBndKey = (kMOffNb + (kMaxSegs + 1) * 4 + 15) / 16 * 16;
-constexpr int kMOffBndPos = kMOffBndKey + kBndCap * 4;
-constexpr int kMOffMisc = kMOffBndPos + kBndCap * 4;
-constexpr int kMergeSmem = kMOffMisc + 256;
+constexpr int merge_smem(int bnd) { return kMOffBndKey + 2 * bnd * 4 + 256; }   // boundary keys, positions, misc
 static_assert(kMergeThreads * 2 == kTopK, "the sort holds two elements per thread");
 static_assert(kMOffSelPos % 8 == 0, "the sort reuses the selection as 64-bit words");
 
@@ -1023,7 +1028,8 @@ struct MergeMisc {
     int32_t scratch[32];
 };
 
-__global__ void __launch_bounds__(kMergeThreads)
+template <int kBnd>
+__global__ void __launch_bounds__(kMergeThreads, kBnd == kBndSmall ? 2 : 1)
 merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__ topk_scores) {
     extern __shared__ __align__(16) uint8_t msm[];
     uint32_t* hist = reinterpret_cast<uint32_t*>(msm + kMOffHist);
@@ -1032,8 +1038,8 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
     int32_t* ns_pre = reinterpret_cast<int32_t*>(msm + kMOffNs);
     int32_t* nb_pre = reinterpret_cast<int32_t*>(msm + kMOffNb);
     uint32_t* bnd_key = reinterpret_cast<uint32_t*>(msm + kMOffBndKey);
-    int32_t* bnd_pos = reinterpret_cast<int32_t*>(msm + kMOffBndPos);
-    MergeMisc* mm = reinterpret_cast<MergeMisc*>(msm + kMOffMisc);
+    int32_t* bnd_pos = reinterpret_cast<int32_t*>(msm + kMOffBndKey + kBnd * 4);
+    MergeMisc* mm = reinterpret_cast<MergeMisc*>(msm + kMOffBndKey + 2 * kBnd * 4);
     pdl_wait();
     pdl_trigger();
     const int64_t row = blockIdx.x;
@@ -1082,7 +1088,7 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
             sel_key[n_sure + i] = ckey[x];
         }
         ns = n_sure + n_bnd;
-    } else if (need > 0 && n_bnd <= kBndCap) {                   // exact selection in shared memory
+    } else if (need > 0 && n_bnd <= kBnd) {                      // exact selection in shared memory
         for (int i = gt; i < n_bnd; i += kMergeThreads) {
             const int j = seg_lookup(nb_pre, nseg, i);
             const int64_t x = (int64_t)j * p.seg_stride + (ns_pre[j + 1] - ns_pre[j]) + (i - nb_pre[j]);
@@ -1117,7 +1123,7 @@ merge_kernel(BatchDev b, Plan p, int32_t* __restrict__ topk, float* __restrict__
         __syncthreads();
         ns = min(mm->n_sel, kTopK);
     }
-    if (n_valid <= (int64_t)kBndCap * 64) {                     // the boundary buffers, free now, hold its bitmap
+    if (n_valid <= (int64_t)kBnd * 64) {                        // the boundary buffers, free now, hold its bitmap
         sel::write_ranked<kMergeThreads>(sel_pos, sel_key, ns, n_valid, reinterpret_cast<uint32_t*>(msm + kMOffBndKey),
                                          ns_pre, reinterpret_cast<uint16_t*>(hist), mm->scratch, out, outs, gt);
         return;
@@ -1231,7 +1237,8 @@ dsa_status launch_indexer_tc(const void* q, const float* w, uint8_t* q8, float* 
     if (!make_index_tmap(cache, b->num_pages, mx, &map)) return DSA_ERR_CUDA;
     if (ensure_smem_limit(reinterpret_cast<const void*>(&itc::score_topk_kernel<false>), itc::kSmemAlloc) != DSA_OK ||
         ensure_smem_limit(reinterpret_cast<const void*>(&itc::score_topk_kernel<true>), itc::kSmemAlloc) != DSA_OK ||
-        ensure_smem_limit(reinterpret_cast<const void*>(&itc::merge_kernel), itc::kMergeSmem) != DSA_OK)
+        ensure_smem_limit(reinterpret_cast<const void*>(&itc::merge_kernel<itc::kBndCap>), itc::merge_smem(itc::kBndCap)) !=
+            DSA_OK)
         return DSA_ERR_CUDA;
     BatchDev bd = to_dev(b);
     Plan p = carve_plan(plan_ws, b->batch, G);
@@ -1250,14 +1257,22 @@ dsa_status launch_indexer_tc(const void* q, const float* w, uint8_t* q8, float* 
 
 dsa_status launch_topk_merge(const dsa_batch* b, Plan p, int64_t max_segs, int32_t* topk, float* topk_scores,
                              cudaStream_t s) {
-    if (ensure_smem_limit(reinterpret_cast<const void*>(&itc::merge_kernel), itc::kMergeSmem) != DSA_OK)
-        return DSA_ERR_CUDA;
+    // more rows than SMs, contexts within the small bitmap: two merge blocks per SM
+    const bool small = b->total_q > device_sm_count() && b->max_seq_len <= (int64_t)itc::kBndSmall * 64;
+    const void* mk = small ? reinterpret_cast<const void*>(&itc::merge_kernel<itc::kBndSmall>)
+                           : reinterpret_cast<const void*>(&itc::merge_kernel<itc::kBndCap>);
+    const int msmem = itc::merge_smem(small ? itc::kBndSmall : itc::kBndCap);
+    if (ensure_smem_limit(mk, msmem) != DSA_OK) return DSA_ERR_CUDA;
     BatchDev bd = to_dev(b);
     if (max_segs > 0) {
         DSA_CHECK(launch_pdl(itc::merge_filter_kernel, dim3((unsigned)max_segs), dim3(itc::kFiltThreads), 0, s, 1, bd, p));
     }
-    DSA_CHECK(launch_pdl(itc::merge_kernel, dim3((unsigned)b->total_q), dim3(itc::kMergeThreads), itc::kMergeSmem, s, 1,
-                         bd, p, topk, topk_scores));
+    if (small)
+        DSA_CHECK(launch_pdl(itc::merge_kernel<itc::kBndSmall>, dim3((unsigned)b->total_q), dim3(itc::kMergeThreads), msmem,
+                             s, 1, bd, p, topk, topk_scores));
+    else
+        DSA_CHECK(launch_pdl(itc::merge_kernel<itc::kBndCap>, dim3((unsigned)b->total_q), dim3(itc::kMergeThreads), msmem,
+                             s, 1, bd, p, topk, topk_scores));
     return DSA_OK;
 }
 

@@ -694,6 +694,20 @@ def test_indexer_scores_multirow_groups_without_rows_and_several_row_blocks(mult
         assert np.all(np.isneginf(sc[i, n:c["w"].seq_len[row["r"]]]))     # causal: j > p masked
 
 
+@pytest.fixture(scope="module")
+def multirow_many_case():
+    # more query rows than SMs: the merge runs two blocks per SM
+    rng = np.random.default_rng(13)
+    seq = rng.integers(2100, 9000, 40).tolist()
+    ql = rng.integers(2, 8, 40).tolist()
+    return _build_indexer_case(seq, ql, 1357, boost_req=5)
+
+
+def test_indexer_topk_multirow_more_rows_than_sms(multirow_many_case):
+    assert multirow_many_case["w"].total_q > torch.cuda.get_device_properties(0).multi_processor_count
+    _check_indexer_topk(multirow_many_case, 8)
+
+
 def test_indexer_topk_multirow_workspace_has_no_score_rows():
     # the workspace holds candidate slots, not T x context score rows: for 8192
     # rows on a 131072-token context it stays far below the 4.29 GB of fp32 rows
