@@ -47,8 +47,8 @@ L2_BYTES = 129 * 1024 * 1024
 NCU_TRAFFIC = {
     ("decode32k", "sparse_mla_decode"): (105.3e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
                                          "a1a0d6a0fabb68c3"),
-    ("decode1m", "indexer_topk"): (554.2e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
-                                   "a15bce1542c95afa"),
+    ("decode1m", "indexer_topk"): (555.6e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
+                                   "3698f0628b4a2c3c"),
     ("verify64k", "indexer_topk"): (1377.5e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_mt.cu",
                                     "a5370c32af216c65"),
 }
