@@ -46,11 +46,11 @@ L2_BYTES = 129 * 1024 * 1024
 # and of the verify64k indexer call.
 NCU_TRAFFIC = {
     ("decode32k", "sparse_mla_decode"): (105.3e6, "dsa_sparse_attention_indexer_gb300/csrc/mla_tc.cu",
-                                         "a1a0d6a0fabb68c3"),
+                                         "d0948466dc982eaf"),
     ("decode1m", "indexer_topk"): (555.6e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_tc.cu",
-                                   "3698f0628b4a2c3c"),
-    ("verify64k", "indexer_topk"): (1377.5e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_mt.cu",
-                                    "a5370c32af216c65"),
+                                   "eec71195355bb8ac"),
+    ("verify64k", "indexer_topk"): (1378.1e6, "dsa_sparse_attention_indexer_gb300/csrc/indexer_mt.cu",
+                                    "ff6049eb5a8293fd"),
 }
 FP8_OVER_BF16 = 2.0          # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s), used only if the
                              # FP8 GEMM measurement below cannot run

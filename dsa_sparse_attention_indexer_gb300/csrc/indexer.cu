@@ -81,6 +81,7 @@ extern "C" dsa_status dsa_indexer_topk_mxfp4(const void* q, const float* w, cons
                                              size_t ws_bytes, int32_t* dev_status, void* stream) {
     dsa_status vs = validate_batch(b);
     if (vs != DSA_OK) return vs;
+    if (b->total_q == 0) return share ? dsa_topk_share_publish(share, layer_id, topk, 0) : DSA_OK;   // no rows
     if (!q || !w || !idxk_cache || !topk) return DSA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(topk) || (reinterpret_cast<uintptr_t>(idxk_cache) & 31)) return DSA_ERR_ALIGNMENT;
     if (b->total_q > 0) {
@@ -122,6 +123,7 @@ extern "C" dsa_status dsa_indexer_topk(const void* q, const float* w, const uint
                                        size_t ws_bytes, int32_t* dev_status, void* stream) {
     dsa_status vs = validate_batch(b);
     if (vs != DSA_OK) return vs;
+    if (b->total_q == 0) return share ? dsa_topk_share_publish(share, layer_id, topk, 0) : DSA_OK;   // no rows
     if (!q || !w || !idxk_cache || !topk) return DSA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(idxk_cache) || !aligned16(topk)) return DSA_ERR_ALIGNMENT;
     if (b->total_q > 0) {

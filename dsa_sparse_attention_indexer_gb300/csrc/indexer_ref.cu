@@ -117,6 +117,7 @@ extern "C" dsa_status dsa_indexer_scores(const void* q, const float* w, const ui
                                          size_t ws_bytes, int32_t* dev_status, void* stream) {
     dsa_status vs = validate_batch(b);
     if (vs != DSA_OK) return vs;
+    if (b->total_q == 0) return DSA_OK;                                  // no rows
     if (!q || !w || !idxk_cache || !scores) return DSA_ERR_INVALID_ARGUMENT;
     if (ld < b->max_seq_len) return DSA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(idxk_cache)) return DSA_ERR_ALIGNMENT;
@@ -139,6 +140,7 @@ extern "C" dsa_status dsa_indexer_scores_cuda_core(const void* q, const float* w
                                                    size_t ws_bytes, int32_t* dev_status, void* stream) {
     dsa_status vs = validate_batch(b);
     if (vs != DSA_OK) return vs;
+    if (b->total_q == 0) return DSA_OK;                                  // no rows
     if (!q || !w || !idxk_cache || !scores) return DSA_ERR_INVALID_ARGUMENT;
     if (ld < b->max_seq_len) return DSA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(idxk_cache)) return DSA_ERR_ALIGNMENT;

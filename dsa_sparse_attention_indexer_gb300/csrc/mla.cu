@@ -38,7 +38,6 @@ dsa_status dsa::sparse_mla_launch(const void* q, const int32_t* topk, const dsa_
                                   void* stream, bool decode) {
     dsa_status vs = validate_batch(b);
     if (vs != DSA_OK) return vs;
-    if (!q || !kv || !out) return DSA_ERR_INVALID_ARGUMENT;
     if (out_dtype != DSA_DTYPE_BF16 && out_dtype != DSA_DTYPE_F32) return DSA_ERR_INVALID_ARGUMENT;
     if (!(softmax_scale > 0.f)) return DSA_ERR_INVALID_ARGUMENT;
     if (!topk) {
@@ -48,8 +47,9 @@ dsa_status dsa::sparse_mla_launch(const void* q, const int32_t* topk, const dsa_
         if (gs != DSA_OK) return gs;
         if (rows != b->total_q) return DSA_ERR_INVALID_ARGUMENT;
     }
+    if (b->total_q == 0) return DSA_OK;                                  // no rows
+    if (!q || !kv || !out || !topk) return DSA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || !aligned16(topk)) return DSA_ERR_ALIGNMENT;
-    if (b->total_q == 0) return DSA_OK;
     (void)decode;
     const int G = mla_tc_ctas(b->total_q, device_sm_count());
     if (!ws) return DSA_ERR_INVALID_ARGUMENT;

@@ -53,6 +53,7 @@ extern "C" dsa_status dsa_indexer_topk_noalloc(const void* q, const float* w, co
                                                void* stream) {
     dsa_status vs = validate_batch(b);
     if (vs != DSA_OK) return vs;
+    if (b->total_q == 0) return share ? dsa_topk_share_publish(share, layer_id, topk, 0) : DSA_OK;   // no rows
     if (!q || !w || !idxk_cache || !topk) return DSA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(idxk_cache) || !aligned16(topk)) return DSA_ERR_ALIGNMENT;
     if (b->total_q > 0) {

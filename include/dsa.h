@@ -23,6 +23,11 @@
  *     as `void* stream` (a cudaStream_t; NULL = the legacy default stream).
  *   - Argument errors (null pointers, sizes, alignment, unsupported shapes) are
  *     detected on the host and returned before anything is launched.
+ *   - A call over zero items (n = 0 tokens or rows, or a batch whose total_q
+ *     is 0) checks its sizes, its batch and its share handle, launches
+ *     nothing and returns DSA_OK; its buffer pointers may then be NULL.  An
+ *     indexer call with no rows still publishes its (empty) top-k to a given
+ *     share handle.
  *   - Errors that only the device can see (a page id outside the cache, a slot
  *     outside the cache, an index outside the context, a wait that timed out)
  *     never fault: the offending element is skipped and recorded in the

@@ -126,6 +126,30 @@ def test_indexer_and_mla_argument_errors(L):
     assert L.dsa_topk_from_scores(fk, 10, fk, 0, 10, fk, None, 0, None) == 0      # zero rows: no launch
 
 
+def test_calls_over_zero_rows_launch_nothing(L):
+    """A batch whose requests bring no query rows: every call returns DSA_OK
+    with NULL buffers, and an indexer call still publishes its empty top-k to
+    a share handle (a shared layer before any full layer is still an error)."""
+    b = ctypes.byref(_fake_batch(B=2, T=0))
+    N = None
+    assert L.dsa_indexer_topk(N, N, N, b, N, N, N, 0, N, 0, N, N) == 0
+    assert L.dsa_indexer_topk_mxfp4(N, N, N, b, N, N, N, 0, N, 0, N, N) == 0
+    assert L.dsa_indexer_topk_noalloc(N, N, N, b, N, N, N, 0, N, N) == 0
+    assert L.dsa_indexer_scores(N, N, N, b, N, 0, N, 0, N, N) == 0
+    assert L.dsa_indexer_scores_cuda_core(N, N, N, b, N, 0, N, 0, N, N) == 0
+    share = ctypes.c_void_p()
+    assert L.dsa_topk_share_create(ctypes.byref(share)) == 0
+    assert L.dsa_sparse_mla_decode(N, N, share, N, b, 0.0625, N, 0, N, N, 0, N, N) == 5   # no full layer yet
+    assert L.dsa_indexer_topk(N, N, N, b, N, N, share, 0, N, 0, N, N) == 0               # publishes 0 rows
+    assert L.dsa_sparse_mla_decode(N, N, share, N, b, 0.0625, N, 0, N, N, 0, N, N) == 0
+    assert L.dsa_sparse_mla_prefill(N, N, share, N, b, 0.0625, N, 1, N, N, 0, N, N) == 0
+    assert L.dsa_topk_share_destroy(share) == 0
+    # zero tokens or rows in the calls that take a count
+    assert L.dsa_index_k_store(N, N, N, 0, N, N, 1e-6, 1e4, N, 1, N, N) == 0
+    assert L.dsa_latent_kv_store(N, N, N, 0, N, 1, N, N) == 0
+    assert L.dsa_topk_from_scores(N, 0, N, 0, 0, N, N, 0, N) == 0
+
+
 def test_cuda_core_scorer_and_mxfp4_rows_argument_errors(L):
     fk = ctypes.c_void_p(0x30000000)
     ws = ctypes.c_void_p(0x40000000)
