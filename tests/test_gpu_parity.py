@@ -708,6 +708,20 @@ def test_indexer_topk_multirow_more_rows_than_sms(multirow_many_case):
     _check_indexer_topk(multirow_many_case, 8)
 
 
+@pytest.mark.parametrize("seq,ql", [([5, 2048, 100, 1], [1, 1, 1, 1]),       # decode, nothing to score
+                                     ([2000, 700, 2048], [6, 3, 8]),         # several rows per request
+                                     ([1, 2048, 40], [1, 5, 1])])
+def test_indexer_topk_when_no_row_sees_more_than_2048_positions(seq, ql):
+    """Every row selects all its positions: 0..n-1 ascending, then -1; the plan
+    holds no tile, and the score and merge kernels must cope with that."""
+    c = _build_indexer_case(seq, ql, 4242)
+    _check_indexer_topk(c, 0)
+    got = D.dsa_indexer_topk(c["q"], c["wt"], c["cache"], c["batch"]).cpu().numpy()
+    for row in c["rows"]:
+        n = row["n"]
+        assert np.array_equal(got[row["i"], :n], np.arange(n)) and np.all(got[row["i"], n:] == -1)
+
+
 def test_indexer_topk_multirow_workspace_has_no_score_rows():
     # the workspace holds candidate slots, not T x context score rows: for 8192
     # rows on a 131072-token context it stays far below the 4.29 GB of fp32 rows
