@@ -236,10 +236,10 @@ class Step:
         self.full = [t == "full" for t in w.layers]
         self.launches_per_step = 0
 
-    def run(self, stream, timers=None, before_layer=None, after_layer=None, external=False):
-        """One step on `stream`.  before_layer(l) / after_layer(l), when given, run
-        just before layer l's first call and just after its sparse MLA (the e2e
-        graph hangs its per-layer copies there)."""
+    def run(self, stream, timers=None, before_layer=None, after_layer=None, external=False, before_mla=None):
+        """One step on `stream`.  before_layer(l) / before_mla(l) / after_layer(l),
+        when given, run just before layer l's first call, just before its sparse
+        MLA and just after it (the e2e graph hangs its copies there)."""
         D, gw = self.D, self.gw
         t = _timer(timers, stream, external)
 
@@ -262,6 +262,8 @@ class Step:
                                                              ws=self.idx_ws, dev_status=gw.dev_status,
                                                              stream=stream))
                 first_full = False
+            if before_mla is not None:
+                before_mla(l)
             t("sparse_mla_decode", lambda: D.dsa_sparse_mla_decode(
                 gw.q_mla[l], None, gw.kv_cache[l], gw.batch, share=self.share, out=self.out[l], ws=self.mla_ws,
                 dev_status=gw.dev_status, stream=stream))
@@ -276,12 +278,14 @@ class Step:
                                          dev_status=gw.dev_status, stream=stream)
 
     def e2e_io(self):
-        """(inputs copied first, inputs per layer, output per layer) of the e2e step."""
+        """(inputs needed first, a layer's other inputs, a layer's sparse-MLA
+        queries, a layer's output) of the e2e step."""
         gw = self.gw
         first = {"q_idx": gw.q_idx, "w_idx": gw.w_idx, "new_k": gw.new_k, "new_pos": gw.new_pos,
                  "new_slot": gw.new_slot}
-        per = {l: {f"c{l}": gw.new_c[l], f"r{l}": gw.new_r[l], f"q{l}": gw.q_mla[l]} for l in gw.layers}
-        return first, per, self.out
+        per = {l: {f"c{l}": gw.new_c[l], f"r{l}": gw.new_r[l]} for l in gw.layers}
+        mla_q = {l: {f"q{l}": gw.q_mla[l]} for l in gw.layers}
+        return first, per, mla_q, self.out
 
     def calls(self):
         """(name, fn) for every call of one step, in order (for per-call timing)."""
@@ -368,7 +372,7 @@ class MtpStep:
                                      share=None if topk is not None else self.share, out=self.out[k],
                                      ws=self.mla_ws, dev_status=self.gw.dev_status, stream=stream)
 
-    def run(self, stream, timers=None, before_layer=None, after_layer=None, external=False):
+    def run(self, stream, timers=None, before_layer=None, after_layer=None, external=False, before_mla=None):
         t = _timer(timers, stream, external)
 
         with self.share.mtp_iteration(enabled=self.reuse, eagle_topk=1):
@@ -379,13 +383,16 @@ class MtpStep:
                 t("latent_kv_store", lambda: self._store_c(k, stream))
                 if self.share.needs_scoring():
                     t("indexer_topk", lambda: self._indexer(k, stream))
+                if before_mla is not None:
+                    before_mla(k)
                 t("sparse_mla_decode", lambda: self._mla(k, stream))
                 if after_layer is not None:
                     after_layer(k)
 
     def e2e_io(self):
-        per = {k: {f"{name}{k}": v for name, v in self.inp[k].items()} for k in range(self.n)}
-        return {}, per, self.out
+        per = {k: {f"{name}{k}": v for name, v in self.inp[k].items() if name != "q_mla"} for k in range(self.n)}
+        mla_q = {k: {f"q_mla{k}": self.inp[k]["q_mla"]} for k in range(self.n)}
+        return {}, per, mla_q, self.out
 
     def calls(self):
         stream = torch.cuda.current_stream()
@@ -660,41 +667,51 @@ def run_ours(args, rank, world, workload=None, with_e2e=True):
                     scorers=scorers)
 
     # ---- end to end: host buffers in, host buffers out, through the same calls
-    first_in, layer_in, outs = step.e2e_io()
+    first_in, layer_in, mla_in, outs = step.e2e_io()
     dev_of = dict(first_in)
     for l in layer_in:
         dev_of.update(layer_in[l])
+        dev_of.update(mla_in[l])
     pinned_in = {k: v.cpu().pin_memory() for k, v in dev_of.items()}
     pinned_out = {l: torch.empty(outs[l].shape, dtype=outs[l].dtype).pin_memory() for l in outs}
     h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
     d2h = sum(t.numel() * t.element_size() for t in pinned_out.values())
     # One e2e step = every input copied in from pinned memory, the step, every
-    # layer's output read back, and a host wait for the result.  The copies of a
-    # layer overlap the compute of earlier layers: the indexer's inputs come
-    # first on the compute stream, a copy-in stream brings each layer's query and
-    # new latent rows, a copy-out stream reads each layer's output as soon as its
-    # sparse MLA is done.  Captured as one graph like the device-timed step.
+    # layer's output read back, and a host wait for the result.  A copy-in
+    # stream brings, in order: the inputs needed first and the first layer's
+    # other inputs, then its sparse-MLA queries, then every later layer's
+    # inputs.  The compute stream waits for each group just before its first
+    # use (the first layer's start, its sparse MLA, the second layer's start):
+    # three waits, since every wait between two kernels costs their overlap.
+    # A copy-out stream reads each layer's output as soon as its sparse MLA is
+    # done.  Captured as one graph like the device-timed step.
     cs_in, cs_out = torch.cuda.Stream(), torch.cuda.Stream()
-    first_keys = list(first_in)
-    layer_keys = {l: list(layer_in[l]) for l in layer_in}
+    layer_ids = list(layer_in)
+    groups = [list(first_in) + list(layer_in[layer_ids[0]]), list(mla_in[layer_ids[0]]),
+              [k for l in layer_ids[1:] for k in list(layer_in[l]) + list(mla_in[l])]]
 
     def e2e_step():
-        for k in first_keys:
-            dev_of[k].copy_(pinned_in[k], non_blocking=True)
         fork = torch.cuda.Event()
         fork.record(stream)
         cs_in.wait_event(fork)
         cs_out.wait_event(fork)
-        ready = {}
+        ready = []
         with torch.cuda.stream(cs_in):
-            for l in layer_keys:
-                for k in layer_keys[l]:
+            for keys in groups:
+                for k in keys:
                     dev_of[k].copy_(pinned_in[k], non_blocking=True)
-                ready[l] = torch.cuda.Event()
-                ready[l].record(cs_in)
+                ready.append(torch.cuda.Event())
+                ready[-1].record(cs_in)
 
         def before(l):
-            stream.wait_event(ready[l])
+            if l == layer_ids[0]:
+                stream.wait_event(ready[0])
+            elif len(layer_ids) > 1 and l == layer_ids[1]:
+                stream.wait_event(ready[2])
+
+        def before_mla(l):
+            if l == layer_ids[0]:
+                stream.wait_event(ready[1])
 
         def after(l):
             done = torch.cuda.Event()
@@ -703,7 +720,9 @@ def run_ours(args, rank, world, workload=None, with_e2e=True):
             with torch.cuda.stream(cs_out):
                 pinned_out[l].copy_(outs[l], non_blocking=True)
 
-        step.run(stream, before_layer=before, after_layer=after)
+        step.run(stream, before_layer=before, after_layer=after, before_mla=before_mla)
+        if len(layer_ids) == 1:
+            stream.wait_event(ready[2])                    # (no later layer: nothing left to copy)
         join = torch.cuda.Event()
         join.record(cs_out)
         stream.wait_event(join)
