@@ -29,11 +29,11 @@
 //                  weights staged in shared memory), times the key scale.
 //  3. top-k (dsa_indexer_topk): no score row is written.  A CTA's share of a
 //     row block is a piece; each row of a piece streams its candidates into a
-//     slot of 4608 in the workspace: scores above the row's rising threshold
+//     slot of 6144 in the workspace: scores above the row's rising threshold
 //     are appended (a warp reserves its rows' room with one shared atomic per
 //     tile and stores the entries after its next tile's arithmetic).  A slot
 //     takes at most 128 entries a tile, so the epilogue checks the slots
-//     (4608 - fullest) / 128 tiles after the last check; a slot that may not
+//     (6144 - fullest) / 128 tiles after the last check; a slot that may not
 //     hold the next four tiles is compacted: loaded into registers (16-byte
 //     loads), one histogram pass over its key range finds the bin of its
 //     2048th key, the entries from that bin up stay (at least 2048; an exact
@@ -87,7 +87,7 @@ constexpr int kSmemAlloc = kSmemUsed + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 static_assert(kOffQ % 1024 == 0 && kQBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
 constexpr int kEpiBar = 1;                      // named barrier of the two epilogue groups
-constexpr int kSlotCap = kSegCandidates;        // candidate entries of one row of a piece
+constexpr int kSlotCap = kRowSlotCandidates;    // candidate entries of one row of a piece
 constexpr int kCheckEvery = 4;                  // tiles between epilogue-wide checks of the slots
 static_assert(kSlotCap - kCheckEvery * 128 > kTopK, "room above the 2048 kept by a compaction");
 
@@ -316,7 +316,7 @@ __device__ uint32_t compact_slot(uint32_t* key, int32_t* pos, int* n, int et, ui
     int32_t ps[kSlotPer];
     uint32_t lo = 0xffffffffu, hi = 0u;
 #pragma unroll
-    for (int g = 0; g < kSlotPer / 4; ++g) {          // 16-byte loads (slots are 16-byte aligned, 4608 long)
+    for (int g = 0; g < kSlotPer / 4; ++g) {          // 16-byte loads (slots are 16-byte aligned, kSlotCap long)
         const int i0 = (g * kEpiThreads + et) * 4;
         uint4 kv = make_uint4(0u, 0u, 0u, 0u), pv = make_uint4(0u, 0u, 0u, 0u);
         if (i0 < cnt) {
@@ -840,7 +840,7 @@ score_rows_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (kStream && (piece_end || ptile == next_check)) {
                 // every tile of the piece so far is in the slots: compact the slots that
                 // may not hold the next kCheckEvery tiles, schedule the next check, and at
-                // the piece end publish the slots (up to 4608 entries each, no compaction)
+                // the piece end publish the slots (up to kSlotCap entries each, no compaction)
                 flush();
                 if (lane == 0 && bad) misc->bad = 1;
                 epi_sync();

@@ -836,8 +836,9 @@ score_topk_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __res
 //    selects the remaining 2048 - sure among the bin-b* entries exactly (ties
 //    -> lower position), sorts the 2048 by position and writes them out.
 constexpr int kFiltThreads = 512;
-constexpr int kFiltPer = kSegCand / kFiltThreads;  // candidates per thread
-static_assert(kSegCand % kFiltThreads == 0 && kFiltPer <= 16, "two class bits per candidate in a 32-bit word");
+constexpr int kFiltCap = kSegCand > kRowSlotCandidates ? kSegCand : kRowSlotCandidates;   // a segment's entries, at most
+constexpr int kFiltPer = kFiltCap / kFiltThreads;  // candidates per thread
+static_assert(kFiltCap % kFiltThreads == 0 && kFiltPer <= 16, "two class bits per candidate in a 32-bit word");
 static_assert(4096 % (kFiltThreads * 4) == 0, "whole 16-byte histogram loads per thread");
 constexpr int kFiltBins = 4096 / kFiltThreads;     // histogram bins per thread
 
@@ -857,7 +858,7 @@ merge_filter_kernel(BatchDev b, Plan p) {
         row = b.q_start[p.segs[s].r];
     }
     const int tid = threadIdx.x;
-    const int cnt = min(p.cand_cnt[s], kSegCand);
+    const int cnt = min(p.cand_cnt[s], kFiltCap);
     uint32_t* key = p.cand_key + (int64_t)s * p.seg_stride;
     int32_t* pos = p.cand_pos + (int64_t)s * p.seg_stride;
     uint32_t k[kFiltPer];

@@ -12,8 +12,11 @@ struct Seg {
     int32_t r, lo, hi, cta;
 };
 
-// Candidate slots of one segment (one query row's share of one CTA's tiles).
+// Candidate slots of one segment (one query row's share of one CTA's tiles):
+// the decode kernel's shared-memory buffer, and the multi-row kernel's larger
+// workspace slots (a compaction there stalls the stream, so fewer of them pay).
 constexpr int kSegCandidates = 4608;
+constexpr int kRowSlotCandidates = 6144;
 
 struct Plan {
     int64_t* tile_start;   // [B+1] tile prefix over requests that need scoring

@@ -230,8 +230,8 @@ dsa_status dsa_latent_kv_store_fused(const void* kv_c, const void* k_pe, const i
  *   ws          device workspace of at least dsa_indexer_topk_workspace_size() bytes.
  *               A decode batch (one query row per request) needs O(T) bytes for
  *               any GPU; a batch with several rows per request needs row
- *               histograms plus candidate slots of 4608 entries per query row
- *               and CTA share, O(T x 4608), sized for the SM count of the device
+ *               histograms plus candidate slots of 6144 entries per query row
+ *               and CTA share, O(T x 6144), sized for the SM count of the device
  *               current at the size call (call both on the same device).       */
 dsa_status dsa_indexer_topk_workspace_size(const dsa_batch* b, size_t* bytes);
 dsa_status dsa_indexer_topk(const void* q, const float* w, const uint8_t* idxk_cache,
