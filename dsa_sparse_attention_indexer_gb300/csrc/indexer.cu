@@ -28,7 +28,7 @@ inline size_t mx_rows_virtual_bytes(const dsa_batch* b) {
 
 // Decode batches: the fused path.  Other batches: row histograms + the
 // multi-row plan with its candidate slots for the current device's SM count
-// (O(T x 4608) candidates, no score rows), or the MXFP4 call's virtual decode
+// (O(T x 6144) candidates, no score rows), or the MXFP4 call's virtual decode
 // batch, whichever is larger.
 inline size_t indexer_ws_bytes(const dsa_batch* b) {
     if (use_tc_path(b)) return decode_ws_bytes(b->total_q, b->batch);
