@@ -722,6 +722,18 @@ def test_indexer_topk_when_no_row_sees_more_than_2048_positions(seq, ql):
         assert np.array_equal(got[row["i"], :n], np.arange(n)) and np.all(got[row["i"], n:] == -1)
 
 
+def test_indexer_topk_multirow_slots_published_above_the_decode_buffer_size():
+    """One request with 2 rows on a 730,000-token context: 5,704 tiles over the
+    SMs give each CTA a piece of about 37 tiles, whose rows publish about 4,736
+    candidates each (more than the decode kernel's 4608-entry buffer) without a
+    compaction.  The merge filter must take every one of them."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    L = 730000
+    assert 36 * 128 * sms < L < 48 * 128 * sms          # pieces longer than 36 tiles, shorter than the first check
+    c = _build_indexer_case([L], [2], 8642)
+    _check_indexer_topk(c, 2)
+
+
 def test_indexer_topk_multirow_workspace_has_no_score_rows():
     # the workspace holds candidate slots, not T x context score rows: for 8192
     # rows on a 131072-token context it stays far below the 4.29 GB of fp32 rows
