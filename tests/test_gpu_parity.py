@@ -747,11 +747,14 @@ def test_indexer_topk_multirow_workspace_has_no_score_rows():
     assert nbytes < 8192 * 131072 * 4 // 4
 
 
-def test_indexer_topk_multirow_all_keys_equal():
+@pytest.mark.parametrize("seq,ql", [([20000, 5000], [4, 7]),
+                                     # more rows than SMs (the two-blocks-per-SM merge): each row's
+                                     # ~6000 tied candidates overflow its 4096-entry boundary buffer
+                                     ([6000] * 40, [5] * 40)])
+def test_indexer_topk_multirow_all_keys_equal(seq, ql):
     """Multi-row batches whose every cached key is the same: every score ties,
     so each row with more than 2048 visible positions selects 0..2047 exactly,
     through compactions of slots made entirely of ties."""
-    seq, ql = [20000, 5000], [4, 7]
     w = _small_workload(seq, ql, 4545)
     g = _gen(4545)
     pt = page_table(w, "cpu")
