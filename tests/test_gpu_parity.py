@@ -265,6 +265,15 @@ def test_indexer_topk_decode_many_requests(decode_many_case):
     _check_indexer_topk(decode_many_case, 4)
 
 
+def test_indexer_topk_decode_more_rows_than_sms_up_to_the_small_merge_bitmap():
+    """More decode rows than SMs select with the two-blocks-per-SM merge, whose
+    position bitmap holds 2^18 positions: contexts up to exactly that size."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    seq = [250000, 262144, 100000] + [2100] * (sms + 1)
+    c = _build_indexer_case(seq, [1] * len(seq), 1212, boost_req=1)
+    _check_indexer_topk(c, 4)
+
+
 @pytest.mark.parametrize("fill", [0x00, 0xAB, 0xFF])
 def test_indexer_topk_decode_dirty_workspace(decode_case, fill):
     """The workspace content on entry must not matter (it is caller memory)."""
